@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV decode step on GB300.
+
+Default workload (N=1): LLaMA-7B-shaped single-layer decode -- 64 sequences,
+32 heads MHA, head_dim 128, block size 16, context lengths U[512, 4096],
+bf16 K/V, physical blocks shuffled across a pool of the needed blocks + 10 %.
+One step = kv_append of one new token per sequence (into its last page, the
+slot of a freshly allocated block where the page was full) followed by
+paged_attn_decode over the context including that token.  The metric is KV
+bytes read per second (logical K+V bytes of every sequence's context) and
+sequence-steps per second.
+
+Under torchrun each rank runs its own replica (own sequences, own pools):
+decode is data-parallel by sequence with no exchange, so scaling is weak and
+the value is the bytes all ranks read divided by the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload instead (the reference arm of this benchmark).
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV-read GB/s vs ~8 TB/s HBM; seq-steps/sec"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+KERNEL_SOURCES = ["paged_kv_decode_26_gb300/csrc/decode_kernel.cuh",
+                  "paged_kv_decode_26_gb300/csrc/pkv_device.cuh",
+                  "paged_kv_decode_26_gb300/csrc/capi.cu",
+                  "paged_kv_decode_26_gb300/csrc/decode_inst.inc"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default 2)")
+    ap.add_argument("--split", type=int, default=0, help="split_tokens (0 = automatic)")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the CPU baseline sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel sources and workload."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    src = re.search(r"^source_sha256:\s*(\S+)", text, re.M)
+    wl = re.search(r"^workload:\s*(.+)$", text, re.M)
+    tb = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", text, re.M)
+    if not (src and wl and tb) or src.group(1) != kernel_source_hash() or wl.group(1).strip() != workload:
+        return None
+    return int(tb.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (100 ms)."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_id: str):
+        self.device_id = device_id
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open("/tmp/pkv_clocks_%d.csv" % os.getpid(), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.device_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), r[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def gpu_id_for_smi(torch, dev: int) -> str:
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        return str(dev)
+
+
+def workload_name(case, config) -> str:
+    from paged_kv_decode_26_gb300 import workloads as wl
+    spec = wl.CONFIGS[config]
+    lens = spec["lens"]
+    return (f"{case.name}: {case.S} seqs, {case.H} q / {case.Hk} kv heads, d={case.D}, "
+            f"block_size={case.B}, lens {lens[0]}{list(lens[1:])}, "
+            f"{str(case.dtype).replace('torch.', '')} K/V, {case.num_blocks} pool blocks, seed {case.seed}")
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample_seconds(case, lens, tables, budget_s):
+    """Run the oracle on whole sequences (all heads) of the step until about
+    `budget_s` seconds of CPU work; returns (kv_bytes, seconds, n_seqs)."""
+    from oracle import oracle as orc
+    row = case.Hk * case.D * 2 * 2
+    done_bytes, t_total, n = 0, 0.0, 0
+    order = list(range(case.S))
+    while t_total < budget_s and n < len(order):
+        s = order[n]
+        t0 = time.perf_counter()
+        orc.decode_two_pass(case.q, case.k_pool, case.v_pool, tables, lens, case.scale,
+                            seq_ids=[s])
+        t_total += time.perf_counter() - t0
+        done_bytes += int(lens[s]) * row
+        n += 1
+    return done_bytes, t_total, n
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle timed on the host cores, each step a
+    bounded sample (a few heads of one sequence) of the same workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    from oracle import build as ob
+    from oracle import oracle as orc
+    from paged_kv_decode_26_gb300 import workloads as wl
+    ob.build()
+    torch.set_num_threads(1)
+    case = wl.make_case(args.config)
+    lens = case.context_lens
+    # choose the per-step sample: h heads of the longest-running sequence
+    s = int(torch.argmax(lens))
+    heads = case.H
+    t0 = time.perf_counter()
+    orc.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables, lens, case.scale,
+                        seq_ids=[s])
+    t_seq = time.perf_counter() - t0
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    h = max(1, min(heads, int(heads * budget / max(t_seq, 1e-6))))
+    G = case.H // case.Hk
+    hk = max(1, h // G)
+    h = hk * G
+    # compact sub-case: the sequence's blocks, the first hk kv heads
+    nb = (int(lens[s]) + case.B - 1) // case.B
+    ids = case.block_tables[s, :nb].long()
+    k_sub = case.k_pool[ids][:, :, :hk].contiguous()
+    v_sub = case.v_pool[ids][:, :, :hk].contiguous()
+    q_sub = case.q[s:s + 1, :h].contiguous()
+    bt_sub = torch.arange(nb, dtype=torch.int32).view(1, nb)
+    l_sub = lens[s:s + 1].clone()
+    step_bytes = int(lens[s]) * hk * case.D * 2 * 2
+    for _ in range(args.warmup):
+        orc.decode_two_pass(q_sub, k_sub, v_sub, bt_sub, l_sub, case.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.decode_two_pass(q_sub, k_sub, v_sub, bt_sub, l_sub, case.scale)
+    dt = time.perf_counter() - t0
+    ms = dt / max(1, args.steps) * 1e3
+    value = step_bytes / (ms / 1e3) / 1e9
+    sample = (f"per step: sequence {s} ({int(lens[s])} tokens), {h} of {case.H} query heads "
+              f"({hk} kv heads), fp64 two-pass oracle, single thread")
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(case, args.config)},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_decode_26_gb300 import build as lib_build
+    if rank == 0:
+        lib_build.build()
+    if world > 1:
+        dist.barrier()
+    import paged_kv_decode_26_gb300 as pkv
+    from paged_kv_decode_26_gb300 import workloads as wl
+
+    # ---- this rank's replica of the workload
+    seed = (args.config - 1) + 1000 * rank
+    # the long-context pool holds exactly the needed blocks; give the
+    # appended tokens room for their new pages
+    extra = {"pool_extra": 0.01} if args.config == 4 else {}
+    case = wl.make_case(args.config, seed=seed, **extra)
+    S = case.S
+    bm = pkv.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)
+    bt_h = case.block_tables.clone()
+    lens_h = case.context_lens.clone()
+    slots_h = torch.empty(S, dtype=torch.int64)
+    if case.k_new is None:
+        case.k_new = wl._normal(np.random.default_rng(seed + 7), (S, case.Hk, case.D), case.dtype)
+        case.v_new = wl._normal(np.random.default_rng(seed + 8), (S, case.Hk, case.D), case.dtype)
+    need_cols = int(((lens_h + 1 + case.B - 1) // case.B).max())
+    if need_cols > bt_h.shape[1]:
+        bt_h = torch.cat([bt_h, torch.full((S, need_cols - bt_h.shape[1]), -1,
+                                           dtype=torch.int32)], 1)
+    st = bm.append_slots(bt_h, lens_h, slots_h)
+    if st != 0:
+        raise RuntimeError("pool has no room for the appended tokens")
+    max_ctx = int(lens_h.max())
+
+    q = case.q.to(dev)
+    k_pool = case.k_pool.to(dev)
+    v_pool = case.v_pool.to(dev)
+    k_new = case.k_new.to(dev)
+    v_new = case.v_new.to(dev)
+    bt = bt_h.to(dev)
+    lens = lens_h.to(dev)
+    slots = slots_h.to(dev)
+    out = torch.empty(S, case.H, case.D, dtype=case.out_dtype, device=dev)
+    ws = pkv.alloc_decode_workspace(q, k_pool, max_ctx, args.split)
+    split_used = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B, max_ctx)
+    with_swaps = args.config == 5
+    if with_swaps:
+        d2d = case.d2d_pairs.to(dev)
+        h2d = case.h2d_pairs.pin_memory()
+        hk_pool = case.host_k_pool.pin_memory()
+        hv_pool = case.host_v_pool.pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pkv.kv_append(k_pool, v_pool, k_new, v_new, slots)
+        pkv.paged_attn_decode(out, q, k_pool, v_pool, bt, lens, case.scale, max_ctx,
+                              split_tokens=args.split, workspace=ws)
+        if with_swaps:
+            pkv.swap_blocks(k_pool, k_pool, d2d)
+            pkv.swap_blocks(v_pool, v_pool, d2d)
+            pkv.swap_blocks(k_pool, hk_pool, h2d)
+            pkv.swap_blocks(v_pool, hv_pool, h2d)
+
+    launches_per_step = 2 + (1 if (max_ctx + split_used - 1) // split_used > 1 else 0) + \
+        (4 if with_swaps else 0)
+
+    # ---- bytes per step
+    row = case.Hk * case.D * 2
+    kv_read = int(lens_h.sum()) * row * 2                 # K and V of every context row
+    es = 2
+    io_bytes = (q.numel() * es + out.numel() * out.element_size() + bt.numel() * 4 + S * 4)
+    decode_alg_bytes = kv_read + io_bytes
+    swap_bytes = 0
+    if with_swaps:
+        bb = case.B * case.Hk * case.D * es
+        swap_bytes = 2 * 2 * bb * (case.d2d_pairs.shape[0] + case.h2d_pairs.shape[0])
+
+    pkv.device_errors(clear=True)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    sampler.start()
+    time.sleep(0.3)
+    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for i in range(args.steps):
+        pkv.kv_append(k_pool, v_pool, k_new, v_new, slots)
+        dec_events[i][0].record(stream)
+        pkv.paged_attn_decode(out, q, k_pool, v_pool, bt, lens, case.scale, max_ctx,
+                              split_tokens=args.split, workspace=ws)
+        dec_events[i][1].record(stream)
+        if with_swaps:
+            pkv.swap_blocks(k_pool, k_pool, d2d)
+            pkv.swap_blocks(v_pool, v_pool, d2d)
+            pkv.swap_blocks(k_pool, hk_pool, h2d)
+            pkv.swap_blocks(v_pool, hv_pool, h2d)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    # keep the GPU under the same load until the sampler has ~1.5 s of samples
+    while time.perf_counter() - wall0 < 1.5:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    ms = t_start.elapsed_time(t_end) / max(1, args.steps)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_events)
+    if world > 1:
+        t = torch.tensor([ms, dec_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, dec_ms = float(t[0]), float(t[1])
+    errors = pkv.device_errors(clear=True)
+    if errors:
+        raise RuntimeError(f"device error flags 0x{errors:x} raised during the benchmark")
+
+    # ---- end to end through the public API with host buffers
+    q_h = case.q.pin_memory()
+    kn_h, vn_h = case.k_new.pin_memory(), case.v_new.pin_memory()
+    bt_p, lens_p, slots_p = bt_h.pin_memory(), lens_h.pin_memory(), slots_h.pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d_bytes = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, bt_p, lens_p, slots_p))
+    d2h_bytes = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        q.copy_(q_h, non_blocking=True)
+        k_new.copy_(kn_h, non_blocking=True)
+        v_new.copy_(vn_h, non_blocking=True)
+        bt.copy_(bt_p, non_blocking=True)
+        lens.copy_(lens_p, non_blocking=True)
+        slots.copy_(slots_p, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import build as ob
+        ob.build()
+        b, secs, nseq = oracle_sample_seconds(case, lens_h, bt_h, args.cpu_budget)
+        cpu = {"value": b / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nseq} of {S} sequences of the step (all {case.H} heads, "
+                         f"{b / 1e6:.1f} MB of K/V), fp64 two-pass oracle, single thread"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak()
+    name = workload_name(case, args.config)
+    total_kv = kv_read * world
+    value = total_kv / (ms / 1e3) / 1e9
+    achieved = decode_alg_bytes / (dec_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "seq_steps_per_s": S * world / (ms / 1e3),
+        "config": {
+            "workload": name,
+            "step": "kv_append (1 token/seq) + paged_attn_decode" +
+                    (" + swap_blocks D2D and pinned-H2D (K and V)" if with_swaps else ""),
+            "num_seqs_per_gpu": S,
+            "kv_bytes_per_step_per_gpu": kv_read,
+            "split_tokens": split_used,
+            "storage_dtype": str(case.dtype).replace("torch.", ""),
+            "out_dtype": str(case.out_dtype).replace("torch.", ""),
+            "l2": ("inputs larger than L2 (%.2f GB of K/V vs 129 MB), no flush" % (kv_read / 1e9)
+                   if kv_read > 4 * L2_BYTES else
+                   "inputs smaller than L2: steps re-read a hot cache"),
+            "parallelism": f"replicas x{world} (sequences per GPU independent)",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": committed_traffic(name),
+            "kernel": "paged_attn_decode (decode kernel + split merge), CUDA events per call",
+            "algorithmic_bytes_per_launch": decode_alg_bytes,
+            "ms_per_launch": dec_ms,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+        },
+        "clocks": clocks,
+        "e2e": {"value": total_kv / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+                "ms_per_step": e2e_ms, "steps": n_e2e},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cpu,
+    }
+    if with_swaps:
+        line["config"]["swap_bytes_per_step"] = swap_bytes
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

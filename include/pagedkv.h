@@ -1,0 +1,238 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: single-query (decode) attention over a
+ * paged KV cache, the append-one-token write into the last page, and batched
+ * block copy, for NVIDIA GB300 (sm_103a).
+ *
+ * Pages the operations come from (cited by title and section):
+ *   [SWAP]   "vLLM 中 FlashAttention 与 KVCache 交换机制深度解析":
+ *            the attention formula softmax(Q K^T / sqrt(d_k)) V; the
+ *            OnlineSoftmax recurrence (M_new, L_new, O_new); PagedAttention
+ *            pages addressed through a page table; the swap_blocks signature
+ *            (src_kv_cache, dst_kv_cache, src_to_dst) and its mock.
+ *   [LAYOUT] "大模型长文本推理基座从 FlashAttention 硬件加速机制到 vLLM 核心
+ *            PagedAttention 显存物理布局深度剖析": section 二.2 (logical
+ *            blocks of 16 tokens, block table, a new physical block appended
+ *            when the last one is full) and section 三 (KVBlockManager,
+ *            append_token, ref counts).
+ *   [OPT]    "vLLM中FlashAttention与KVCache优化解析": "Block Table 管理",
+ *            "Swap Blocks 机制" (Key and Value caches copied by separate
+ *            calls) and FlashAttentionMetadata (context_lens_tensor,
+ *            block_tables, max_decode_seq_len).
+ *
+ * Conventions for every entry point:
+ *   - Buffers belong to the caller.  The library allocates no device memory
+ *     and never synchronises a stream; all work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *   - "device" pointers must be device memory of the current CUDA device
+ *     (or host memory the device can address, where stated).
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns PKV_ERR_INVALID / PKV_ERR_UNSUPPORTED and enqueues
+ *     nothing.  The host never reads device arrays (block tables, lengths,
+ *     slot maps, pairs); the kernels check those themselves: an out-of-range
+ *     index is skipped (never dereferenced) and recorded in the device error
+ *     word read by pkv_device_errors().
+ *   - Launch failures return PKV_ERR_CUDA (cudaGetLastError after launch).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,      /* bad pointer, shape, alignment or range */
+    PKV_ERR_UNSUPPORTED = 2,  /* valid but not compiled (head_dim, block_size, group) */
+    PKV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    PKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+    PKV_ERR_NO_BLOCKS = 5     /* block manager: no free physical block */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
+
+/* Bits of the device error word (pkv_device_errors). */
+#define PKV_DEVERR_BLOCK_ID 0x1u    /* decode: block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_CONTEXT 0x2u     /* decode: context_len < 0, beyond the table, or beyond max_context_len */
+#define PKV_DEVERR_SLOT 0x4u        /* append: slot beyond num_blocks * block_size */
+#define PKV_DEVERR_PAIR 0x8u        /* copy: pair index beyond its pool */
+#define PKV_DEVERR_TIMEOUT 0x10u    /* a pipeline wait gave up (should never happen) */
+
+/* Human-readable name of a status code (static string). */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Text of the last failure on the calling thread (validation reason or
+ * CUDA error string); empty when none.  Static thread-local storage. */
+PKV_API const char* pkv_last_error_detail(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+PKV_API int pkv_version(void);
+
+/*
+ * Device error word of the current device: OR of PKV_DEVERR_* bits set by
+ * kernels since the last clear.  Synchronises the current device (it is a
+ * diagnostic, not part of the hot path).  clear != 0 resets it to 0.
+ */
+PKV_API pkv_status pkv_device_errors(uint32_t* flags, int clear);
+
+/*
+ * Workspace bytes paged_attn_decode needs for the given problem and split
+ * length (split_tokens = 0 means the automatic choice; the same arguments
+ * must then be passed to the decode call).  Returns 0 when no workspace is
+ * needed (every sequence fits one split).
+ */
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads,
+                                          int head_dim, int block_size, int max_context_len,
+                                          int split_tokens);
+
+/* The split length (tokens per work unit) the automatic choice takes. */
+PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, int head_dim,
+                                    int block_size, int max_context_len);
+
+/*
+ * paged_attn_decode -- for every sequence s and query head h:
+ *
+ *     out[s,h,:] = sum_t softmax_t(scale * q[s,h,:] . K_t) * V_t,
+ *     t < context_lens[s],
+ *
+ * where token t of sequence s lives in physical block
+ * block_tables[s][t / block_size] at row t % block_size ([SWAP]
+ * PagedAttention; [LAYOUT] section 二.2; [OPT] "Block Table 管理"), and
+ * query head h reads KV head h / (n_heads / n_kv_heads).  Computed in one
+ * pass per work unit with the [SWAP] OnlineSoftmax recurrence in fp32; long
+ * contexts are cut into splits of split_tokens whose partial (M, L, O)
+ * states are merged by the same recurrence in a second kernel.
+ *
+ *   out          device, [num_seqs, n_heads, head_dim] of out_dtype
+ *                (F16, BF16 or F32), written completely.  A sequence with
+ *                context_len 0 gets zeros.
+ *   q            device, [num_seqs, n_heads, head_dim] of kv_dtype
+ *   k_pool,v_pool device, [num_blocks, block_size, n_kv_heads, head_dim] of
+ *                kv_dtype (F16 or BF16), 16-byte aligned
+ *   block_tables device int32 [num_seqs, max_blocks_per_seq]; only the
+ *                first ceil(context_lens[s] / block_size) entries of a row
+ *                are read
+ *   context_lens device int32 [num_seqs]
+ *   scale        multiplies q . k (normally 1/sqrt(head_dim))
+ *   max_context_len  host-side upper bound of context_lens (sizes the grid;
+ *                the metadata's max_decode_seq_len).  A longer context is
+ *                clamped and flagged PKV_DEVERR_CONTEXT.
+ *   split_tokens tokens per split (a multiple of block_size), 0 = automatic
+ *   workspace    device, >= pkv_decode_workspace_bytes(...) bytes, 256-byte
+ *                aligned; may be NULL when that size is 0.  Scratch only:
+ *                contents on entry are ignored.
+ * Supported: head_dim 64 or 128; block_size 16 or 32;
+ * n_heads / n_kv_heads in {1, 2, 4, 8}.
+ */
+PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void* q,
+                                     const void* k_pool, const void* v_pool, pkv_dtype kv_dtype,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int n_heads,
+                                     int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                                     float scale, int max_context_len, int split_tokens,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kv_append -- write one new token per sequence into its page
+ * (reshape-and-cache; [LAYOUT] section 三 append_token):
+ *
+ *     k_pool[slot / block_size, slot % block_size, :, :] = k_new[s, :, :]
+ *     v_pool[...same...]                                 = v_new[s, :, :]
+ *
+ * with slot = slot_mapping[s]; a negative slot skips the sequence, a slot
+ * >= num_blocks * block_size is skipped and flagged PKV_DEVERR_SLOT.
+ *   k_pool, v_pool device [num_blocks, block_size, n_kv_heads, head_dim]
+ *   k_new, v_new   device [num_seqs, n_kv_heads, head_dim], same dtype
+ *   slot_mapping   device int64 [num_seqs]
+ * Bit-exact copy.  dtype F16, BF16 or F32; head_dim * element size must be a
+ * multiple of 16 bytes and all four buffers 16-byte aligned.
+ */
+PKV_API pkv_status kv_append(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                             pkv_dtype dtype, const int64_t* slot_mapping, int num_seqs,
+                             int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                             void* stream);
+
+/*
+ * swap_blocks -- batched block copy ([SWAP] swap_blocks; [OPT] "Swap Blocks
+ * 机制", one call per cache: Key, then Value):
+ *
+ *     dst_pool[j] = src_pool[i]   for each pair (i, j) = pairs[k]
+ *
+ *   dst_pool  device memory, num_dst_blocks blocks of block_bytes
+ *   src_pool  device memory, or pinned host memory the device can address
+ *             (cudaHostAlloc / cudaHostRegister); num_src_blocks blocks
+ *   pairs     int64 [n_pairs, 2] (source, destination), device memory or
+ *             device-addressable pinned host memory.  A pair with a negative
+ *             entry is skipped; one out of range is skipped and flagged
+ *             PKV_DEVERR_PAIR.  Destinations must be distinct and must not
+ *             be sources of the same call (otherwise the result is
+ *             undefined).
+ *   block_bytes a positive multiple of 16; both pools 16-byte aligned.
+ * Bit-exact copy; bytes outside the destination blocks are not touched.
+ */
+PKV_API pkv_status swap_blocks(void* dst_pool, const void* src_pool, size_t block_bytes,
+                               const int64_t* pairs, int n_pairs, int64_t num_src_blocks,
+                               int64_t num_dst_blocks, void* stream);
+
+/*
+ * Host-side physical block manager ([LAYOUT] section 三 KVBlockManager):
+ * a pool of num_blocks ids with reference counts.  allocate() hands out the
+ * lowest free id and sets its count to 1; free() decrements a held block's
+ * count and returns the id to the free set when it reaches 0;
+ * add_reference() increments the count of a held block (prefix sharing,
+ * [LAYOUT] section 四.2).  Plain host code; not thread-safe.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A pool with every block free.  NULL on bad arguments or no host memory. */
+PKV_API pkv_block_manager* pkv_block_manager_create(int num_blocks, int block_size);
+/* A pool where exactly the listed ids are free and every other block is
+ * held once (to start from an existing cache state). */
+PKV_API pkv_block_manager* pkv_block_manager_create_with_free(int num_blocks, int block_size,
+                                                              const int32_t* free_ids,
+                                                              int n_free);
+PKV_API void pkv_block_manager_destroy(pkv_block_manager* mgr);
+/* PKV_ERR_NO_BLOCKS (and *block_id = -1) when the pool is empty. */
+PKV_API pkv_status pkv_block_allocate(pkv_block_manager* mgr, int32_t* block_id);
+/* PKV_ERR_INVALID for an id outside the pool; a free block is left as is. */
+PKV_API pkv_status pkv_block_free(pkv_block_manager* mgr, int32_t block_id);
+/* PKV_ERR_INVALID for an id outside the pool or a block that is free. */
+PKV_API pkv_status pkv_block_add_reference(pkv_block_manager* mgr, int32_t block_id);
+PKV_API int pkv_block_free_count(const pkv_block_manager* mgr);
+/* Reference count of a block, -1 for an id outside the pool. */
+PKV_API int pkv_block_ref_count(const pkv_block_manager* mgr, int32_t block_id);
+/* Writes up to `cap` free ids in increasing order; returns how many exist. */
+PKV_API int pkv_block_free_ids(const pkv_block_manager* mgr, int32_t* out, int cap);
+
+/*
+ * pkv_append_slots -- one decode step's bookkeeping for every sequence, in
+ * sequence order ([LAYOUT] section 三 append_token): when context_lens[s]
+ * is a multiple of block_size (the last page is full, or there is none) a
+ * block is allocated and written to block_tables[s][context_lens[s] /
+ * block_size]; then slot_mapping[s] = block_tables[s][n / B] * B + n % B
+ * for the old length n, and context_lens[s] = n + 1.  A sequence whose
+ * allocation fails (pool empty) or whose table row is full gets slot -1
+ * and keeps its table and length; the call then returns PKV_ERR_NO_BLOCKS
+ * after processing every sequence.
+ *   block_tables host int32 [num_seqs, max_blocks_per_seq], updated in place
+ *   context_lens host int32 [num_seqs], updated in place
+ *   slot_mapping host int64 [num_seqs], written
+ */
+PKV_API pkv_status pkv_append_slots(pkv_block_manager* mgr, int32_t* block_tables,
+                                    int max_blocks_per_seq, int32_t* context_lens, int num_seqs,
+                                    int64_t* slot_mapping);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,14 @@
+"""GB300-native paged-KV decode attention.
+
+C ABI: include/pagedkv.h, implemented by libpagedkv.so (CUDA, sm_103a).
+This package holds the CUDA sources (csrc/), the in-tree build, a thin torch
+binding with the same entry-point names, and the seeded workload generator.
+"""
+from .api import (BlockManager, alloc_decode_workspace, decode_split_tokens,
+                  decode_workspace_bytes, device_errors, kv_append, paged_attn_decode,
+                  swap_blocks)
+from ._lib import PagedKVError, lib
+
+__all__ = ["paged_attn_decode", "kv_append", "swap_blocks", "decode_workspace_bytes",
+           "decode_split_tokens", "alloc_decode_workspace", "device_errors", "BlockManager",
+           "PagedKVError", "lib"]

@@ -1,0 +1,198 @@
+"""torch-facing binding of the C ABI: the same entry points as include/pagedkv.h,
+taking tensors and doing argument marshalling only (shapes, dtypes, pointers,
+the current CUDA stream).  Every step of the computation runs in the library's
+CUDA kernels; torch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import check, lib
+
+_DT = {torch.float16: _lib.PKV_F16, torch.bfloat16: _lib.PKV_BF16, torch.float32: _lib.PKV_F32}
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return C.c_void_p(t.data_ptr()) if t is not None and t.numel() else C.c_void_p(0)
+
+
+def _need_cuda(name: str, t: torch.Tensor):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def decode_workspace_bytes(num_seqs: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                           block_size: int, max_context_len: int, split_tokens: int = 0) -> int:
+    return int(lib().pkv_decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim,
+                                                block_size, max_context_len, split_tokens))
+
+
+def decode_split_tokens(num_seqs: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                        block_size: int, max_context_len: int) -> int:
+    return int(lib().pkv_decode_split_tokens(num_seqs, n_heads, n_kv_heads, head_dim, block_size,
+                                             max_context_len))
+
+
+def alloc_decode_workspace(q: torch.Tensor, k_pool: torch.Tensor, max_context_len: int,
+                           split_tokens: int = 0) -> Optional[torch.Tensor]:
+    S, H, D = q.shape
+    _, B, Hk, _ = k_pool.shape
+    n = decode_workspace_bytes(S, H, Hk, D, B, max_context_len, split_tokens)
+    if n == 0:
+        return None
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                      v_pool: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: float, max_context_len: int,
+                      split_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out[s,h] = softmax(scale * q[s,h] . K^T) V over the paged context of s.
+    Shapes: q/out [S, H, D], pools [num_blocks, B, Hk, D], block_tables int32
+    [S, max_blocks], context_lens int32 [S]."""
+    for name, t in (("out", out), ("q", q), ("k_pool", k_pool), ("v_pool", v_pool),
+                    ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need_cuda(name, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    S, H, D = q.shape
+    nb, B, Hk, D2 = k_pool.shape
+    if (D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != (S, H, D)
+            or q.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype
+            or block_tables.dim() != 2 or block_tables.shape[0] != S
+            or context_lens.shape != (S,)):
+        raise ValueError("inconsistent shapes or dtypes")
+    if workspace is None:
+        workspace = alloc_decode_workspace(q, k_pool, max_context_len, split_tokens)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().paged_attn_decode(_ptr(out), _DT[out.dtype], _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                 _DT[k_pool.dtype], _ptr(block_tables), block_tables.shape[1],
+                                 _ptr(context_lens), S, H, Hk, D, B, nb, float(scale),
+                                 int(max_context_len), int(split_tokens), _ptr(workspace),
+                                 ws_bytes, _stream_ptr(stream))
+    check(st, "paged_attn_decode")
+    return out
+
+
+def kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
+              v_new: torch.Tensor, slot_mapping: torch.Tensor,
+              stream: Optional[torch.cuda.Stream] = None) -> None:
+    """k_pool.view(-1, Hk, D)[slot_mapping[s]] = k_new[s] (same for V);
+    slot -1 skips."""
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_new", k_new), ("v_new", v_new),
+                    ("slot_mapping", slot_mapping)):
+        _need_cuda(name, t)
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    nb, B, Hk, D = k_pool.shape
+    S = k_new.shape[0]
+    if (tuple(k_new.shape) != (S, Hk, D) or k_new.shape != v_new.shape
+            or v_pool.shape != k_pool.shape or slot_mapping.shape != (S,)
+            or len({k_pool.dtype, v_pool.dtype, k_new.dtype, v_new.dtype}) != 1):
+        raise ValueError("inconsistent shapes or dtypes")
+    st = lib().kv_append(_ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new), _DT[k_pool.dtype],
+                         _ptr(slot_mapping), S, Hk, D, B, nb, _stream_ptr(stream))
+    check(st, "kv_append")
+
+
+def swap_blocks(dst_pool: torch.Tensor, src_pool: torch.Tensor, pairs: torch.Tensor,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """dst_pool[j] = src_pool[i] for each (i, j) row of `pairs` (int64 [n, 2]).
+    src_pool and pairs may live in pinned host memory."""
+    _need_cuda("dst_pool", dst_pool)
+    for name, t in (("src_pool", src_pool), ("pairs", pairs)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if pairs.dtype != torch.int64 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int64 [n, 2]")
+    bb = dst_pool[0].numel() * dst_pool.element_size() if dst_pool.shape[0] else 0
+    if src_pool.shape[0] and src_pool[0].numel() * src_pool.element_size() != bb:
+        raise ValueError("source and destination blocks differ in size")
+    st = lib().swap_blocks(_ptr(dst_pool), _ptr(src_pool), bb, _ptr(pairs), pairs.shape[0],
+                           src_pool.shape[0], dst_pool.shape[0], _stream_ptr(stream))
+    check(st, "swap_blocks")
+
+
+def device_errors(clear: bool = True) -> int:
+    """PKV_DEVERR_* bits raised by kernels on the current device (synchronises)."""
+    v = C.c_uint32(0)
+    check(lib().pkv_device_errors(C.byref(v), 1 if clear else 0), "pkv_device_errors")
+    return int(v.value)
+
+
+class BlockManager:
+    """Host block manager of the library (lowest free id first, reference
+    counts).  Wraps pkv_block_manager_*; arrays are CPU int32/int64 tensors."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_ids=None):
+        L = lib()
+        if free_ids is None:
+            h = L.pkv_block_manager_create(num_blocks, block_size)
+        else:
+            ids = torch.as_tensor(list(free_ids), dtype=torch.int32).contiguous()
+            h = L.pkv_block_manager_create_with_free(num_blocks, block_size, _ptr(ids), ids.numel())
+        if not h:
+            raise ValueError("pkv_block_manager_create failed (bad arguments)")
+        self._h = C.c_void_p(h)
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib._lib is not None:
+            _lib._lib.pkv_block_manager_destroy(h)
+            self._h = None
+
+    def allocate(self) -> int:
+        b = C.c_int32(-1)
+        check(lib().pkv_block_allocate(self._h, C.byref(b)), "pkv_block_allocate")
+        return int(b.value)
+
+    def free(self, block_id: int) -> None:
+        check(lib().pkv_block_free(self._h, block_id), "pkv_block_free")
+
+    def add_reference(self, block_id: int) -> None:
+        check(lib().pkv_block_add_reference(self._h, block_id), "pkv_block_add_reference")
+
+    def free_count(self) -> int:
+        return int(lib().pkv_block_free_count(self._h))
+
+    def ref_count(self, block_id: int) -> int:
+        return int(lib().pkv_block_ref_count(self._h, block_id))
+
+    def free_ids(self) -> list:
+        n = lib().pkv_block_free_ids(self._h, None, 0)
+        buf = torch.empty(max(n, 1), dtype=torch.int32)
+        lib().pkv_block_free_ids(self._h, _ptr(buf), n)
+        return buf[:n].tolist()
+
+    def append_slots(self, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                     slot_mapping: torch.Tensor) -> int:
+        """In place on CPU tensors (int32 tables/lengths, int64 slots).
+        Returns the status (PKV_OK or PKV_ERR_NO_BLOCKS) instead of raising,
+        since a failed sequence is reported through slot -1."""
+        for t, dt in ((block_tables, torch.int32), (context_lens, torch.int32),
+                      (slot_mapping, torch.int64)):
+            if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != dt:
+                raise ValueError("append_slots takes contiguous CPU int32/int32/int64 tensors")
+        S = context_lens.shape[0]
+        st = lib().pkv_append_slots(self._h, _ptr(block_tables), block_tables.shape[1],
+                                    _ptr(context_lens), S, _ptr(slot_mapping))
+        if st not in (_lib.PKV_OK, _lib.PKV_ERR_NO_BLOCKS):
+            check(st, "pkv_append_slots")
+        return int(st)

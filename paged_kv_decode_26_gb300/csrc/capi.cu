@@ -1,0 +1,473 @@
+// capi.cu -- the C ABI of libpagedkv.so: host-side validation, launch
+// configuration (split length, heads per CTA, pipeline depth), TMA tensor
+// maps, the device error word, and the launches of the decode, split-merge,
+// append and block-copy kernels.  Declarations and contracts: pagedkv.h.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "copy_kernels.cuh"
+#include "decode_launch.h"
+
+// ----------------------------------------------------------------- errors
+
+// The device error word (PKV_DEVERR_* bits), one per device that loads the
+// library.  Kernels get its address as a parameter.
+__device__ unsigned int g_pkv_device_errors = 0;
+
+namespace {
+
+thread_local char t_detail[256] = "";
+
+void set_detail(const char* fmt, const char* what) {
+    std::snprintf(t_detail, sizeof(t_detail), fmt, what);
+}
+
+pkv_status invalid(const char* why) {
+    set_detail("invalid argument: %s", why);
+    return PKV_ERR_INVALID;
+}
+
+pkv_status unsupported(const char* why) {
+    set_detail("unsupported: %s", why);
+    return PKV_ERR_UNSUPPORTED;
+}
+
+pkv_status cuda_fail(cudaError_t e) {
+    set_detail("CUDA error: %s", cudaGetErrorString(e));
+    return PKV_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    unsigned int* errors = nullptr;
+    int sm_count = 0;
+    int smem_optin = 0;
+    int smem_per_sm = 0;
+    bool ready = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+// Per-device facts, looked up once with that device current.
+cudaError_t device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_pkv_device_errors)) != cudaSuccess) return e;
+        d.errors = static_cast<unsigned int*>(p);
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)))
+            return e;
+        if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                        dev)))
+            return e;
+        if ((e = cudaDeviceGetAttribute(&d.smem_per_sm,
+                                        cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)))
+            return e;
+        d.ready = true;
+    }
+    *out = &d;
+    return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int env_int(const char* name, int fallback) {
+    const char* v = std::getenv(name);
+    if (!v || !*v) return fallback;
+    return std::atoi(v);
+}
+
+// ------------------------------------------------------ decode configuration
+
+struct DecodeConfig {
+    int qpw;     // query heads per consumer warp
+    int wpk;     // consumer warps per kv head
+    int hpc;     // kv heads per CTA
+    int stages;  // ring depth
+    int split_tokens;
+    int max_splits;
+    int max_pages;
+    size_t smem;
+    int threads;
+};
+
+constexpr int kDefaultSplitTokens = 512;
+constexpr int kMaxPagesPerSplit = 4096;
+
+bool supported_shape(int n_heads, int n_kv_heads, int head_dim, int block_size) {
+    if (n_kv_heads <= 0 || n_heads <= 0 || n_heads % n_kv_heads) return false;
+    const int G = n_heads / n_kv_heads;
+    return (head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32) &&
+           (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+// Heads per CTA, ring depth and warp roles.  A pipeline stage holds one page
+// of K and V for the CTA's kv heads; about 32 KB per stage and ~96 KB per CTA
+// keep two CTAs resident per SM with 2-3 stages of loads in flight each.
+void shape_config(int n_heads, int n_kv_heads, int head_dim, int block_size, DecodeConfig* c) {
+    const int G = n_heads / n_kv_heads;
+    c->qpw = G < 4 ? G : 4;
+    c->wpk = G / c->qpw;
+    const int per_head_stage = 2 * block_size * head_dim * 2;
+    int target = env_int("PKV_DECODE_HPC", 32768 / per_head_stage);
+    if (target < 1) target = 1;
+    int hpc = 1;
+    for (int h = 1; h <= n_kv_heads; ++h)
+        if (n_kv_heads % h == 0 && h <= target && h * c->wpk <= pkv::kMaxConsumerWarps) hpc = h;
+    c->hpc = hpc;
+    int stages = env_int("PKV_DECODE_STAGES", 98304 / (hpc * per_head_stage));
+    c->stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+    c->threads = 32 * (1 + c->hpc * c->wpk);
+}
+
+int auto_split_tokens(int num_seqs, int n_kv_heads, int hpc, int block_size, int max_context_len,
+                      int sm_count) {
+    const int full = ((max_context_len > 0 ? max_context_len : 1) + block_size - 1) / block_size *
+                     block_size;
+    int split = env_int("PKV_DECODE_SPLIT", kDefaultSplitTokens);
+    split = (split + block_size - 1) / block_size * block_size;
+    if (split <= 0) split = kDefaultSplitTokens;
+    // Enough (sequence, head-group) units to fill the GPU many times over
+    // without cutting the context: no split, no merge pass.
+    const long long units = (long long)num_seqs * (n_kv_heads / hpc);
+    if (units >= 16LL * (sm_count > 0 ? sm_count : 1)) split = full;
+    if (split > full) split = full;
+    if (split / block_size > kMaxPagesPerSplit) split = kMaxPagesPerSplit * block_size;
+    return split;
+}
+
+pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, int block_size,
+                       int max_context_len, int split_tokens, int sm_count, DecodeConfig* c) {
+    shape_config(n_heads, n_kv_heads, head_dim, block_size, c);
+    if (split_tokens == 0) {
+        split_tokens = auto_split_tokens(num_seqs, n_kv_heads, c->hpc, block_size,
+                                         max_context_len, sm_count);
+    } else if (split_tokens < 0 || split_tokens % block_size) {
+        return invalid("split_tokens must be a positive multiple of block_size (or 0)");
+    }
+    if (split_tokens / block_size > kMaxPagesPerSplit)
+        return invalid("split_tokens exceeds 4096 pages");
+    c->split_tokens = split_tokens;
+    const long long ms = ((long long)(max_context_len > 0 ? max_context_len : 0) + split_tokens - 1) /
+                         split_tokens;
+    c->max_splits = ms < 1 ? 1 : (int)ms;
+    c->max_pages = split_tokens / block_size;
+    c->smem = pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc, c->wpk, c->stages,
+                                     c->max_pages);
+    return PKV_OK;
+}
+
+size_t workspace_bytes_for(int num_seqs, int n_heads, int head_dim, const DecodeConfig& c,
+                           size_t* ml_offset) {
+    if (c.max_splits <= 1) {
+        if (ml_offset) *ml_offset = 0;
+        return 0;
+    }
+    const size_t units = (size_t)num_seqs * n_heads * c.max_splits;
+    const size_t o_bytes = (units * head_dim * sizeof(float) + 255) / 256 * 256;
+    if (ml_offset) *ml_offset = o_bytes;
+    return o_bytes + units * 2 * sizeof(float);
+}
+
+cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, pkv_dtype dt, int num_blocks,
+                            int block_size, int n_kv_heads, int head_dim, int hpc) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t es = 2;
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)n_kv_heads, (cuuint64_t)block_size,
+                          (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {head_dim * es, (cuuint64_t)n_kv_heads * head_dim * es,
+                             (cuuint64_t)block_size * n_kv_heads * head_dim * es};
+    cuuint32_t box[4] = {(cuuint32_t)head_dim, (cuuint32_t)hpc, (cuuint32_t)block_size, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = encode(map, dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        4, const_cast<void*>(pool), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+namespace pkv {
+
+cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+    int optin = 0;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
+        return e;
+    if (bytes > (size_t)optin) return cudaErrorInvalidValue;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin)))
+        return e;
+    __atomic_fetch_or(done_mask, bit, __ATOMIC_RELEASE);
+    return cudaSuccess;
+}
+
+}  // namespace pkv
+
+// ================================================================== C ABI
+
+extern "C" {
+
+PKV_API const char* pkv_status_string(pkv_status status) {
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID: return "PKV_ERR_INVALID";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_NO_BLOCKS: return "PKV_ERR_NO_BLOCKS";
+    }
+    return "PKV_ERR_UNKNOWN";
+}
+
+PKV_API const char* pkv_last_error_detail(void) { return t_detail; }
+
+PKV_API int pkv_version(void) { return 100; }
+
+PKV_API pkv_status pkv_device_errors(uint32_t* flags, int clear) {
+    if (!flags) return invalid("flags is NULL");
+    DeviceInfo* d = nullptr;
+    cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int v = 0;
+    if ((e = cudaMemcpy(&v, d->errors, sizeof(v), cudaMemcpyDeviceToHost))) return cuda_fail(e);
+    *flags = v;
+    if (clear) {
+        if ((e = cudaMemset(d->errors, 0, sizeof(unsigned int)))) return cuda_fail(e);
+        if ((e = cudaDeviceSynchronize())) return cuda_fail(e);
+    }
+    return PKV_OK;
+}
+
+PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, int head_dim,
+                                    int block_size, int max_context_len) {
+    if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size) || num_seqs < 0) return 0;
+    DeviceInfo* d = nullptr;
+    const int sms = device_info(&d) == cudaSuccess ? d->sm_count : 0;
+    DecodeConfig c;
+    if (make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size, max_context_len, 0, sms,
+                    &c) != PKV_OK)
+        return 0;
+    return c.split_tokens;
+}
+
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads,
+                                          int head_dim, int block_size, int max_context_len,
+                                          int split_tokens) {
+    if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size) || num_seqs < 0) return 0;
+    DeviceInfo* d = nullptr;
+    const int sms = device_info(&d) == cudaSuccess ? d->sm_count : 0;
+    DecodeConfig c;
+    if (make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size, max_context_len,
+                    split_tokens, sms, &c) != PKV_OK)
+        return 0;
+    return workspace_bytes_for(num_seqs, n_heads, head_dim, c, nullptr);
+}
+
+PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void* q,
+                                     const void* k_pool, const void* v_pool, pkv_dtype kv_dtype,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int n_heads,
+                                     int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                                     float scale, int max_context_len, int split_tokens,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    // ---- host-side validation (nothing is launched on failure)
+    if (num_seqs < 0) return invalid("num_seqs < 0");
+    if (num_seqs > 65535) return unsupported("more than 65535 sequences per call");
+    if (n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads)
+        return invalid("n_heads must be a positive multiple of n_kv_heads");
+    if (kv_dtype != PKV_BF16 && kv_dtype != PKV_F16) return unsupported("kv_dtype must be F16 or BF16");
+    if (out_dtype != PKV_BF16 && out_dtype != PKV_F16 && out_dtype != PKV_F32)
+        return invalid("out_dtype");
+    if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size))
+        return unsupported("head_dim 64/128, block_size 16/32, group 1/2/4/8");
+    if (num_blocks <= 0) return invalid("num_blocks must be positive");
+    if (max_blocks_per_seq <= 0) return invalid("max_blocks_per_seq must be positive");
+    if (max_context_len < 0) return invalid("max_context_len < 0");
+    if (!std::isfinite(scale)) return invalid("scale is not finite");
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens)
+        return invalid("a required pointer is NULL");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return invalid("out, q, k_pool and v_pool must be 16-byte aligned");
+    if (!aligned16(block_tables) && ((uintptr_t)block_tables & 3)) return invalid("block_tables alignment");
+
+    DeviceInfo* dev = nullptr;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    DecodeConfig c;
+    pkv_status st = make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size,
+                                max_context_len, split_tokens, dev->sm_count, &c);
+    if (st != PKV_OK) return st;
+    if (c.smem > (size_t)dev->smem_optin) return unsupported("shared memory of this configuration");
+    size_t ml_off = 0;
+    const size_t need = workspace_bytes_for(num_seqs, n_heads, head_dim, c, &ml_off);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) {
+            set_detail("%s", "workspace smaller than pkv_decode_workspace_bytes()");
+            return PKV_ERR_WORKSPACE;
+        }
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return invalid("workspace must be 256-byte aligned");
+    }
+
+    pkv::DecodeLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    if ((e = encode_pool_map(&L.tm_k, k_pool, kv_dtype, num_blocks, block_size, n_kv_heads,
+                             head_dim, c.hpc)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = encode_pool_map(&L.tm_v, v_pool, kv_dtype, num_blocks, block_size, n_kv_heads,
+                             head_dim, c.hpc)) != cudaSuccess)
+        return cuda_fail(e);
+
+    pkv::DecodeParams& p = L.p;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.num_seqs = num_seqs;
+    p.n_heads = n_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = n_heads / n_kv_heads;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.split_tokens = c.split_tokens;
+    p.max_splits = c.max_splits;
+    p.heads_per_cta = c.hpc;
+    p.warps_per_kv = c.wpk;
+    p.stages = c.stages;
+    p.max_pages_per_split = c.max_pages;
+    p.ws_o = need ? static_cast<float*>(workspace) : nullptr;
+    p.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off) : nullptr;
+    p.errors = dev->errors;
+
+    L.grid = dim3((unsigned)c.max_splits, (unsigned)(n_kv_heads / c.hpc), (unsigned)num_seqs);
+    L.block = dim3((unsigned)c.threads);
+    L.smem_bytes = c.smem;
+    L.stream = static_cast<cudaStream_t>(stream);
+    if (c.max_splits > 65535 * 1024) return unsupported("context too long for the grid");
+
+    e = kv_dtype == PKV_BF16 ? pkv::launch_decode_bf16(head_dim, block_size, c.qpw, L)
+                             : pkv::launch_decode_f16(head_dim, block_size, c.qpw, L);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    if (c.max_splits > 1) {
+        pkv::ReduceParams r;
+        r.out = out;
+        r.out_dtype = out_dtype;
+        r.context_lens = context_lens;
+        r.num_seqs = num_seqs;
+        r.n_heads = n_heads;
+        r.split_tokens = c.split_tokens;
+        r.max_splits = c.max_splits;
+        r.cap_tokens = std::min((long long)max_blocks_per_seq * block_size,
+                                (long long)c.max_splits * c.split_tokens) > 0x7fffffffLL
+                           ? 0x7fffffff
+                           : (int)std::min((long long)max_blocks_per_seq * block_size,
+                                           (long long)c.max_splits * c.split_tokens);
+        r.ws_o = p.ws_o;
+        r.ws_ml = p.ws_ml;
+        const unsigned units = (unsigned)num_seqs * (unsigned)n_heads;
+        const dim3 grid((units + 3) / 4);
+        if (head_dim == 128)
+            pkv::paged_decode_reduce_kernel<128><<<grid, 128, 0, L.stream>>>(r);
+        else
+            pkv::paged_decode_reduce_kernel<64><<<grid, 128, 0, L.stream>>>(r);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    }
+    return PKV_OK;
+}
+
+PKV_API pkv_status kv_append(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                             pkv_dtype dtype, const int64_t* slot_mapping, int num_seqs,
+                             int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                             void* stream) {
+    if (num_seqs < 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return invalid("sizes");
+    int es = 0;
+    switch (dtype) {
+        case PKV_F16:
+        case PKV_BF16: es = 2; break;
+        case PKV_F32: es = 4; break;
+        default: return invalid("dtype");
+    }
+    const long long row_bytes = (long long)n_kv_heads * head_dim * es;
+    if (row_bytes % 16) return unsupported("n_kv_heads * head_dim * element size must be a multiple of 16 bytes");
+    if (num_seqs == 0) return PKV_OK;
+    if (!k_pool || !v_pool || !k_new || !v_new || !slot_mapping) return invalid("NULL pointer");
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new))
+        return invalid("buffers must be 16-byte aligned");
+    if (((uintptr_t)slot_mapping & 7) != 0) return invalid("slot_mapping must be 8-byte aligned");
+    if (row_bytes / 16 > 0x7fffffffLL) return unsupported("row too large");
+    DeviceInfo* dev = nullptr;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int row_vec = (int)(row_bytes / 16);
+    const long long total = (long long)num_seqs * row_vec;
+    long long blocks = (total + 255) / 256;
+    const long long cap = 8LL * dev->sm_count;
+    if (blocks > cap) blocks = cap;
+    pkv::kv_append_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
+        num_seqs, row_vec, (int64_t)num_blocks * block_size, dev->errors);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    return PKV_OK;
+}
+
+PKV_API pkv_status swap_blocks(void* dst_pool, const void* src_pool, size_t block_bytes,
+                               const int64_t* pairs, int n_pairs, int64_t num_src_blocks,
+                               int64_t num_dst_blocks, void* stream) {
+    if (n_pairs < 0 || num_src_blocks < 0 || num_dst_blocks < 0) return invalid("sizes");
+    if (block_bytes == 0 || block_bytes % 16) return invalid("block_bytes must be a positive multiple of 16");
+    if (n_pairs == 0) return PKV_OK;
+    if (!dst_pool || !src_pool || !pairs) return invalid("NULL pointer");
+    if (!aligned16(dst_pool) || !aligned16(src_pool)) return invalid("pools must be 16-byte aligned");
+    if (((uintptr_t)pairs & 7) != 0) return invalid("pairs must be 8-byte aligned");
+    DeviceInfo* dev = nullptr;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const unsigned grid = (unsigned)std::min<long long>(n_pairs, 1LL << 20);
+    pkv::swap_blocks_kernel<<<grid, pkv::kSwapThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4*>(dst_pool), static_cast<const uint4*>(src_pool),
+        (int64_t)(block_bytes / 16), pairs, n_pairs, num_src_blocks, num_dst_blocks,
+        dev->errors);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    return PKV_OK;
+}
+
+}  // extern "C"

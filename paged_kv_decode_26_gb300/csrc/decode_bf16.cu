@@ -1,0 +1,4 @@
+// decode_bf16.cu -- decode kernel instances for bf16 query / K / V.
+#define PKV_ELEM __nv_bfloat16
+#define PKV_FN launch_decode_bf16
+#include "decode_inst.inc"

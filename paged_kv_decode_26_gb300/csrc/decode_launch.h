@@ -1,0 +1,30 @@
+// decode_launch.h -- host-side launch interface between the C ABI (capi.cu)
+// and the translation units that instantiate the decode kernel templates.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "decode_kernel.cuh"
+
+namespace pkv {
+
+struct DecodeLaunch {
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    DecodeParams p;
+    dim3 grid;
+    dim3 block;
+    size_t smem_bytes;
+    cudaStream_t stream;
+};
+
+// Launch paged_decode_kernel<D, BS, QPW, T> for T = __nv_bfloat16 / __half.
+// Returns cudaErrorInvalidValue for a combination that is not compiled.
+cudaError_t launch_decode_bf16(int D, int BS, int QPW, const DecodeLaunch& L);
+cudaError_t launch_decode_f16(int D, int BS, int QPW, const DecodeLaunch& L);
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask, size_t bytes);
+
+}  // namespace pkv

@@ -113,13 +113,33 @@ def _lens(rng, spec, S):
     raise ValueError(kind)
 
 
-def _normal(rng, shape, dtype, chunk_elems=1 << 26):
-    """N(0,1) drawn as float32 in chunks, rounded to `dtype`."""
+_CHUNK = 1 << 24
+
+
+def _normal(rng, shape, dtype, chunk_elems=_CHUNK):
+    """N(0,1) drawn as float32 and rounded to `dtype`.  Large tensors are
+    drawn in fixed-size chunks, each from its own generator spawned from one
+    seed taken from `rng`, so the values do not depend on how many threads
+    draw them."""
+    import concurrent.futures as cf
+    import os
     n = int(np.prod(shape)) if len(shape) else 1
     out = torch.empty(n, dtype=dtype)
-    for a in range(0, n, chunk_elems):
+    children = np.random.SeedSequence(int(rng.integers(0, 2 ** 63))).spawn(
+        (n + chunk_elems - 1) // chunk_elems)
+
+    def fill(k):
+        a = k * chunk_elems
         b = min(n, a + chunk_elems)
-        out[a:b] = torch.from_numpy(rng.standard_normal(b - a, dtype=np.float32)).to(dtype)
+        g = np.random.Generator(np.random.PCG64(children[k]))
+        out[a:b] = torch.from_numpy(g.standard_normal(b - a, dtype=np.float32)).to(dtype)
+
+    if len(children) <= 1:
+        for k in range(len(children)):
+            fill(k)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+            list(ex.map(fill, range(len(children))))
     return out.view(*shape)
 
 

@@ -1,0 +1,140 @@
+"""The C-ABI library loads, exports every symbol include/pagedkv.h declares,
+and rejects invalid calls on the host before touching a GPU.  CPU only."""
+import ctypes as C
+import os
+import re
+
+import pytest
+import torch
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from paged_kv_decode_26_gb300 import build
+    build.build()
+    from paged_kv_decode_26_gb300._lib import lib
+    return lib()
+
+
+def _declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^PKV_API\s+[^(]*?(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_entry_points():
+    names = _declared_symbols()
+    for n in ("paged_attn_decode", "kv_append", "swap_blocks", "pkv_decode_workspace_bytes",
+              "pkv_status_string", "pkv_device_errors"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_binding_covers_every_declared_symbol():
+    from paged_kv_decode_26_gb300._lib import SIGNATURES
+    assert sorted(SIGNATURES) == _declared_symbols()
+
+
+def test_exports_nothing_else():
+    """Only the declared C symbols are visible (built with -fvisibility=hidden)."""
+    import subprocess
+    from paged_kv_decode_26_gb300._lib import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set()
+    for line in out.splitlines():
+        parts = line.split()
+        if len(parts) == 3 and parts[1] in ("T", "W"):
+            exported.add(parts[2])
+    ours = {s for s in exported if s.startswith(("pkv_", "paged_", "kv_", "swap_"))}
+    assert ours == set(_declared_symbols())
+
+
+def test_status_strings(L):
+    assert L.pkv_status_string(0) == b"PKV_OK"
+    assert L.pkv_status_string(1) == b"PKV_ERR_INVALID"
+    assert L.pkv_status_string(5) == b"PKV_ERR_NO_BLOCKS"
+    assert L.pkv_version() >= 100
+
+
+NULL = C.c_void_p(0)
+FAKE = C.c_void_p(4096)  # never dereferenced: every call below fails validation first
+
+
+def _decode(L, **kw):
+    a = dict(out=FAKE, out_dtype=1, q=FAKE, k=FAKE, v=FAKE, kv_dtype=1, bt=FAKE, mb=4, cl=FAKE,
+             S=2, H=8, Hk=8, D=128, B=16, nb=10, scale=0.1, maxc=64, split=0, ws=NULL, wsb=0,
+             stream=NULL)
+    a.update(kw)
+    return L.paged_attn_decode(a["out"], a["out_dtype"], a["q"], a["k"], a["v"], a["kv_dtype"],
+                               a["bt"], a["mb"], a["cl"], a["S"], a["H"], a["Hk"], a["D"], a["B"],
+                               a["nb"], a["scale"], a["maxc"], a["split"], a["ws"], a["wsb"],
+                               a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(S=-1), 1),
+    (dict(H=6, Hk=4), 1),
+    (dict(Hk=0), 1),
+    (dict(D=96), 2),
+    (dict(B=8), 2),
+    (dict(H=48, Hk=4), 2),
+    (dict(kv_dtype=2), 2),
+    (dict(out_dtype=7), 1),
+    (dict(nb=0), 1),
+    (dict(mb=0), 1),
+    (dict(maxc=-5), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(q=NULL), 1),
+    (dict(bt=NULL), 1),
+    (dict(out=C.c_void_p(4104)), 1),   # 8-byte aligned only
+])
+def test_decode_rejects_invalid_arguments(L, kw, code):
+    assert _decode(L, **kw) == code
+    assert L.pkv_last_error_detail()
+
+
+def test_decode_zero_sequences_is_a_no_op(L):
+    assert _decode(L, S=0, q=NULL, out=NULL) == 0
+
+
+def test_append_rejects_invalid_arguments(L):
+    assert L.kv_append(FAKE, FAKE, FAKE, FAKE, 1, FAKE, -1, 8, 128, 16, 4, NULL) == 1
+    assert L.kv_append(FAKE, FAKE, FAKE, FAKE, 9, FAKE, 1, 8, 128, 16, 4, NULL) == 1
+    assert L.kv_append(FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 1, 4, 16, 4, NULL) == 2  # 8-byte rows
+    assert L.kv_append(FAKE, NULL, FAKE, FAKE, 1, FAKE, 1, 8, 128, 16, 4, NULL) == 1
+    assert L.kv_append(FAKE, FAKE, FAKE, FAKE, 1, FAKE, 0, 8, 128, 16, 4, NULL) == 0
+
+
+def test_swap_rejects_invalid_arguments(L):
+    assert L.swap_blocks(FAKE, FAKE, 24, FAKE, 1, 4, 4, NULL) == 1      # not a multiple of 16
+    assert L.swap_blocks(FAKE, FAKE, 0, FAKE, 1, 4, 4, NULL) == 1
+    assert L.swap_blocks(FAKE, FAKE, 32, FAKE, -1, 4, 4, NULL) == 1
+    assert L.swap_blocks(NULL, FAKE, 32, FAKE, 1, 4, 4, NULL) == 1
+    assert L.swap_blocks(C.c_void_p(4100), FAKE, 32, FAKE, 1, 4, 4, NULL) == 1
+    assert L.swap_blocks(FAKE, FAKE, 32, FAKE, 0, 4, 4, NULL) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import paged_kv_decode_26_gb300._lib as lb
+    monkeypatch.setattr(lb, "_lib", None)
+    monkeypatch.setattr(lb, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        lb.lib()
+
+
+def test_binding_requires_cuda_tensors():
+    import paged_kv_decode_26_gb300 as pkv
+    q = torch.zeros(1, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkv.paged_attn_decode(q.clone(), q, torch.zeros(2, 16, 8, 128, dtype=torch.bfloat16),
+                              torch.zeros(2, 16, 8, 128, dtype=torch.bfloat16),
+                              torch.zeros(1, 2, dtype=torch.int32),
+                              torch.ones(1, dtype=torch.int32), 0.1, 16)

@@ -1,0 +1,179 @@
+"""Bit-exact parity of the append and block-copy kernels (through the C ABI)
+with the oracle's plain loops, and the whole continuous-batching step
+(allocate -> append -> decode -> copy device-to-device and host-to-device)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from oracle.block_manager import append_slots
+from paged_kv_decode_26_gb300 import workloads as wl
+from tests.parity import assert_attention_close, run_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_decode_26_gb300 import build
+    build.build()
+    import paged_kv_decode_26_gb300 as pkv
+    pkv.device_errors(clear=True)
+    yield pkv
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16) if t.element_size() == 2 else t.contiguous().view(torch.int32)
+
+
+def test_swap_tiny_workload(lib):
+    case = wl.make_case(1)
+    dk, dv = case.swap_dst_k.cuda(), case.swap_dst_v.cuda()
+    sk, sv = case.swap_src_k.cuda(), case.swap_src_v.cuda()
+    pairs = case.swap_pairs.cuda()
+    lib.swap_blocks(dk, sk, pairs)
+    lib.swap_blocks(dv, sv, pairs)
+    rk, rv = case.swap_dst_k.clone(), case.swap_dst_v.clone()
+    assert orc.swap_blocks(rk, case.swap_src_k, case.swap_pairs) == 0
+    assert orc.swap_blocks(rv, case.swap_src_v, case.swap_pairs) == 0
+    assert torch.equal(_bits(dk.cpu()), _bits(rk)) and torch.equal(_bits(dv.cpu()), _bits(rv))
+    assert lib.device_errors() == 0
+
+
+def test_swap_page_mock_example(lib, golden):
+    g = golden("swap_mock_example.json")
+    src = torch.randn(g["num_src_blocks"], 32, 64, 16)
+    dst = torch.zeros(g["num_dst_blocks"], 32, 64, 16)
+    pairs = torch.tensor([[i, j] for i, j in enumerate(g["mapping"])], dtype=torch.int64)
+    d = dst.cuda()
+    lib.swap_blocks(d, src.cuda(), pairs.cuda())
+    assert lib.device_errors() & 0x8          # target 5 does not exist
+    orc.swap_blocks(dst, src, pairs)
+    assert torch.equal(d.cpu(), dst)
+    assert int((d.sum(dim=[1, 2, 3]) != 0).sum()) == g["filled_blocks"]
+
+
+@pytest.mark.parametrize("block_bytes", [16, 48, 4096, 32768, 40976])
+def test_swap_sizes_and_untouched_bytes(lib, block_bytes):
+    rng = np.random.default_rng(block_bytes)
+    ns, nd, n = 37, 41, 23
+    src = torch.from_numpy(rng.integers(0, 255, size=(ns, block_bytes), dtype=np.uint8))
+    dst = torch.from_numpy(rng.integers(0, 255, size=(nd, block_bytes), dtype=np.uint8))
+    si = rng.choice(ns, n, replace=False)
+    di = rng.choice(nd, n, replace=False)
+    pairs = torch.from_numpy(np.stack([si, di], 1).astype(np.int64))
+    pairs[3] = torch.tensor([-1, 5])
+    d = dst.cuda()
+    lib.swap_blocks(d, src.cuda(), pairs.cuda())
+    orc.swap_blocks(dst, src, pairs)
+    assert torch.equal(d.cpu(), dst)
+    assert lib.device_errors() == 0
+
+
+def test_swap_from_pinned_host(lib):
+    case = wl.make_case(5, S=8, lens=("uniform", 16, 64), d2d_pairs=4, h2d_pairs=32,
+                        host_pool_blocks=64)
+    hk = case.host_k_pool.pin_memory()
+    pairs_host = case.h2d_pairs.pin_memory()
+    dk = case.k_pool.cuda()
+    lib.swap_blocks(dk, hk, pairs_host)          # source and pairs in pinned host memory
+    ref = case.k_pool.clone()
+    orc.swap_blocks(ref, case.host_k_pool, case.h2d_pairs)
+    assert torch.equal(_bits(dk.cpu()), _bits(ref))
+    assert lib.device_errors() == 0
+
+
+def test_append_matches_oracle_and_flags_bad_slots(lib):
+    case = wl.make_case(5, S=40, lens=("uniform", 1, 70), d2d_pairs=4, h2d_pairs=4,
+                        host_pool_blocks=8)
+    tables = [[int(x) for x in row if x >= 0] for row in case.block_tables]
+    _, _, slots, _ = append_slots(tables, case.context_lens.tolist(), case.B, case.free_ids,
+                                  case.num_blocks)
+    slots = torch.tensor(slots, dtype=torch.int64)
+    slots[5] = -1
+    k, v = case.k_pool.clone(), case.v_pool.clone()
+    orc.kv_append(k, v, case.k_new, case.v_new, slots)
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    lib.kv_append(dk, dv, case.k_new.cuda(), case.v_new.cuda(), slots.cuda())
+    assert torch.equal(_bits(dk.cpu()), _bits(k)) and torch.equal(_bits(dv.cpu()), _bits(v))
+    assert lib.device_errors() == 0
+    bad = slots.clone()
+    bad[0] = case.num_blocks * case.B          # one past the pool
+    lib.kv_append(dk, dv, case.k_new.cuda(), case.v_new.cuda(), bad.cuda())
+    assert lib.device_errors() & 0x4
+    assert torch.equal(_bits(dk.cpu()), _bits(k))
+
+
+def test_append_f32_and_fp16_rows(lib):
+    for dtype, D in ((torch.float32, 4), (torch.float16, 64)):
+        k = torch.randn(6, 16, 2, D).to(dtype)
+        v = torch.randn(6, 16, 2, D).to(dtype)
+        kn = torch.randn(3, 2, D).to(dtype)
+        vn = torch.randn(3, 2, D).to(dtype)
+        slots = torch.tensor([95, 0, 17])
+        dk, dv = k.cuda(), v.cuda()
+        lib.kv_append(dk, dv, kn.cuda(), vn.cuda(), slots.cuda())
+        orc.kv_append(k, v, kn, vn, slots)
+        assert torch.equal(dk.cpu(), k) and torch.equal(dv.cpu(), v)
+    assert lib.device_errors() == 0
+
+
+def _continuous_step(lib, case):
+    """Library side of one continuous-batching step."""
+    bm = lib.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)
+    bt = case.block_tables.clone()
+    lens = case.context_lens.clone()
+    slots = torch.empty(case.S, dtype=torch.int64)
+    assert bm.append_slots(bt, lens, slots) == 0
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    q = case.q.cuda()
+    lib.kv_append(dk, dv, case.k_new.cuda(), case.v_new.cuda(), slots.cuda())
+    out = torch.empty(case.S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+    lib.paged_attn_decode(out, q, dk, dv, bt.cuda(), lens.cuda(), case.scale,
+                          int(lens.max()))
+    d2d = case.d2d_pairs.cuda()
+    lib.swap_blocks(dk, dk, d2d)
+    lib.swap_blocks(dv, dv, d2d)
+    hk, hv = case.host_k_pool.pin_memory(), case.host_v_pool.pin_memory()
+    h2d = case.h2d_pairs.pin_memory()
+    lib.swap_blocks(dk, hk, h2d)
+    lib.swap_blocks(dv, hv, h2d)
+    torch.cuda.synchronize()
+    return bt, lens, slots, out, dk.cpu(), dv.cpu()
+
+
+def _continuous_oracle(case):
+    tables = [[int(x) for x in row if x >= 0] for row in case.block_tables]
+    new_tables, new_lens, slots, _ = append_slots(tables, case.context_lens.tolist(), case.B,
+                                                  case.free_ids, case.num_blocks)
+    k, v = case.k_pool.clone(), case.v_pool.clone()
+    orc.kv_append(k, v, case.k_new, case.v_new, torch.tensor(slots))
+    bt = torch.full_like(case.block_tables, -1)
+    for s, row in enumerate(new_tables):
+        bt[s, :len(row)] = torch.tensor(row, dtype=torch.int32)
+    lens = torch.tensor(new_lens, dtype=torch.int32)
+    out = orc.decode_two_pass(case.q, k, v, bt, lens, case.scale)
+    for pool in (k, v):
+        assert orc.swap_blocks(pool, pool.clone(), case.d2d_pairs) == 0
+    assert orc.swap_blocks(k, case.host_k_pool, case.h2d_pairs) == 0
+    assert orc.swap_blocks(v, case.host_v_pool, case.h2d_pairs) == 0
+    return bt, lens, slots, out, k, v
+
+
+@pytest.mark.parametrize("small", [True, False])
+def test_continuous_batching_step(lib, small):
+    if small:
+        case = wl.make_case(5, S=48, lens=("pareto", 1.5, 16, 700), d2d_pairs=32, h2d_pairs=32,
+                            host_pool_blocks=64, poison=True)
+    else:
+        case = wl.make_case(5)            # the stated workload at full size
+    bt, lens, slots, out, k, v = _continuous_step(lib, case)
+    rbt, rlens, rslots, rout, rk, rv = _continuous_oracle(case)
+    assert slots.tolist() == rslots
+    assert torch.equal(lens, rlens)
+    assert torch.equal(bt, rbt)
+    assert torch.equal(_bits(k), _bits(rk)) and torch.equal(_bits(v), _bits(rv))
+    assert_attention_close(out, rout, case.out_dtype, "continuous step")
+    assert lib.device_errors() == 0

@@ -1,0 +1,193 @@
+"""Parity of the CUDA decode path (through the C ABI) with the fp64 oracle on
+the five workloads: small cases compared element by element, full-size
+cases on sampled sequences in the benchmark's launch configuration, plus edge
+cases and the kernels' own index checks."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from paged_kv_decode_26_gb300 import workloads as wl
+from tests.parity import assert_attention_close, run_decode, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_decode_26_gb300 import build
+    build.build()
+    import paged_kv_decode_26_gb300 as pkv
+    pkv.device_errors(clear=True)
+    yield pkv
+
+
+def _oracle(case, seq_ids=None, lens=None, tables=None, k=None, v=None):
+    return orc.decode_two_pass(case.q, case.k_pool if k is None else k,
+                               case.v_pool if v is None else v,
+                               case.block_tables if tables is None else tables,
+                               case.context_lens if lens is None else lens, case.scale,
+                               seq_ids=seq_ids)
+
+
+def _no_device_errors(pkv):
+    assert pkv.device_errors(clear=True) == 0
+
+
+# ----------------------------------------------------------- small cases
+
+SMALL = {
+    1: dict(),                                                    # the tiny workload itself
+    2: dict(S=6, lens=("uniform", 1, 700)),
+    3: dict(S=16, lens=("loguniform", 1, 2000), share_blocks=8),
+    4: dict(S=2, lens=("const", 3000)),
+    5: dict(S=24, lens=("pareto", 1.5, 16, 600), d2d_pairs=8, h2d_pairs=8, host_pool_blocks=16),
+}
+
+
+@pytest.mark.parametrize("config", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("split", [0, 16, 64, 512])
+def test_small_case_matches_oracle(lib, config, split):
+    case = wl.make_case(config, poison=True, **SMALL[config])
+    if split % case.B:
+        pytest.skip("split must be a multiple of the block size")
+    got = run_decode(case, split_tokens=split)
+    ref = _oracle(case)
+    assert_attention_close(got, ref, case.out_dtype, f"config {config} split {split}")
+    _no_device_errors(lib)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("B", [16, 32])
+@pytest.mark.parametrize("H,Hk", [(8, 8), (8, 4), (16, 4), (16, 2)])
+@pytest.mark.parametrize("dtype,out_dtype", [(torch.bfloat16, torch.bfloat16),
+                                             (torch.float16, torch.float16),
+                                             (torch.float16, torch.float32),
+                                             (torch.bfloat16, torch.float32)])
+def test_shape_matrix(lib, D, B, H, Hk, dtype, out_dtype):
+    case = wl.make_case(2, S=3, lens=("uniform", 1, 300), H=H, Hk=Hk, D=D, B=B, dtype=dtype,
+                        out_dtype=out_dtype, poison=True, seed=D + B + H + Hk)
+    for split in (0, 4 * B):
+        got = run_decode(case, split_tokens=split)
+        assert_attention_close(got, _oracle(case), out_dtype, f"{D} {B} {H}/{Hk} split {split}")
+    _no_device_errors(lib)
+
+
+def test_split_invariance(lib):
+    case = wl.make_case(2, S=4, lens=("uniform", 900, 2000), out_dtype=torch.float32)
+    outs = [run_decode(case, split_tokens=s) for s in (16, 48, 256, 1024, 2048)]
+    for o in outs[1:]:
+        assert torch.allclose(o, outs[0], rtol=1e-5, atol=2e-6)
+    _no_device_errors(lib)
+
+
+def test_physical_placement_invariance(lib):
+    case = wl.make_case(3, S=8, lens=("uniform", 1, 400), share_blocks=4)
+    a = run_decode(case, split_tokens=64)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(case.num_blocks))
+    k2 = torch.empty_like(case.k_pool)
+    v2 = torch.empty_like(case.v_pool)
+    k2[perm] = case.k_pool
+    v2[perm] = case.v_pool
+    bt = case.block_tables.clone()
+    bt[bt >= 0] = perm.to(torch.int32)[bt[bt >= 0].long()]
+    case.k_pool, case.v_pool, case.block_tables = k2, v2, bt
+    b = run_decode(case, split_tokens=64)
+    assert torch.equal(a, b)
+    _no_device_errors(lib)
+
+
+# ----------------------------------------------------------- edge cases
+
+def test_context_one_and_empty(lib):
+    case = wl.make_case(2, lens_override=[1, 0, 1, 17, 0, 16], H=8, Hk=8)
+    got = run_decode(case, split_tokens=16)
+    G = case.H // case.Hk
+    for s in (0, 2):
+        p = int(case.block_tables[s, 0])
+        for h in range(case.H):
+            assert torch.equal(got[s, h].cpu(), case.v_pool[p, 0, h // G])
+    assert torch.count_nonzero(got[1]) == 0 and torch.count_nonzero(got[4]) == 0
+    assert_attention_close(got, _oracle(case), case.out_dtype)
+    _no_device_errors(lib)
+
+
+def test_all_empty_batch(lib):
+    case = wl.make_case(2, lens_override=[0, 0, 0], H=4, Hk=4)
+    got = run_decode(case, max_context_len=0)
+    assert torch.count_nonzero(got) == 0
+    _no_device_errors(lib)
+
+
+def test_dominant_key(lib):
+    case = wl.make_case(2, lens_override=[300], H=2, Hk=2, out_dtype=torch.float32)
+    t = 123
+    p = int(case.block_tables[0, t // case.B])
+    case.q[:] = 1.0
+    case.k_pool[p, t % case.B] = 8.0  # score 8*128/sqrt(128) ~ 90 above the rest
+    got = run_decode(case, split_tokens=64)
+    for h in range(case.H):
+        assert torch.allclose(got[0, h].cpu(), case.v_pool[p, t % case.B, h].float(), atol=1e-6)
+    _no_device_errors(lib)
+
+
+def test_maximum_split_and_max_pages(lib):
+    """One split covering 4096 pages (the per-split maximum) and a context
+    of 32768 tokens at block size 16."""
+    case = wl.make_case(2, lens_override=[32768, 5], H=2, Hk=2)
+    got = run_decode(case, split_tokens=4096 * 16)
+    assert_attention_close(got, _oracle(case), case.out_dtype)
+    _no_device_errors(lib)
+
+
+def test_workspace_too_small_is_rejected(lib):
+    case = wl.make_case(2, S=2, lens=("const", 2000), H=4, Hk=4)
+    dev = to_device(case)
+    out = torch.empty(case.S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+    ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lib.PagedKVError, match="WORKSPACE"):
+        lib.paged_attn_decode(out, dev["q"], dev["k_pool"], dev["v_pool"], dev["block_tables"],
+                              dev["context_lens"], case.scale, 2000, split_tokens=64,
+                              workspace=ws)
+
+
+def test_out_of_range_block_id_is_flagged_not_read(lib):
+    case = wl.make_case(2, S=3, lens=("const", 100), H=4, Hk=4)
+    bt = case.block_tables.clone()
+    bt[1, 2] = case.num_blocks + 5
+    bt[1, 3] = -7
+    dev = to_device(case)
+    got = run_decode(case, split_tokens=32, dev=dev, tables=bt.cuda())
+    assert lib.device_errors(clear=True) & 0x1
+    ref = _oracle(case, seq_ids=[0, 2])
+    assert_attention_close(got[[0, 2]], ref, case.out_dtype)
+    assert torch.isfinite(got[1].float()).all()
+
+
+def test_context_beyond_bound_is_flagged(lib):
+    case = wl.make_case(2, S=2, lens=("const", 100), H=4, Hk=4)
+    got = run_decode(case, split_tokens=32, max_context_len=40)
+    assert lib.device_errors(clear=True) & 0x2
+    assert torch.isfinite(got.float()).all()
+
+
+# ------------------------------------------------- full sizes (sampled)
+
+@pytest.mark.parametrize("config,k", [(2, 6), (3, 6), (4, 2)])
+def test_full_size_sampled(lib, config, k):
+    """The stated workload at full size, in the launch configuration the
+    benchmark times (automatic split), checked on sampled sequences (all
+    heads) against the oracle."""
+    case = wl.make_case(config)
+    got = run_decode(case)
+    seqs = wl.sampled_seqs(case, k)
+    ref = _oracle(case, seq_ids=seqs)
+    assert_attention_close(got[seqs], ref, case.out_dtype, f"config {config} seqs {seqs}")
+    # properties that hold for every row: finite, and bounded by max |V| = the
+    # convex-combination bound of softmax weights
+    g = got.float()
+    assert torch.isfinite(g).all()
+    assert g.abs().max() <= case.v_pool.float().abs().max() + 1e-2
+    _no_device_errors(lib)
