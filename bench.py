@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, help="workload 1..5 (default 2)")
     ap.add_argument("--split", type=int, default=0, help="split_tokens (0 = automatic)")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="override the number of sequences (smaller cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -272,6 +274,8 @@ def main():
     # the long-context pool holds exactly the needed blocks; give the
     # appended tokens room for their new pages
     extra = {"pool_extra": 0.01} if args.config == 4 else {}
+    if args.seqs:
+        extra["S"] = args.seqs
     case = wl.make_case(args.config, seed=seed, **extra)
     S = case.S
     bm = pkv.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)

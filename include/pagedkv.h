@@ -117,7 +117,8 @@ PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, i
  *                context_len 0 gets zeros.
  *   q            device, [num_seqs, n_heads, head_dim] of kv_dtype
  *   k_pool,v_pool device, [num_blocks, block_size, n_kv_heads, head_dim] of
- *                kv_dtype (F16 or BF16), 16-byte aligned
+ *                kv_dtype (F16 or BF16), 16-byte aligned; num_blocks may be 0
+ *                (then the pools may be NULL and every context must be empty)
  *   block_tables device int32 [num_seqs, max_blocks_per_seq]; only the
  *                first ceil(context_lens[s] / block_size) entries of a row
  *                are read

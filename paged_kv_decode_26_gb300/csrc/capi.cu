@@ -313,13 +313,14 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
         return invalid("out_dtype");
     if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size))
         return unsupported("head_dim 64/128, block_size 16/32, group 1/2/4/8");
-    if (num_blocks <= 0) return invalid("num_blocks must be positive");
+    if (num_blocks < 0) return invalid("num_blocks < 0");
     if (max_blocks_per_seq <= 0) return invalid("max_blocks_per_seq must be positive");
     if (max_context_len < 0) return invalid("max_context_len < 0");
     if (!std::isfinite(scale)) return invalid("scale is not finite");
     if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens)
+    if (!out || !q || !block_tables || !context_lens)
         return invalid("a required pointer is NULL");
+    if (num_blocks > 0 && (!k_pool || !v_pool)) return invalid("k_pool or v_pool is NULL");
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return invalid("out, q, k_pool and v_pool must be 16-byte aligned");
     if (!aligned16(block_tables) && ((uintptr_t)block_tables & 3)) return invalid("block_tables alignment");
@@ -345,10 +346,15 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
 
     pkv::DecodeLaunch L;
     std::memset(&L, 0, sizeof(L));
-    if ((e = encode_pool_map(&L.tm_k, k_pool, kv_dtype, num_blocks, block_size, n_kv_heads,
+    // An empty pool (every context empty) still needs well-formed maps; no
+    // block id can pass the kernel's range check then, so nothing is loaded.
+    const void* kmap_base = num_blocks > 0 ? k_pool : q;
+    const void* vmap_base = num_blocks > 0 ? v_pool : q;
+    const int map_blocks = num_blocks > 0 ? num_blocks : 1;
+    if ((e = encode_pool_map(&L.tm_k, kmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
                              head_dim, c.hpc)) != cudaSuccess)
         return cuda_fail(e);
-    if ((e = encode_pool_map(&L.tm_v, v_pool, kv_dtype, num_blocks, block_size, n_kv_heads,
+    if ((e = encode_pool_map(&L.tm_v, vmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
                              head_dim, c.hpc)) != cudaSuccess)
         return cuda_fail(e);
 

@@ -7,8 +7,10 @@ Tolerance (attention output vs the fp64 oracle, N(0,1) inputs):
     half-ulp of bf16 is 7.8e-3) and |err| <= half an ulp of the output type
     at |oracle| + 1e-5;
   * and, tighter, every element is within one ulp of the oracle rounded to
-    the output type (fp32 output: |err| <= 2e-5 + 1e-5 |oracle|), which
-    bounds the fp32 accumulation error of the kernel itself.
+    the output type plus 2e-6 absolute (fp32 output: |err| <= 2e-5 +
+    1e-5 |oracle|), which bounds the fp32 accumulation error of the kernel
+    itself.  The absolute floor covers outputs that cancel to nearly zero,
+    where a relative ulp is smaller than fp32 rounding of the summands.
 """
 from __future__ import annotations
 
@@ -42,7 +44,12 @@ def attention_errors(got: torch.Tensor, ref: np.ndarray, out_dtype: torch.dtype)
         stats["rounding_limited"] = int(limited.sum())
         stats["violations"] = int((over & ~limited).sum())
         r = torch.from_numpy(ref).to(out_dtype).to(torch.float64).numpy()
-        stats["beyond_one_ulp"] = int((np.abs(g - r) > ulp(r, out_dtype) * 1.0001).sum())
+        beyond = np.abs(g - r) > ulp(r, out_dtype) * 1.0001 + 2e-6
+        stats["beyond_one_ulp"] = int(beyond.sum())
+        if beyond.any():
+            i = np.unravel_index(np.argmax(np.abs(g - r) * beyond), g.shape)
+            stats["worst"] = {"index": [int(x) for x in i], "got": float(g[i]),
+                              "oracle": float(ref[i]), "oracle_rounded": float(r[i])}
     else:
         stats["rounding_limited"] = 0
         stats["violations"] = int(over.sum())

@@ -88,7 +88,8 @@ def _decode(L, **kw):
     (dict(H=48, Hk=4), 2),
     (dict(kv_dtype=2), 2),
     (dict(out_dtype=7), 1),
-    (dict(nb=0), 1),
+    (dict(nb=-1), 1),
+    (dict(nb=3, k=NULL), 1),
     (dict(mb=0), 1),
     (dict(maxc=-5), 1),
     (dict(scale=float("nan")), 1),
