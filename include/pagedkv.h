@@ -143,6 +143,39 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * paged_attn_decode_noalloc -- paged_attn_decode for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is an
+ * interface addition of this library.
+ *
+ * Some callers cannot hand over a workspace buffer: a serving loop that
+ * reserved all of HBM for its KV pool at start-up and may not call
+ * cudaMalloc again (which can also wait for the whole device), or a host
+ * framework or plugin that owns the allocator and forbids allocations
+ * outside it.  This entry point computes exactly what paged_attn_decode
+ * computes, with the same inputs and outputs, but keeps the split partials
+ * in a scratch array compiled into the library (PKV_NOALLOC_SCRATCH_BYTES
+ * per device that loads it, held until exit) and allocates nothing.
+ *   - A problem whose split partials need more than that
+ *     (pkv_decode_workspace_bytes > PKV_NOALLOC_SCRATCH_BYTES) returns
+ *     PKV_ERR_WORKSPACE before any launch.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents (nothing in it needs to start at zero).  Calls whose
+ *     kernels may overlap on the GPU (different streams without ordering)
+ *     race on it.
+ *   - The first call on each device looks up the array's device address;
+ *     make that first call before any stream capture begins.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+PKV_API pkv_status paged_attn_decode_noalloc(void* out, pkv_dtype out_dtype, const void* q,
+                                             const void* k_pool, const void* v_pool,
+                                             pkv_dtype kv_dtype, const int32_t* block_tables,
+                                             int max_blocks_per_seq, const int32_t* context_lens,
+                                             int num_seqs, int n_heads, int n_kv_heads,
+                                             int head_dim, int block_size, int num_blocks,
+                                             float scale, int max_context_len, int split_tokens,
+                                             void* stream);
+
+/*
  * kv_append -- write one new token per sequence into its page
  * (reshape-and-cache; [LAYOUT] section 三 append_token):
  *

@@ -218,6 +218,10 @@ cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, pkv_dtype dt, in
 
 namespace pkv {
 
+// Lets other translation units of the library report a failure reason
+// through pkv_last_error_detail().
+void record_detail(const char* msg) { set_detail("%s", msg); }
+
 cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask, size_t bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
