@@ -56,6 +56,10 @@ def parse_args():
     ap.add_argument("--seqs", type=int, default=0,
                     help="override the number of sequences (smaller cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each step as one CUDA graph")
+    ap.add_argument("--replicas", type=int, default=1,
+                    help="independent copies of the workload (own pools) per GPU, one graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
@@ -243,6 +247,65 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ ours
 
+def build_replicas(args, rank, dev, pkv, wl, torch, np):
+    """R independent copies of the workload (own pools, own sequences), with
+    the per-step inputs of all copies packed in contiguous buffers (so that
+    the end-to-end step moves them with one copy each)."""
+    R = max(1, args.replicas)
+    extra = {"pool_extra": 0.01} if args.config == 4 else {}
+    if args.seqs:
+        extra["S"] = args.seqs
+    reps = []
+    for r in range(R):
+        seed = (args.config - 1) + 1000 * rank + 7919 * r
+        case = wl.make_case(args.config, seed=seed, **extra)
+        S = case.S
+        bm = pkv.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)
+        bt_h = case.block_tables.clone()
+        lens_h = case.context_lens.clone()
+        slots_h = torch.empty(S, dtype=torch.int64)
+        if case.k_new is None:
+            case.k_new = wl._normal(np.random.default_rng(seed + 7), (S, case.Hk, case.D), case.dtype)
+            case.v_new = wl._normal(np.random.default_rng(seed + 8), (S, case.Hk, case.D), case.dtype)
+        need_cols = int(((lens_h + 1 + case.B - 1) // case.B).max())
+        if need_cols > bt_h.shape[1]:
+            bt_h = torch.cat([bt_h, torch.full((S, need_cols - bt_h.shape[1]), -1,
+                                               dtype=torch.int32)], 1)
+        if bm.append_slots(bt_h, lens_h, slots_h) != 0:
+            raise RuntimeError("pool has no room for the appended tokens")
+        reps.append({"case": case, "bt_h": bt_h, "lens_h": lens_h, "slots_h": slots_h})
+    S = reps[0]["case"].S
+    mb = max(r["bt_h"].shape[1] for r in reps)
+    host = {
+        "q": torch.cat([r["case"].q for r in reps]).pin_memory(),
+        "k_new": torch.cat([r["case"].k_new for r in reps]).pin_memory(),
+        "v_new": torch.cat([r["case"].v_new for r in reps]).pin_memory(),
+        "bt": torch.stack([torch.nn.functional.pad(r["bt_h"], (0, mb - r["bt_h"].shape[1]),
+                                                   value=-1) for r in reps]).pin_memory(),
+        "lens": torch.cat([r["lens_h"] for r in reps]).pin_memory(),
+        "slots": torch.cat([r["slots_h"] for r in reps]).pin_memory(),
+    }
+    devb = {k: v.to(dev) for k, v in host.items()}
+    c0 = reps[0]["case"]
+    out_all = torch.empty(R * S, c0.H, c0.D, dtype=c0.out_dtype, device=dev)
+    host["out"] = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+    devb["out"] = out_all
+    for i, r in enumerate(reps):
+        case = r["case"]
+        sl = slice(i * S, (i + 1) * S)
+        r["q"], r["k_new"], r["v_new"] = devb["q"][sl], devb["k_new"][sl], devb["v_new"][sl]
+        r["bt"], r["lens"], r["slots"] = devb["bt"][i], devb["lens"][sl], devb["slots"][sl]
+        r["out"] = out_all[sl]
+        r["k_pool"], r["v_pool"] = case.k_pool.to(dev), case.v_pool.to(dev)
+        r["max_ctx"] = int(r["lens_h"].max())
+        r["ws"] = pkv.alloc_decode_workspace(r["q"], r["k_pool"], r["max_ctx"], args.split)
+        if case.d2d_pairs is not None:
+            r["d2d"] = case.d2d_pairs.to(dev)
+            r["h2d"] = case.h2d_pairs.pin_memory()
+            r["hk"], r["hv"] = case.host_k_pool.pin_memory(), case.host_v_pool.pin_memory()
+    return reps, host, devb
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -269,115 +332,128 @@ def main():
     import paged_kv_decode_26_gb300 as pkv
     from paged_kv_decode_26_gb300 import workloads as wl
 
-    # ---- this rank's replica of the workload
-    seed = (args.config - 1) + 1000 * rank
-    # the long-context pool holds exactly the needed blocks; give the
-    # appended tokens room for their new pages
-    extra = {"pool_extra": 0.01} if args.config == 4 else {}
-    if args.seqs:
-        extra["S"] = args.seqs
-    case = wl.make_case(args.config, seed=seed, **extra)
+    reps, host, devb = build_replicas(args, rank, dev, pkv, wl, torch, np)
+    R = len(reps)
+    case = reps[0]["case"]
     S = case.S
-    bm = pkv.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)
-    bt_h = case.block_tables.clone()
-    lens_h = case.context_lens.clone()
-    slots_h = torch.empty(S, dtype=torch.int64)
-    if case.k_new is None:
-        case.k_new = wl._normal(np.random.default_rng(seed + 7), (S, case.Hk, case.D), case.dtype)
-        case.v_new = wl._normal(np.random.default_rng(seed + 8), (S, case.Hk, case.D), case.dtype)
-    need_cols = int(((lens_h + 1 + case.B - 1) // case.B).max())
-    if need_cols > bt_h.shape[1]:
-        bt_h = torch.cat([bt_h, torch.full((S, need_cols - bt_h.shape[1]), -1,
-                                           dtype=torch.int32)], 1)
-    st = bm.append_slots(bt_h, lens_h, slots_h)
-    if st != 0:
-        raise RuntimeError("pool has no room for the appended tokens")
-    max_ctx = int(lens_h.max())
-
-    q = case.q.to(dev)
-    k_pool = case.k_pool.to(dev)
-    v_pool = case.v_pool.to(dev)
-    k_new = case.k_new.to(dev)
-    v_new = case.v_new.to(dev)
-    bt = bt_h.to(dev)
-    lens = lens_h.to(dev)
-    slots = slots_h.to(dev)
-    out = torch.empty(S, case.H, case.D, dtype=case.out_dtype, device=dev)
-    ws = pkv.alloc_decode_workspace(q, k_pool, max_ctx, args.split)
-    split_used = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B, max_ctx)
-    with_swaps = args.config == 5
-    if with_swaps:
-        d2d = case.d2d_pairs.to(dev)
-        h2d = case.h2d_pairs.pin_memory()
-        hk_pool = case.host_k_pool.pin_memory()
-        hv_pool = case.host_v_pool.pin_memory()
+    with_swaps = case.d2d_pairs is not None
     stream = torch.cuda.current_stream()
+    use_graph = args.graph or R > 1
 
-    def step():
-        pkv.kv_append(k_pool, v_pool, k_new, v_new, slots)
-        pkv.paged_attn_decode(out, q, k_pool, v_pool, bt, lens, case.scale, max_ctx,
-                              split_tokens=args.split, workspace=ws)
-        if with_swaps:
-            pkv.swap_blocks(k_pool, k_pool, d2d)
-            pkv.swap_blocks(v_pool, v_pool, d2d)
-            pkv.swap_blocks(k_pool, hk_pool, h2d)
-            pkv.swap_blocks(v_pool, hv_pool, h2d)
+    def decode(r):
+        pkv.paged_attn_decode(r["out"], r["q"], r["k_pool"], r["v_pool"], r["bt"], r["lens"],
+                              case.scale, r["max_ctx"], split_tokens=args.split, workspace=r["ws"])
 
-    launches_per_step = 2 + (1 if (max_ctx + split_used - 1) // split_used > 1 else 0) + \
-        (4 if with_swaps else 0)
+    def swaps(r):
+        pkv.swap_blocks(r["k_pool"], r["k_pool"], r["d2d"])
+        pkv.swap_blocks(r["v_pool"], r["v_pool"], r["d2d"])
+        pkv.swap_blocks(r["k_pool"], r["hk"], r["h2d"])
+        pkv.swap_blocks(r["v_pool"], r["hv"], r["h2d"])
 
-    # ---- bytes per step
-    row = case.Hk * case.D * 2
-    kv_read = int(lens_h.sum()) * row * 2                 # K and V of every context row
+    def step_eager():
+        for r in reps:
+            pkv.kv_append(r["k_pool"], r["v_pool"], r["k_new"], r["v_new"], r["slots"])
+            decode(r)
+            if with_swaps:
+                swaps(r)
+
+    def decode_eager():
+        for r in reps:
+            decode(r)
+
+    # ---- bytes per step (all replicas of this rank)
     es = 2
-    io_bytes = (q.numel() * es + out.numel() * out.element_size() + bt.numel() * 4 + S * 4)
-    decode_alg_bytes = kv_read + io_bytes
+    kv_read = kv_unique = io_bytes = 0
+    launches_per_step = 0
+    for r in reps:
+        lo, un = wl.kv_bytes(r["case"], r["lens_h"].numpy(), r["bt_h"].numpy())
+        kv_read += lo
+        kv_unique += un
+        io_bytes += (S * case.H * case.D * (es + devb["out"].element_size()) +
+                     r["bt"].numel() * 4 + S * 4)
+        split_r = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B,
+                                                        r["max_ctx"])
+        launches_per_step += 2 + (1 if (r["max_ctx"] + split_r - 1) // split_r > 1 else 0) + \
+            (4 if with_swaps else 0)
+    split_used = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B,
+                                                       reps[0]["max_ctx"])
+    decode_alg_bytes = kv_unique + io_bytes       # shared prefix rows counted once
+    bb = case.B * case.Hk * case.D * es
     swap_bytes = 0
     if with_swaps:
-        bb = case.B * case.Hk * case.D * es
-        swap_bytes = 2 * 2 * bb * (case.d2d_pairs.shape[0] + case.h2d_pairs.shape[0])
+        n_d2d, n_h2d = case.d2d_pairs.shape[0], case.h2d_pairs.shape[0]
+        swap_bytes = R * 2 * 2 * bb * (n_d2d + n_h2d)
+    # Workloads whose bytes fit in L2 are timed step by step with an L2
+    # flush (a 512 MB write) between steps, outside the timed events.
+    flush_mode = with_swaps or kv_read < 4 * L2_BYTES
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush_mode else None
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
 
     pkv.device_errors(clear=True)
     for _ in range(max(3, args.warmup)):
-        step()
+        step_eager()
     torch.cuda.synchronize()
+
+    if use_graph:
+        g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
+            step_eager()
+        with torch.cuda.graph(g_dec):
+            decode_eager()
+        run_step, run_decode = g_step.replay, g_dec.replay
+        for _ in range(3):
+            run_step()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+    else:
+        run_step, run_decode = step_eager, decode_eager
 
     sampler = ClockSampler(gpu_id_for_smi(torch, local))
     sampler.start()
     time.sleep(0.3)
-    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    step_events = [(ev(), ev()) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    t_start.record(stream)
-    for i in range(args.steps):
-        pkv.kv_append(k_pool, v_pool, k_new, v_new, slots)
-        dec_events[i][0].record(stream)
-        pkv.paged_attn_decode(out, q, k_pool, v_pool, bt, lens, case.scale, max_ctx,
-                              split_tokens=args.split, workspace=ws)
-        dec_events[i][1].record(stream)
-        if with_swaps:
-            pkv.swap_blocks(k_pool, k_pool, d2d)
-            pkv.swap_blocks(v_pool, v_pool, d2d)
-            pkv.swap_blocks(k_pool, hk_pool, h2d)
-            pkv.swap_blocks(v_pool, hv_pool, h2d)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    if flush_mode:
+        for i in range(args.steps):
+            flush_buf.fill_(i & 255)
+            step_events[i][0].record(stream)
+            run_step()
+            step_events[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in step_events)
+    else:
+        t_start, t_end = ev(), ev()
+        t_start.record(stream)
+        for i in range(args.steps):
+            run_step()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        ms = t_start.elapsed_time(t_end) / max(1, args.steps)
     if world > 1:
         dist.barrier()
     # keep the GPU under the same load until the sampler has ~1.5 s of samples
     while time.perf_counter() - wall0 < 1.5:
         for _ in range(20):
-            step()
+            run_step()
         torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    ms = t_start.elapsed_time(t_end) / max(1, args.steps)
+    # ---- the decode call alone (the dominant kernel), timed per launch
+    dec_events = [(ev(), ev()) for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush_mode:
+            flush_buf.fill_(i & 255)
+        dec_events[i][0].record(stream)
+        run_decode()
+        dec_events[i][1].record(stream)
+    torch.cuda.synchronize()
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_events)
+
     if world > 1:
         t = torch.tensor([ms, dec_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -386,38 +462,79 @@ def main():
     if errors:
         raise RuntimeError(f"device error flags 0x{errors:x} raised during the benchmark")
 
+    # ---- swap_blocks alone (continuous-batching workload), with copy references
+    swap = None
+    if with_swaps and rank == 0:
+        r0 = reps[0]
+        d2d_t, h2d_t, d2d_ref_t, h2d_ref_t = [], [], [], []
+        n_ref_d2d, n_ref_h2d = n_d2d * bb, n_h2d * bb
+        src_d = torch.empty(n_ref_d2d, dtype=torch.uint8, device=dev)
+        dst_d = torch.empty(n_ref_d2d, dtype=torch.uint8, device=dev)
+        src_h = torch.empty(n_ref_h2d, dtype=torch.uint8).pin_memory()
+        dst_h = torch.empty(n_ref_h2d, dtype=torch.uint8, device=dev)
+        for i in range(max(20, min(args.steps, 200))):
+            for fn, acc in (
+                    (lambda: (pkv.swap_blocks(r0["k_pool"], r0["k_pool"], r0["d2d"]),
+                              pkv.swap_blocks(r0["v_pool"], r0["v_pool"], r0["d2d"])), d2d_t),
+                    (lambda: (pkv.swap_blocks(r0["k_pool"], r0["hk"], r0["h2d"]),
+                              pkv.swap_blocks(r0["v_pool"], r0["hv"], r0["h2d"])), h2d_t),
+                    (lambda: (dst_d.copy_(src_d, non_blocking=True),
+                              dst_d.copy_(src_d, non_blocking=True)), d2d_ref_t),
+                    (lambda: (dst_h.copy_(src_h, non_blocking=True),
+                              dst_h.copy_(src_h, non_blocking=True)), h2d_ref_t)):
+                flush_buf.fill_(i & 255)
+                a, b = ev(), ev()
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                acc.append(a.elapsed_time(b))
+        peak_copy, _ = measured_peak()
+        moved_d2d, moved_h2d = 2 * n_d2d * bb, 2 * n_h2d * bb       # K and V
+        d2d_ms, h2d_ms = statistics.median(d2d_t), statistics.median(h2d_t)
+        d2d_ref_ms, h2d_ref_ms = statistics.median(d2d_ref_t), statistics.median(h2d_ref_t)
+        swap = {
+            "d2d": {"pairs": n_d2d, "block_bytes": bb, "ms_k_and_v": d2d_ms,
+                    "gbs_read_write": 2 * moved_d2d / (d2d_ms / 1e3) / 1e9,
+                    "vs_measured_copy_peak": 2 * moved_d2d / (d2d_ms / 1e3) / 1e9 / peak_copy,
+                    "contiguous_copy_same_bytes_gbs_read_write":
+                        2 * moved_d2d / (d2d_ref_ms / 1e3) / 1e9,
+                    "vs_contiguous_copy": d2d_ref_ms / d2d_ms},
+            "h2d": {"pairs": n_h2d, "ms_k_and_v": h2d_ms,
+                    "gbs": moved_h2d / (h2d_ms / 1e3) / 1e9,
+                    "memcpy_h2d_same_bytes_gbs": moved_h2d / (h2d_ref_ms / 1e3) / 1e9,
+                    "vs_memcpy": h2d_ref_ms / h2d_ms},
+            "timing": "median of per-call CUDA events, L2 flushed before each",
+        }
+
     # ---- end to end through the public API with host buffers
-    q_h = case.q.pin_memory()
-    kn_h, vn_h = case.k_new.pin_memory(), case.v_new.pin_memory()
-    bt_p, lens_p, slots_p = bt_h.pin_memory(), lens_h.pin_memory(), slots_h.pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d_bytes = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, bt_p, lens_p, slots_p))
-    d2h_bytes = out_h.numel() * out_h.element_size()
+    h2d_bytes = sum(host[k].numel() * host[k].element_size()
+                    for k in ("q", "k_new", "v_new", "bt", "lens", "slots"))
+    d2h_bytes = host["out"].numel() * host["out"].element_size()
 
     def e2e_step():
-        q.copy_(q_h, non_blocking=True)
-        k_new.copy_(kn_h, non_blocking=True)
-        v_new.copy_(vn_h, non_blocking=True)
-        bt.copy_(bt_p, non_blocking=True)
-        lens.copy_(lens_p, non_blocking=True)
-        slots.copy_(slots_p, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
+        for k in ("q", "k_new", "v_new", "bt", "lens", "slots"):
+            devb[k].copy_(host[k], non_blocking=True)
+        run_step()
+        host["out"].copy_(devb["out"], non_blocking=True)
         stream.synchronize()
 
     for _ in range(3):
         e2e_step()
     n_e2e = max(1, min(args.e2e_steps, args.steps))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
-    e0.record(stream)
-    for _ in range(n_e2e):
+    e2e_times = []
+    for i in range(n_e2e):
+        if flush_mode:
+            flush_buf.fill_(i & 255)
+        a, b = ev(), ev()
+        a.record(stream)
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_times.append(a.elapsed_time(b))
+    e2e_ms = statistics.mean(e2e_times)
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -428,7 +545,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import build as ob
         ob.build()
-        b, secs, nseq = oracle_sample_seconds(case, lens_h, bt_h, args.cpu_budget)
+        b, secs, nseq = oracle_sample_seconds(case, reps[0]["lens_h"], reps[0]["bt_h"],
+                                              args.cpu_budget)
         cpu = {"value": b / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{nseq} of {S} sequences of the step (all {case.H} heads, "
                          f"{b / 1e6:.1f} MB of K/V), fp64 two-pass oracle, single thread"}
@@ -443,6 +561,7 @@ def main():
     total_kv = kv_read * world
     value = total_kv / (ms / 1e3) / 1e9
     achieved = decode_alg_bytes / (dec_ms / 1e3) / 1e9
+    logical_gbs = (kv_read + io_bytes) / (dec_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": value,
@@ -456,19 +575,22 @@ def main():
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "seq_steps_per_s": S * world / (ms / 1e3),
+        "seq_steps_per_s": R * S * world / (ms / 1e3),
         "config": {
             "workload": name,
             "step": "kv_append (1 token/seq) + paged_attn_decode" +
                     (" + swap_blocks D2D and pinned-H2D (K and V)" if with_swaps else ""),
-            "num_seqs_per_gpu": S,
+            "replicas_per_gpu": R,
+            "launch": "one CUDA graph per step over all replicas" if use_graph else "eager",
+            "num_seqs_per_gpu": R * S,
             "kv_bytes_per_step_per_gpu": kv_read,
+            "kv_unique_bytes_per_step_per_gpu": kv_unique,
             "split_tokens": split_used,
             "storage_dtype": str(case.dtype).replace("torch.", ""),
             "out_dtype": str(case.out_dtype).replace("torch.", ""),
             "l2": ("inputs larger than L2 (%.2f GB of K/V vs 129 MB), no flush" % (kv_read / 1e9)
-                   if kv_read > 4 * L2_BYTES else
-                   "inputs smaller than L2: steps re-read a hot cache"),
+                   if not flush_mode else
+                   "L2 flushed (512 MB write) before every step, outside the timed events"),
             "parallelism": f"replicas x{world} (sequences per GPU independent)",
         },
         "roofline": {
@@ -477,8 +599,11 @@ def main():
             "peak": peak,
             "unit": "GB/s",
             "frac": achieved / peak,
-            "traffic": committed_traffic(name),
-            "kernel": "paged_attn_decode (decode kernel + split merge), CUDA events per call",
+            "traffic": committed_traffic(name) if R == 1 else None,
+            "kernel": "paged_attn_decode (decode kernel + split merge), CUDA events per call" +
+                      (" (all replicas, one graph)" if use_graph else ""),
+            "bytes": "unique K/V rows read (shared prefix rows once) + q + out + tables",
+            "logical_gbs": logical_gbs,
             "algorithmic_bytes_per_launch": decode_alg_bytes,
             "ms_per_launch": dec_ms,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -493,6 +618,7 @@ def main():
     }
     if with_swaps:
         line["config"]["swap_bytes_per_step"] = swap_bytes
+        line["swap_blocks"] = swap
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -66,6 +66,7 @@ typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 #define PKV_DEVERR_SLOT 0x4u        /* append: slot beyond num_blocks * block_size */
 #define PKV_DEVERR_PAIR 0x8u        /* copy: pair index beyond its pool */
 #define PKV_DEVERR_TIMEOUT 0x10u    /* a pipeline wait gave up (should never happen) */
+#define PKV_DEVERR_CONFIG 0x20u     /* inconsistent launch configuration (should never happen) */
 
 /* Human-readable name of a status code (static string). */
 PKV_API const char* pkv_status_string(pkv_status status);

@@ -107,7 +107,8 @@ int env_int(const char* name, int fallback) {
 
 struct DecodeConfig {
     int qpw;     // query heads per consumer warp
-    int wpk;     // consumer warps per kv head
+    int wpk;     // consumer warps per kv head, splitting its query heads
+    int wpt;     // consumer warps per kv head, taking turns on its pages
     int hpc;     // kv heads per CTA
     int stages;  // ring depth
     int split_tokens;
@@ -128,22 +129,40 @@ bool supported_shape(int n_heads, int n_kv_heads, int head_dim, int block_size) 
 }
 
 // Heads per CTA, ring depth and warp roles.  A pipeline stage holds one page
-// of K and V for the CTA's kv heads; about 32 KB per stage and ~96 KB per CTA
-// keep two CTAs resident per SM with 2-3 stages of loads in flight each.
+// of K and V for the CTA's kv heads: HPC * head_dim = 512 elements, i.e.
+// 1 KB contiguous per token row and 32 KB (block size 16) or 64 KB (block
+// size 32) per stage.  Three stages keep two CTAs (block size 16) or one CTA
+// (block size 32) resident per SM with ~192 KB of loads in flight per SM,
+// which measured best on GB300 for both block sizes.  PKV_DECODE_HPC,
+// _STAGES, _WPT and _QPW override the choice (for tuning sweeps).
 void shape_config(int n_heads, int n_kv_heads, int head_dim, int block_size, DecodeConfig* c) {
     const int G = n_heads / n_kv_heads;
-    c->qpw = G < 4 ? G : 4;
+    int qpw = env_int("PKV_DECODE_QPW", G < 4 ? G : 4);
+    if (qpw < 1 || qpw > 4 || (qpw & (qpw - 1)) || G % qpw) qpw = G < 4 ? G : 4;
+    c->qpw = qpw;
     c->wpk = G / c->qpw;
-    const int per_head_stage = 2 * block_size * head_dim * 2;
-    int target = env_int("PKV_DECODE_HPC", 32768 / per_head_stage);
+    int target = env_int("PKV_DECODE_HPC", 512 / head_dim);
     if (target < 1) target = 1;
     int hpc = 1;
     for (int h = 1; h <= n_kv_heads; ++h)
         if (n_kv_heads % h == 0 && h <= target && h * c->wpk <= pkv::kMaxConsumerWarps) hpc = h;
     c->hpc = hpc;
-    int stages = env_int("PKV_DECODE_STAGES", 98304 / (hpc * per_head_stage));
+    int stages = env_int("PKV_DECODE_STAGES", 3);
     c->stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-    c->threads = 32 * (1 + c->hpc * c->wpk);
+    // Optionally let several warps take turns on the pages of a kv head
+    // (merged in shared memory at the end of the CTA).
+    int wpt = env_int("PKV_DECODE_WPT", 1);
+    if (wpt < 1) wpt = 1;
+    while (wpt > 1 && c->hpc * c->wpk * wpt > pkv::kMaxConsumerWarps) --wpt;
+    c->wpt = wpt;
+    // Page i goes to ring slot i % stages and to warp subset i % wpt.  With
+    // stages a multiple of wpt every slot belongs to one subset, which then
+    // waits on each phase of that slot's barrier in turn; otherwise a subset
+    // would skip phases and its parity wait could match an older phase.
+    c->stages = c->stages / wpt * wpt;
+    if (c->stages < wpt) c->stages = wpt;
+    if (c->stages < 2) c->stages = 2;
+    c->threads = 32 * (1 + c->hpc * c->wpk * c->wpt);
 }
 
 int auto_split_tokens(int num_seqs, int n_kv_heads, int hpc, int block_size, int max_context_len,
@@ -178,8 +197,8 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
                          split_tokens;
     c->max_splits = ms < 1 ? 1 : (int)ms;
     c->max_pages = split_tokens / block_size;
-    c->smem = pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc, c->wpk, c->stages,
-                                     c->max_pages);
+    c->smem = pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc, c->wpk, c->wpt,
+                                     c->stages, c->max_pages);
     return PKV_OK;
 }
 
@@ -379,6 +398,7 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
     p.max_splits = c.max_splits;
     p.heads_per_cta = c.hpc;
     p.warps_per_kv = c.wpk;
+    p.warps_per_tok = c.wpt;
     p.stages = c.stages;
     p.max_pages_per_split = c.max_pages;
     p.ws_o = need ? static_cast<float*>(workspace) : nullptr;

@@ -17,17 +17,20 @@
 // (prefetched into shared memory) and issues one 4-D TMA tile load per page
 // for K and one for V, covering the HPC heads of the group
 // ([B, HPC, D] boxes out of the [num_blocks, B, Hk, D] pool), into a ring of
-// `stages` shared-memory buffers guarded by full/empty mbarriers.  Every
-// other warp is a consumer owning QPW query heads of one kv head: lane l
-// holds head dims [l*D/32, (l+1)*D/32) of q and of the fp32 accumulator O,
-// computes 16 partial dot products per chunk of 16 tokens, reduces them
-// across the warp with a transpose-reduce (one shuffle per score), updates
-// the running max M and per-lane sum L with exp2 (scores pre-scaled by
-// log2 e), broadcasts the 16 weights through shared memory and accumulates
-// P V.  O is normalised once at the end (algebraically the same as the
-// pages' per-step normalisation).  A context longer than one split leaves a
-// normalised partial state (O, M, L) in the workspace; a second kernel
-// merges them with the same recurrence.
+// `stages` shared-memory buffers guarded by full/empty mbarriers.  The other
+// warps are consumers.  A consumer owns QPW query heads of one kv head and
+// every WPT-th page of the split (WPT warps share a head and merge their
+// states in shared memory at the end).  Inside a warp, LPR = D/8 lanes cover
+// one K/V row (8 dims, 16 bytes each) and the warp walks TPI = 32/LPR rows
+// at a time; per chunk of 16 tokens each lane forms its partial dot
+// products, a transpose-reduce across the LPR lanes of a row completes them
+// (each halving step trades half of the values with the partner lane), the
+// running max M and per-lane sum L are updated with exp2 (scores pre-scaled
+// by log2 e), the weights are broadcast through shared memory and P V is
+// accumulated with packed fp32x2 FMAs.  O is normalised once at the end
+// (algebraically the same as the pages' per-step normalisation).  A context
+// longer than one split leaves a normalised partial state (O, M, L) in the
+// workspace; a second kernel merges them with the same recurrence.
 #pragma once
 
 #include "pkv_device.cuh"
@@ -54,7 +57,8 @@ struct DecodeParams {
     int split_tokens;  // a multiple of the block size
     int max_splits;    // grid extent over splits
     int heads_per_cta;  // HPC
-    int warps_per_kv;   // consumer warps per kv head
+    int warps_per_kv;   // consumer warps sharing a kv head's pages by query heads
+    int warps_per_tok;  // consumer warps sharing a kv head's query heads by pages
     int stages;
     int max_pages_per_split;
     float* ws_o;   // [num_seqs, n_heads, max_splits, D]
@@ -63,12 +67,17 @@ struct DecodeParams {
 };
 
 // Shared-memory bytes of one CTA (must match the carve-up in the kernel).
+// The ring doubles as the buffer of the end-of-CTA merge between the WPT
+// warps of a kv head.
 inline size_t decode_smem_bytes(int D, int BS, int QPW, int elem_bytes, int hpc, int wpk,
-                                int stages, int max_pages_per_split) {
+                                int wpt, int stages, int max_pages_per_split) {
     size_t tile = (size_t)BS * hpc * D * elem_bytes;
-    size_t bytes = (size_t)stages * 2 * tile;
+    size_t ring = (size_t)stages * 2 * tile;
+    size_t merge = (size_t)(wpt - 1) * hpc * wpk * QPW * (D + 2) * sizeof(float);
+    size_t bytes = ring > merge ? ring : merge;
+    bytes = (bytes + 15) / 16 * 16;
     bytes += (size_t)stages * 2 * sizeof(uint64_t);
-    bytes += (size_t)hpc * wpk * QPW * kChunk * sizeof(float);
+    bytes += (size_t)hpc * wpk * wpt * QPW * kChunk * sizeof(float);
     bytes += (size_t)max_pages_per_split * sizeof(int);
     bytes += 2 * sizeof(int);  // abort flag, pages issued
     return bytes;
@@ -76,12 +85,13 @@ inline size_t decode_smem_bytes(int D, int BS, int QPW, int elem_bytes, int hpc,
 
 // ------------------------------------------------------------ warp helpers
 
-// Transpose-reduce: every lane holds N partial sums v[0..N); afterwards lane
-// l holds the complete (32-lane) sums of indices [idx0, idx0 + max(1,N/32))
-// in v[0..), with idx0 = l * N / 32 for N >= 32 and l / 2 for N == 16
-// (lanes 2k and 2k+1 then hold the same sum).  Each halving step trades
-// half of the values with the partner lane, so the whole reduction costs
-// N - 1 shuffles for N >= 32 instead of 5 N.
+// Transpose-reduce over the lanes that differ in bits O, O/2, ..., 1: every
+// lane holds N partial sums v[0..N); each halving step keeps one half and
+// adds the partner lane's copy of it, so the complete sums end up spread
+// over the lanes (lane-index bits select which values a lane keeps) at a
+// cost of one shuffle per value instead of one per value per step.  When
+// the values run out before the lanes do, the remaining steps are plain
+// butterflies and neighbouring lanes hold duplicates.
 template <int N, int O>
 __device__ __forceinline__ void transpose_reduce(float* v, int lane) {
     if constexpr (O >= 1) {
@@ -102,45 +112,47 @@ __device__ __forceinline__ void transpose_reduce(float* v, int lane) {
     }
 }
 
-template <int D, typename T>
-struct RowLoad {
-    static constexpr int DL = D / 32;
-    // Loads this lane's DL elements of a row and widens them to fp32.
-    __device__ __forceinline__ static void load(const T* row, int lane, float (&f)[DL]) {
-        if constexpr (DL == 4) {
-            const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 4);
-            const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y);
-            f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-        } else {
-            static_assert(DL == 2, "head_dim 64 or 128");
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 2);
-            const float2 a = unpack2<T>(w);
-            f[0] = a.x; f[1] = a.y;
-        }
-    }
-};
+// 8 consecutive 16-bit elements (16 bytes) -> 4 fp32 pairs (exact widening);
+// with ok == false the row counts as zeros.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float2 (&f)[4], bool ok = true) {
+    uint4 w = *reinterpret_cast<const uint4*>(p);
+    if (!ok) w = make_uint4(0u, 0u, 0u, 0u);
+    f[0] = unpack2<T>(w.x);
+    f[1] = unpack2<T>(w.y);
+    f[2] = unpack2<T>(w.z);
+    f[3] = unpack2<T>(w.w);
+}
 
-template <int DL>
-__device__ __forceinline__ void store_row(void* base, size_t elem_off, int out_dtype,
-                                          const float (&v)[DL]) {
-    if (out_dtype == PKV_F32) {
-        float* p = reinterpret_cast<float*>(base) + elem_off;
-        if constexpr (DL == 4) {
-            *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-        } else {
-            *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
-        }
-    } else if (out_dtype == PKV_BF16) {
-        __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + elem_off;
-#pragma unroll
-        for (int i = 0; i < DL; i += 2)
-            *reinterpret_cast<__nv_bfloat162*>(p + i) = __floats2bfloat162_rn(v[i], v[i + 1]);
-    } else {
-        __half* p = reinterpret_cast<__half*>(base) + elem_off;
-#pragma unroll
-        for (int i = 0; i < DL; i += 2)
-            *reinterpret_cast<__half2*>(p + i) = __floats2half2_rn(v[i], v[i + 1]);
+__device__ __forceinline__ uint32_t pack_out(float a, float b, int out_dtype) {
+    if (out_dtype == PKV_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
     }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Store 8 fp32 values as out_dtype at base + elem_off (16/32-byte aligned).
+__device__ __forceinline__ void store8(void* base, size_t elem_off, int out_dtype,
+                                       const float2 (&v)[4]) {
+    if (out_dtype == PKV_F32) {
+        float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + elem_off);
+        p[0] = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+        p[1] = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+    } else {
+        uint4 w;
+        w.x = pack_out(v[0].x, v[0].y, out_dtype);
+        w.y = pack_out(v[1].x, v[1].y, out_dtype);
+        w.z = pack_out(v[2].x, v[2].y, out_dtype);
+        w.w = pack_out(v[3].x, v[3].y, out_dtype);
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + elem_off) = w;
+    }
+}
+
+// Named barrier over the consumer warps only (the producer does not join).
+__device__ __forceinline__ void consumer_sync(int n_threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(n_threads) : "memory");
 }
 
 // ------------------------------------------------------------ the kernel
@@ -149,11 +161,15 @@ template <int D, int BS, int QPW, typename T>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-    constexpr int DL = D / 32;
-    constexpr int N = QPW * kChunk;            // partial sums per lane per chunk
-    constexpr int NL = N >= 32 ? N / 32 : 1;   // complete sums per lane after reduce
-    constexpr int LANES_PER_Q = 32 / QPW;      // lanes sharing one query head's sums
+    constexpr int LPR = D / 8;                   // lanes per K/V row (8 dims each)
+    constexpr int TPI = 32 / LPR;                // rows per warp iteration
+    constexpr int IPC = kChunk / TPI;            // iterations per 16-token chunk
+    constexpr int N = QPW * IPC;                 // partial dots per lane per chunk
+    constexpr int NL = N >= LPR ? N / LPR : 1;   // complete dots per lane after reduce
+    constexpr int DUP = N >= LPR ? 1 : LPR / N;  // lanes holding the same dot
+    constexpr int GL = LPR / QPW;                // lanes of a row sharing a query head
     static_assert(BS % kChunk == 0, "block size must be a multiple of 16");
+    static_assert(LPR % QPW == 0 && IPC % 4 == 0, "lane layout");
 
     extern __shared__ __align__(128) unsigned char smem[];
 
@@ -161,7 +177,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int hg = blockIdx.y;
     const int s = blockIdx.z;
     const int HPC = p.heads_per_cta;
-    const int n_cons = HPC * p.warps_per_kv;
+    const int per_sub = HPC * p.warps_per_kv;   // consumer warps per page
+    const int n_cons = per_sub * p.warps_per_tok;
+    // Each ring slot must belong to one warp subset (see the host-side
+    // configuration); refuse an inconsistent launch before any barrier.
+    if (p.stages % p.warps_per_tok != 0 || (int)blockDim.x != 32 * (1 + n_cons)) {
+        if (threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONFIG);
+        return;
+    }
 
     // ---- this CTA's token range (clamped to what the grid and table cover)
     int n = p.context_lens[s];
@@ -179,11 +202,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
     // ---- shared-memory carve-up
     const uint32_t tile_bytes = (uint32_t)(BS * HPC * D * sizeof(T));
+    size_t ring = (size_t)p.stages * 2 * tile_bytes;
+    const size_t merge =
+        (size_t)(p.warps_per_tok - 1) * per_sub * QPW * (D + 2) * sizeof(float);
+    ring = ((ring > merge ? ring : merge) + 15) / 16 * 16;
     unsigned char* tiles = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * 2 * tile_bytes);
+    float* merge_buf = reinterpret_cast<float*>(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring);
     uint64_t* empty = full + p.stages;
     float* ps_all = reinterpret_cast<float*>(empty + p.stages);
-    int* s_bid = reinterpret_cast<int*>(ps_all + n_cons * N);
+    int* s_bid = reinterpret_cast<int*>(ps_all + n_cons * QPW * kChunk);
     int* s_abort = s_bid + p.max_pages_per_split;
     int* s_issued = s_abort + 1;
 
@@ -198,7 +226,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (threadIdx.x == 0) {
         for (int st = 0; st < p.stages; ++st) {
             mbar_init(&full[st], 1);
-            mbar_init(&empty[st], n_cons);
+            mbar_init(&empty[st], per_sub);
         }
         *s_abort = 0;
         *s_issued = 0;
@@ -241,36 +269,41 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     } else {
         // ================= consumers =================
         const int c = warp - 1;
-        const int kv_local = c / p.warps_per_kv;
-        const int qh0 = (hg * HPC + kv_local) * p.group + (c % p.warps_per_kv) * QPW;
-        float* ps = ps_all + c * N;
+        const int sub = c / per_sub;          // pages i with i % WPT == sub
+        const int r = c % per_sub;            // role within one page
+        const int kv_local = r / p.warps_per_kv;
+        const int qh0 = (hg * HPC + kv_local) * p.group + (r % p.warps_per_kv) * QPW;
+        float* ps = ps_all + c * QPW * kChunk;
+        const int tq = lane / LPR;            // row of the iteration this lane reads
+        const int dl = lane % LPR;            // dims [8 dl, 8 dl + 8)
 
-        float qf[QPW][DL];
+        float2 q2[QPW][4];
 #pragma unroll
         for (int g = 0; g < QPW; ++g) {
             const T* qrow = reinterpret_cast<const T*>(p.q) + ((size_t)s * p.n_heads + qh0 + g) * D;
-            float f[DL];
-            RowLoad<D, T>::load(qrow, lane, f);
+            float2 f[4];
+            load8<T>(qrow + dl * 8, f);
 #pragma unroll
-            for (int i = 0; i < DL; ++i) qf[g][i] = f[i] * p.scale_log2;
+            for (int k = 0; k < 4; ++k)
+                q2[g][k] = make_float2(f[k].x * p.scale_log2, f[k].y * p.scale_log2);
         }
 
-        float o[QPW][DL];
+        float2 o2[QPW][4];
         float m[QPW];
 #pragma unroll
         for (int g = 0; g < QPW; ++g) {
             m[g] = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < DL; ++i) o[g][i] = 0.f;
+            for (int k = 0; k < 4; ++k) o2[g][k] = make_float2(0.f, 0.f);
         }
         float l_part = 0.f;
 
-        const int idx0 = (N >= 32) ? lane * NL : (lane >> 1);
-        const int g_own = idx0 / kChunk;
-        const bool counts = (N >= 32) || ((lane & 1) == 0);  // de-duplicate N == 16
+        const int idx0 = ((lane & (LPR - 1)) * N) / LPR;
+        const int g_own = idx0 / IPC;
+        const bool counts = (DUP == 1) || ((lane & (DUP - 1)) == 0);
         const int row_stride = HPC * D;
 
-        for (int i = 0; i < n_pages; ++i) {
+        for (int i = sub; i < n_pages; i += p.warps_per_tok) {
             const int st = i % p.stages;
             if (!mbar_wait(&full[st], (i / p.stages) & 1, p.errors)) {
                 atomicExch(s_abort, 1);
@@ -286,36 +319,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                     const int tok0 = page_tok + ch * kChunk;
                     const int valid = min(kChunk, tok_end - tok0);
                     if (valid <= 0) break;
-                    const T* kbase = sK + ((size_t)ch * kChunk * HPC + kv_local) * D;
-                    const T* vbase = sV + ((size_t)ch * kChunk * HPC + kv_local) * D;
+                    const size_t row0 = ((size_t)(ch * kChunk + tq) * HPC + kv_local) * D + dl * 8;
+                    const T* kbase = sK + row0;
+                    const T* vbase = sV + row0;
 
-                    // -- partial scores of 16 tokens x QPW heads
+                    // -- partial scores: IPC rows x QPW heads, 8 dims each
                     float acc[N];
 #pragma unroll
-                    for (int t = 0; t < kChunk; ++t) {
-                        float kf[DL];
-                        RowLoad<D, T>::load(kbase + t * row_stride, lane, kf);
+                    for (int it = 0; it < IPC; ++it) {
+                        float2 k2[4];
+                        load8<T>(kbase + it * TPI * row_stride, k2);
 #pragma unroll
                         for (int g = 0; g < QPW; ++g) {
-                            float a = qf[g][0] * kf[0];
-#pragma unroll
-                            for (int d = 1; d < DL; ++d) a = fmaf(qf[g][d], kf[d], a);
-                            acc[g * kChunk + t] = a;
+                            float2 a = __fmul2_rn(q2[g][0], k2[0]);
+                            a = __ffma2_rn(q2[g][1], k2[1], a);
+                            a = __ffma2_rn(q2[g][2], k2[2], a);
+                            a = __ffma2_rn(q2[g][3], k2[3], a);
+                            acc[g * IPC + it] = a.x + a.y;
                         }
                     }
-                    transpose_reduce<N, 16>(acc, lane);
+                    transpose_reduce<N, LPR / 2>(acc, lane);
 
                     // -- mask, chunk max per query head
-                    float r[NL];
                     float cmax = -INFINITY;
 #pragma unroll
                     for (int j = 0; j < NL; ++j) {
-                        const int t = (idx0 + j) % kChunk;
-                        r[j] = (t < valid) ? acc[j] : -INFINITY;
-                        cmax = fmaxf(cmax, r[j]);
+                        const int t = ((idx0 + j) % IPC) * TPI + tq;
+                        if (t >= valid) acc[j] = -INFINITY;
+                        cmax = fmaxf(cmax, acc[j]);
                     }
 #pragma unroll
-                    for (int off = LANES_PER_Q / 2; off >= 1; off >>= 1)
+                    for (int off = 1; off < GL; off <<= 1)
+                        cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, off));
+#pragma unroll
+                    for (int off = LPR; off < 32; off <<= 1)
                         cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, off));
 
                     float m_own = m[0];
@@ -328,7 +365,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                     float alpha_own = 1.f;
 #pragma unroll
                     for (int g = 0; g < QPW; ++g) {
-                        const float mn = __shfl_sync(0xffffffffu, mnew_own, g * LANES_PER_Q);
+                        const float mn = __shfl_sync(0xffffffffu, mnew_own, g * GL);
                         const float mu = (mn == -INFINITY) ? 0.f : mn;
                         alpha[g] = exp2f(m[g] - mu);
                         m[g] = mn;
@@ -338,39 +375,41 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                     float psum = 0.f;
 #pragma unroll
                     for (int j = 0; j < NL; ++j) {
-                        const float pj = exp2f(r[j] - mu_own);
+                        const float pj = exp2f(acc[j] - mu_own);
                         psum += pj;
-                        ps[idx0 + j] = pj;
+                        ps[g_own * kChunk + tq * IPC + (idx0 + j) % IPC] = pj;
                     }
                     l_part = l_part * alpha_own + (counts ? psum : 0.f);
 #pragma unroll
-                    for (int g = 0; g < QPW; ++g)
+                    for (int g = 0; g < QPW; ++g) {
+                        const float2 a2 = make_float2(alpha[g], alpha[g]);
 #pragma unroll
-                        for (int d = 0; d < DL; ++d) o[g][d] *= alpha[g];
+                        for (int k = 0; k < 4; ++k) o2[g][k] = __fmul2_rn(o2[g][k], a2);
+                    }
                     __syncwarp();
 
-                    // -- O += P V over the valid rows
+                    // -- O += P V over this lane's rows (rows past the context add 0)
+                    float pw[QPW][IPC];
 #pragma unroll
-                    for (int t4 = 0; t4 < kChunk; t4 += 4) {
-                        float4 pw[QPW];
+                    for (int g = 0; g < QPW; ++g)
 #pragma unroll
-                        for (int g = 0; g < QPW; ++g)
-                            pw[g] = *reinterpret_cast<const float4*>(ps + g * kChunk + t4);
+                        for (int it = 0; it < IPC; it += 4) {
+                            const float4 x = *reinterpret_cast<const float4*>(
+                                ps + g * kChunk + tq * IPC + it);
+                            pw[g][it] = x.x;
+                            pw[g][it + 1] = x.y;
+                            pw[g][it + 2] = x.z;
+                            pw[g][it + 3] = x.w;
+                        }
 #pragma unroll
-                        for (int tt = 0; tt < 4; ++tt) {
-                            if (t4 + tt < valid) {
-                                float vf[DL];
-                                RowLoad<D, T>::load(vbase + (t4 + tt) * row_stride, lane, vf);
+                    for (int it = 0; it < IPC; ++it) {
+                        float2 v2[4];
+                        load8<T>(vbase + it * TPI * row_stride, v2, it * TPI + tq < valid);
 #pragma unroll
-                                for (int g = 0; g < QPW; ++g) {
-                                    const float w = tt == 0 ? pw[g].x
-                                                  : tt == 1 ? pw[g].y
-                                                  : tt == 2 ? pw[g].z
-                                                            : pw[g].w;
+                        for (int g = 0; g < QPW; ++g) {
+                            const float2 w2 = make_float2(pw[g][it], pw[g][it]);
 #pragma unroll
-                                    for (int d = 0; d < DL; ++d) o[g][d] = fmaf(w, vf[d], o[g][d]);
-                                }
-                            }
+                            for (int k = 0; k < 4; ++k) o2[g][k] = __ffma2_rn(w2, v2[k], o2[g][k]);
                         }
                     }
                     __syncwarp();
@@ -380,26 +419,87 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             if (lane == 0) mbar_arrive(&empty[st]);
         }
 
-        // ---- epilogue: L per query head, normalise, write
+        // ---- combine the rows of the warp: O over tq, L over the head's lanes
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1)
+#pragma unroll
+            for (int g = 0; g < QPW; ++g)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o2[g][k].x += __shfl_xor_sync(0xffffffffu, o2[g][k].x, off);
+                    o2[g][k].y += __shfl_xor_sync(0xffffffffu, o2[g][k].y, off);
+                }
         float lsum = l_part;
 #pragma unroll
-        for (int off = LANES_PER_Q / 2; off >= 1; off >>= 1)
-            lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        for (int off = 1; off < GL; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
 #pragma unroll
-        for (int g = 0; g < QPW; ++g) {
-            const float lg = __shfl_sync(0xffffffffu, lsum, g * LANES_PER_Q);
-            const float inv = lg > 0.f ? 1.f / lg : 0.f;
-            float v[DL];
+        for (int off = LPR; off < 32; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        float lg[QPW];
 #pragma unroll
-            for (int d = 0; d < DL; ++d) v[d] = o[g][d] * inv;
-            const int qh = qh0 + g;
-            if (n_splits == 1) {
-                store_row<DL>(p.out, ((size_t)s * p.n_heads + qh) * D + lane * DL, p.out_dtype, v);
-            } else {
-                const size_t unit = ((size_t)s * p.n_heads + qh) * p.max_splits + split;
-                store_row<DL>(p.ws_o, unit * D + lane * DL, PKV_F32, v);
-                if (lane == 0)
-                    *reinterpret_cast<float2*>(p.ws_ml + unit * 2) = make_float2(m[g], lg);
+        for (int g = 0; g < QPW; ++g) lg[g] = __shfl_sync(0xffffffffu, lsum, g * GL);
+
+        // ---- merge the WPT warps that took turns on this kv head's pages
+        if (p.warps_per_tok > 1) {
+            consumer_sync(n_cons * 32);  // every warp is done with the ring
+            if (sub > 0) {
+                float* st = merge_buf + ((size_t)(sub - 1) * per_sub + r) * QPW * (D + 2);
+#pragma unroll
+                for (int g = 0; g < QPW; ++g) {
+                    float* e = st + g * (D + 2);
+                    if (tq == 0) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            e[2 + dl * 8 + 2 * k] = o2[g][k].x;
+                            e[2 + dl * 8 + 2 * k + 1] = o2[g][k].y;
+                        }
+                    }
+                    if (lane == 0) {
+                        e[0] = m[g];
+                        e[1] = lg[g];
+                    }
+                }
+            }
+            consumer_sync(n_cons * 32);
+            if (sub == 0) {
+                for (int w = 1; w < p.warps_per_tok; ++w) {
+                    const float* st = merge_buf + ((size_t)(w - 1) * per_sub + r) * QPW * (D + 2);
+#pragma unroll
+                    for (int g = 0; g < QPW; ++g) {
+                        const float* e = st + g * (D + 2);
+                        const float mo = e[0];
+                        const float mx = fmaxf(m[g], mo);
+                        const float mu = (mx == -INFINITY) ? 0.f : mx;
+                        const float a_self = exp2f(m[g] - mu);
+                        const float a_other = exp2f(mo - mu);
+                        lg[g] = lg[g] * a_self + e[1] * a_other;
+                        m[g] = mx;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            o2[g][k].x = o2[g][k].x * a_self + e[2 + dl * 8 + 2 * k] * a_other;
+                            o2[g][k].y = o2[g][k].y * a_self + e[2 + dl * 8 + 2 * k + 1] * a_other;
+                        }
+                    }
+                }
+            }
+        }
+
+        // ---- epilogue: normalise, write
+        if (sub == 0 && tq == 0) {
+#pragma unroll
+            for (int g = 0; g < QPW; ++g) {
+                const float inv = lg[g] > 0.f ? 1.f / lg[g] : 0.f;
+                float2 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[k] = make_float2(o2[g][k].x * inv, o2[g][k].y * inv);
+                const int qh = qh0 + g;
+                if (n_splits == 1) {
+                    store8(p.out, ((size_t)s * p.n_heads + qh) * D + dl * 8, p.out_dtype, v);
+                } else {
+                    const size_t unit = ((size_t)s * p.n_heads + qh) * p.max_splits + split;
+                    store8(p.ws_o, unit * D + dl * 8, PKV_F32, v);
+                    if (lane == 0)
+                        *reinterpret_cast<float2*>(p.ws_ml + unit * 2) = make_float2(m[g], lg[g]);
+                }
             }
         }
     }
@@ -414,6 +514,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             const int last = st + ((issued - 1 - st) / p.stages) * p.stages;
             mbar_wait(&full[st], (last / p.stages) & 1, p.errors);
         }
+    }
+}
+
+template <int DL>
+__device__ __forceinline__ void store_row(void* base, size_t elem_off, int out_dtype,
+                                          const float (&v)[DL]) {
+    if (out_dtype == PKV_F32) {
+        float* q = reinterpret_cast<float*>(base) + elem_off;
+#pragma unroll
+        for (int i = 0; i < DL; ++i) q[i] = v[i];
+    } else {
+        uint32_t* q = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(base) + elem_off);
+#pragma unroll
+        for (int i = 0; i < DL; i += 2) q[i / 2] = pack_out(v[i], v[i + 1], out_dtype);
     }
 }
 

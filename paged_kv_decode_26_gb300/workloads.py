@@ -255,12 +255,12 @@ def make_case(config: int, seed: Optional[int] = None, S: Optional[int] = None,
     return case
 
 
-def covered_rows(case: DecodeCase, lens=None) -> np.ndarray:
+def covered_rows(case: DecodeCase, lens=None, tables=None) -> np.ndarray:
     """Boolean [num_blocks, B]: True where some sequence's context (of the
-    given lengths, default the case's) covers that pool row."""
+    given lengths and tables, default the case's) covers that pool row."""
     lens = case.context_lens.numpy() if lens is None else np.asarray(lens)
     cov = np.zeros((case.num_blocks, case.B), dtype=bool)
-    bt = case.block_tables.numpy()
+    bt = case.block_tables.numpy() if tables is None else np.asarray(tables)
     for s in range(case.S):
         ns = int(lens[s])
         for j in range((ns + case.B - 1) // case.B):
@@ -277,13 +277,13 @@ def poison_pools(case: DecodeCase) -> None:
         pool[~cov] = nan
 
 
-def kv_bytes(case: DecodeCase, lens=None) -> tuple[int, int]:
+def kv_bytes(case: DecodeCase, lens=None, tables=None) -> tuple[int, int]:
     """(logical, unique) K+V bytes a decode step reads: logical counts every
     sequence's context rows; unique counts each physical pool row once."""
     lens = case.context_lens.numpy() if lens is None else np.asarray(lens)
     row = case.row_bytes()
     logical = int(np.sum(lens)) * row * 2
-    unique = int(covered_rows(case, lens).sum()) * row * 2
+    unique = int(covered_rows(case, lens, tables).sum()) * row * 2
     return logical, unique
 
 

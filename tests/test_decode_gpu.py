@@ -75,6 +75,33 @@ def test_shape_matrix(lib, D, B, H, Hk, dtype, out_dtype):
     _no_device_errors(lib)
 
 
+@pytest.mark.parametrize("env", [
+    {"PKV_DECODE_WPT": "2"},
+    {"PKV_DECODE_WPT": "2", "PKV_DECODE_STAGES": "4"},
+    {"PKV_DECODE_WPT": "4", "PKV_DECODE_HPC": "2"},
+    {"PKV_DECODE_HPC": "1", "PKV_DECODE_STAGES": "6"},
+    {"PKV_DECODE_HPC": "2", "PKV_DECODE_STAGES": "2"},
+    {"PKV_DECODE_QPW": "2"},
+    {"PKV_DECODE_QPW": "1", "PKV_DECODE_HPC": "2"},
+], ids=lambda e: ",".join(f"{k[11:]}={v}" for k, v in e.items()))
+@pytest.mark.parametrize("config", [1, 2, 3, 4])
+def test_launch_configurations(lib, monkeypatch, config, env):
+    """Every tuning choice of the launch (kv heads per CTA, ring depth, warps
+    taking turns on pages, query heads per warp) computes the same result."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    case = wl.make_case(config, poison=True, **SMALL[config])
+    for split in (0, 2 * case.B * 4):
+        try:
+            got = run_decode(case, split_tokens=split)
+        except lib.PagedKVError as e:
+            # a combination whose ring does not fit in shared memory is refused
+            assert e.status == 2 and "shared memory" in str(e)
+            pytest.skip(f"{env} does not fit: {e}")
+        assert_attention_close(got, _oracle(case), case.out_dtype, f"{env} split {split}")
+    _no_device_errors(lib)
+
+
 def test_split_invariance(lib):
     case = wl.make_case(2, S=4, lens=("uniform", 900, 2000), out_dtype=torch.float32)
     outs = [run_decode(case, split_tokens=s) for s in (16, 48, 256, 1024, 2048)]
