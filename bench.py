@@ -60,6 +60,8 @@ def parse_args():
                     help="replay each step as one CUDA graph")
     ap.add_argument("--replicas", type=int, default=1,
                     help="independent copies of the workload (own pools) per GPU, one graph")
+    ap.add_argument("--graph-streams", type=int, default=32,
+                    help="parallel branches of the replica graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
@@ -345,10 +347,8 @@ def main():
                               case.scale, r["max_ctx"], split_tokens=args.split, workspace=r["ws"])
 
     def swaps(r):
-        pkv.swap_blocks(r["k_pool"], r["k_pool"], r["d2d"])
-        pkv.swap_blocks(r["v_pool"], r["v_pool"], r["d2d"])
-        pkv.swap_blocks(r["k_pool"], r["hk"], r["h2d"])
-        pkv.swap_blocks(r["v_pool"], r["hv"], r["h2d"])
+        pkv.swap_blocks_kv(r["k_pool"], r["v_pool"], r["k_pool"], r["v_pool"], r["d2d"])
+        pkv.swap_blocks_kv(r["k_pool"], r["v_pool"], r["hk"], r["hv"], r["h2d"])
 
     def step_eager():
         for r in reps:
@@ -374,7 +374,7 @@ def main():
         split_r = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B,
                                                         r["max_ctx"])
         launches_per_step += 2 + (1 if (r["max_ctx"] + split_r - 1) // split_r > 1 else 0) + \
-            (4 if with_swaps else 0)
+            (2 if with_swaps else 0)
     split_used = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B,
                                                        reps[0]["max_ctx"])
     decode_alg_bytes = kv_unique + io_bytes       # shared prefix rows counted once
@@ -396,12 +396,36 @@ def main():
         step_eager()
     torch.cuda.synchronize()
 
+    def fan_out(body):
+        """Capture body(r) for every replica on `graph_streams` parallel
+        branches (independent replicas need no ordering between them)."""
+        cap = torch.cuda.current_stream()
+        n_br = max(1, min(args.graph_streams, R))
+        branches = [torch.cuda.Stream() for _ in range(n_br)]
+        fork = torch.cuda.Event()
+        fork.record(cap)
+        for b in branches:
+            b.wait_event(fork)
+        for i, r in enumerate(reps):
+            with torch.cuda.stream(branches[i % n_br]):
+                body(r)
+        for b in branches:
+            join = torch.cuda.Event()
+            join.record(b)
+            cap.wait_event(join)
+
+    def step_one(r):
+        pkv.kv_append(r["k_pool"], r["v_pool"], r["k_new"], r["v_new"], r["slots"])
+        decode(r)
+        if with_swaps:
+            swaps(r)
+
     if use_graph:
         g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_step):
-            step_eager()
+            fan_out(step_one)
         with torch.cuda.graph(g_dec):
-            decode_eager()
+            fan_out(decode)
         run_step, run_decode = g_step.replay, g_dec.replay
         for _ in range(3):
             run_step()
@@ -466,7 +490,7 @@ def main():
     swap = None
     if with_swaps and rank == 0:
         r0 = reps[0]
-        d2d_t, h2d_t, d2d_ref_t, h2d_ref_t = [], [], [], []
+        d2d_t, h2d_t, d2d_ref_t, h2d_ref_t, d2d_two_t = [], [], [], [], []
         n_ref_d2d, n_ref_h2d = n_d2d * bb, n_h2d * bb
         src_d = torch.empty(n_ref_d2d, dtype=torch.uint8, device=dev)
         dst_d = torch.empty(n_ref_d2d, dtype=torch.uint8, device=dev)
@@ -474,10 +498,12 @@ def main():
         dst_h = torch.empty(n_ref_h2d, dtype=torch.uint8, device=dev)
         for i in range(max(20, min(args.steps, 200))):
             for fn, acc in (
+                    (lambda: pkv.swap_blocks_kv(r0["k_pool"], r0["v_pool"], r0["k_pool"],
+                                                r0["v_pool"], r0["d2d"]), d2d_t),
                     (lambda: (pkv.swap_blocks(r0["k_pool"], r0["k_pool"], r0["d2d"]),
-                              pkv.swap_blocks(r0["v_pool"], r0["v_pool"], r0["d2d"])), d2d_t),
-                    (lambda: (pkv.swap_blocks(r0["k_pool"], r0["hk"], r0["h2d"]),
-                              pkv.swap_blocks(r0["v_pool"], r0["hv"], r0["h2d"])), h2d_t),
+                              pkv.swap_blocks(r0["v_pool"], r0["v_pool"], r0["d2d"])), d2d_two_t),
+                    (lambda: pkv.swap_blocks_kv(r0["k_pool"], r0["v_pool"], r0["hk"], r0["hv"],
+                                                r0["h2d"]), h2d_t),
                     (lambda: (dst_d.copy_(src_d, non_blocking=True),
                               dst_d.copy_(src_d, non_blocking=True)), d2d_ref_t),
                     (lambda: (dst_h.copy_(src_h, non_blocking=True),
@@ -499,12 +525,14 @@ def main():
                     "vs_measured_copy_peak": 2 * moved_d2d / (d2d_ms / 1e3) / 1e9 / peak_copy,
                     "contiguous_copy_same_bytes_gbs_read_write":
                         2 * moved_d2d / (d2d_ref_ms / 1e3) / 1e9,
-                    "vs_contiguous_copy": d2d_ref_ms / d2d_ms},
+                    "vs_contiguous_copy": d2d_ref_ms / d2d_ms,
+                    "ms_two_calls_swap_blocks": statistics.median(d2d_two_t)},
             "h2d": {"pairs": n_h2d, "ms_k_and_v": h2d_ms,
                     "gbs": moved_h2d / (h2d_ms / 1e3) / 1e9,
                     "memcpy_h2d_same_bytes_gbs": moved_h2d / (h2d_ref_ms / 1e3) / 1e9,
                     "vs_memcpy": h2d_ref_ms / h2d_ms},
-            "timing": "median of per-call CUDA events, L2 flushed before each",
+            "timing": "median of per-call CUDA events, L2 flushed before each; "
+                      "K and V in one swap_blocks_kv launch",
         }
 
     # ---- end to end through the public API with host buffers
@@ -581,7 +609,8 @@ def main():
             "step": "kv_append (1 token/seq) + paged_attn_decode" +
                     (" + swap_blocks D2D and pinned-H2D (K and V)" if with_swaps else ""),
             "replicas_per_gpu": R,
-            "launch": "one CUDA graph per step over all replicas" if use_graph else "eager",
+            "launch": (f"one CUDA graph per step, replicas on {min(args.graph_streams, R)} "
+                       "parallel branches" if use_graph else "eager"),
             "num_seqs_per_gpu": R * S,
             "kv_bytes_per_step_per_gpu": kv_read,
             "kv_unique_bytes_per_step_per_gpu": kv_unique,

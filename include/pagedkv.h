@@ -219,6 +219,18 @@ PKV_API pkv_status swap_blocks(void* dst_pool, const void* src_pool, size_t bloc
                                int64_t num_dst_blocks, void* stream);
 
 /*
+ * swap_blocks_kv -- swap_blocks on the Key and the Value cache in one
+ * launch, with the same pairs: [SWAP] swap_blocks takes the whole KV cache
+ * (src_kv_cache, dst_kv_cache) and [OPT] "Swap Blocks 机制" copies its Key
+ * half and its Value half with the same src_to_dst map.  Same arguments,
+ * rules and errors as swap_blocks, for two pools of equal block size.
+ */
+PKV_API pkv_status swap_blocks_kv(void* dst_k, void* dst_v, const void* src_k,
+                                  const void* src_v, size_t block_bytes, const int64_t* pairs,
+                                  int n_pairs, int64_t num_src_blocks, int64_t num_dst_blocks,
+                                  void* stream);
+
+/*
  * Host-side physical block manager ([LAYOUT] section 三 KVBlockManager):
  * a pool of num_blocks ids with reference counts.  allocate() hands out the
  * lowest free id and sets its count to 1; free() decrements a held block's

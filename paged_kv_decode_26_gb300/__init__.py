@@ -6,9 +6,9 @@ binding with the same entry-point names, and the seeded workload generator.
 """
 from .api import (BlockManager, alloc_decode_workspace, decode_split_tokens,
                   decode_workspace_bytes, device_errors, kv_append, paged_attn_decode,
-                  swap_blocks)
+                  swap_blocks, swap_blocks_kv)
 from ._lib import PagedKVError, lib
 
-__all__ = ["paged_attn_decode", "kv_append", "swap_blocks", "decode_workspace_bytes",
+__all__ = ["paged_attn_decode", "kv_append", "swap_blocks", "swap_blocks_kv", "decode_workspace_bytes",
            "decode_split_tokens", "alloc_decode_workspace", "device_errors", "BlockManager",
            "PagedKVError", "lib"]

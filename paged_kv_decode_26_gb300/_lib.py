@@ -37,6 +37,7 @@ SIGNATURES = {
                                        _i, _f, _i, _i, _p]),
     "kv_append": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _p]),
     "swap_blocks": (_i, [_p, _p, _sz, _p, _i, _i64, _i64, _p]),
+    "swap_blocks_kv": (_i, [_p, _p, _p, _p, _sz, _p, _i, _i64, _i64, _p]),
     "pkv_block_manager_create": (_p, [_i, _i]),
     "pkv_block_manager_create_with_free": (_p, [_i, _i, _p, _i]),
     "pkv_block_manager_destroy": (None, [_p]),

@@ -128,6 +128,29 @@ def swap_blocks(dst_pool: torch.Tensor, src_pool: torch.Tensor, pairs: torch.Ten
     check(st, "swap_blocks")
 
 
+def swap_blocks_kv(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor,
+                   src_v: torch.Tensor, pairs: torch.Tensor,
+                   stream: Optional[torch.cuda.Stream] = None) -> None:
+    """swap_blocks on the Key and the Value cache in one launch (same pairs)."""
+    for name, t in (("dst_k", dst_k), ("dst_v", dst_v)):
+        _need_cuda(name, t)
+    for name, t in (("src_k", src_k), ("src_v", src_v), ("pairs", pairs)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if pairs.dtype != torch.int64 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int64 [n, 2]")
+    if dst_k.shape != dst_v.shape or src_k.shape != src_v.shape:
+        raise ValueError("Key and Value pools must have the same shapes")
+    bb = dst_k[0].numel() * dst_k.element_size() if dst_k.shape[0] else 0
+    if src_k.shape[0] and src_k[0].numel() * src_k.element_size() != bb:
+        raise ValueError("source and destination blocks differ in size")
+    st = lib().swap_blocks_kv(_ptr(dst_k), _ptr(dst_v), _ptr(src_k), _ptr(src_v), bb, _ptr(pairs),
+                              pairs.shape[0], src_k.shape[0], dst_k.shape[0], _stream_ptr(stream))
+    check(st, "swap_blocks_kv")
+
+
 def device_errors(clear: bool = True) -> int:
     """PKV_DEVERR_* bits raised by kernels on the current device (synchronises)."""
     v = C.c_uint32(0)

@@ -479,25 +479,59 @@ PKV_API pkv_status kv_append(void* k_pool, void* v_pool, const void* k_new, cons
     return PKV_OK;
 }
 
-PKV_API pkv_status swap_blocks(void* dst_pool, const void* src_pool, size_t block_bytes,
-                               const int64_t* pairs, int n_pairs, int64_t num_src_blocks,
-                               int64_t num_dst_blocks, void* stream) {
+}  // extern "C"
+
+namespace {
+
+pkv_status launch_swap(void* const* dst_pools, const void* const* src_pools, int n_pools,
+                       size_t block_bytes, const int64_t* pairs, int n_pairs,
+                       int64_t num_src_blocks, int64_t num_dst_blocks, void* stream) {
     if (n_pairs < 0 || num_src_blocks < 0 || num_dst_blocks < 0) return invalid("sizes");
-    if (block_bytes == 0 || block_bytes % 16) return invalid("block_bytes must be a positive multiple of 16");
+    if (block_bytes == 0 || block_bytes % 16)
+        return invalid("block_bytes must be a positive multiple of 16");
     if (n_pairs == 0) return PKV_OK;
-    if (!dst_pool || !src_pool || !pairs) return invalid("NULL pointer");
-    if (!aligned16(dst_pool) || !aligned16(src_pool)) return invalid("pools must be 16-byte aligned");
+    if (!pairs) return invalid("NULL pointer");
+    pkv::SwapPools pools;
+    for (int k = 0; k < n_pools; ++k) {
+        if (!dst_pools[k] || !src_pools[k]) return invalid("NULL pointer");
+        if (!aligned16(dst_pools[k]) || !aligned16(src_pools[k]))
+            return invalid("pools must be 16-byte aligned");
+        pools.dst[k] = static_cast<uint4*>(dst_pools[k]);
+        pools.src[k] = static_cast<const uint4*>(src_pools[k]);
+    }
     if (((uintptr_t)pairs & 7) != 0) return invalid("pairs must be 8-byte aligned");
     DeviceInfo* dev = nullptr;
     cudaError_t e = device_info(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    const unsigned grid = (unsigned)std::min<long long>(n_pairs, 1LL << 20);
+    const dim3 grid((unsigned)std::min<long long>(n_pairs, 1LL << 20), (unsigned)n_pools);
     pkv::swap_blocks_kernel<<<grid, pkv::kSwapThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint4*>(dst_pool), static_cast<const uint4*>(src_pool),
-        (int64_t)(block_bytes / 16), pairs, n_pairs, num_src_blocks, num_dst_blocks,
+        pools, (int64_t)(block_bytes / 16), pairs, n_pairs, num_src_blocks, num_dst_blocks,
         dev->errors);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+PKV_API pkv_status swap_blocks(void* dst_pool, const void* src_pool, size_t block_bytes,
+                               const int64_t* pairs, int n_pairs, int64_t num_src_blocks,
+                               int64_t num_dst_blocks, void* stream) {
+    void* dst[1] = {dst_pool};
+    const void* src[1] = {src_pool};
+    return launch_swap(dst, src, 1, block_bytes, pairs, n_pairs, num_src_blocks, num_dst_blocks,
+                       stream);
+}
+
+PKV_API pkv_status swap_blocks_kv(void* dst_k, void* dst_v, const void* src_k,
+                                  const void* src_v, size_t block_bytes, const int64_t* pairs,
+                                  int n_pairs, int64_t num_src_blocks, int64_t num_dst_blocks,
+                                  void* stream) {
+    void* dst[2] = {dst_k, dst_v};
+    const void* src[2] = {src_k, src_v};
+    return launch_swap(dst, src, 2, block_bytes, pairs, n_pairs, num_src_blocks, num_dst_blocks,
+                       stream);
 }
 
 }  // extern "C"

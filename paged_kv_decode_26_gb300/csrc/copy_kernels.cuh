@@ -47,18 +47,28 @@ __global__ void __launch_bounds__(256)
 constexpr int kSwapThreads = 256;
 constexpr int kSwapUnroll = 8;
 
-// One CTA per pair (grid-strided), each thread moving up to kSwapUnroll
-// 16-byte vectors per round with all loads issued before the stores.
+// Up to two caches (Key and Value) copied by one launch with the same pairs.
+struct SwapPools {
+    uint4* dst[2];
+    const uint4* src[2];
+};
+
+// One CTA per (pair, cache) (grid-strided over pairs, blockIdx.y = cache),
+// each thread moving up to kSwapUnroll 16-byte vectors per round with all
+// loads issued before the stores.  The data is touched once: loads and
+// stores use the streaming (evict-first) cache policy.
 __global__ void __launch_bounds__(kSwapThreads)
-    swap_blocks_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t block_vec,
+    swap_blocks_kernel(const SwapPools pools, int64_t block_vec,
                        const int64_t* __restrict__ pairs, int n_pairs, int64_t num_src,
                        int64_t num_dst, unsigned int* errors) {
+    uint4* __restrict__ dst = pools.dst[blockIdx.y];
+    const uint4* __restrict__ src = pools.src[blockIdx.y];
     for (int k = blockIdx.x; k < n_pairs; k += gridDim.x) {
         const int64_t i = pairs[2 * (int64_t)k];
         const int64_t j = pairs[2 * (int64_t)k + 1];
         if (i < 0 || j < 0) continue;
         if (i >= num_src || j >= num_dst) {
-            if (threadIdx.x == 0) raise_error(errors, PKV_DEVERR_PAIR);
+            if (threadIdx.x == 0 && blockIdx.y == 0) raise_error(errors, PKV_DEVERR_PAIR);
             continue;
         }
         const uint4* s = src + i * block_vec;
@@ -68,12 +78,12 @@ __global__ void __launch_bounds__(kSwapThreads)
 #pragma unroll
             for (int u = 0; u < kSwapUnroll; ++u) {
                 const int64_t e = base + (int64_t)u * kSwapThreads + threadIdx.x;
-                if (e < block_vec) r[u] = s[e];
+                if (e < block_vec) r[u] = __ldcs(s + e);
             }
 #pragma unroll
             for (int u = 0; u < kSwapUnroll; ++u) {
                 const int64_t e = base + (int64_t)u * kSwapThreads + threadIdx.x;
-                if (e < block_vec) d[e] = r[u];
+                if (e < block_vec) __stcs(d + e, r[u]);
             }
         }
     }

@@ -85,6 +85,29 @@ def test_swap_from_pinned_host(lib):
     assert lib.device_errors() == 0
 
 
+@pytest.mark.parametrize("pinned_source", [False, True])
+def test_swap_kv_one_launch_matches_two_calls(lib, pinned_source):
+    case = wl.make_case(5, S=8, lens=("uniform", 16, 64), d2d_pairs=4, h2d_pairs=40,
+                        host_pool_blocks=64)
+    pairs = case.h2d_pairs.clone()
+    pairs[7, 0] = -1                           # a skipped pair
+    if pinned_source:
+        sk, sv, pr = case.host_k_pool.pin_memory(), case.host_v_pool.pin_memory(), pairs.pin_memory()
+    else:
+        sk, sv, pr = case.host_k_pool.cuda(), case.host_v_pool.cuda(), pairs.cuda()
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    lib.swap_blocks_kv(dk, dv, sk, sv, pr)
+    rk, rv = case.k_pool.clone(), case.v_pool.clone()
+    orc.swap_blocks(rk, case.host_k_pool, pairs)
+    orc.swap_blocks(rv, case.host_v_pool, pairs)
+    assert torch.equal(_bits(dk.cpu()), _bits(rk)) and torch.equal(_bits(dv.cpu()), _bits(rv))
+    assert lib.device_errors() == 0
+    bad = pairs.clone()
+    bad[0, 1] = case.num_blocks                # destination past the pool
+    lib.swap_blocks_kv(dk, dv, sk, sv, bad.cuda() if not pinned_source else bad.pin_memory())
+    assert lib.device_errors() & 0x8
+
+
 def test_append_matches_oracle_and_flags_bad_slots(lib):
     case = wl.make_case(5, S=40, lens=("uniform", 1, 70), d2d_pairs=4, h2d_pairs=4,
                         host_pool_blocks=8)
@@ -138,8 +161,7 @@ def _continuous_step(lib, case):
     lib.swap_blocks(dv, dv, d2d)
     hk, hv = case.host_k_pool.pin_memory(), case.host_v_pool.pin_memory()
     h2d = case.h2d_pairs.pin_memory()
-    lib.swap_blocks(dk, hk, h2d)
-    lib.swap_blocks(dv, hv, h2d)
+    lib.swap_blocks_kv(dk, dv, hk, hv, h2d)
     torch.cuda.synchronize()
     return bt, lens, slots, out, dk.cpu(), dv.cpu()
 
