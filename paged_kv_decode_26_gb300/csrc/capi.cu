@@ -106,6 +106,7 @@ int env_int(const char* name, int fallback) {
 // ------------------------------------------------------ decode configuration
 
 struct DecodeConfig {
+    bool mma;    // tensor-core consumer (one warp per kv head, all its query heads)
     int qpw;     // query heads per consumer warp
     int wpk;     // consumer warps per kv head, splitting its query heads
     int wpt;     // consumer warps per kv head, taking turns on its pages
@@ -137,6 +138,24 @@ bool supported_shape(int n_heads, int n_kv_heads, int head_dim, int block_size) 
 // _STAGES, _WPT and _QPW override the choice (for tuning sweeps).
 void shape_config(int n_heads, int n_kv_heads, int head_dim, int block_size, DecodeConfig* c) {
     const int G = n_heads / n_kv_heads;
+    // Groups of four or more query heads per kv head make each page a small
+    // dense contraction: the tensor-core consumer takes them.
+    c->mma = env_int("PKV_DECODE_MMA", G >= 4 ? 1 : 0) != 0 && G >= 2;
+    if (c->mma) {
+        c->qpw = G;
+        c->wpk = 1;
+        c->wpt = 1;
+        int target = env_int("PKV_DECODE_HPC", 512 / head_dim);
+        if (target < 1) target = 1;
+        int hpc = 1;
+        for (int h = 1; h <= n_kv_heads; ++h)
+            if (n_kv_heads % h == 0 && h <= target && h <= pkv::kMmaMaxWarps) hpc = h;
+        c->hpc = hpc;
+        const int stages = env_int("PKV_DECODE_STAGES", 3);
+        c->stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+        c->threads = 32 * (1 + c->hpc);
+        return;
+    }
     int qpw = env_int("PKV_DECODE_QPW", G < 4 ? G : 4);
     if (qpw < 1 || qpw > 4 || (qpw & (qpw - 1)) || G % qpw) qpw = G < 4 ? G : 4;
     c->qpw = qpw;
@@ -197,8 +216,10 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
                          split_tokens;
     c->max_splits = ms < 1 ? 1 : (int)ms;
     c->max_pages = split_tokens / block_size;
-    c->smem = pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc, c->wpk, c->wpt,
-                                     c->stages, c->max_pages);
+    c->smem = c->mma ? pkv::decode_mma_smem_bytes(head_dim, block_size, 2, c->hpc, c->stages,
+                                                  c->max_pages)
+                     : pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc, c->wpk,
+                                              c->wpt, c->stages, c->max_pages);
     return PKV_OK;
 }
 
@@ -214,21 +235,29 @@ size_t workspace_bytes_for(int num_seqs, int n_heads, int head_dim, const Decode
     return o_bytes + units * 2 * sizeof(float);
 }
 
+// The pool [num_blocks, B, Hk, D] as a 4-D tensor for TMA.
+//   CUDA-core path: dims (D, Hk, B, blocks), box (D, hpc, B, 1): one page of
+//     hpc heads lands as [B][hpc][D], rows unswizzled.
+//   Tensor-core path: dims (64, Hk*D/64, B, blocks), box (64, 1, B, 1) with
+//     128-byte swizzle: one 64-element half of one head's page per load,
+//     landing as [B][64] with each 128-byte row's 16-byte chunks permuted.
 cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, pkv_dtype dt, int num_blocks,
-                            int block_size, int n_kv_heads, int head_dim, int hpc) {
+                            int block_size, int n_kv_heads, int head_dim, int hpc, bool mma) {
     auto encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t es = 2;
-    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)n_kv_heads, (cuuint64_t)block_size,
-                          (cuuint64_t)num_blocks};
-    cuuint64_t strides[3] = {head_dim * es, (cuuint64_t)n_kv_heads * head_dim * es,
+    const cuuint64_t inner = mma ? 64 : (cuuint64_t)head_dim;
+    const cuuint64_t rows = mma ? (cuuint64_t)n_kv_heads * head_dim / 64 : (cuuint64_t)n_kv_heads;
+    cuuint64_t dims[4] = {inner, rows, (cuuint64_t)block_size, (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {inner * es, (cuuint64_t)n_kv_heads * head_dim * es,
                              (cuuint64_t)block_size * n_kv_heads * head_dim * es};
-    cuuint32_t box[4] = {(cuuint32_t)head_dim, (cuuint32_t)hpc, (cuuint32_t)block_size, 1};
+    cuuint32_t box[4] = {(cuuint32_t)inner, mma ? 1u : (cuuint32_t)hpc, (cuuint32_t)block_size, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = encode(map, dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         4, const_cast<void*>(pool), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        mma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -375,10 +404,10 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
     const void* vmap_base = num_blocks > 0 ? v_pool : q;
     const int map_blocks = num_blocks > 0 ? num_blocks : 1;
     if ((e = encode_pool_map(&L.tm_k, kmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
-                             head_dim, c.hpc)) != cudaSuccess)
+                             head_dim, c.hpc, c.mma)) != cudaSuccess)
         return cuda_fail(e);
     if ((e = encode_pool_map(&L.tm_v, vmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
-                             head_dim, c.hpc)) != cudaSuccess)
+                             head_dim, c.hpc, c.mma)) != cudaSuccess)
         return cuda_fail(e);
 
     pkv::DecodeParams& p = L.p;
@@ -411,8 +440,12 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
     L.stream = static_cast<cudaStream_t>(stream);
     if (c.max_splits > 65535 * 1024) return unsupported("context too long for the grid");
 
-    e = kv_dtype == PKV_BF16 ? pkv::launch_decode_bf16(head_dim, block_size, c.qpw, L)
-                             : pkv::launch_decode_f16(head_dim, block_size, c.qpw, L);
+    if (c.mma)
+        e = kv_dtype == PKV_BF16 ? pkv::launch_decode_mma_bf16(head_dim, block_size, L)
+                                 : pkv::launch_decode_mma_f16(head_dim, block_size, L);
+    else
+        e = kv_dtype == PKV_BF16 ? pkv::launch_decode_bf16(head_dim, block_size, c.qpw, L)
+                                 : pkv::launch_decode_f16(head_dim, block_size, c.qpw, L);
     if (e != cudaSuccess) return cuda_fail(e);
 
     if (c.max_splits > 1) {

@@ -1,4 +1,5 @@
 // decode_f16.cu -- decode kernel instances for fp16 query / K / V.
 #define PKV_ELEM __half
 #define PKV_FN launch_decode_f16
+#define PKV_MMA_FN launch_decode_mma_f16
 #include "decode_inst.inc"

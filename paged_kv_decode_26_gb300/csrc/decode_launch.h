@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "decode_kernel.cuh"
+#include "decode_mma_kernel.cuh"
 
 namespace pkv {
 
@@ -23,6 +23,9 @@ struct DecodeLaunch {
 // Returns cudaErrorInvalidValue for a combination that is not compiled.
 cudaError_t launch_decode_bf16(int D, int BS, int QPW, const DecodeLaunch& L);
 cudaError_t launch_decode_f16(int D, int BS, int QPW, const DecodeLaunch& L);
+// Launch paged_decode_mma_kernel<D, BS, T> (tensor-core path for query-head groups).
+cudaError_t launch_decode_mma_bf16(int D, int BS, const DecodeLaunch& L);
+cudaError_t launch_decode_mma_f16(int D, int BS, const DecodeLaunch& L);
 
 // Raise a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask, size_t bytes);

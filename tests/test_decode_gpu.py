@@ -83,6 +83,8 @@ def test_shape_matrix(lib, D, B, H, Hk, dtype, out_dtype):
     {"PKV_DECODE_HPC": "2", "PKV_DECODE_STAGES": "2"},
     {"PKV_DECODE_QPW": "2"},
     {"PKV_DECODE_QPW": "1", "PKV_DECODE_HPC": "2"},
+    {"PKV_DECODE_MMA": "0"},
+    {"PKV_DECODE_MMA": "1", "PKV_DECODE_HPC": "2", "PKV_DECODE_STAGES": "4"},
 ], ids=lambda e: ",".join(f"{k[11:]}={v}" for k, v in e.items()))
 @pytest.mark.parametrize("config", [1, 2, 3, 4])
 def test_launch_configurations(lib, monkeypatch, config, env):
@@ -99,6 +101,23 @@ def test_launch_configurations(lib, monkeypatch, config, env):
             assert e.status == 2 and "shared memory" in str(e)
             pytest.skip(f"{env} does not fit: {e}")
         assert_attention_close(got, _oracle(case), case.out_dtype, f"{env} split {split}")
+    _no_device_errors(lib)
+
+
+@pytest.mark.parametrize("mma", ["0", "1"])
+@pytest.mark.parametrize("D,B", [(64, 16), (128, 16), (64, 32), (128, 32)])
+@pytest.mark.parametrize("H,Hk", [(8, 4), (16, 4), (32, 4)])
+@pytest.mark.parametrize("dtype,out_dtype", [(torch.bfloat16, torch.bfloat16),
+                                             (torch.float16, torch.float32)])
+def test_grouped_heads_both_paths(lib, monkeypatch, mma, D, B, H, Hk, dtype, out_dtype):
+    """Query-head groups of 2, 4 and 8 on the CUDA-core and the tensor-core
+    consumer, ragged tails and NaN padding included."""
+    monkeypatch.setenv("PKV_DECODE_MMA", mma)
+    case = wl.make_case(3, S=4, lens=("uniform", 1, 400), H=H, Hk=Hk, D=D, B=B, dtype=dtype,
+                        out_dtype=out_dtype, share_blocks=2, poison=True, seed=H + D + B)
+    for split in (0, 2 * B):
+        got = run_decode(case, split_tokens=split)
+        assert_attention_close(got, _oracle(case), out_dtype, f"mma={mma} split {split}")
     _no_device_errors(lib)
 
 
