@@ -247,6 +247,28 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- multi-rank helpers
+
+def rank_seed(config: int, rank: int, replica: int = 0) -> int:
+    """Seed of one rank's replica: every rank decodes its own sequences."""
+    return (config - 1) + 1000 * rank + 7919 * replica
+
+
+def reduce_over_ranks(values, op: str, dist, world: int, device):
+    """Element-wise max or sum of a list of floats over all ranks."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(total_bytes: float, ms: float) -> float:
+    """Whole-job throughput: bytes of all ranks over the slowest rank's time."""
+    return total_bytes / (ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------------ ours
 
 def build_replicas(args, rank, dev, pkv, wl, torch, np):
@@ -259,7 +281,7 @@ def build_replicas(args, rank, dev, pkv, wl, torch, np):
         extra["S"] = args.seqs
     reps = []
     for r in range(R):
-        seed = (args.config - 1) + 1000 * rank + 7919 * r
+        seed = rank_seed(args.config, rank, r)
         case = wl.make_case(args.config, seed=seed, **extra)
         S = case.S
         bm = pkv.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)
@@ -478,10 +500,8 @@ def main():
     torch.cuda.synchronize()
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_events)
 
-    if world > 1:
-        t = torch.tensor([ms, dec_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, dec_ms = float(t[0]), float(t[1])
+    ms, dec_ms = reduce_over_ranks([ms, dec_ms], "max", dist, world, dev)
+    total_kv, = reduce_over_ranks([kv_read], "sum", dist, world, dev)
     errors = pkv.device_errors(clear=True)
     if errors:
         raise RuntimeError(f"device error flags 0x{errors:x} raised during the benchmark")
@@ -563,10 +583,7 @@ def main():
         torch.cuda.synchronize()
         e2e_times.append(a.elapsed_time(b))
     e2e_ms = statistics.mean(e2e_times)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms, = reduce_over_ranks([e2e_ms], "max", dist, world, dev)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
     cpu = None
@@ -586,8 +603,7 @@ def main():
 
     peak, peak_kind = measured_peak()
     name = workload_name(case, args.config)
-    total_kv = kv_read * world
-    value = total_kv / (ms / 1e3) / 1e9
+    value = job_gbs(total_kv, ms)
     achieved = decode_alg_bytes / (dec_ms / 1e3) / 1e9
     logical_gbs = (kv_read + io_bytes) / (dec_ms / 1e3) / 1e9
     line = {
@@ -604,6 +620,7 @@ def main():
         "dtype": "f32",
         "data": "synthetic",
         "seq_steps_per_s": R * S * world / (ms / 1e3),
+        "kv_bytes_per_step_all_gpus": total_kv,
         "config": {
             "workload": name,
             "step": "kv_append (1 token/seq) + paged_attn_decode" +
@@ -639,7 +656,7 @@ def main():
             else "fallback 6.8 TB/s",
         },
         "clocks": clocks,
-        "e2e": {"value": total_kv / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_gbs(total_kv, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                 "ms_per_step": e2e_ms, "steps": n_e2e},
         "gpu_launches": launches_per_step * args.steps,

@@ -8,6 +8,7 @@ tensors (or numpy arrays) in their storage dtype; the C code decodes the
 from __future__ import annotations
 
 import ctypes as C
+import os
 
 import numpy as np
 import torch
@@ -28,7 +29,9 @@ _d = C.c_double
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
+        # PKV_ORACLE_LIB points the oracle at another build of the same C
+        # source (the mutation tests use it to plant mistakes).
+        path = os.environ.get("PKV_ORACLE_LIB") or _build.build()
         L = C.CDLL(path)
         L.orc_f16_bits_to_double.restype = _d
         L.orc_f16_bits_to_double.argtypes = [C.c_uint16]
