@@ -372,12 +372,28 @@ def main():
         pkv.swap_blocks_kv(r["k_pool"], r["v_pool"], r["k_pool"], r["v_pool"], r["d2d"])
         pkv.swap_blocks_kv(r["k_pool"], r["v_pool"], r["hk"], r["hv"], r["h2d"])
 
+    # The block copies of the continuous-batching step touch only blocks
+    # that neither the append nor the decode uses (free targets, read-only
+    # sources), so they run on a side stream, overlapped with the decode.
+    side = torch.cuda.Stream() if with_swaps else None
+
+    def step_one(r):
+        if with_swaps:
+            fork = torch.cuda.Event()
+            fork.record(torch.cuda.current_stream())
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                swaps(r)
+        pkv.kv_append(r["k_pool"], r["v_pool"], r["k_new"], r["v_new"], r["slots"])
+        decode(r)
+        if with_swaps:
+            join = torch.cuda.Event()
+            join.record(side)
+            torch.cuda.current_stream().wait_event(join)
+
     def step_eager():
         for r in reps:
-            pkv.kv_append(r["k_pool"], r["v_pool"], r["k_new"], r["v_new"], r["slots"])
-            decode(r)
-            if with_swaps:
-                swaps(r)
+            step_one(r)
 
     def decode_eager():
         for r in reps:
@@ -435,12 +451,6 @@ def main():
             join = torch.cuda.Event()
             join.record(b)
             cap.wait_event(join)
-
-    def step_one(r):
-        pkv.kv_append(r["k_pool"], r["v_pool"], r["k_new"], r["v_new"], r["slots"])
-        decode(r)
-        if with_swaps:
-            swaps(r)
 
     if use_graph:
         g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
@@ -624,7 +634,8 @@ def main():
         "config": {
             "workload": name,
             "step": "kv_append (1 token/seq) + paged_attn_decode" +
-                    (" + swap_blocks D2D and pinned-H2D (K and V)" if with_swaps else ""),
+                    (" + swap_blocks_kv D2D and pinned-H2D on a side stream, overlapped"
+                     if with_swaps else ""),
             "replicas_per_gpu": R,
             "launch": (f"one CUDA graph per step, replicas on {min(args.graph_streams, R)} "
                        "parallel branches" if use_graph else "eager"),

@@ -278,6 +278,26 @@ PKV_API pkv_status pkv_append_slots(pkv_block_manager* mgr, int32_t* block_table
                                     int max_blocks_per_seq, int32_t* context_lens, int num_seqs,
                                     int64_t* slot_mapping);
 
+/*
+ * pkv_append_slots_cow -- pkv_append_slots with copy-on-write ([LAYOUT]
+ * section 四.2: requests that share a prompt point at the same physical
+ * blocks, and only a request that writes its own next token into a shared
+ * block gets a private copy of it).  For a sequence whose token lands in an
+ * existing block with reference count > 1, a block is allocated, the
+ * sequence's reference to the shared block is dropped, the table is
+ * repointed and the pair (shared, private) is appended to copy_pairs.
+ * The caller copies those pairs (swap_blocks / swap_blocks_kv) before
+ * kv_append writes the new tokens.
+ *   copy_pairs   host int64 [num_seqs, 2], written (n_copy_pairs rows used)
+ *   n_copy_pairs host int, written
+ * Other arguments, updates and errors as pkv_append_slots; a table entry
+ * outside the pool gives slot -1 and PKV_ERR_INVALID.
+ */
+PKV_API pkv_status pkv_append_slots_cow(pkv_block_manager* mgr, int32_t* block_tables,
+                                        int max_blocks_per_seq, int32_t* context_lens,
+                                        int num_seqs, int64_t* slot_mapping,
+                                        int64_t* copy_pairs, int* n_copy_pairs);
+
 #ifdef __cplusplus
 }
 #endif

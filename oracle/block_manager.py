@@ -127,6 +127,53 @@ class PagedAttentionScheduler:
                 self.manager.free(block_id)
 
 
+def append_slots_cow(tables, context_lens, block_size: int, free_ids, num_blocks: int,
+                     ref_counts):
+    """append_slots with copy-on-write ([LAYOUT] section 四.2): several
+    requests may point at one physical block (ref_count > 1).  The page
+    says only a request that writes its own next token into such a block
+    triggers the copy: it gets a freshly allocated private block holding a
+    copy of the shared one, and drops its reference to the shared block.
+
+    Readings: the copy happens when the token's page is an existing shared
+    block (a partly filled last page; a full page opens a new block as in
+    append_token).  ref_counts gives the starting count of every block
+    (free ids have 0).  Returns (new_tables, new_lens, slots, copy_pairs,
+    free_after, ref_after); copy_pairs lists (shared block, private block)
+    in sequence order, for the caller to copy before writing.
+    """
+    mgr = KVBlockManager(num_blocks, block_size, free_ids)
+    for b in range(num_blocks):
+        mgr.gpu_blocks[b].ref_count = int(ref_counts[b])
+    tables = [list(map(int, t)) for t in tables]
+    lens = [int(n) for n in context_lens]
+    slots, pairs = [], []
+    for s in range(len(tables)):
+        n = lens[s]
+        j = n // block_size
+        if n % block_size == 0:
+            try:
+                tables[s].append(mgr.allocate())
+            except OutOfBlocks:
+                slots.append(-1)
+                continue
+        else:
+            b = tables[s][j]
+            if mgr.gpu_blocks[b].ref_count > 1:
+                try:
+                    nb = mgr.allocate()
+                except OutOfBlocks:
+                    slots.append(-1)
+                    continue
+                mgr.free(b)
+                tables[s][j] = nb
+                pairs.append((b, nb))
+        slots.append(tables[s][j] * block_size + n % block_size)
+        lens[s] = n + 1
+    refs = [blk.ref_count for blk in mgr.gpu_blocks]
+    return tables, lens, slots, pairs, list(mgr.free_blocks), refs
+
+
 def append_slots(tables, context_lens, block_size: int, free_ids, num_blocks: int):
     """One decode step's append for every sequence, in sequence order: each
     sequence gets one new token through ``append_token`` (a new block from the

@@ -48,6 +48,7 @@ SIGNATURES = {
     "pkv_block_ref_count": (_i, [_p, _i32]),
     "pkv_block_free_ids": (_i, [_p, _p, _i]),
     "pkv_append_slots": (_i, [_p, _p, _i, _p, _i, _p]),
+    "pkv_append_slots_cow": (_i, [_p, _p, _i, _p, _i, _p, _p, C.POINTER(_i)]),
 }
 
 _lib = None

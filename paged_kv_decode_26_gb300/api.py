@@ -219,3 +219,21 @@ class BlockManager:
         if st not in (_lib.PKV_OK, _lib.PKV_ERR_NO_BLOCKS):
             check(st, "pkv_append_slots")
         return int(st)
+
+    def append_slots_cow(self, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                         slot_mapping: torch.Tensor):
+        """append_slots with copy-on-write of shared pages.  Returns (status,
+        copy_pairs int64 [n, 2]) -- copy those pairs before kv_append."""
+        for t, dt in ((block_tables, torch.int32), (context_lens, torch.int32),
+                      (slot_mapping, torch.int64)):
+            if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != dt:
+                raise ValueError("append_slots_cow takes contiguous CPU int32/int32/int64 tensors")
+        S = context_lens.shape[0]
+        pairs = torch.empty(max(S, 1), 2, dtype=torch.int64)
+        n = C.c_int(0)
+        st = lib().pkv_append_slots_cow(self._h, _ptr(block_tables), block_tables.shape[1],
+                                        _ptr(context_lens), S, _ptr(slot_mapping), _ptr(pairs),
+                                        C.byref(n))
+        if st not in (_lib.PKV_OK, _lib.PKV_ERR_NO_BLOCKS):
+            check(st, "pkv_append_slots_cow")
+        return int(st), pairs[:n.value].clone()

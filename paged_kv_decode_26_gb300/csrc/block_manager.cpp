@@ -10,6 +10,8 @@
 //   - add_reference() increments the count of a held block;
 //   - append_token opens a new block when the token count is a multiple of
 //     the block size, then counts the token.
+// Copy-on-write (section 四.2): a request that writes its next token into a
+// block other requests still reference gets a private copy of that block.
 // The free set is a bitmap with a "lowest possibly free word" hint, so
 // allocate/free cost O(1) amortised instead of the page's list sort.
 #include <stdint.h>
@@ -182,6 +184,63 @@ PKV_API pkv_status pkv_append_slots(pkv_block_manager* mgr, int32_t* block_table
         slot_mapping[s] = (int64_t)row[j] * B + n % B;
         context_lens[s] = n + 1;
     }
+    return result;
+}
+
+PKV_API pkv_status pkv_append_slots_cow(pkv_block_manager* mgr, int32_t* block_tables,
+                                        int max_blocks_per_seq, int32_t* context_lens,
+                                        int num_seqs, int64_t* slot_mapping,
+                                        int64_t* copy_pairs, int* n_copy_pairs) {
+    if (!mgr || num_seqs < 0 || max_blocks_per_seq < 0 || !n_copy_pairs) return PKV_ERR_INVALID;
+    if (num_seqs > 0 && (!block_tables || !context_lens || !slot_mapping || !copy_pairs))
+        return PKV_ERR_INVALID;
+    const int B = mgr->block_size;
+    pkv_status result = PKV_OK;
+    int n_pairs = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int n = context_lens[s];
+        int32_t* row = block_tables + (size_t)s * max_blocks_per_seq;
+        const int j = n / B;
+        if (n < 0 || j >= max_blocks_per_seq) {
+            slot_mapping[s] = -1;
+            result = PKV_ERR_NO_BLOCKS;
+            continue;
+        }
+        if (n % B == 0) {
+            // the last page is full (or there is none): open a new block
+            int32_t b = -1;
+            if (pkv_block_allocate(mgr, &b) != PKV_OK) {
+                slot_mapping[s] = -1;
+                result = PKV_ERR_NO_BLOCKS;
+                continue;
+            }
+            row[j] = b;
+        } else {
+            const int32_t shared = row[j];
+            if (shared < 0 || shared >= mgr->num_blocks) {
+                slot_mapping[s] = -1;
+                result = PKV_ERR_INVALID;
+                continue;
+            }
+            if (mgr->ref[shared] > 1) {
+                // the page is shared: write into a private copy instead
+                int32_t b = -1;
+                if (pkv_block_allocate(mgr, &b) != PKV_OK) {
+                    slot_mapping[s] = -1;
+                    result = PKV_ERR_NO_BLOCKS;
+                    continue;
+                }
+                pkv_block_free(mgr, shared);
+                row[j] = b;
+                copy_pairs[2 * n_pairs] = shared;
+                copy_pairs[2 * n_pairs + 1] = b;
+                ++n_pairs;
+            }
+        }
+        slot_mapping[s] = (int64_t)row[j] * B + n % B;
+        context_lens[s] = n + 1;
+    }
+    *n_copy_pairs = n_pairs;
     return result;
 }
 

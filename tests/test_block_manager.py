@@ -122,3 +122,56 @@ def test_append_with_exhausted_pool(pkv):
     assert bt[0, 0] == 0 and bt[1, 0] == -1
     tables, new_lens, ref_slots, _ = append_slots([[], []], [0, 0], 16, [0], 1)
     assert ref_slots == [0, -1] and new_lens == [1, 0]
+
+
+def _fork_state(rng, nb, B, n_parents, n_children):
+    """Random parents with private blocks, then children sharing a parent's
+    whole table (references added), as (tables, lens, refs, free_ids)."""
+    perm = rng.permutation(nb).tolist()
+    tables, lens = [], []
+    for _ in range(n_parents):
+        n = int(rng.integers(1, 5 * B))
+        k = (n + B - 1) // B
+        tables.append([perm.pop() for _ in range(k)])
+        lens.append(n)
+    for _ in range(n_children):
+        p = int(rng.integers(n_parents))
+        tables.append(list(tables[p]))
+        lens.append(lens[p])
+    refs = [0] * nb
+    for t in tables:
+        for b in t:
+            refs[b] += 1
+    free_ids = sorted(b for b in range(nb) if refs[b] == 0)
+    return tables, lens, refs, free_ids
+
+
+def test_copy_on_write_matches_oracle(pkv):
+    from oracle.block_manager import append_slots_cow
+    rng = np.random.default_rng(5)
+    B = 16
+    for trial in range(30):
+        nb = 200
+        tables, lens, refs, free_ids = _fork_state(rng, nb, B, 6, int(rng.integers(0, 8)))
+        S = len(tables)
+        ref = append_slots_cow(tables, lens, B, free_ids, nb, refs)
+        bm = pkv.BlockManager(nb, B, free_ids=free_ids)
+        for b in range(nb):
+            for _ in range(refs[b] - 1):
+                bm.add_reference(b)
+        mb = 8
+        bt = torch.full((S, mb), -1, dtype=torch.int32)
+        for s, t in enumerate(tables):
+            bt[s, :len(t)] = torch.tensor(t, dtype=torch.int32)
+        lt = torch.tensor(lens, dtype=torch.int32)
+        slots = torch.empty(S, dtype=torch.int64)
+        st, pairs = bm.append_slots_cow(bt, lt, slots)
+        assert st == 0
+        new_tables, new_lens, ref_slots, ref_pairs, free_after, refs_after = ref
+        assert slots.tolist() == ref_slots
+        assert [tuple(x) for x in pairs.tolist()] == ref_pairs
+        assert lt.tolist() == new_lens
+        for s in range(S):
+            assert bt[s][bt[s] >= 0].tolist() == new_tables[s]
+        assert bm.free_ids() == free_after
+        assert [bm.ref_count(b) for b in range(nb)] == refs_after

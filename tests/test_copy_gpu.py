@@ -199,3 +199,65 @@ def test_continuous_batching_step(lib, small):
     assert torch.equal(_bits(k), _bits(rk)) and torch.equal(_bits(v), _bits(rv))
     assert_attention_close(out, rout, case.out_dtype, "continuous step")
     assert lib.device_errors() == 0
+
+
+def test_copy_on_write_step(lib):
+    """Forked sequences share their parent's blocks (partly filled last pages
+    included).  One step: copy-on-write bookkeeping (native manager), copy of
+    the shared pages (swap_blocks_kv), append, decode -- against the oracle's
+    allocator, copy, append and decode.  Parents must keep their own pages."""
+    from oracle.block_manager import append_slots_cow
+    lens = [20, 37, 5, 50, 20, 37, 37]           # seqs 4..6 fork seqs 0, 1, 1
+    parents = {4: 0, 5: 1, 6: 1}
+    case = wl.make_case(5, lens_override=lens, H=8, Hk=2, D=64, d2d_pairs=0, h2d_pairs=0,
+                        host_pool_blocks=1, poison=False)
+    for c, p in parents.items():
+        case.block_tables[c] = case.block_tables[p]
+    nb, B, S = case.num_blocks, case.B, case.S
+    refs = [0] * nb
+    for row in case.block_tables.tolist():
+        for b in row:
+            if b >= 0:
+                refs[b] += 1
+    free_ids = sorted(b for b in range(nb) if refs[b] == 0)
+    tables = [[x for x in row if x >= 0] for row in case.block_tables.tolist()]
+
+    # ---- library
+    bm = lib.BlockManager(nb, B, free_ids=free_ids)
+    for b in range(nb):
+        for _ in range(refs[b] - 1):
+            bm.add_reference(b)
+    bt, lt = case.block_tables.clone(), case.context_lens.clone()
+    slots = torch.empty(S, dtype=torch.int64)
+    st, pairs = bm.append_slots_cow(bt, lt, slots)
+    assert st == 0 and pairs.shape[0] == 3       # each child's shared partial page
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    lib.swap_blocks_kv(dk, dv, dk, dv, pairs.cuda())
+    lib.kv_append(dk, dv, case.k_new.cuda(), case.v_new.cuda(), slots.cuda())
+    out = torch.empty(S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+    lib.paged_attn_decode(out, case.q.cuda(), dk, dv, bt.cuda(), lt.cuda(), case.scale,
+                          int(lt.max()))
+    torch.cuda.synchronize()
+
+    # ---- oracle
+    new_tables, new_lens, ref_slots, ref_pairs, _, _ = append_slots_cow(
+        tables, lens, B, free_ids, nb, refs)
+    assert slots.tolist() == ref_slots and [tuple(x) for x in pairs.tolist()] == ref_pairs
+    k, v = case.k_pool.clone(), case.v_pool.clone()
+    pr = torch.tensor(ref_pairs, dtype=torch.int64)
+    orc.swap_blocks(k, k.clone(), pr)
+    orc.swap_blocks(v, v.clone(), pr)
+    orc.kv_append(k, v, case.k_new, case.v_new, torch.tensor(ref_slots))
+    rbt = torch.full_like(case.block_tables, -1)
+    for s, row in enumerate(new_tables):
+        rbt[s, :len(row)] = torch.tensor(row, dtype=torch.int32)
+    assert torch.equal(bt, rbt)
+    ref = orc.decode_two_pass(case.q, k, v, rbt, torch.tensor(new_lens, dtype=torch.int32),
+                              case.scale)
+    assert torch.equal(_bits(dk.cpu()), _bits(k)) and torch.equal(_bits(dv.cpu()), _bits(v))
+    assert_attention_close(out, ref, case.out_dtype, "copy-on-write step")
+    # whichever of a parent and its child wrote first into their shared page
+    # got a private copy: afterwards they no longer share the page they wrote
+    for c, p in parents.items():
+        assert bt[c, lens[c] // B] != bt[p, lens[p] // B]
+    assert lib.device_errors() == 0

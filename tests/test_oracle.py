@@ -421,3 +421,24 @@ def test_append_slots_page_boundary():
     assert slots == [0 * 16 + 0, 9 * 16 + 1, 1 * 16 + 0]
     assert new_lens == [17, 18, 1]
     assert free_after == [2, 4]
+
+
+def test_copy_on_write_fork_walkthrough():
+    """[LAYOUT] section 四.2: a parent (blocks 0, 1; 20 tokens, so block 1 is
+    partly filled) is shared by two forked children.  Each child's first
+    append lands in the shared block 1 and gets a private copy (lowest free
+    ids 2, then 3); once the parent is the last holder it writes in place."""
+    from oracle.block_manager import append_slots_cow
+    tables = [[0, 1], [0, 1], [0, 1]]          # children 0, 1 and the parent
+    refs = [3, 3] + [0] * 6
+    new_tables, lens, slots, pairs, free_after, refs_after = append_slots_cow(
+        tables, [20, 20, 20], 16, list(range(2, 8)), 8, refs)
+    assert pairs == [(1, 2), (1, 3)]
+    assert new_tables == [[0, 2], [0, 3], [0, 1]]
+    assert slots == [2 * 16 + 4, 3 * 16 + 4, 1 * 16 + 4]
+    assert lens == [21, 21, 21]
+    assert refs_after[:4] == [3, 1, 1, 1] and free_after == [4, 5, 6, 7]
+    # a full page never copies: it opens a new block
+    t2, _, s2, p2, _, _ = append_slots_cow([[0, 1], [0, 1]], [32, 32], 16, [2, 3], 4,
+                                           [2, 2, 0, 0])
+    assert p2 == [] and t2 == [[0, 1, 2], [0, 1, 3]] and s2 == [32, 48]
