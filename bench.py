@@ -565,6 +565,43 @@ def main():
                       "K and V in one swap_blocks_kv launch",
         }
 
+    # ---- the step's allocation on the device (continuous-batching workload):
+    # pkv_device_append_slots from the pre-step state, restored before each
+    # timed call
+    dev_alloc = None
+    if with_swaps and rank == 0:
+        r0 = reps[0]
+        c0 = r0["case"]
+        refs = torch.zeros(c0.num_blocks, dtype=torch.int32)
+        bt0 = c0.block_tables
+        mbd = r0["bt_h"].shape[1]
+        bt_init = torch.full((S, mbd), -1, dtype=torch.int32)
+        bt_init[:, :bt0.shape[1]] = bt0
+        refs.index_add_(0, bt0[bt0 >= 0].long(), torch.ones(int((bt0 >= 0).sum()),
+                                                            dtype=torch.int32))
+        dm = pkv.DeviceBlockManager(refs, c0.B)
+        saved = (dm.ref_counts.clone(), dm.free_ids.clone(), dm.state.clone())
+        bt_d0, lens_d0 = bt_init.to(dev), c0.context_lens.to(dev)
+        bt_d, lens_d = bt_d0.clone(), lens_d0.clone()
+        slots_d = torch.empty(S, dtype=torch.int64, device=dev)
+        times = []
+        for i in range(50):
+            dm.ref_counts.copy_(saved[0])
+            dm.free_ids.copy_(saved[1])
+            dm.state.copy_(saved[2])
+            bt_d.copy_(bt_d0)
+            lens_d.copy_(lens_d0)
+            a, b = ev(), ev()
+            a.record(stream)
+            dm.append_slots(bt_d, lens_d, slots_d)
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        same = torch.equal(slots_d.cpu(), reps[0]["slots_h"]) and \
+            torch.equal(bt_d.cpu(), reps[0]["bt_h"])
+        dev_alloc = {"us": statistics.median(times) * 1e3, "sequences": S,
+                     "matches_host_manager": bool(same)}
+
     # ---- end to end through the public API with host buffers
     h2d_bytes = sum(host[k].numel() * host[k].element_size()
                     for k in ("q", "k_new", "v_new", "bt", "lens", "slots"))
@@ -676,6 +713,7 @@ def main():
     if with_swaps:
         line["config"]["swap_bytes_per_step"] = swap_bytes
         line["swap_blocks"] = swap
+        line["device_append_slots"] = dev_alloc
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

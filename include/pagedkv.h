@@ -298,6 +298,47 @@ PKV_API pkv_status pkv_append_slots_cow(pkv_block_manager* mgr, int32_t* block_t
                                         int num_seqs, int64_t* slot_mapping,
                                         int64_t* copy_pairs, int* n_copy_pairs);
 
+/*
+ * Block manager on the GPU ([LAYOUT] section 三, same semantics as the host
+ * manager above: reference counts, lowest free id first, sequences served in
+ * order, a new block when the token count is a multiple of the block size),
+ * so that a decode step's bookkeeping runs on the device without a host
+ * round trip.  State, all caller-owned device memory:
+ *   ref_counts int32 [num_blocks]
+ *   free_ids   int32 [num_blocks]: free ids in increasing order, entries
+ *              state[0] .. state[0] + state[1] - 1
+ *   state      int32 [4]: head, count, sequences left without a slot by the
+ *              last pkv_device_append_slots, spare
+ * Calls on one state must be ordered (one stream); each is one or two
+ * single-CTA kernels.
+ */
+
+/* free_ids / state from ref_counts (every id with count 0 is free). */
+PKV_API pkv_status pkv_device_rebuild_free_list(const int32_t* ref_counts, int32_t* free_ids,
+                                                int32_t* state, int num_blocks, void* stream);
+
+/*
+ * pkv_append_slots on the device: block_tables (int32 [num_seqs,
+ * max_blocks_per_seq]), context_lens (int32 [num_seqs]) updated in place,
+ * slot_mapping (int64 [num_seqs]) written; a sequence that gets no block
+ * (pool empty, table row full, negative length) keeps its row and length,
+ * gets slot -1 and is counted in state[2].
+ */
+PKV_API pkv_status pkv_device_append_slots(int32_t* ref_counts, const int32_t* free_ids,
+                                           int32_t* state, int32_t* block_tables,
+                                           int max_blocks_per_seq, int32_t* context_lens,
+                                           int num_seqs, int block_size, int num_blocks,
+                                           int64_t* slot_mapping, void* stream);
+
+/*
+ * Drop one reference per listed block id (device int32 [n_ids]; an id
+ * listed twice is dropped twice, a free block stays free, an id outside the
+ * pool is skipped and flagged PKV_DEVERR_PAIR), then rebuild the free list.
+ */
+PKV_API pkv_status pkv_device_free_blocks(int32_t* ref_counts, int32_t* free_ids, int32_t* state,
+                                          const int32_t* block_ids, int n_ids, int num_blocks,
+                                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

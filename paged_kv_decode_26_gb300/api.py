@@ -237,3 +237,52 @@ class BlockManager:
         if st not in (_lib.PKV_OK, _lib.PKV_ERR_NO_BLOCKS):
             check(st, "pkv_append_slots_cow")
         return int(st), pairs[:n.value].clone()
+
+
+class DeviceBlockManager:
+    """The block manager's state in device memory, driven by kernels (same
+    semantics as BlockManager).  ref_counts / free_ids / state are CUDA int32
+    tensors owned by this object."""
+
+    def __init__(self, ref_counts, block_size: int, device="cuda"):
+        rc = torch.as_tensor(ref_counts, dtype=torch.int32).to(device).contiguous()
+        self.num_blocks = rc.numel()
+        self.block_size = block_size
+        self.ref_counts = rc
+        self.free_ids = torch.empty(max(1, self.num_blocks), dtype=torch.int32, device=device)
+        self.state = torch.zeros(4, dtype=torch.int32, device=device)
+        check(lib().pkv_device_rebuild_free_list(_ptr(self.ref_counts), _ptr(self.free_ids),
+                                                 _ptr(self.state), self.num_blocks,
+                                                 _stream_ptr(None)),
+              "pkv_device_rebuild_free_list")
+
+    def append_slots(self, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                     slot_mapping: torch.Tensor, stream=None) -> None:
+        for name, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                        ("slot_mapping", slot_mapping)):
+            _need_cuda(name, t)
+        if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or \
+                slot_mapping.dtype != torch.int64:
+            raise ValueError("int32 tables and lengths, int64 slots")
+        check(lib().pkv_device_append_slots(_ptr(self.ref_counts), _ptr(self.free_ids),
+                                            _ptr(self.state), _ptr(block_tables),
+                                            block_tables.shape[1], _ptr(context_lens),
+                                            context_lens.shape[0], self.block_size,
+                                            self.num_blocks, _ptr(slot_mapping),
+                                            _stream_ptr(stream)),
+              "pkv_device_append_slots")
+
+    def free(self, block_ids: torch.Tensor, stream=None) -> None:
+        _need_cuda("block_ids", block_ids)
+        ids = block_ids.to(torch.int32).contiguous()
+        check(lib().pkv_device_free_blocks(_ptr(self.ref_counts), _ptr(self.free_ids),
+                                           _ptr(self.state), _ptr(ids), ids.numel(),
+                                           self.num_blocks, _stream_ptr(stream)),
+              "pkv_device_free_blocks")
+
+    def free_list(self) -> list:
+        st = self.state.tolist()
+        return self.free_ids[st[0]:st[0] + st[1]].tolist()
+
+    def failed_last_append(self) -> int:
+        return int(self.state[2].item())

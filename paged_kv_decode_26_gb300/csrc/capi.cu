@@ -270,6 +270,12 @@ namespace pkv {
 // through pkv_last_error_detail().
 void record_detail(const char* msg) { set_detail("%s", msg); }
 
+// Address of the current device's error word (NULL if the device is unusable).
+unsigned int* device_error_word() {
+    DeviceInfo* d = nullptr;
+    return device_info(&d) == cudaSuccess ? d->errors : nullptr;
+}
+
 cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask, size_t bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -139,3 +139,14 @@ def test_binding_requires_cuda_tensors():
                               torch.zeros(2, 16, 8, 128, dtype=torch.bfloat16),
                               torch.zeros(1, 2, dtype=torch.int32),
                               torch.ones(1, dtype=torch.int32), 0.1, 16)
+
+
+def test_device_allocator_rejects_invalid_arguments(L):
+    assert L.pkv_device_append_slots(FAKE, FAKE, FAKE, FAKE, 4, FAKE, -1, 16, 8, FAKE, NULL) == 1
+    assert L.pkv_device_append_slots(NULL, FAKE, FAKE, FAKE, 4, FAKE, 2, 16, 8, FAKE, NULL) == 1
+    assert L.pkv_device_append_slots(FAKE, FAKE, FAKE, FAKE, 4, FAKE, 2, 0, 8, FAKE, NULL) == 1
+    assert L.pkv_device_append_slots(FAKE, FAKE, FAKE, FAKE, 4, FAKE, 2, 16, 8,
+                                     C.c_void_p(4100), NULL) == 1   # slots not 8-byte aligned
+    assert L.pkv_device_rebuild_free_list(FAKE, NULL, FAKE, 8, NULL) == 1
+    assert L.pkv_device_free_blocks(FAKE, FAKE, FAKE, NULL, 3, 8, NULL) == 1
+    assert L.pkv_device_append_slots(FAKE, FAKE, FAKE, FAKE, 4, FAKE, 0, 16, 8, FAKE, NULL) == 0
