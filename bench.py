@@ -600,6 +600,7 @@ def main():
         same = torch.equal(slots_d.cpu(), reps[0]["slots_h"]) and \
             torch.equal(bt_d.cpu(), reps[0]["bt_h"])
         dev_alloc = {"us": statistics.median(times) * 1e3, "sequences": S,
+                     "timing": "events around one eager call, launch latency included",
                      "matches_host_manager": bool(same)}
 
     # ---- end to end through the public API with host buffers

@@ -299,6 +299,24 @@ PKV_API pkv_status pkv_append_slots_cow(pkv_block_manager* mgr, int32_t* block_t
                                         int64_t* copy_pairs, int* n_copy_pairs);
 
 /*
+ * pkv_defrag -- plan a compaction of the pool ([SWAP]: swap_blocks also
+ * serves to rearrange scattered pages into a more compact layout).  With n
+ * blocks in use, every used block whose id is >= n is paired with a free
+ * id < n (both taken in increasing order); the manager's counts and free set
+ * and the given host block tables are updated as if the blocks had moved.
+ * The caller then copies the pairs (swap_blocks / swap_blocks_kv; sources
+ * and destinations are disjoint) and uploads the tables.  Afterwards the
+ * used blocks are exactly [0, n).
+ *   block_tables host int32 [num_seqs, max_blocks_per_seq], updated in place
+ *   pairs        host int64 [cap, 2], written; *n_pairs rows used
+ * PKV_ERR_INVALID if cap is too small (nothing is changed then, *n_pairs =
+ * rows needed so far) or the counts are inconsistent.
+ */
+PKV_API pkv_status pkv_defrag(pkv_block_manager* mgr, int32_t* block_tables,
+                              int max_blocks_per_seq, int num_seqs, int64_t* pairs, int cap,
+                              int* n_pairs);
+
+/*
  * Block manager on the GPU ([LAYOUT] section 三, same semantics as the host
  * manager above: reference counts, lowest free id first, sequences served in
  * order, a new block when the token count is a multiple of the block size),

@@ -198,3 +198,29 @@ def append_slots(tables, context_lens, block_size: int, free_ids, num_blocks: in
     new_tables = [list(sch.active_requests[s].physical_block_ids) for s in range(len(tables))]
     new_lens = [sch.active_requests[s].num_allocated_tokens for s in range(len(tables))]
     return new_tables, new_lens, slots, list(sch.manager.free_blocks)
+
+
+def defrag_plan(ref_counts):
+    """Defragmentation by block copies ("vLLM 中 FlashAttention 与 KVCache 交换
+    机制深度解析": swap_blocks also serves to rearrange scattered pages into a
+    more compact layout).  Reading: with n blocks in use, every used block
+    whose id is >= n moves to a free id < n, the lowest used ids outside
+    going to the lowest free ids inside, so that afterwards the used blocks
+    are exactly [0, n).  Returns the (source, destination) pairs."""
+    nb = len(ref_counts)
+    used = [b for b in range(nb) if ref_counts[b] > 0]
+    n = len(used)
+    holes = [b for b in range(n) if ref_counts[b] == 0]
+    movers = [b for b in used if b >= n]
+    assert len(holes) == len(movers)
+    return list(zip(movers, holes))
+
+
+def apply_defrag(tables, ref_counts, pairs):
+    """Tables and reference counts after the pairs' blocks moved."""
+    where = dict(pairs)
+    new_tables = [[where.get(b, b) for b in t] for t in tables]
+    refs = list(ref_counts)
+    for src, dst in pairs:
+        refs[dst], refs[src] = refs[src], 0
+    return new_tables, refs

@@ -49,6 +49,7 @@ SIGNATURES = {
     "pkv_block_free_ids": (_i, [_p, _p, _i]),
     "pkv_append_slots": (_i, [_p, _p, _i, _p, _i, _p]),
     "pkv_append_slots_cow": (_i, [_p, _p, _i, _p, _i, _p, _p, C.POINTER(_i)]),
+    "pkv_defrag": (_i, [_p, _p, _i, _i, _p, _i, C.POINTER(_i)]),
     "pkv_device_rebuild_free_list": (_i, [_p, _p, _p, _i, _p]),
     "pkv_device_append_slots": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _p, _p]),
     "pkv_device_free_blocks": (_i, [_p, _p, _p, _p, _i, _i, _p]),

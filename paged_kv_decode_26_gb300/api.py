@@ -239,6 +239,23 @@ class BlockManager:
         return int(st), pairs[:n.value].clone()
 
 
+def _defrag(self, block_tables: torch.Tensor):
+    """Plan a compaction (used blocks to [0, n)); updates this manager and the
+    CPU int32 tables in place and returns the int64 [n, 2] pairs to copy."""
+    if block_tables.device.type != "cpu" or block_tables.dtype != torch.int32 or \
+            not block_tables.is_contiguous():
+        raise ValueError("defrag takes a contiguous CPU int32 block table")
+    cap = self.num_blocks
+    pairs = torch.empty(max(cap, 1), 2, dtype=torch.int64)
+    n = C.c_int(0)
+    check(lib().pkv_defrag(self._h, _ptr(block_tables), block_tables.shape[1],
+                           block_tables.shape[0], _ptr(pairs), cap, C.byref(n)), "pkv_defrag")
+    return pairs[:n.value].clone()
+
+
+BlockManager.defrag = _defrag
+
+
 class DeviceBlockManager:
     """The block manager's state in device memory, driven by kernels (same
     semantics as BlockManager).  ref_counts / free_ids / state are CUDA int32

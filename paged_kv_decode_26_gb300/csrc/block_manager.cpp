@@ -10,6 +10,9 @@
 //   - add_reference() increments the count of a held block;
 //   - append_token opens a new block when the token count is a multiple of
 //     the block size, then counts the token.
+// Defragmentation (page "vLLM 中 FlashAttention 与 KVCache 交换机制深度解析":
+// swap_blocks also rearranges scattered pages into a compact layout): the
+// used blocks move to [0, n_used).
 // Copy-on-write (section 四.2): a request that writes its next token into a
 // block other requests still reference gets a private copy of that block.
 // The free set is a bitmap with a "lowest possibly free word" hint, so
@@ -242,6 +245,50 @@ PKV_API pkv_status pkv_append_slots_cow(pkv_block_manager* mgr, int32_t* block_t
     }
     *n_copy_pairs = n_pairs;
     return result;
+}
+
+PKV_API pkv_status pkv_defrag(pkv_block_manager* mgr, int32_t* block_tables,
+                              int max_blocks_per_seq, int num_seqs, int64_t* pairs, int cap,
+                              int* n_pairs) {
+    if (!mgr || num_seqs < 0 || max_blocks_per_seq < 0 || cap < 0 || !n_pairs)
+        return PKV_ERR_INVALID;
+    if ((num_seqs > 0 && !block_tables) || (cap > 0 && !pairs)) return PKV_ERR_INVALID;
+    const int nb = mgr->num_blocks;
+    const int n_used = nb - mgr->free_count;
+    // pair the used ids at or above n_used (increasing) with the free ids
+    // below n_used (increasing)
+    std::vector<int32_t> dst_of(nb, -1);
+    int k = 0, hole = 0;
+    for (int b = n_used; b < nb; ++b) {
+        if (mgr->ref[b] == 0) continue;
+        while (hole < n_used && mgr->ref[hole] != 0) ++hole;
+        if (hole >= n_used) return PKV_ERR_INVALID;  // inconsistent counts
+        if (k >= cap) {
+            *n_pairs = k;
+            return PKV_ERR_INVALID;                    // pairs buffer too small
+        }
+        pairs[2 * k] = b;
+        pairs[2 * k + 1] = hole;
+        dst_of[b] = hole;
+        ++k;
+        ++hole;
+    }
+    // move the counts and the free set, then repoint the tables
+    for (int i = 0; i < k; ++i) {
+        const int src = (int)pairs[2 * i], dst = (int)pairs[2 * i + 1];
+        mgr->mark_held(dst);
+        mgr->ref[dst] = mgr->ref[src];
+        mgr->ref[src] = 0;
+        mgr->mark_free(src);
+    }
+    for (int s = 0; s < num_seqs; ++s) {
+        int32_t* row = block_tables + (size_t)s * max_blocks_per_seq;
+        for (int j = 0; j < max_blocks_per_seq; ++j)
+            if (row[j] >= 0 && row[j] < nb && dst_of[row[j]] >= 0) row[j] = dst_of[row[j]];
+    }
+    mgr->hint = 0;
+    *n_pairs = k;
+    return PKV_OK;
 }
 
 }  // extern "C"

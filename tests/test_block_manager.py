@@ -175,3 +175,35 @@ def test_copy_on_write_matches_oracle(pkv):
             assert bt[s][bt[s] >= 0].tolist() == new_tables[s]
         assert bm.free_ids() == free_after
         assert [bm.ref_count(b) for b in range(nb)] == refs_after
+
+
+def test_defrag_matches_oracle(pkv):
+    from oracle.block_manager import apply_defrag, defrag_plan
+    rng = np.random.default_rng(8)
+    for trial in range(25):
+        nb, B = int(rng.integers(10, 300)), 16
+        tables, lens, refs, free_ids = _fork_state(rng, nb * 2, B, 3, int(rng.integers(0, 4)))
+        # shrink to ids < nb by taking a random used subset mapping
+        tables = [[b % nb for b in t] for t in tables]
+        refs = [0] * nb
+        for t in tables:
+            for b in t:
+                refs[b] += 1
+        free_ids = [b for b in range(nb) if refs[b] == 0]
+        pairs_ref = defrag_plan(refs)
+        tables_ref, refs_ref = apply_defrag(tables, refs, pairs_ref)
+        bm = pkv.BlockManager(nb, B, free_ids=free_ids)
+        for b in range(nb):
+            for _ in range(refs[b] - 1):
+                bm.add_reference(b)
+        mb = max(len(t) for t in tables) + 1
+        bt = torch.full((len(tables), mb), -1, dtype=torch.int32)
+        for s, t in enumerate(tables):
+            bt[s, :len(t)] = torch.tensor(t, dtype=torch.int32)
+        pairs = bm.defrag(bt)
+        assert [tuple(p) for p in pairs.tolist()] == pairs_ref
+        for s, t in enumerate(tables_ref):
+            assert bt[s][bt[s] >= 0].tolist() == t
+        assert [bm.ref_count(b) for b in range(nb)] == refs_ref
+        n_used = sum(1 for r in refs if r > 0)
+        assert bm.free_ids() == list(range(n_used, nb))

@@ -261,3 +261,35 @@ def test_copy_on_write_step(lib):
     for c, p in parents.items():
         assert bt[c, lens[c] // B] != bt[p, lens[p] // B]
     assert lib.device_errors() == 0
+
+
+def test_defragmentation_keeps_decode_identical(lib):
+    """Compact the pool (used blocks to the lowest ids) with the planner and
+    one swap_blocks_kv, then decode: bit-identical to the decode before."""
+    case = wl.make_case(3, S=12, lens=("uniform", 1, 300), share_blocks=3, pool_extra=1.5)
+    nb, B = case.num_blocks, case.B
+    refs = [0] * nb
+    for row in case.block_tables.tolist():
+        for b in row:
+            if b >= 0:
+                refs[b] += 1
+    free_ids = [b for b in range(nb) if refs[b] == 0]
+    bm = lib.BlockManager(nb, B, free_ids=free_ids)
+    for b in range(nb):
+        for _ in range(refs[b] - 1):
+            bm.add_reference(b)
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    before = torch.empty(case.S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+    lib.paged_attn_decode(before, case.q.cuda(), dk, dv, case.block_tables.cuda(),
+                          case.context_lens.cuda(), case.scale, case.max_context_len)
+    bt = case.block_tables.clone()
+    pairs = bm.defrag(bt)
+    assert pairs.shape[0] > 0
+    lib.swap_blocks_kv(dk, dv, dk, dv, pairs.cuda())
+    after = torch.empty_like(before)
+    lib.paged_attn_decode(after, case.q.cuda(), dk, dv, bt.cuda(), case.context_lens.cuda(),
+                          case.scale, case.max_context_len)
+    assert torch.equal(before, after)
+    n_used = sum(1 for r in refs if r > 0)
+    assert int(bt.max()) == n_used - 1 and bm.free_ids() == list(range(n_used, nb))
+    assert lib.device_errors() == 0

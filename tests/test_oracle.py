@@ -442,3 +442,15 @@ def test_copy_on_write_fork_walkthrough():
     t2, _, s2, p2, _, _ = append_slots_cow([[0, 1], [0, 1]], [32, 32], 16, [2, 3], 4,
                                            [2, 2, 0, 0])
     assert p2 == [] and t2 == [[0, 1, 2], [0, 1, 3]] and s2 == [32, 48]
+
+
+def test_defrag_plan_hand_example():
+    """Used blocks 0, 2, 4, 5 (4 in use): 4 and 5 move into the holes 1 and 3."""
+    from oracle.block_manager import apply_defrag, defrag_plan
+    refs = [1, 0, 2, 0, 1, 1]
+    pairs = defrag_plan(refs)
+    assert pairs == [(4, 1), (5, 3)]
+    tables, new_refs = apply_defrag([[0, 4], [2, 5], [2]], refs, pairs)
+    assert tables == [[0, 1], [2, 3], [2]]
+    assert new_refs == [1, 1, 2, 1, 0, 0]
+    assert defrag_plan([1, 1, 0, 0]) == []          # already compact
