@@ -49,6 +49,9 @@ def lib():
         L.orc_paged_decode_online.argtypes = [_p, _p, _p, _p, _p, _p, C.c_int, _p, C.c_int, _p,
                                               _p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                               C.c_int, C.c_int, _d, C.c_int, C.c_int, C.c_int]
+        L.orc_paged_multi_query.restype = C.c_int
+        L.orc_paged_multi_query.argtypes = [_p, _p, _p, _p, C.c_int, _p, C.c_int, _p, _p, C.c_int,
+                                            C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _d]
         L.orc_merge_states.restype = None
         L.orc_merge_states.argtypes = [_p, _p, _p, _p, C.c_int, C.c_int]
         L.orc_kv_append.restype = C.c_int
@@ -138,6 +141,28 @@ def decode_online(q, k_pool, v_pool, block_tables, context_lens, scale, tile_tok
     if rc != 0:
         raise OracleError(f"orc_paged_decode_online failed with code {rc}")
     return (out, m, l_) if return_state else out
+
+
+def multi_query(q, k_pool, v_pool, block_tables, context_lens, q_start, scale):
+    """fp64 causal attention of each sequence's last q_len tokens over its
+    paged context.  q [total_q, H, D], q_start int32 [S + 1].  Returns
+    float64 ndarray [total_q, H, D]."""
+    q, k, v = _cpu(q), _cpu(k_pool), _cpu(v_pool)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise OracleError("q, k_pool and v_pool must share one dtype")
+    bt = _cpu(block_tables).to(torch.int32).contiguous()
+    cl = _cpu(context_lens).to(torch.int32).contiguous()
+    qs = _cpu(q_start).to(torch.int32).contiguous()
+    T, H, D = q.shape
+    nb, B, Hk, _ = k.shape
+    S = cl.numel()
+    out = np.zeros((T, H, D), dtype=np.float64)
+    rc = lib().orc_paged_multi_query(out.ctypes.data, _ptr(q), _ptr(k), _ptr(v), _DT[q.dtype],
+                                     _ptr(bt), bt.shape[1] if bt.dim() == 2 else 0, _ptr(cl),
+                                     _ptr(qs), S, H, Hk, D, B, nb, float(scale))
+    if rc != 0:
+        raise OracleError(f"orc_paged_multi_query failed with code {rc}")
+    return out
 
 
 def merge_states(m, l_, o):

@@ -245,6 +245,84 @@ int orc_paged_decode_two_pass(double* out, const void* q, const void* k_pool, co
 }
 
 /*
+ * Several query tokens per sequence (a prefill chunk, or tokens to verify):
+ * sequence s owns query rows q_start[s] .. q_start[s+1]-1 of q; they are its
+ * last q_len = q_start[s+1] - q_start[s] tokens, so row i (0-based within
+ * the sequence) sits at position p = context_lens[s] - q_len + i and attends
+ * to the keys t <= p (causal).  Per (row, head) the plain definition as in
+ * orc_paged_decode_two_pass: scores, maximum pass, sum pass, normalise pass.
+ *   out : fp64 [q_start[num_seqs], n_heads, head_dim]
+ * ([SWAP] standard attention formula and its FlashAttention tiling over many
+ * query rows; the causal restriction is the plain reading of prefill, where a
+ * token attends to itself and the tokens before it.)
+ */
+int orc_paged_multi_query(double* out, const void* q, const void* k_pool, const void* v_pool,
+                          int dtype, const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, const int32_t* q_start, int num_seqs,
+                          int n_heads, int n_kv_heads, int head_dim, int block_size,
+                          int num_blocks, double scale)
+{
+    int rc = orc_check(block_tables, max_blocks_per_seq, context_lens, NULL, num_seqs, num_seqs,
+                       n_heads, n_kv_heads, head_dim, block_size, num_blocks);
+    if (rc != ORC_OK)
+        return rc;
+    int group = n_heads / n_kv_heads;
+    for (int s = 0; s < num_seqs; ++s) {
+        int q_len = q_start[s + 1] - q_start[s];
+        int n = context_lens[s];
+        if (q_len < 0 || q_len > n)
+            return ORC_BAD_INDEX;
+        for (int i = 0; i < q_len; ++i) {
+            int row = q_start[s] + i;
+            int pos = n - q_len + i;      /* keys 0 .. pos */
+            int cnt = pos + 1;
+            for (int h = 0; h < n_heads; ++h) {
+                double* o = out + ((size_t)row * n_heads + h) * head_dim;
+                int kvh = h / group;
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                double* x = (double*)malloc(sizeof(double) * (size_t)cnt);
+                if (!x)
+                    return ORC_NO_MEM;
+                for (int t = 0; t < cnt; ++t) {
+                    double acc = 0.0;
+                    for (int d = 0; d < head_dim; ++d) {
+                        double qi = orc_load(q, ((size_t)row * n_heads + h) * head_dim + d, dtype);
+                        double ki = orc_load(k_pool,
+                                             orc_kv_index(block_tables, max_blocks_per_seq, s, t,
+                                                          kvh, d, n_kv_heads, head_dim,
+                                                          block_size),
+                                             dtype);
+                        acc += qi * ki;
+                    }
+                    x[t] = scale * acc;
+                }
+                double m = x[0];
+                for (int t = 1; t < cnt; ++t)
+                    if (x[t] > m)
+                        m = x[t];
+                double z = 0.0;
+                for (int t = 0; t < cnt; ++t)
+                    z += exp(x[t] - m);
+                for (int t = 0; t < cnt; ++t) {
+                    double w = exp(x[t] - m) / z;
+                    for (int d = 0; d < head_dim; ++d) {
+                        double vi = orc_load(v_pool,
+                                             orc_kv_index(block_tables, max_blocks_per_seq, s, t,
+                                                          kvh, d, n_kv_heads, head_dim,
+                                                          block_size),
+                                             dtype);
+                        o[d] += w * vi;
+                    }
+                }
+                free(x);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/*
  * The pages' one-pass method: [SWAP] OnlineSoftmax, [OPT] "关键公式推导".
  * The logical context is cut into consecutive tiles of `tile_tokens` keys;
  * per tile X_i (scaled scores of the tile):

@@ -296,3 +296,22 @@ def sampled_seqs(case: DecodeCase, k: int, seed: int = 1234) -> list:
     rest = [s for s in rng.permutation(case.S).tolist() if s not in pick]
     pick.update(rest[:max(0, k - len(pick))])
     return sorted(pick)[:max(k, 2)]
+
+
+def multi_query_inputs(case: DecodeCase, q_len_spec, seed: int = 77):
+    """Query rows for attention of several new tokens per sequence (a prefill
+    chunk, or tokens to verify): sequence s gets q_len_s <= context_lens[s]
+    rows, its last q_len_s tokens.  q_len_spec is ("const", n) or ("uniform",
+    lo, hi) (clipped to the context).  Returns (q [total, H, D] in the case's
+    dtype, q_start int32 [S + 1])."""
+    rng = np.random.default_rng(seed)
+    lens = case.context_lens.numpy()
+    if q_len_spec[0] == "const":
+        ql = np.full(case.S, q_len_spec[1], dtype=np.int64)
+    else:
+        ql = rng.integers(q_len_spec[1], q_len_spec[2] + 1, size=case.S)
+    ql = np.minimum(ql, lens)
+    q_start = np.zeros(case.S + 1, dtype=np.int32)
+    q_start[1:] = np.cumsum(ql)
+    q = _normal(rng, (int(q_start[-1]), case.H, case.D), case.dtype)
+    return q, torch.from_numpy(q_start)

@@ -454,3 +454,59 @@ def test_defrag_plan_hand_example():
     assert tables == [[0, 1], [2, 3], [2]]
     assert new_refs == [1, 1, 2, 1, 0, 0]
     assert defrag_plan([1, 1, 0, 0]) == []          # already compact
+
+
+# ------------------------------------------------- several query tokens
+
+def test_multi_query_one_token_is_decode():
+    case = wl.make_case(3, S=5, lens=("uniform", 1, 90), share_blocks=2)
+    q, qs = wl.multi_query_inputs(case, ("const", 1))
+    got = orc.multi_query(q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, qs,
+                          case.scale)
+    ref = orc.decode_two_pass(q, case.k_pool, case.v_pool, case.block_tables, case.context_lens,
+                              case.scale)
+    assert np.array_equal(got, ref)
+
+
+def test_multi_query_rows_are_decodes_of_their_prefix():
+    """Row i of a sequence attends exactly to the keys up to its position."""
+    case = wl.make_case(2, S=3, lens=("uniform", 5, 60), H=4, Hk=2, D=32)
+    q, qs = wl.multi_query_inputs(case, ("uniform", 1, 9))
+    got = orc.multi_query(q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, qs,
+                          case.scale)
+    for s in range(case.S):
+        n = int(case.context_lens[s])
+        ql = int(qs[s + 1] - qs[s])
+        for i in range(ql):
+            row = int(qs[s]) + i
+            lens = case.context_lens.clone()
+            lens[s] = n - ql + i + 1
+            qq = case.q.clone()
+            qq[s] = q[row]
+            ref = orc.decode_two_pass(qq, case.k_pool, case.v_pool, case.block_tables, lens,
+                                      case.scale, seq_ids=[s])
+            assert np.array_equal(got[row], ref[0])
+
+
+def test_multi_query_matches_torch_sdpa_causal():
+    S, H, Hk, D, B = 2, 4, 2, 16, 4
+    lens = [11, 7]
+    q_lens = [4, 7]
+    q, k, v, bt, cl, mb = _contiguous_case(S, H, Hk, D, B, lens, seed=21)
+    g = torch.Generator().manual_seed(3)
+    qs = torch.tensor([0, 4, 11], dtype=torch.int32)
+    qm = torch.randn(11, H, D, generator=g, dtype=torch.float64)
+    got = orc.multi_query(qm, k, v, bt, cl, qs, 0.25)
+    K = _logical(k, S, mb, B, Hk, D)
+    V = _logical(v, S, mb, B, Hk, D)
+    for s in range(S):
+        n, ql = lens[s], q_lens[s]
+        Ks = K[s, :n].permute(1, 0, 2).repeat_interleave(H // Hk, dim=0)    # [H, n, D]
+        Vs = V[s, :n].permute(1, 0, 2).repeat_interleave(H // Hk, dim=0)
+        Qs = qm[int(qs[s]):int(qs[s + 1])].permute(1, 0, 2)                 # [H, ql, D]
+        pos = torch.arange(n - ql, n).unsqueeze(1)
+        mask = torch.arange(n).unsqueeze(0) <= pos                           # [ql, n]
+        ref = torch.nn.functional.scaled_dot_product_attention(Qs, Ks, Vs, attn_mask=mask,
+                                                               scale=0.25)
+        np.testing.assert_allclose(got[int(qs[s]):int(qs[s + 1])], ref.permute(1, 0, 2).numpy(),
+                                   rtol=1e-12, atol=1e-13)

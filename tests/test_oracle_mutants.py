@@ -39,6 +39,8 @@ MUTANTS = [
     ("bf16 subnormals dropped", "mag = ldexp((double)frac, -133);", "mag = 0.0;"),
     ("kv bytes without the K/V factor", "return 2u * elem_bytes * n_layers",
      "return elem_bytes * n_layers"),
+    ("query rows reversed", "int row = q_start[s] + i;", "int row = q_start[s] + (q_len - 1 - i);"),
+    ("causal window one short", "int cnt = pos + 1;", "int cnt = pos > 0 ? pos : 1;"),
 ]
 
 
