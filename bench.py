@@ -60,6 +60,8 @@ def parse_args():
                     help="replay each step as one CUDA graph")
     ap.add_argument("--replicas", type=int, default=1,
                     help="independent copies of the workload (own pools) per GPU, one graph")
+    ap.add_argument("--multi-query", type=int, default=0,
+                    help="time paged_attn_multi_query with this many new tokens per sequence")
     ap.add_argument("--graph-streams", type=int, default=32,
                     help="parallel branches of the replica graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -330,10 +332,73 @@ def build_replicas(args, rank, dev, pkv, wl, torch, np):
     return reps, host, devb
 
 
+def run_multi_query(args):
+    """Causal attention of a chunk of `--multi-query` new tokens per sequence
+    over the workload's paged context (the prefill / verification side of the
+    decode path).  Prints one JSON line with TFLOP/s of algorithmic work
+    (4 * head_dim flops per key per query row and head)."""
+    import torch
+    from paged_kv_decode_26_gb300 import build as lib_build
+    lib_build.build()
+    import paged_kv_decode_26_gb300 as pkv
+    from paged_kv_decode_26_gb300 import workloads as wl
+    case = wl.make_case(args.config, seed=rank_seed(args.config, 0),
+                        **({"S": args.seqs} if args.seqs else {}))
+    q, qs = wl.multi_query_inputs(case, ("const", args.multi_query))
+    dev = torch.device("cuda", 0)
+    t = {k: getattr(case, k).to(dev) for k in ("k_pool", "v_pool", "block_tables", "context_lens")}
+    qd, qsd = q.to(dev), qs.to(dev)
+    out = torch.empty(q.shape[0], case.H, case.D, dtype=case.out_dtype, device=dev)
+    ql = (qs[1:] - qs[:-1]).numpy()
+    lens = case.context_lens.numpy()
+    keys = sum(int(ql[s]) * (int(lens[s]) - int(ql[s])) + int(ql[s]) * (int(ql[s]) + 1) // 2
+               for s in range(case.S))
+    flops = 4.0 * case.H * case.D * keys
+    kv_bytes, kv_unique = wl.kv_bytes(case)
+
+    def call():
+        pkv.paged_attn_multi_query(out, qd, qsd, t["k_pool"], t["v_pool"], t["block_tables"],
+                                   t["context_lens"], case.scale, int(ql.max()),
+                                   case.max_context_len)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if pkv.device_errors(clear=True):
+        raise RuntimeError("device error flags raised")
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    tflops = flops / (ms / 1e3) / 1e12
+    print(json.dumps({
+        "metric": "paged multi-query attention TFLOP/s (causal chunk per sequence)",
+        "value": tflops, "unit": "TFLOP/s", "ms_per_call": ms, "steps": args.steps,
+        "config": {"workload": workload_name(case, args.config), "q_len": args.multi_query,
+                   "query_rows": int(qs[-1]), "keys_attended": keys},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "peak_kind": "measured cuBLAS bf16 burst "
+                     "(MEASURED_PEAKS.json bf16_tflops)",
+                     "kv_gbs_unique": kv_unique / (ms / 1e3) / 1e9},
+        "dtype": "bf16 in, f32 accumulate"}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.multi_query:
+        run_multi_query(args)
         return
 
     import numpy as np

@@ -177,6 +177,40 @@ PKV_API pkv_status paged_attn_decode_noalloc(void* out, pkv_dtype out_dtype, con
                                              void* stream);
 
 /*
+ * paged_attn_multi_query -- several new tokens per sequence attend causally
+ * to the paged context: a prefill chunk, or tokens to verify ([SWAP]: the
+ * serving loop's prefill step computes attention for all of a request's
+ * tokens with FlashAttention and writes their KV into pages; FlashAttention
+ * tiles Q, K and V through on-chip memory with the OnlineSoftmax
+ * recurrence).  Sequence s owns rows q_start[s] .. q_start[s+1]-1 of q, its
+ * last q_len = q_start[s+1] - q_start[s] tokens (their K and V already in
+ * the pool, e.g. by kv_append or a cache write); row i sits at position
+ * p = context_lens[s] - q_len + i and attends to the keys t <= p:
+ *
+ *     out[row, h, :] = sum_{t <= p} softmax_t(scale * q[row, h, :] . K_t) V_t
+ *
+ *   out, q       device [total_q, n_heads, head_dim]; q of kv_dtype, out of
+ *                out_dtype (F16, BF16, F32); 16-byte aligned
+ *   q_start      device int32 [num_seqs + 1], non-decreasing, q_start[0] >= 0,
+ *                q_start[num_seqs] <= total_q
+ *   max_q_len    host-side bound of q_len (sizes the grid)
+ *   max_context_len host-side bound of context_lens
+ *   other arguments as paged_attn_decode.
+ * A sequence whose q_len is negative, above its context, above max_q_len or
+ * whose context exceeds max_context_len is skipped (its rows are not
+ * written) and flagged PKV_DEVERR_CONTEXT.  Tensor cores (mma.sync): query
+ * tokens x query heads of one kv head form the tile rows.
+ */
+PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const void* q,
+                                          const int32_t* q_start, int total_q, int max_q_len,
+                                          const void* k_pool, const void* v_pool,
+                                          pkv_dtype kv_dtype, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* context_lens,
+                                          int num_seqs, int n_heads, int n_kv_heads,
+                                          int head_dim, int block_size, int num_blocks,
+                                          float scale, int max_context_len, void* stream);
+
+/*
  * kv_append -- write one new token per sequence into its page
  * (reshape-and-cache; [LAYOUT] section 三 append_token):
  *

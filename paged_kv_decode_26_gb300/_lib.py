@@ -35,6 +35,8 @@ SIGNATURES = {
                                _i, _i, _p, _sz, _p]),
     "paged_attn_decode_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i,
                                        _i, _f, _i, _i, _p]),
+    "paged_attn_multi_query": (_i, [_p, _i, _p, _p, _i, _i, _p, _p, _i, _p, _i, _p, _i, _i, _i,
+                                    _i, _i, _i, _f, _i, _p]),
     "kv_append": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _p]),
     "swap_blocks": (_i, [_p, _p, _sz, _p, _i, _i64, _i64, _p]),
     "swap_blocks_kv": (_i, [_p, _p, _p, _p, _sz, _p, _i, _i64, _i64, _p]),

@@ -87,6 +87,36 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     return out
 
 
+def paged_attn_multi_query(out: torch.Tensor, q: torch.Tensor, q_start: torch.Tensor,
+                           k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           max_q_len: int, max_context_len: int,
+                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Causal attention of each sequence's last q_len tokens (rows
+    q_start[s] .. q_start[s+1]-1 of q [total_q, H, D]) over its paged context."""
+    for name, t in (("out", out), ("q", q), ("q_start", q_start), ("k_pool", k_pool),
+                    ("v_pool", v_pool), ("block_tables", block_tables),
+                    ("context_lens", context_lens)):
+        _need_cuda(name, t)
+    if q_start.dtype != torch.int32 or block_tables.dtype != torch.int32 or \
+            context_lens.dtype != torch.int32:
+        raise ValueError("q_start, block_tables and context_lens must be int32")
+    T, H, D = q.shape
+    nb, B, Hk, D2 = k_pool.shape
+    S = context_lens.shape[0]
+    if (D2 != D or tuple(out.shape) != (T, H, D) or tuple(v_pool.shape) != tuple(k_pool.shape)
+            or q.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype
+            or q_start.shape != (S + 1,) or block_tables.shape[0] != S):
+        raise ValueError("inconsistent shapes or dtypes")
+    st = lib().paged_attn_multi_query(_ptr(out), _DT[out.dtype], _ptr(q), _ptr(q_start), T,
+                                      int(max_q_len), _ptr(k_pool), _ptr(v_pool),
+                                      _DT[k_pool.dtype], _ptr(block_tables), block_tables.shape[1],
+                                      _ptr(context_lens), S, H, Hk, D, B, nb, float(scale),
+                                      int(max_context_len), _stream_ptr(stream))
+    check(st, "paged_attn_multi_query")
+    return out
+
+
 def kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
               v_new: torch.Tensor, slot_mapping: torch.Tensor,
               stream: Optional[torch.cuda.Stream] = None) -> None:

@@ -481,6 +481,89 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
     return PKV_OK;
 }
 
+PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const void* q,
+                                          const int32_t* q_start, int total_q, int max_q_len,
+                                          const void* k_pool, const void* v_pool,
+                                          pkv_dtype kv_dtype, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* context_lens,
+                                          int num_seqs, int n_heads, int n_kv_heads,
+                                          int head_dim, int block_size, int num_blocks,
+                                          float scale, int max_context_len, void* stream) {
+    if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_context_len < 0)
+        return invalid("sizes");
+    if (num_seqs > 65535) return unsupported("more than 65535 sequences per call");
+    if (n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads)
+        return invalid("n_heads must be a positive multiple of n_kv_heads");
+    if (kv_dtype != PKV_BF16 && kv_dtype != PKV_F16) return unsupported("kv_dtype must be F16 or BF16");
+    if (out_dtype != PKV_BF16 && out_dtype != PKV_F16 && out_dtype != PKV_F32)
+        return invalid("out_dtype");
+    if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size))
+        return unsupported("head_dim 64/128, block_size 16/32, group 1/2/4/8");
+    if (num_blocks < 0 || max_blocks_per_seq <= 0) return invalid("pool / table sizes");
+    if (!std::isfinite(scale)) return invalid("scale is not finite");
+    if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+    if (!out || !q || !q_start || !block_tables || !context_lens) return invalid("NULL pointer");
+    if (num_blocks > 0 && (!k_pool || !v_pool)) return invalid("k_pool or v_pool is NULL");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return invalid("out, q, k_pool and v_pool must be 16-byte aligned");
+    const long long max_pages_ll = ((long long)max_context_len + block_size - 1) / block_size;
+    if (max_pages_ll > max_blocks_per_seq || max_pages_ll > 16384)
+        return invalid("max_context_len beyond the block table (or 16384 pages)");
+    const int max_pages = (int)(max_pages_ll > 0 ? max_pages_ll : 1);
+    DeviceInfo* dev = nullptr;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    const int G = n_heads / n_kv_heads;
+    const int qt = 16 / G;  // query tokens per warp
+    int warps = (max_q_len + qt - 1) / qt;
+    warps = warps < 1 ? 1 : (warps > 4 ? 4 : warps);
+    int stages = env_int("PKV_MQ_STAGES", 4);
+    stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+    pkv::MultiQueryLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const size_t smem = pkv::multi_query_smem_bytes(head_dim, block_size, 2, stages, max_pages);
+    if (smem > (size_t)dev->smem_optin) return unsupported("shared memory of this configuration");
+    const void* kmap_base = num_blocks > 0 ? k_pool : q;
+    const void* vmap_base = num_blocks > 0 ? v_pool : q;
+    const int map_blocks = num_blocks > 0 ? num_blocks : 1;
+    if ((e = encode_pool_map(&L.tm_k, kmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
+                             head_dim, 1, true)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = encode_pool_map(&L.tm_v, vmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
+                             head_dim, 1, true)) != cudaSuccess)
+        return cuda_fail(e);
+    pkv::MultiQueryParams& p = L.p;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.q = q;
+    p.q_start = q_start;
+    p.total_q = total_q;
+    p.max_q_len = max_q_len;
+    p.block_tables = block_tables;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.num_seqs = num_seqs;
+    p.n_heads = n_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = G;
+    p.num_blocks = num_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.stages = stages;
+    p.max_pages = max_pages;
+    p.errors = dev->errors;
+    const int tile_tokens = warps * qt;
+    L.grid = dim3((unsigned)((max_q_len + tile_tokens - 1) / tile_tokens), (unsigned)n_kv_heads,
+                  (unsigned)num_seqs);
+    L.block = dim3((unsigned)(32 * (1 + warps)));
+    L.smem_bytes = smem;
+    L.stream = static_cast<cudaStream_t>(stream);
+    e = kv_dtype == PKV_BF16 ? pkv::launch_multi_query_bf16(head_dim, block_size, L)
+                             : pkv::launch_multi_query_f16(head_dim, block_size, L);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return PKV_OK;
+}
+
 PKV_API pkv_status kv_append(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
                              pkv_dtype dtype, const int64_t* slot_mapping, int num_seqs,
                              int n_kv_heads, int head_dim, int block_size, int num_blocks,

@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "decode_mma_kernel.cuh"
+#include "multi_query_kernel.cuh"
 
 namespace pkv {
 
@@ -26,6 +26,20 @@ cudaError_t launch_decode_f16(int D, int BS, int QPW, const DecodeLaunch& L);
 // Launch paged_decode_mma_kernel<D, BS, T> (tensor-core path for query-head groups).
 cudaError_t launch_decode_mma_bf16(int D, int BS, const DecodeLaunch& L);
 cudaError_t launch_decode_mma_f16(int D, int BS, const DecodeLaunch& L);
+
+struct MultiQueryLaunch {
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    MultiQueryParams p;
+    dim3 grid;
+    dim3 block;
+    size_t smem_bytes;
+    cudaStream_t stream;
+};
+
+// Launch paged_multi_query_kernel<D, BS, T>.
+cudaError_t launch_multi_query_bf16(int D, int BS, const MultiQueryLaunch& L);
+cudaError_t launch_multi_query_f16(int D, int BS, const MultiQueryLaunch& L);
 
 // Raise a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask, size_t bytes);

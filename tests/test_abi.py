@@ -150,3 +150,21 @@ def test_device_allocator_rejects_invalid_arguments(L):
     assert L.pkv_device_rebuild_free_list(FAKE, NULL, FAKE, 8, NULL) == 1
     assert L.pkv_device_free_blocks(FAKE, FAKE, FAKE, NULL, 3, 8, NULL) == 1
     assert L.pkv_device_append_slots(FAKE, FAKE, FAKE, FAKE, 4, FAKE, 0, 16, 8, FAKE, NULL) == 0
+
+
+def test_multi_query_rejects_invalid_arguments(L):
+    def mq(**kw):
+        a = dict(out=FAKE, od=1, q=FAKE, qs=FAKE, T=8, mq=4, k=FAKE, v=FAKE, kd=1, bt=FAKE, mb=4,
+                 cl=FAKE, S=2, H=8, Hk=2, D=128, B=16, nb=10, scale=0.1, mc=64, st=NULL)
+        a.update(kw)
+        return L.paged_attn_multi_query(a["out"], a["od"], a["q"], a["qs"], a["T"], a["mq"],
+                                        a["k"], a["v"], a["kd"], a["bt"], a["mb"], a["cl"],
+                                        a["S"], a["H"], a["Hk"], a["D"], a["B"], a["nb"],
+                                        a["scale"], a["mc"], a["st"])
+    assert mq(S=-1) == 1
+    assert mq(H=6, Hk=4) == 1
+    assert mq(D=96) == 2
+    assert mq(qs=NULL) == 1
+    assert mq(mc=1000) == 1          # beyond the block table (4 blocks of 16)
+    assert mq(out=C.c_void_p(4104)) == 1
+    assert mq(T=0) == 0 and mq(S=0) == 0
