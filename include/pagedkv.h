@@ -198,8 +198,10 @@ PKV_API pkv_status paged_attn_decode_noalloc(void* out, pkv_dtype out_dtype, con
  *   other arguments as paged_attn_decode.
  * A sequence whose q_len is negative, above its context, above max_q_len or
  * whose context exceeds max_context_len is skipped (its rows are not
- * written) and flagged PKV_DEVERR_CONTEXT.  Tensor cores (mma.sync): query
- * tokens x query heads of one kv head form the tile rows.
+ * written) and flagged PKV_DEVERR_CONTEXT.  Tensor cores: query tokens x
+ * query heads of one kv head form the tile rows, 16 per warp on mma.sync,
+ * or 128 per CTA on tcgen05 with the environment variable PKV_MQ_TC=1
+ * (where total_q >= 128 / group).
  */
 PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const void* q,
                                           const int32_t* q_start, int total_q, int max_q_len,

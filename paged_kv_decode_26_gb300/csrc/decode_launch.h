@@ -28,6 +28,7 @@ cudaError_t launch_decode_mma_bf16(int D, int BS, const DecodeLaunch& L);
 cudaError_t launch_decode_mma_f16(int D, int BS, const DecodeLaunch& L);
 
 struct MultiQueryLaunch {
+    CUtensorMap tm_q;   // tcgen05 kernel only
     CUtensorMap tm_k;
     CUtensorMap tm_v;
     MultiQueryParams p;
@@ -40,6 +41,9 @@ struct MultiQueryLaunch {
 // Launch paged_multi_query_kernel<D, BS, T>.
 cudaError_t launch_multi_query_bf16(int D, int BS, const MultiQueryLaunch& L);
 cudaError_t launch_multi_query_f16(int D, int BS, const MultiQueryLaunch& L);
+// Launch paged_multi_query_tc_kernel<D, BS, T> (tcgen05 tensor cores, 128 rows per CTA).
+cudaError_t launch_multi_query_tc_bf16(int D, int BS, const MultiQueryLaunch& L);
+cudaError_t launch_multi_query_tc_f16(int D, int BS, const MultiQueryLaunch& L);
 
 // Raise a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask, size_t bytes);

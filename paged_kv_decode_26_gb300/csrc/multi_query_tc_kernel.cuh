@@ -1,0 +1,490 @@
+// multi_query_tc_kernel.cuh -- causal attention of several new tokens per
+// sequence over the paged KV cache on Blackwell's 5th-generation tensor
+// cores (tcgen05: MMAs issued by one thread from shared-memory descriptors,
+// fp32 accumulators in tensor memory), sm_103a.  Same operation, inputs and
+// outputs as paged_multi_query_kernel; chosen when a CTA's 128 query rows
+// are well filled.
+//
+// Pages followed (cited by title and section):
+//   [SWAP]   "vLLM 中 FlashAttention 与 KVCache 交换机制深度解析": FlashAttention
+//            (Kernel Fusion + Tiling + OnlineSoftmax: Q, K, V tiles through
+//            on-chip memory, the running max M and sum L, O rescaled) and the
+//            serving loop's prefill step.
+//   [LAYOUT] "大模型长文本推理基座从 FlashAttention 硬件加速机制到 vLLM 核心
+//            PagedAttention 显存物理布局深度剖析", section 二.2: block table.
+//
+// One CTA per (query tile, kv head, sequence).  Its 128 rows are 128/G query
+// tokens x the G query heads of the kv head (row r: token r / G, head r % G).
+// Warps 0-3 run the softmax, one thread per row (thread r owns tensor-memory
+// lane r); warp 4 owns the tensor memory and its lane 0 issues every TMA
+// load and MMA.  Per tile j of 64 keys:
+//   K_j, V_j            pages by TMA into a ring of `stages` slots, per head
+//                       64-element boxes with 128-byte swizzle
+//   S_j = Q K_j^T       M=128 N=64, A = Q (K-major), B = K_j (K-major), into
+//                       one of two S buffers in tensor memory
+//   P_j                 2^(x - m) as hi + lo 16-bit parts, written by the
+//                       softmax threads into one of two swizzled buffers
+//   O += P_j V_j        M=128 N=D, B = V_j (MN-major: D contiguous), O in
+//                       tensor memory
+// S_{j+2} is computed while the softmax works on tile j+1, and P_{j+1} is
+// written while P_j V_j runs.  Rescaling O costs a tensor-memory round
+// trip, so a row keeps an older maximum until a new score exceeds it by
+// more than 2^8 (P <= 256 meanwhile; O and the sum L share the maximum they
+// were built with, so the quotient is unchanged).  V rows past the context,
+// on a missing page or never loaded are zeroed before the P V product
+// (P is 0 there, but 0 * NaN is not).
+#pragma once
+
+#include <type_traits>
+
+#include "multi_query_kernel.cuh"
+
+namespace pkv {
+
+constexpr int kTcKeys = 64;          // keys per tile (N of S = Q K^T)
+constexpr int kTcRows = 128;         // query rows per CTA (M)
+constexpr int kTcThreads = 160;      // 4 softmax warps + 1 issuer warp
+constexpr float kTcRescale = 8.0f;   // log2 of the growth tolerated before O is rescaled
+
+// ---------------------------------------------------------------- tcgen05
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start, leading and
+// stride byte offsets (>> 4), descriptor version 1.
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulator, A and B both of type
+// T, A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
+template <typename T>
+__device__ __forceinline__ uint32_t tc_idesc(int M, int N, int b_mn) {
+    const uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// `bar` completes once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Makes this thread's ordinary shared-memory stores visible to the tensor
+// core (async proxy) once a barrier orders them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+#define PKV_TC_REGS32(r)                                                                       \
+    "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),         \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),          \
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),          \
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+
+// 32 consecutive 32-bit columns of one tensor-memory lane per thread
+// (32x32b shape: thread i of warp w reads lane 32 (w % 4) + i).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : PKV_TC_REGS32(r)
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared memory of one CTA: 1 KB alignment slack, Q, the K/V ring, two P
+// buffers (hi, lo each), barriers, block ids, one word.
+inline size_t multi_query_tc_smem_bytes(int D, int stages, int max_pages) {
+    const size_t q = (size_t)kTcRows * D * 2;
+    const size_t kv = (size_t)stages * 2 * kTcKeys * D * 2;
+    const size_t pp = 2 * 2 * (size_t)kTcRows * kTcKeys * 2;
+    return 1024 + q + kv + pp + (size_t)(2 * stages + 8) * sizeof(uint64_t) +
+           (size_t)max_pages * sizeof(int) + sizeof(int);
+}
+
+template <int D, int BS, typename T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    paged_multi_query_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                const __grid_constant__ CUtensorMap tm_k,
+                                const __grid_constant__ CUtensorMap tm_v,
+                                const MultiQueryParams p) {
+    constexpr int HALVES = D / 64;
+    constexpr int PAGES = kTcKeys / BS;                 // pages per key tile
+    constexpr uint32_t KV_HALF = kTcKeys * 128;         // [64 keys x 64 elements]
+    constexpr uint32_t KV_BYTES = HALVES * KV_HALF;     // one K (or V) tile
+    constexpr uint32_t Q_HALF = kTcRows * 128;          // [128 rows x 64 elements]
+    constexpr uint32_t P_BYTES = kTcRows * 128;         // [128 rows x 64 keys]
+    constexpr uint32_t TMEM_COLS = (D + 2 * kTcKeys) <= 128 ? 128 : 256;
+    constexpr uint32_t O_COL = 0, S_COL = D;            // O, then the two S buffers
+    static_assert(kTcKeys % BS == 0 && D % 64 == 0 && D + 2 * kTcKeys <= 256, "shape");
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+
+    const int tile = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int s = blockIdx.z;
+    const int G = p.group;
+    // stages >= 3: tile j+2 is already on its way when S_{j+2} is issued
+    if (blockDim.x != kTcThreads || G < 1 || G > 8 || kTcRows % G != 0 || p.stages < 3) {
+        if (threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONFIG);
+        return;
+    }
+    const int QT = kTcRows / G;                  // query tokens per CTA
+    const int qs0 = p.q_start[s], qs1 = p.q_start[s + 1];
+    const int n = p.context_lens[s];
+    const int q_len = qs1 - qs0;
+    if (q_len < 0 || q_len > n || qs0 < 0 || qs1 > p.total_q || q_len > p.max_q_len ||
+        n > p.max_blocks_per_seq * BS || (n + BS - 1) / BS > p.max_pages) {
+        if (tile == 0 && kvh == 0 && threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONTEXT);
+        return;
+    }
+    const int tok_lo = tile * QT;
+    if (tok_lo >= q_len) return;
+    const int tok_hi = min(q_len, tok_lo + QT);
+    const int first_pos = n - q_len;                 // position of query token 0
+    const int n_keys = first_pos + tok_hi;           // keys the last row sees
+    const int n_tiles = (n_keys + kTcKeys - 1) / kTcKeys;
+    const int n_pages = (n_keys + BS - 1) / BS;
+
+    // ---- shared memory (1024-byte aligned for the swizzle)
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    unsigned char* sQ = sm;                                        // HALVES x [128 x 128 B]
+    unsigned char* sKV = sQ + HALVES * Q_HALF;                     // stages x (K, V)
+    unsigned char* sP = sKV + (size_t)p.stages * 2 * KV_BYTES;     // 2 x (hi, lo)
+    uint64_t* kv_full = reinterpret_cast<uint64_t*>(sP + 4 * P_BYTES);  // [stages]
+    uint64_t* kv_free = kv_full + p.stages;      // [stages]: P V of the slot's tile done
+    uint64_t* q_full = kv_free + p.stages;
+    uint64_t* s_full = q_full + 1;               // [2]: S of tile j in buffer j & 1
+    uint64_t* p_full = q_full + 3;               // [2]: P of tile j written (128 arrivals)
+    uint64_t* o_done = q_full + 5;               // [2]: P_j V_j done
+    uint64_t* fin = q_full + 7;                  // every MMA done
+    int* s_bid = reinterpret_cast<int*>(fin + 1);
+    int* s_tmem = s_bid + p.max_pages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
+        int b = p.block_tables[(size_t)s * p.max_blocks_per_seq + i];
+        if (b < 0 || b >= p.num_blocks) {
+            raise_error(p.errors, PKV_DEVERR_BLOCK_ID);
+            b = -1;
+        }
+        s_bid[i] = b;
+    }
+    if (warp == 4) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(s_tmem)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < p.stages; ++st) {
+            mbar_init(&kv_full[st], 1);
+            mbar_init(&kv_free[st], 1);
+        }
+        mbar_init(q_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], kTcRows);
+            mbar_init(&o_done[b], 1);
+        }
+        mbar_init(fin, 1);
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = (uint32_t)*s_tmem;
+
+    if (warp == 4) {
+        // ================= issuer: TMA loads and tcgen05.mma =================
+        if (lane == 0) {
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            const uint64_t keep = l2_policy_evict_normal();   // pages serve other query tiles
+            int issued = 0;      // tiles whose loads were issued
+            int consumed = 0;    // tiles whose arrival the issuer has seen
+            auto load_tile = [&](int j) {
+                const int st = j % p.stages;
+                unsigned char* dk = sKV + (size_t)st * 2 * KV_BYTES;
+                uint32_t bytes = 0;
+                for (int pg = 0; pg < PAGES; ++pg) {
+                    const int page = j * PAGES + pg;
+                    if (page < n_pages && s_bid[page] >= 0) bytes += 2 * HALVES * BS * 128;
+                }
+                if (bytes == 0) {
+                    mbar_arrive(&kv_full[st]);
+                } else {
+                    mbar_arrive_expect_tx(&kv_full[st], bytes);
+                    for (int pg = 0; pg < PAGES; ++pg) {
+                        const int page = j * PAGES + pg;
+                        if (page >= n_pages || s_bid[page] < 0) continue;
+                        for (int h = 0; h < HALVES; ++h) {
+                            tma_load_4d(dk + h * KV_HALF + pg * BS * 128, &tm_k, &kv_full[st], 0,
+                                        kvh * HALVES + h, 0, s_bid[page], keep);
+                            tma_load_4d(dk + KV_BYTES + h * KV_HALF + pg * BS * 128, &tm_v,
+                                        &kv_full[st], 0, kvh * HALVES + h, 0, s_bid[page], keep);
+                        }
+                    }
+                }
+                issued = j + 1;
+            };
+            // S_j = Q K_j^T into S buffer j & 1
+            const uint32_t id_s = tc_idesc<T>(kTcRows, kTcKeys, 0);
+            const uint32_t id_o = tc_idesc<T>(kTcRows, D, 1);
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % p.stages;
+                if (!mbar_wait(&kv_full[st], (j / p.stages) & 1, p.errors)) return false;
+                consumed = j + 1;
+                tc_fence_after();
+                const uint32_t kb = smem_addr(sKV + (size_t)st * 2 * KV_BYTES);
+                const uint32_t qb = smem_addr(sQ);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int h = ks / 4, kin = ks % 4;
+                    tc_mma(tmem + S_COL + (j & 1) * kTcKeys,
+                           tc_desc_sw128(qb + h * Q_HALF + kin * 32, 16, 1024),
+                           tc_desc_sw128(kb + h * KV_HALF + kin * 32, 16, 1024), id_s,
+                           ks > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[j & 1]);
+                return true;
+            };
+
+            mbar_arrive_expect_tx(q_full, HALVES * Q_HALF);
+            for (int h = 0; h < HALVES; ++h)
+                tma_load_4d(sQ + h * Q_HALF, &tm_q, q_full, 0, h, kvh * G, qs0 + tok_lo,
+                            l2_policy_evict_first());
+            for (int j = 0; j < n_tiles && j < p.stages; ++j) load_tile(j);
+
+            bool ok = mbar_wait(q_full, 0, p.errors);
+            for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = issue_s(j);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int st = j % p.stages;
+                if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, p.errors)) { ok = false; break; }
+                // O += P_j V_j (hi part, then lo part)
+                tc_fence_after();
+                const uint32_t vb = smem_addr(sKV + (size_t)st * 2 * KV_BYTES + KV_BYTES);
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t pb = smem_addr(sP + ((j & 1) * 2 + part) * P_BYTES);
+#pragma unroll
+                    for (int ks = 0; ks < kTcKeys / 16; ++ks)
+                        tc_mma(tmem + O_COL, tc_desc_sw128(pb + ks * 32, 16, 1024),
+                               tc_desc_sw128(vb + ks * 16 * 128, KV_HALF, 1024), id_o,
+                               (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc_commit(&o_done[j & 1]);
+                tc_commit(&kv_free[st]);
+                if (j + 2 < n_tiles && !issue_s(j + 2)) { ok = false; break; }
+                if (j + p.stages < n_tiles) {
+                    if (!mbar_wait(&kv_free[st], (j / p.stages) & 1, p.errors)) { ok = false; break; }
+                    load_tile(j + p.stages);
+                }
+            }
+            // every MMA complete before the tensor memory is released
+            tc_commit(fin);
+            mbar_wait(fin, 0, p.errors);
+            if (!ok) {
+                // loads still in flight must land before the CTA exits
+                for (int t = consumed; t < issued; ++t)
+                    mbar_wait(&kv_full[t % p.stages], (t / p.stages) & 1, p.errors);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax: thread r owns row r =================
+        const int r = threadIdx.x;                       // 0..127 = tensor-memory lane
+        const int tok = tok_lo + r / G;
+        const bool real = tok < tok_hi;
+        const int pos = real ? first_pos + tok : -1;     // last key of this row
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int b = j & 1;
+            const int st = j % p.stages;
+            bool w = mbar_wait(&s_full[b], (j >> 1) & 1, p.errors);
+            w = w && mbar_wait(&kv_full[st], (j / p.stages) & 1, p.errors);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[kTcKeys];
+            tc_ld32(t_lane + S_COL + b * kTcKeys, sr);
+            tc_ld32(t_lane + S_COL + b * kTcKeys + 32, sr + 32);
+            tc_wait_ld();
+            float x[kTcKeys];
+            const int key0 = j * kTcKeys;
+            // keys key0 .. last_key are causally visible to this row; a key on
+            // a missing page is dropped (last_key < n_pages * BS always)
+            const int last_key = min(pos, key0 + kTcKeys - 1);
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTcKeys; ++c) {
+                const int key = key0 + c;
+                const bool keep = key <= last_key && s_bid[min(key, n_pages * BS - 1) / BS] >= 0;
+                x[c] = keep ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
+                tmax = fmaxf(tmax, x[c]);
+            }
+            const bool first = m_used == -INFINITY;
+            const bool grow = tmax > m_used + kTcRescale;
+            float alpha = 1.f;
+            if (grow) {
+                alpha = first ? 1.f : exp2f(m_used - tmax);
+                m_used = tmax;
+            }
+            if (__any_sync(0xffffffffu, grow && !first)) {
+                // O of this warp's rows must hold P V up to tile j-1 before rescaling
+                const bool w2 = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.errors);
+                if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t ov[32];
+                    tc_ld32(t_lane + O_COL + c0, ov);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                    tc_st32(t_lane + O_COL + c0, ov);
+                }
+                tc_wait_st();
+            } else if (j >= 2) {
+                // P buffer b is free once P_{j-2} V_{j-2} is done
+                const bool w2 = mbar_wait(&o_done[b], ((j - 2) >> 1) & 1, p.errors);
+                if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+            }
+            l *= alpha;
+            const float mu = m_used == -INFINITY ? 0.f : m_used;
+            unsigned char* prow_hi = sP + (b * 2) * P_BYTES + r * 128;
+            unsigned char* prow_lo = prow_hi + P_BYTES;
+#pragma unroll
+            for (int cch = 0; cch < kTcKeys / 8; ++cch) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = exp2f(x[cch * 8 + 2 * e] - mu);
+                    const float c = exp2f(x[cch * 8 + 2 * e + 1] - mu);
+                    l += a + c;
+                    hw[e] = pack2<T>(a, c);
+                    const float2 h2 = unpack2<T>(hw[e]);
+                    lw[e] = pack2<T>(a - h2.x, c - h2.y);
+                }
+                const int sw = (cch ^ (r & 7)) * 16;
+                *reinterpret_cast<uint4*>(prow_hi + sw) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(prow_lo + sw) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            // V rows past the context, on a missing page or never loaded
+            // (beyond the last page this CTA reads) become zeros
+            {
+                unsigned char* sv = sKV + (size_t)st * 2 * KV_BYTES + KV_BYTES;
+                for (int idx = r; idx < kTcKeys * HALVES; idx += kTcRows) {
+                    const int row = idx % kTcKeys, h = idx / kTcKeys;
+                    const int key = key0 + row;
+                    if (key >= n || key >= n_pages * BS || s_bid[key / BS] < 0) {
+                        uint4* z = reinterpret_cast<uint4*>(sv + h * KV_HALF + row * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&p_full[b]);
+        }
+        // ---- O / L of this row
+        const int jl = n_tiles - 1;
+        const bool w3 = ok && mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, p.errors);
+        if (__all_sync(0xffffffffu, w3)) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int qh = kvh * G + r % G;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t ov[32];
+                tc_ld32(t_lane + O_COL + c0, ov);
+                tc_wait_ld();
+                if (!real) continue;
+                const size_t e = ((size_t)(qs0 + tok) * p.n_heads + qh) * D + c0;
+                if (p.out_dtype == PKV_F32) {
+                    float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        o4[c / 4] = make_float4(__uint_as_float(ov[c]) * inv,
+                                                __uint_as_float(ov[c + 1]) * inv,
+                                                __uint_as_float(ov[c + 2]) * inv,
+                                                __uint_as_float(ov[c + 3]) * inv);
+                } else {
+                    uint4* o4 = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + e);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8)
+                        o4[c / 8] = make_uint4(
+                            pack_out(__uint_as_float(ov[c]) * inv,
+                                     __uint_as_float(ov[c + 1]) * inv, p.out_dtype),
+                            pack_out(__uint_as_float(ov[c + 2]) * inv,
+                                     __uint_as_float(ov[c + 3]) * inv, p.out_dtype),
+                            pack_out(__uint_as_float(ov[c + 4]) * inv,
+                                     __uint_as_float(ov[c + 5]) * inv, p.out_dtype),
+                            pack_out(__uint_as_float(ov[c + 6]) * inv,
+                                     __uint_as_float(ov[c + 7]) * inv, p.out_dtype));
+                }
+            }
+        }
+    }
+
+    // ---- tensor memory is released after every thread is done with it
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+}
+
+}  // namespace pkv

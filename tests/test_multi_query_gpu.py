@@ -2,7 +2,9 @@
 causal attention of each sequence's last q_len tokens over its paged
 context, for query-head groups 1-8, head dims 64/128, block sizes 16/32,
 fp16/bf16 inputs, speculative-sized and prefill-sized chunks, ragged pages
-and NaN padding."""
+and NaN padding.  Both kernels are covered: the mma.sync kernel (16 rows
+per warp) and the tcgen05 kernel (128 rows per CTA), selected through
+PKV_MQ_TC."""
 import numpy as np
 import pytest
 import torch
@@ -35,34 +37,54 @@ def _run(pkv, case, q, qs, out_dtype=None):
     return out
 
 
+def _abs_v(case, q, qs):
+    """sum_t w_t |V_t| per output element (the oracle's attention with |V|),
+    for the weight-rounding term of the parity bound."""
+    return lambda: orc.multi_query(q, case.k_pool, case.v_pool.abs(), case.block_tables,
+                                   case.context_lens, qs, case.scale)
+
+
+def _close(got, ref, case, q, qs, out_dtype=None, what=""):
+    assert_attention_close(got, ref, out_dtype or case.out_dtype, what,
+                           abs_weighted=_abs_v(case, q, qs), kv_dtype=case.dtype)
+
+
+@pytest.fixture(params=["mma", "tc"])
+def path(request, monkeypatch):
+    """Forces one multi-query kernel (the tcgen05 one needs at least 128/G
+    query rows in the call; smaller calls take the mma.sync kernel)."""
+    monkeypatch.setenv("PKV_MQ_TC", "1" if request.param == "tc" else "0")
+    return request.param
+
+
 @pytest.mark.parametrize("D,B", [(128, 16), (64, 16), (128, 32), (64, 32)])
 @pytest.mark.parametrize("H,Hk", [(8, 8), (8, 4), (16, 4), (16, 2)])
 @pytest.mark.parametrize("q_len", [("const", 1), ("uniform", 1, 7), ("uniform", 20, 90)])
-def test_matches_oracle(pkv, D, B, H, Hk, q_len):
+def test_matches_oracle(pkv, path, D, B, H, Hk, q_len):
     case = wl.make_case(3, S=5, lens=("uniform", 1, 300), H=H, Hk=Hk, D=D, B=B, share_blocks=2,
                         poison=True, seed=D + B + H + Hk)
     q, qs = wl.multi_query_inputs(case, q_len, seed=H + D)
     got = _run(pkv, case, q, qs)
     ref = orc.multi_query(q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, qs,
                           case.scale)
-    assert_attention_close(got, ref, case.out_dtype, f"{D} {B} {H}/{Hk} {q_len}")
+    _close(got, ref, case, q, qs, what=f"{D} {B} {H}/{Hk} {q_len}")
     assert pkv.device_errors(clear=True) == 0
 
 
 @pytest.mark.parametrize("dtype,out_dtype", [(torch.float16, torch.float32),
                                              (torch.float16, torch.float16),
                                              (torch.bfloat16, torch.float32)])
-def test_dtypes(pkv, dtype, out_dtype):
+def test_dtypes(pkv, path, dtype, out_dtype):
     case = wl.make_case(2, S=4, lens=("uniform", 30, 200), H=8, Hk=2, D=128, dtype=dtype,
                         out_dtype=out_dtype, poison=True)
     q, qs = wl.multi_query_inputs(case, ("uniform", 1, 40))
     got = _run(pkv, case, q, qs)
     ref = orc.multi_query(q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, qs,
                           case.scale)
-    assert_attention_close(got, ref, out_dtype)
+    _close(got, ref, case, q, qs, out_dtype)
 
 
-def test_whole_context_prefill_and_one_token_rows(pkv):
+def test_whole_context_prefill_and_one_token_rows(pkv, path):
     """q_len = context (a prefill from scratch: row 0 sees one key, so its
     output is exactly V_0) and q_len = 1 (equals paged_attn_decode)."""
     case = wl.make_case(2, S=3, lens_override=[70, 16, 33], H=4, Hk=4, D=128,
@@ -71,7 +93,7 @@ def test_whole_context_prefill_and_one_token_rows(pkv):
     got = _run(pkv, case, q, qs)
     ref = orc.multi_query(q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, qs,
                           case.scale)
-    assert_attention_close(got, ref, torch.float32)
+    _close(got, ref, case, q, qs, torch.float32)
     for s in range(case.S):
         p0 = int(case.block_tables[s, 0])
         assert torch.equal(got[int(qs[s])].cpu(), case.v_pool[p0, 0].float())
@@ -94,3 +116,105 @@ def test_bad_q_start_is_flagged(pkv):
                                case.block_tables.cuda(), case.context_lens.cuda(), case.scale, 40,
                                20)
     assert pkv.device_errors(clear=True) & 0x2
+
+
+# ------------------------------------------------- tcgen05 kernel specifics
+
+def _oracle(case, q, qs):
+    return orc.multi_query(q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, qs,
+                           case.scale)
+
+
+@pytest.mark.parametrize("D,B", [(128, 16), (64, 32), (128, 32), (64, 16)])
+@pytest.mark.parametrize("H,Hk", [(8, 8), (8, 4), (32, 4), (16, 8)])
+def test_tc_several_tiles_ragged(pkv, monkeypatch, D, B, H, Hk):
+    """Chunks of 100-400 tokens: several 128-row tiles per (sequence, kv
+    head) with a ragged last tile, contexts of many 64-key tiles with a
+    ragged last tile, shared pages and NaN in every row outside a context."""
+    monkeypatch.setenv("PKV_MQ_TC", "1")
+    case = wl.make_case(2, S=4, lens=("uniform", 150, 700), H=H, Hk=Hk, D=D, B=B, share_blocks=3,
+                        poison=True, seed=D * B + H)
+    q, qs = wl.multi_query_inputs(case, ("uniform", 100, 400), seed=H * Hk)
+    got = _run(pkv, case, q, qs)
+    _close(got, _oracle(case, q, qs), case, q, qs, what=f"{D} {B} {H}/{Hk}")
+    assert pkv.device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("gain", [8.0, 40.0])
+def test_tc_rescale_of_wide_scores(pkv, monkeypatch, gain):
+    """Queries scaled up so that scores spread over tens of binary orders:
+    the running maximum of a row grows by more than 2^8 from one key tile to
+    the next, which takes the kernel's O-rescaling branch."""
+    monkeypatch.setenv("PKV_MQ_TC", "1")
+    case = wl.make_case(2, S=3, lens=("uniform", 300, 600), H=8, Hk=2, D=128,
+                        out_dtype=torch.float32, poison=True, seed=5)
+    q, qs = wl.multi_query_inputs(case, ("uniform", 150, 300), seed=6)
+    q = (q.float() * gain).to(case.dtype)
+    got = _run(pkv, case, q, qs)
+    _close(got, _oracle(case, q, qs), case, q, qs, torch.float32, f"gain {gain}")
+    assert pkv.device_errors(clear=True) == 0
+
+
+def test_tc_increasing_scores(pkv, monkeypatch):
+    """Key t scores t * c against every query, so each new key tile raises
+    every row's maximum (rescale on every tile once the growth passes 2^8)."""
+    monkeypatch.setenv("PKV_MQ_TC", "1")
+    case = wl.make_case(2, S=2, lens_override=[640, 517], H=4, Hk=1, D=64,
+                        out_dtype=torch.float32, poison=True, seed=9)
+    k = case.k_pool.float()
+    for s in range(case.S):
+        for t in range(int(case.context_lens[s])):
+            blk = int(case.block_tables[s, t // case.B])
+            k[blk, t % case.B, 0, :] = 0.05 * t
+    case.k_pool = k.to(case.dtype)
+    q, qs = wl.multi_query_inputs(case, ("const", 256), seed=3)
+    q = q.float().abs().to(case.dtype)
+    got = _run(pkv, case, q, qs)
+    _close(got, _oracle(case, q, qs), case, q, qs, torch.float32)
+    assert pkv.device_errors(clear=True) == 0
+
+
+def test_tc_missing_pages_are_skipped(pkv, monkeypatch):
+    """A block id of -1 inside a context (a page the table does not hold)
+    is skipped like in the mma.sync kernel, and flagged."""
+    case = wl.make_case(2, S=3, lens_override=[400, 300, 260], H=8, Hk=4, D=128,
+                        out_dtype=torch.float32, seed=12)
+    q, qs = wl.multi_query_inputs(case, ("const", 200), seed=13)
+    bt = case.block_tables.clone()
+    bt[0, 3] = -1
+    bt[1, 0] = -1
+    case.block_tables = bt
+    outs = {}
+    for mode in ("0", "1"):
+        monkeypatch.setenv("PKV_MQ_TC", mode)
+        outs[mode] = _run(pkv, case, q, qs)
+        assert pkv.device_errors(clear=True) & 0x1
+    ref = _oracle_skip_missing(case, q, qs)
+    for mode, got in outs.items():
+        assert_attention_close(got, ref, torch.float32, f"PKV_MQ_TC={mode}",
+                               abs_weighted=lambda: _oracle_skip_missing(case, q, qs, True),
+                               kv_dtype=case.dtype)
+
+
+def _oracle_skip_missing(case, q, qs, abs_v=False):
+    """Attention over the keys whose page the table holds (fp64, plain
+    softmax): the kernels skip an out-of-range block id, so its keys drop out
+    of both the scores and the sum.  abs_v: attention of |V| instead."""
+    out = torch.zeros(q.shape[0], case.H, case.D, dtype=torch.float64)
+    bt, G = case.block_tables, case.H // case.Hk
+    for s in range(case.S):
+        n = int(case.context_lens[s])
+        a, b = int(qs[s]), int(qs[s + 1])
+        keep = torch.tensor([t for t in range(n) if int(bt[s, t // case.B]) >= 0])
+        blk = torch.tensor([int(bt[s, int(t) // case.B]) for t in keep])
+        K = case.k_pool[blk, keep % case.B].double()          # [n_keep, Hk, D]
+        V = case.v_pool[blk, keep % case.B].double()
+        if abs_v:
+            V = V.abs()
+        pos = torch.arange(n - (b - a), n)                    # positions of the rows
+        visible = keep[None, :] <= pos[:, None]               # [rows, n_keep]
+        for h in range(case.H):
+            sc = (q[a:b, h].double() @ K[:, h // G].T) * case.scale
+            sc = sc.masked_fill(~visible, float("-inf"))
+            out[a:b, h] = torch.softmax(sc, 1) @ V[:, h // G]
+    return out.numpy()
