@@ -542,14 +542,16 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
     const void* vmap_base = num_blocks > 0 ? v_pool : q;
     const int map_blocks = num_blocks > 0 ? num_blocks : 1;
 
-    // tcgen05 path: 128 rows (128/G tokens x G heads) per CTA, taken with
-    // PKV_MQ_TC=1 where it applies.
+    // tcgen05 path: two query tiles of 128 rows (128/G tokens x G heads) per
+    // CTA.  Chosen when the longest chunk fills at least one such tile;
+    // PKV_MQ_TC=0/1 forces it off/on where it applies.
     {
         const int tc_tokens = pkv::kTcRows / G;
-        const int want = env_int("PKV_MQ_TC", 0);
-        int stages = env_int("PKV_MQ_TC_STAGES", head_dim == 64 ? 4 : 3);
-        stages = stages < 3 ? 3 : (stages > 8 ? 8 : stages);
-        while (stages > 3 && pkv::multi_query_tc_smem_bytes(head_dim, stages, max_pages) >
+        int want = env_int("PKV_MQ_TC", -1);
+        if (want < 0) want = (long long)max_q_len * G >= pkv::kTcRows ? 1 : 0;
+        int stages = env_int("PKV_MQ_TC_STAGES", head_dim == 64 ? 6 : 4);
+        stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+        while (stages > 2 && pkv::multi_query_tc_smem_bytes(head_dim, stages, max_pages) >
                                  (size_t)dev->smem_optin)
             --stages;
         const size_t smem = pkv::multi_query_tc_smem_bytes(head_dim, stages, max_pages);
@@ -584,7 +586,8 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
             p.stages = stages;
             p.max_pages = max_pages;
             p.errors = dev->errors;
-            L.grid = dim3((unsigned)((max_q_len + tc_tokens - 1) / tc_tokens),
+            const int cta_tokens = pkv::kTcQTiles * tc_tokens;
+            L.grid = dim3((unsigned)((max_q_len + cta_tokens - 1) / cta_tokens),
                           (unsigned)n_kv_heads, (unsigned)num_seqs);
             L.block = dim3((unsigned)pkv::kTcThreads);
             L.smem_bytes = smem;

@@ -13,26 +13,28 @@
 //   [LAYOUT] "大模型长文本推理基座从 FlashAttention 硬件加速机制到 vLLM 核心
 //            PagedAttention 显存物理布局深度剖析", section 二.2: block table.
 //
-// One CTA per (query tile, kv head, sequence).  Its 128 rows are 128/G query
-// tokens x the G query heads of the kv head (row r: token r / G, head r % G).
-// Warps 0-3 run the softmax, one thread per row (thread r owns tensor-memory
-// lane r); warp 4 owns the tensor memory and its lane 0 issues every TMA
-// load and MMA.  Per tile j of 64 keys:
+// One CTA per (pair of query tiles, kv head, sequence).  A query tile is 128
+// rows: 128/G consecutive query tokens x the G query heads of the kv head
+// (row r: token r / G, head r % G); the pair shares every K/V page it loads.
+// Warps 0-3 and 4-7 run the softmax of tile 0 and tile 1, one thread per row
+// (thread r of a group owns tensor-memory lane r); warp 8 owns the tensor
+// memory and its lane 0 issues every MMA; lane 0 of warp 9 issues the TMA
+// loads.  Per key tile j of 64 keys and query tile t:
 //   K_j, V_j            pages by TMA into a ring of `stages` slots, per head
 //                       64-element boxes with 128-byte swizzle
-//   S_j = Q K_j^T       M=128 N=64, A = Q (K-major), B = K_j (K-major), into
-//                       one of two S buffers in tensor memory
-//   P_j                 2^(x - m) as hi + lo 16-bit parts, written by the
-//                       softmax threads into one of two swizzled buffers
-//   O += P_j V_j        M=128 N=D, B = V_j (MN-major: D contiguous), O in
-//                       tensor memory
-// S_{j+2} is computed while the softmax works on tile j+1, and P_{j+1} is
-// written while P_j V_j runs.  Rescaling O costs a tensor-memory round
-// trip, so a row keeps an older maximum until a new score exceeds it by
-// more than 2^8 (P <= 256 meanwhile; O and the sum L share the maximum they
-// were built with, so the quotient is unchanged).  V rows past the context,
-// on a missing page or never loaded are zeroed before the P V product
-// (P is 0 there, but 0 * NaN is not).
+//   S_tj = Q_t K_j^T    M=128 N=64, A = Q_t (K-major), B = K_j (K-major), into
+//                       one of two S buffers of tile t in tensor memory
+//   P_tj                2^(x - m) as hi + lo 16-bit parts, written by the
+//                       softmax threads into the S buffer they just read
+//   O_t += P_tj V_j     M=128 N=D, A = P from tensor memory, B = V_j
+//                       (MN-major: D contiguous), O_t in tensor memory
+// S_t,j+1 is ready while the softmax works on tile j, so the tensor core
+// alternates between the groups' products.  Rescaling O costs a
+// tensor-memory round trip, so a row keeps an older maximum until a new
+// score exceeds it by more than 2^8 (P <= 256 meanwhile; O and the sum L
+// share the maximum they were built with, so the quotient is unchanged).
+// V rows past the context, on a missing page or never loaded are zeroed
+// before the P V product (P is 0 there, but 0 * NaN is not).
 #pragma once
 
 #include <type_traits>
@@ -42,8 +44,9 @@
 namespace pkv {
 
 constexpr int kTcKeys = 64;          // keys per tile (N of S = Q K^T)
-constexpr int kTcRows = 128;         // query rows per CTA (M)
-constexpr int kTcThreads = 160;      // 4 softmax warps + 1 issuer warp
+constexpr int kTcRows = 128;         // query rows per query tile (M)
+constexpr int kTcQTiles = 2;         // query tiles per CTA
+constexpr int kTcThreads = 320;      // 8 softmax warps, 1 MMA warp, 1 TMA warp
 constexpr float kTcRescale = 8.0f;   // log2 of the growth tolerated before O is rescaled
 
 // ---------------------------------------------------------------- tcgen05
@@ -75,6 +78,18 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Same with A read from tensor memory: row i of A in lane i, 16-bit
+// elements k = 2c, 2c + 1 in the low and high half of column c (one K=16
+// step spans 8 columns).
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -136,13 +151,12 @@ __device__ __forceinline__ void tc_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Shared memory of one CTA: 1 KB alignment slack, Q, the K/V ring, two P
-// buffers (hi, lo each), barriers, block ids, one word.
+// Shared memory of one CTA: 1 KB alignment slack, the two Q tiles, the K/V
+// ring, barriers, block ids, one word.
 inline size_t multi_query_tc_smem_bytes(int D, int stages, int max_pages) {
-    const size_t q = (size_t)kTcRows * D * 2;
+    const size_t q = (size_t)kTcQTiles * kTcRows * D * 2;
     const size_t kv = (size_t)stages * 2 * kTcKeys * D * 2;
-    const size_t pp = 2 * 2 * (size_t)kTcRows * kTcKeys * 2;
-    return 1024 + q + kv + pp + (size_t)(2 * stages + 8) * sizeof(uint64_t) +
+    return 1024 + q + kv + (size_t)(2 * stages + 14) * sizeof(uint64_t) +
            (size_t)max_pages * sizeof(int) + sizeof(int);
 }
 
@@ -157,10 +171,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr uint32_t KV_HALF = kTcKeys * 128;         // [64 keys x 64 elements]
     constexpr uint32_t KV_BYTES = HALVES * KV_HALF;     // one K (or V) tile
     constexpr uint32_t Q_HALF = kTcRows * 128;          // [128 rows x 64 elements]
-    constexpr uint32_t P_BYTES = kTcRows * 128;         // [128 rows x 64 keys]
-    constexpr uint32_t TMEM_COLS = (D + 2 * kTcKeys) <= 128 ? 128 : 256;
-    constexpr uint32_t O_COL = 0, S_COL = D;            // O, then the two S buffers
-    static_assert(kTcKeys % BS == 0 && D % 64 == 0 && D + 2 * kTcKeys <= 256, "shape");
+    constexpr uint32_t Q_BYTES = HALVES * Q_HALF;       // one query tile
+    constexpr uint32_t TMEM_COLS = 512;
+    constexpr uint32_t TILE_COLS = 256;                 // per query tile: O, then two S buffers
+    constexpr uint32_t S_COL = D;
+    constexpr int ALL_PAGES = (1 << PAGES) - 1;
+    static_assert(kTcKeys % BS == 0 && D % 64 == 0 && D + 2 * kTcKeys <= TILE_COLS, "shape");
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
 
@@ -168,12 +184,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int kvh = blockIdx.y;
     const int s = blockIdx.z;
     const int G = p.group;
-    // stages >= 3: tile j+2 is already on its way when S_{j+2} is issued
-    if (blockDim.x != kTcThreads || G < 1 || G > 8 || kTcRows % G != 0 || p.stages < 3) {
+    if (blockDim.x != kTcThreads || G < 1 || G > 8 || kTcRows % G != 0 || p.stages < 2) {
         if (threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONFIG);
         return;
     }
-    const int QT = kTcRows / G;                  // query tokens per CTA
+    const int QT = kTcRows / G;                  // query tokens per query tile
     const int qs0 = p.q_start[s], qs1 = p.q_start[s + 1];
     const int n = p.context_lens[s];
     const int q_len = qs1 - qs0;
@@ -182,27 +197,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (tile == 0 && kvh == 0 && threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONTEXT);
         return;
     }
-    const int tok_lo = tile * QT;
+    const int tok_lo = tile * kTcQTiles * QT;
     if (tok_lo >= q_len) return;
-    const int tok_hi = min(q_len, tok_lo + QT);
     const int first_pos = n - q_len;                 // position of query token 0
-    const int n_keys = first_pos + tok_hi;           // keys the last row sees
-    const int n_tiles = (n_keys + kTcKeys - 1) / kTcKeys;
+    // key tiles each query tile needs (0: the tile has no token)
+    int nt[kTcQTiles];
+#pragma unroll
+    for (int t = 0; t < kTcQTiles; ++t) {
+        const int lo = tok_lo + t * QT;
+        const int hi = min(q_len, lo + QT);
+        nt[t] = lo < q_len ? (first_pos + hi + kTcKeys - 1) / kTcKeys : 0;
+    }
+    const int n_tiles = max(nt[0], nt[1]);
+    const int n_keys = first_pos + min(q_len, tok_lo + kTcQTiles * QT);
     const int n_pages = (n_keys + BS - 1) / BS;
+    const int zero_from = min(n, n_pages * BS);      // V rows from here on are zeroed
 
     // ---- shared memory (1024-byte aligned for the swizzle)
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    unsigned char* sQ = sm;                                        // HALVES x [128 x 128 B]
-    unsigned char* sKV = sQ + HALVES * Q_HALF;                     // stages x (K, V)
-    unsigned char* sP = sKV + (size_t)p.stages * 2 * KV_BYTES;     // 2 x (hi, lo)
-    uint64_t* kv_full = reinterpret_cast<uint64_t*>(sP + 4 * P_BYTES);  // [stages]
-    uint64_t* kv_free = kv_full + p.stages;      // [stages]: P V of the slot's tile done
+    unsigned char* sQ = sm;                                         // 2 x HALVES x [128 x 128 B]
+    unsigned char* sKV = sQ + kTcQTiles * Q_BYTES;                  // stages x (K, V)
+    uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + (size_t)p.stages * 2 * KV_BYTES);
+    uint64_t* kv_free = kv_full + p.stages;      // [stages]: every P V of the slot's tile done
     uint64_t* q_full = kv_free + p.stages;
-    uint64_t* s_full = q_full + 1;               // [2]: S of tile j in buffer j & 1
-    uint64_t* p_full = q_full + 3;               // [2]: P of tile j written (128 arrivals)
-    uint64_t* o_done = q_full + 5;               // [2]: P_j V_j done
-    uint64_t* fin = q_full + 7;                  // every MMA done
+    uint64_t* s_full = q_full + 1;               // [tile][buffer]: S ready
+    uint64_t* p_full = s_full + 4;               // [tile][buffer]: P written (128 arrivals)
+    uint64_t* o_done = p_full + 4;               // [tile][parity of key tile]: P V done
+    uint64_t* fin = o_done + 4;                  // every MMA done
     int* s_bid = reinterpret_cast<int*>(fin + 1);
     int* s_tmem = s_bid + p.max_pages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         s_bid[i] = b;
     }
-    if (warp == 4) {
+    if (warp == 8) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(s_tmem)),
                      "r"(TMEM_COLS)
@@ -228,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&kv_free[st], 1);
         }
         mbar_init(q_full, 1);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 4; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], kTcRows);
             mbar_init(&o_done[b], 1);
@@ -241,17 +263,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem = (uint32_t)*s_tmem;
 
-    if (warp == 4) {
-        // ================= issuer: TMA loads and tcgen05.mma =================
+    // pages of key tile j that are present: bit pg for page j * PAGES + pg
+    auto page_mask = [&](int j) -> int {
+        int m = 0;
+#pragma unroll
+        for (int pg = 0; pg < PAGES; ++pg) {
+            const int page = j * PAGES + pg;
+            if (page < n_pages && s_bid[page] >= 0) m |= 1 << pg;
+        }
+        return m;
+    };
+    // V rows of key tile j that must be zeroed before P V: past the context,
+    // never loaded, or on a missing page
+    auto needs_zero = [&](int j) -> bool {
+        return (j + 1) * kTcKeys > zero_from || page_mask(j) != ALL_PAGES;
+    };
+
+    if (warp == 9) {
+        // ================= TMA producer =================
         if (lane == 0) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
+            uint32_t q_bytes = 0;
+#pragma unroll
+            for (int t = 0; t < kTcQTiles; ++t) q_bytes += nt[t] > 0 ? Q_BYTES : 0;
+            mbar_arrive_expect_tx(q_full, q_bytes);
+            const uint64_t once = l2_policy_evict_first();
+#pragma unroll
+            for (int t = 0; t < kTcQTiles; ++t) {
+                if (nt[t] == 0) continue;
+                for (int h = 0; h < HALVES; ++h)
+                    tma_load_4d(sQ + t * Q_BYTES + h * Q_HALF, &tm_q, q_full, 0, h, kvh * G,
+                                qs0 + tok_lo + t * QT, once);
+            }
             const uint64_t keep = l2_policy_evict_normal();   // pages serve other query tiles
-            int issued = 0;      // tiles whose loads were issued
-            int consumed = 0;    // tiles whose arrival the issuer has seen
-            auto load_tile = [&](int j) {
+            int issued = 0;
+            for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % p.stages;
+                if (j >= p.stages &&
+                    !mbar_wait(&kv_free[st], ((j / p.stages) - 1) & 1, p.errors))
+                    break;
                 unsigned char* dk = sKV + (size_t)st * 2 * KV_BYTES;
                 uint32_t bytes = 0;
                 for (int pg = 0; pg < PAGES; ++pg) {
@@ -274,204 +326,241 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 issued = j + 1;
-            };
-            // S_j = Q K_j^T into S buffer j & 1
+            }
+            // every load issued has landed before the CTA may exit (earlier
+            // tiles of a slot were consumed before the slot was refilled)
+            for (int j = max(0, issued - p.stages); j < issued; ++j)
+                mbar_wait(&kv_full[j % p.stages], (j / p.stages) & 1, p.errors);
+        }
+        __syncwarp();
+    } else if (warp == 8) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
             const uint32_t id_s = tc_idesc<T>(kTcRows, kTcKeys, 0);
             const uint32_t id_o = tc_idesc<T>(kTcRows, D, 1);
+            // S_tj = Q_t K_j^T for every query tile that needs key tile j
             auto issue_s = [&](int j) -> bool {
                 const int st = j % p.stages;
                 if (!mbar_wait(&kv_full[st], (j / p.stages) & 1, p.errors)) return false;
-                consumed = j + 1;
                 tc_fence_after();
                 const uint32_t kb = smem_addr(sKV + (size_t)st * 2 * KV_BYTES);
-                const uint32_t qb = smem_addr(sQ);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const int h = ks / 4, kin = ks % 4;
-                    tc_mma(tmem + S_COL + (j & 1) * kTcKeys,
-                           tc_desc_sw128(qb + h * Q_HALF + kin * 32, 16, 1024),
-                           tc_desc_sw128(kb + h * KV_HALF + kin * 32, 16, 1024), id_s,
-                           ks > 0 ? 1u : 0u);
+                for (int t = 0; t < kTcQTiles; ++t) {
+                    if (j >= nt[t]) continue;
+                    const uint32_t qb = smem_addr(sQ + t * Q_BYTES);
+                    const uint32_t d = tmem + t * TILE_COLS + S_COL + (j & 1) * kTcKeys;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const int h = ks / 4, kin = ks % 4;
+                        tc_mma(d, tc_desc_sw128(qb + h * Q_HALF + kin * 32, 16, 1024),
+                               tc_desc_sw128(kb + h * KV_HALF + kin * 32, 16, 1024), id_s,
+                               ks > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&s_full[t * 2 + (j & 1)]);
                 }
-                tc_commit(&s_full[j & 1]);
                 return true;
             };
-
-            mbar_arrive_expect_tx(q_full, HALVES * Q_HALF);
-            for (int h = 0; h < HALVES; ++h)
-                tma_load_4d(sQ + h * Q_HALF, &tm_q, q_full, 0, h, kvh * G, qs0 + tok_lo,
-                            l2_policy_evict_first());
-            for (int j = 0; j < n_tiles && j < p.stages; ++j) load_tile(j);
-
             bool ok = mbar_wait(q_full, 0, p.errors);
             for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = issue_s(j);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j % p.stages;
-                if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, p.errors)) { ok = false; break; }
-                // O += P_j V_j (hi part, then lo part)
-                tc_fence_after();
+                const uint32_t ph = (j >> 1) & 1;
+                // where V rows get zeroed, both groups finish writing before
+                // any P V of the tile reads V
+                const bool zero = needs_zero(j);
+                if (zero) {
+#pragma unroll
+                    for (int t = 0; t < kTcQTiles; ++t)
+                        if (j < nt[t] && !mbar_wait(&p_full[t * 2 + (j & 1)], ph, p.errors))
+                            ok = false;
+                    if (!ok) break;
+                }
                 const uint32_t vb = smem_addr(sKV + (size_t)st * 2 * KV_BYTES + KV_BYTES);
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t pb = smem_addr(sP + ((j & 1) * 2 + part) * P_BYTES);
+                for (int t = 0; t < kTcQTiles; ++t) {
+                    if (j >= nt[t]) continue;
+                    if (!zero && !mbar_wait(&p_full[t * 2 + (j & 1)], ph, p.errors)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t base = tmem + t * TILE_COLS;
+                    const uint32_t pa = base + S_COL + (j & 1) * kTcKeys;
 #pragma unroll
-                    for (int ks = 0; ks < kTcKeys / 16; ++ks)
-                        tc_mma(tmem + O_COL, tc_desc_sw128(pb + ks * 32, 16, 1024),
-                               tc_desc_sw128(vb + ks * 16 * 128, KV_HALF, 1024), id_o,
-                               (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int ks = 0; ks < kTcKeys / 16; ++ks)
+                            tc_mma_tmem_a(base, pa + part * (kTcKeys / 2) + ks * 8,
+                                          tc_desc_sw128(vb + ks * 16 * 128, KV_HALF, 1024), id_o,
+                                          (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                    tc_commit(&o_done[t * 2 + (j & 1)]);
                 }
-                tc_commit(&o_done[j & 1]);
+                if (!ok) break;
                 tc_commit(&kv_free[st]);
-                if (j + 2 < n_tiles && !issue_s(j + 2)) { ok = false; break; }
-                if (j + p.stages < n_tiles) {
-                    if (!mbar_wait(&kv_free[st], (j / p.stages) & 1, p.errors)) { ok = false; break; }
-                    load_tile(j + p.stages);
-                }
+                if (j + 2 < n_tiles) ok = issue_s(j + 2);
             }
             // every MMA complete before the tensor memory is released
             tc_commit(fin);
             mbar_wait(fin, 0, p.errors);
-            if (!ok) {
-                // loads still in flight must land before the CTA exits
-                for (int t = consumed; t < issued; ++t)
-                    mbar_wait(&kv_full[t % p.stages], (t / p.stages) & 1, p.errors);
-            }
         }
         __syncwarp();
     } else {
-        // ================= softmax: thread r owns row r =================
-        const int r = threadIdx.x;                       // 0..127 = tensor-memory lane
-        const int tok = tok_lo + r / G;
-        const bool real = tok < tok_hi;
-        const int pos = real ? first_pos + tok : -1;     // last key of this row
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-        float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1;
-            const int st = j % p.stages;
-            bool w = mbar_wait(&s_full[b], (j >> 1) & 1, p.errors);
-            w = w && mbar_wait(&kv_full[st], (j / p.stages) & 1, p.errors);
-            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t sr[kTcKeys];
-            tc_ld32(t_lane + S_COL + b * kTcKeys, sr);
-            tc_ld32(t_lane + S_COL + b * kTcKeys + 32, sr + 32);
-            tc_wait_ld();
-            float x[kTcKeys];
-            const int key0 = j * kTcKeys;
-            // keys key0 .. last_key are causally visible to this row; a key on
-            // a missing page is dropped (last_key < n_pages * BS always)
-            const int last_key = min(pos, key0 + kTcKeys - 1);
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kTcKeys; ++c) {
-                const int key = key0 + c;
-                const bool keep = key <= last_key && s_bid[min(key, n_pages * BS - 1) / BS] >= 0;
-                x[c] = keep ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-                tmax = fmaxf(tmax, x[c]);
-            }
-            const bool first = m_used == -INFINITY;
-            const bool grow = tmax > m_used + kTcRescale;
-            float alpha = 1.f;
-            if (grow) {
-                alpha = first ? 1.f : exp2f(m_used - tmax);
-                m_used = tmax;
-            }
-            if (__any_sync(0xffffffffu, grow && !first)) {
-                // O of this warp's rows must hold P V up to tile j-1 before rescaling
-                const bool w2 = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.errors);
-                if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+        // ================= softmax: group t, thread r owns row r of tile t =================
+        const int t = warp >> 2;
+        const int r = (warp & 3) * 32 + lane;            // tensor-memory lane
+        if (nt[t] > 0) {
+            const int tok = tok_lo + t * QT + r / G;
+            const bool real = tok < q_len;
+            const int pos = real ? first_pos + tok : -1;     // last key of this row
+            const uint32_t t_lane = tmem + t * TILE_COLS + ((uint32_t)((warp & 3) * 32) << 16);
+            const float sc = p.scale_log2;
+            const bool pos_sc = sc > 0.f;                    // the usual case
+            float m_used = -INFINITY;
+            float2 l2 = make_float2(0.f, 0.f);
+            bool ok = true;
+            for (int j = 0; j < nt[t]; ++j) {
+                const int b = j & 1;
+                const bool w = mbar_wait(&s_full[t * 2 + b], (j >> 1) & 1, p.errors);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 tc_fence_after();
+                uint32_t sr[kTcKeys];
+                tc_ld32(t_lane + S_COL + b * kTcKeys, sr);
+                tc_ld32(t_lane + S_COL + b * kTcKeys + 32, sr + 32);
+                tc_wait_ld();
+                const int key0 = j * kTcKeys;
+                const int pm = page_mask(j);
+                const bool full = key0 + kTcKeys - 1 <= pos && pm == ALL_PAGES;
+                // y: raw scores (scaled ones if the scale is not positive),
+                // -inf where a key is hidden from this row
+                float y[kTcKeys];
+                float mx = -INFINITY;
+                if (full && pos_sc) {
+#pragma unroll
+                    for (int c = 0; c < kTcKeys; ++c) {
+                        y[c] = __uint_as_float(sr[c]);
+                        mx = fmaxf(mx, y[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kTcKeys; ++c) {
+                        const bool keep = key0 + c <= pos && ((pm >> (c / BS)) & 1);
+                        const float v = pos_sc ? __uint_as_float(sr[c]) : __uint_as_float(sr[c]) * sc;
+                        y[c] = keep ? v : -INFINITY;
+                        mx = fmaxf(mx, y[c]);
+                    }
+                }
+                const float a = pos_sc ? sc : 1.f;           // exponent = y * a - m
+                const float tmax = mx * a;
+                const bool first = m_used == -INFINITY;
+                const bool grow = tmax > m_used + kTcRescale;
+                float alpha = 1.f;
+                if (grow) {
+                    alpha = first ? 1.f : exp2f(m_used - tmax);
+                    m_used = tmax;
+                }
+                if (__any_sync(0xffffffffu, grow && !first)) {
+                    // O of this warp's rows holds P V up to key tile j-1 first
+                    const bool w2 = mbar_wait(&o_done[t * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1,
+                                              p.errors);
+                    if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t ov[32];
+                        tc_ld32(t_lane + c0, ov);
+                        tc_wait_ld();
+                        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float2 v = __fmul2_rn(
+                                make_float2(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1])), a2);
+                            ov[c] = __float_as_uint(v.x);
+                            ov[c + 1] = __float_as_uint(v.y);
+                        }
+                        tc_st32(t_lane + c0, ov);
+                    }
+                }
+                if (j >= 2) {
+                    // keeps this barrier's phases in step with the waits above
+                    const bool w2 = mbar_wait(&o_done[t * 2 + b], ((j - 2) >> 1) & 1, p.errors);
+                    if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+                }
+                l2 = __fmul2_rn(l2, make_float2(alpha, alpha));
+                const float mu = m_used == -INFINITY ? 0.f : m_used;
+                const float2 a2 = make_float2(a, a), nmu2 = make_float2(-mu, -mu);
+                const float2 neg1 = make_float2(-1.f, -1.f);
+                // P = 2^(y a - m) as hi + lo over the S buffer just read: hi in
+                // its columns [0, 32), lo in [32, 64), keys 2i and 2i+1 in column i
+                uint32_t ph[kTcKeys / 2], pl[kTcKeys / 2];
+#pragma unroll
+                for (int i = 0; i < kTcKeys / 2; ++i) {
+                    const float2 e = __ffma2_rn(make_float2(y[2 * i], y[2 * i + 1]), a2, nmu2);
+                    const float2 pv = make_float2(exp2f(e.x), exp2f(e.y));
+                    l2 = __fadd2_rn(l2, pv);
+                    ph[i] = pack2<T>(pv.x, pv.y);
+                    const float2 lo = __ffma2_rn(unpack2<T>(ph[i]), neg1, pv);
+                    pl[i] = pack2<T>(lo.x, lo.y);
+                }
+                tc_st32(t_lane + S_COL + b * kTcKeys, ph);
+                tc_st32(t_lane + S_COL + b * kTcKeys + 32, pl);
+                if (needs_zero(j)) {
+                    const int st = j % p.stages;
+                    const bool w3 = mbar_wait(&kv_full[st], (j / p.stages) & 1, p.errors);
+                    if (!__all_sync(0xffffffffu, w3)) { ok = false; break; }
+                    unsigned char* sv = sKV + (size_t)st * 2 * KV_BYTES + KV_BYTES;
+                    for (int idx = r; idx < kTcKeys * HALVES; idx += kTcRows) {
+                        const int row = idx % kTcKeys, h = idx / kTcKeys;
+                        const int key = key0 + row;
+                        if (key >= zero_from || !((pm >> (row / BS)) & 1)) {
+                            uint4* z = reinterpret_cast<uint4*>(sv + h * KV_HALF + row * 128);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_full[t * 2 + b]);
+            }
+            // ---- O / L of this row
+            const int jl = nt[t] - 1;
+            const bool w4 = ok && mbar_wait(&o_done[t * 2 + (jl & 1)], (jl >> 1) & 1, p.errors);
+            if (__all_sync(0xffffffffu, w4)) {
+                tc_fence_after();
+                const float l = l2.x + l2.y;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int qh = kvh * G + r % G;
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t ov[32];
-                    tc_ld32(t_lane + O_COL + c0, ov);
+                    tc_ld32(t_lane + c0, ov);
                     tc_wait_ld();
+                    if (!real) continue;
+                    const size_t e = ((size_t)(qs0 + tok) * p.n_heads + qh) * D + c0;
+                    if (p.out_dtype == PKV_F32) {
+                        float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-                    tc_st32(t_lane + O_COL + c0, ov);
-                }
-                tc_wait_st();
-            } else if (j >= 2) {
-                // P buffer b is free once P_{j-2} V_{j-2} is done
-                const bool w2 = mbar_wait(&o_done[b], ((j - 2) >> 1) & 1, p.errors);
-                if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
-            }
-            l *= alpha;
-            const float mu = m_used == -INFINITY ? 0.f : m_used;
-            unsigned char* prow_hi = sP + (b * 2) * P_BYTES + r * 128;
-            unsigned char* prow_lo = prow_hi + P_BYTES;
+                        for (int c = 0; c < 32; c += 4)
+                            o4[c / 4] = make_float4(__uint_as_float(ov[c]) * inv,
+                                                    __uint_as_float(ov[c + 1]) * inv,
+                                                    __uint_as_float(ov[c + 2]) * inv,
+                                                    __uint_as_float(ov[c + 3]) * inv);
+                    } else {
+                        uint4* o4 =
+                            reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + e);
 #pragma unroll
-            for (int cch = 0; cch < kTcKeys / 8; ++cch) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = exp2f(x[cch * 8 + 2 * e] - mu);
-                    const float c = exp2f(x[cch * 8 + 2 * e + 1] - mu);
-                    l += a + c;
-                    hw[e] = pack2<T>(a, c);
-                    const float2 h2 = unpack2<T>(hw[e]);
-                    lw[e] = pack2<T>(a - h2.x, c - h2.y);
-                }
-                const int sw = (cch ^ (r & 7)) * 16;
-                *reinterpret_cast<uint4*>(prow_hi + sw) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(prow_lo + sw) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-            // V rows past the context, on a missing page or never loaded
-            // (beyond the last page this CTA reads) become zeros
-            {
-                unsigned char* sv = sKV + (size_t)st * 2 * KV_BYTES + KV_BYTES;
-                for (int idx = r; idx < kTcKeys * HALVES; idx += kTcRows) {
-                    const int row = idx % kTcKeys, h = idx / kTcKeys;
-                    const int key = key0 + row;
-                    if (key >= n || key >= n_pages * BS || s_bid[key / BS] < 0) {
-                        uint4* z = reinterpret_cast<uint4*>(sv + h * KV_HALF + row * 128);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+                        for (int c = 0; c < 32; c += 8)
+                            o4[c / 8] = make_uint4(
+                                pack_out(__uint_as_float(ov[c]) * inv,
+                                         __uint_as_float(ov[c + 1]) * inv, p.out_dtype),
+                                pack_out(__uint_as_float(ov[c + 2]) * inv,
+                                         __uint_as_float(ov[c + 3]) * inv, p.out_dtype),
+                                pack_out(__uint_as_float(ov[c + 4]) * inv,
+                                         __uint_as_float(ov[c + 5]) * inv, p.out_dtype),
+                                pack_out(__uint_as_float(ov[c + 6]) * inv,
+                                         __uint_as_float(ov[c + 7]) * inv, p.out_dtype));
                     }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&p_full[b]);
-        }
-        // ---- O / L of this row
-        const int jl = n_tiles - 1;
-        const bool w3 = ok && mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, p.errors);
-        if (__all_sync(0xffffffffu, w3)) {
-            tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int qh = kvh * G + r % G;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tc_ld32(t_lane + O_COL + c0, ov);
-                tc_wait_ld();
-                if (!real) continue;
-                const size_t e = ((size_t)(qs0 + tok) * p.n_heads + qh) * D + c0;
-                if (p.out_dtype == PKV_F32) {
-                    float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e);
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        o4[c / 4] = make_float4(__uint_as_float(ov[c]) * inv,
-                                                __uint_as_float(ov[c + 1]) * inv,
-                                                __uint_as_float(ov[c + 2]) * inv,
-                                                __uint_as_float(ov[c + 3]) * inv);
-                } else {
-                    uint4* o4 = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + e);
-#pragma unroll
-                    for (int c = 0; c < 32; c += 8)
-                        o4[c / 8] = make_uint4(
-                            pack_out(__uint_as_float(ov[c]) * inv,
-                                     __uint_as_float(ov[c + 1]) * inv, p.out_dtype),
-                            pack_out(__uint_as_float(ov[c + 2]) * inv,
-                                     __uint_as_float(ov[c + 3]) * inv, p.out_dtype),
-                            pack_out(__uint_as_float(ov[c + 4]) * inv,
-                                     __uint_as_float(ov[c + 5]) * inv, p.out_dtype),
-                            pack_out(__uint_as_float(ov[c + 6]) * inv,
-                                     __uint_as_float(ov[c + 7]) * inv, p.out_dtype));
                 }
             }
         }
@@ -481,7 +570,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4)
+    if (warp == 8)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(TMEM_COLS)
                      : "memory");
