@@ -17,9 +17,12 @@
 // rows: 128/G consecutive query tokens x the G query heads of the kv head
 // (row r: token r / G, head r % G); the pair shares every K/V page it loads.
 // Warps 0-3 and 4-7 run the softmax of tile 0 and tile 1, one thread per row
-// (thread r of a group owns tensor-memory lane r); warp 8 owns the tensor
-// memory and its lane 0 issues every MMA; lane 0 of warp 9 issues the TMA
-// loads.  Per key tile j of 64 keys and query tile t:
+// (thread r of a group owns tensor-memory lane r).  Lane 0 of warp 8 issues
+// every MMA of tile 0 and lane 0 of warp 10 those of tile 1 (a thread issues
+// one tcgen05.mma per ~100 cycles, so two issuers double the MMA rate;
+// keeping each tile's products in one thread keeps them in order); warp 8
+// also owns the tensor memory.  Warp 9 loads K/V by TMA and zeroes V rows
+// that must not reach a product.  Per key tile j of 64 keys and query tile t:
 //   K_j, V_j            pages by TMA into a ring of `stages` slots, per head
 //                       64-element boxes with 128-byte swizzle
 //   S_tj = Q_t K_j^T    M=128 N=64, A = Q_t (K-major), B = K_j (K-major), into
@@ -33,8 +36,9 @@
 // tensor-memory round trip, so a row keeps an older maximum until a new
 // score exceeds it by more than 2^8 (P <= 256 meanwhile; O and the sum L
 // share the maximum they were built with, so the quotient is unchanged).
-// V rows past the context, on a missing page or never loaded are zeroed
-// before the P V product (P is 0 there, but 0 * NaN is not).
+// V rows past the context, on a missing page or never loaded are zeroed by
+// the loading warp before the tile is marked full (P is 0 there, but 0 * NaN
+// is not).
 #pragma once
 
 #include <type_traits>
@@ -46,7 +50,7 @@ namespace pkv {
 constexpr int kTcKeys = 64;          // keys per tile (N of S = Q K^T)
 constexpr int kTcRows = 128;         // query rows per query tile (M)
 constexpr int kTcQTiles = 2;         // query tiles per CTA
-constexpr int kTcThreads = 320;      // 8 softmax warps, 1 MMA warp, 1 TMA warp
+constexpr int kTcThreads = 352;      // 8 softmax warps, 2 MMA warps, 1 TMA warp
 constexpr float kTcRescale = 8.0f;   // log2 of the growth tolerated before O is rescaled
 
 // ---------------------------------------------------------------- tcgen05
@@ -77,8 +81,7 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 // Same with A read from tensor memory: row i of A in lane i, 16-bit
@@ -89,8 +92,7 @@ __device__ __forceinline__ void tc_mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, 
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 // `bar` completes once every MMA this thread issued so far has completed.
@@ -156,7 +158,7 @@ __device__ __forceinline__ void tc_wait_st() {
 inline size_t multi_query_tc_smem_bytes(int D, int stages, int max_pages) {
     const size_t q = (size_t)kTcQTiles * kTcRows * D * 2;
     const size_t kv = (size_t)stages * 2 * kTcKeys * D * 2;
-    return 1024 + q + kv + (size_t)(2 * stages + 14) * sizeof(uint64_t) +
+    return 1024 + q + kv + (size_t)(3 * stages + 15) * sizeof(uint64_t) +
            (size_t)max_pages * sizeof(int) + sizeof(int);
 }
 
@@ -201,14 +203,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tok_lo >= q_len) return;
     const int first_pos = n - q_len;                 // position of query token 0
     // key tiles each query tile needs (0: the tile has no token)
-    int nt[kTcQTiles];
-#pragma unroll
-    for (int t = 0; t < kTcQTiles; ++t) {
-        const int lo = tok_lo + t * QT;
-        const int hi = min(q_len, lo + QT);
-        nt[t] = lo < q_len ? (first_pos + hi + kTcKeys - 1) / kTcKeys : 0;
-    }
-    const int n_tiles = max(nt[0], nt[1]);
+    const int nt0 = (first_pos + min(q_len, tok_lo + QT) + kTcKeys - 1) / kTcKeys;
+    const int nt1 = tok_lo + QT < q_len
+                        ? (first_pos + min(q_len, tok_lo + 2 * QT) + kTcKeys - 1) / kTcKeys
+                        : 0;
+    auto ntiles = [&](int t) { return t ? nt1 : nt0; };
+    const int n_tiles = max(nt0, nt1);
     const int n_keys = first_pos + min(q_len, tok_lo + kTcQTiles * QT);
     const int n_pages = (n_keys + BS - 1) / BS;
     const int zero_from = min(n, n_pages * BS);      // V rows from here on are zeroed
@@ -219,21 +219,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* sQ = sm;                                         // 2 x HALVES x [128 x 128 B]
     unsigned char* sKV = sQ + kTcQTiles * Q_BYTES;                  // stages x (K, V)
     uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + (size_t)p.stages * 2 * KV_BYTES);
-    uint64_t* kv_free = kv_full + p.stages;      // [stages]: every P V of the slot's tile done
-    uint64_t* q_full = kv_free + p.stages;
+    uint64_t* kv_free = kv_full + p.stages;      // [stages]: both issuers done with the slot
+    uint64_t* kv_land = kv_free + p.stages;      // [stages]: loads landed (tiles to zero)
+    uint64_t* q_full = kv_land + p.stages;
     uint64_t* s_full = q_full + 1;               // [tile][buffer]: S ready
     uint64_t* p_full = s_full + 4;               // [tile][buffer]: P written (128 arrivals)
     uint64_t* o_done = p_full + 4;               // [tile][parity of key tile]: P V done
-    uint64_t* fin = o_done + 4;                  // every MMA done
-    int* s_bid = reinterpret_cast<int*>(fin + 1);
+    uint64_t* fin = o_done + 4;                  // [tile]: every MMA of the tile's issuer done
+    int* s_bid = reinterpret_cast<int*>(fin + 2);
     int* s_tmem = s_bid + p.max_pages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    int missing = 0;
     for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
         int b = p.block_tables[(size_t)s * p.max_blocks_per_seq + i];
         if (b < 0 || b >= p.num_blocks) {
             raise_error(p.errors, PKV_DEVERR_BLOCK_ID);
             b = -1;
+            missing = 1;
         }
         s_bid[i] = b;
     }
@@ -247,7 +250,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         for (int st = 0; st < p.stages; ++st) {
             mbar_init(&kv_full[st], 1);
-            mbar_init(&kv_free[st], 1);
+            mbar_init(&kv_free[st], kTcQTiles);
+            mbar_init(&kv_land[st], 1);
         }
         mbar_init(q_full, 1);
         for (int b = 0; b < 4; ++b) {
@@ -255,16 +259,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&p_full[b], kTcRows);
             mbar_init(&o_done[b], 1);
         }
-        mbar_init(fin, 1);
+        mbar_init(&fin[0], 1);
+        mbar_init(&fin[1], 1);
         fence_barrier_init();
     }
     tc_fence_before();
-    __syncthreads();
+    const bool any_missing = __syncthreads_or(missing) != 0;   // a page of the context is absent
     tc_fence_after();
     const uint32_t tmem = (uint32_t)*s_tmem;
 
     // pages of key tile j that are present: bit pg for page j * PAGES + pg
+    // (all bits where no page is absent: pages past n_pages hold only keys
+    // that every row masks by position)
     auto page_mask = [&](int j) -> int {
+        if (!any_missing) return ALL_PAGES;
         int m = 0;
 #pragma unroll
         for (int pg = 0; pg < PAGES; ++pg) {
@@ -278,137 +286,177 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto needs_zero = [&](int j) -> bool {
         return (j + 1) * kTcKeys > zero_from || page_mask(j) != ALL_PAGES;
     };
+    // (with every page present, a tile ending at or before zero_from lies
+    // wholly on pages below n_pages)
 
     if (warp == 9) {
-        // ================= TMA producer =================
+        // ================= TMA producer (the whole warp zeroes V rows) =================
         if (lane == 0) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
             uint32_t q_bytes = 0;
 #pragma unroll
-            for (int t = 0; t < kTcQTiles; ++t) q_bytes += nt[t] > 0 ? Q_BYTES : 0;
+            for (int t = 0; t < kTcQTiles; ++t) q_bytes += ntiles(t) > 0 ? Q_BYTES : 0;
             mbar_arrive_expect_tx(q_full, q_bytes);
             const uint64_t once = l2_policy_evict_first();
 #pragma unroll
             for (int t = 0; t < kTcQTiles; ++t) {
-                if (nt[t] == 0) continue;
+                if (ntiles(t) == 0) continue;
                 for (int h = 0; h < HALVES; ++h)
                     tma_load_4d(sQ + t * Q_BYTES + h * Q_HALF, &tm_q, q_full, 0, h, kvh * G,
                                 qs0 + tok_lo + t * QT, once);
             }
-            const uint64_t keep = l2_policy_evict_normal();   // pages serve other query tiles
-            int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % p.stages;
-                if (j >= p.stages &&
-                    !mbar_wait(&kv_free[st], ((j / p.stages) - 1) & 1, p.errors))
-                    break;
-                unsigned char* dk = sKV + (size_t)st * 2 * KV_BYTES;
+        }
+        const uint64_t keep = l2_policy_evict_normal();   // pages serve other query tiles
+        int issued = 0;
+        int st = 0, round = 0;               // slot of tile j, times the ring wrapped
+        uint32_t land_par = 0;               // bit st: phase of kv_land[st] to wait for next
+        for (int j = 0; j < n_tiles; ++j) {
+            const bool w = round == 0 || mbar_wait(&kv_free[st], (round - 1) & 1, p.errors);
+            if (!__all_sync(0xffffffffu, w)) break;
+            const bool zero = needs_zero(j);
+            // a tile with rows to zero lands on kv_land; kv_full follows the zeroing
+            uint64_t* bar = zero ? &kv_land[st] : &kv_full[st];
+            unsigned char* dk = sKV + (size_t)st * 2 * KV_BYTES;
+            if (lane == 0) {
                 uint32_t bytes = 0;
                 for (int pg = 0; pg < PAGES; ++pg) {
                     const int page = j * PAGES + pg;
                     if (page < n_pages && s_bid[page] >= 0) bytes += 2 * HALVES * BS * 128;
                 }
                 if (bytes == 0) {
-                    mbar_arrive(&kv_full[st]);
+                    mbar_arrive(bar);
                 } else {
-                    mbar_arrive_expect_tx(&kv_full[st], bytes);
+                    mbar_arrive_expect_tx(bar, bytes);
                     for (int pg = 0; pg < PAGES; ++pg) {
                         const int page = j * PAGES + pg;
                         if (page >= n_pages || s_bid[page] < 0) continue;
                         for (int h = 0; h < HALVES; ++h) {
-                            tma_load_4d(dk + h * KV_HALF + pg * BS * 128, &tm_k, &kv_full[st], 0,
+                            tma_load_4d(dk + h * KV_HALF + pg * BS * 128, &tm_k, bar, 0,
                                         kvh * HALVES + h, 0, s_bid[page], keep);
-                            tma_load_4d(dk + KV_BYTES + h * KV_HALF + pg * BS * 128, &tm_v,
-                                        &kv_full[st], 0, kvh * HALVES + h, 0, s_bid[page], keep);
+                            tma_load_4d(dk + KV_BYTES + h * KV_HALF + pg * BS * 128, &tm_v, bar,
+                                        0, kvh * HALVES + h, 0, s_bid[page], keep);
                         }
                     }
                 }
-                issued = j + 1;
             }
-            // every load issued has landed before the CTA may exit (earlier
-            // tiles of a slot were consumed before the slot was refilled)
+            issued = j + 1;
+            if (zero) {
+                const bool w2 = mbar_wait(&kv_land[st], (land_par >> st) & 1u, p.errors);
+                land_par ^= 1u << st;
+                if (!__all_sync(0xffffffffu, w2)) break;
+                const int pm = page_mask(j);
+                unsigned char* sv = dk + KV_BYTES;
+                for (int idx = lane; idx < kTcKeys * HALVES; idx += 32) {
+                    const int row = idx % kTcKeys, h = idx / kTcKeys;
+                    const int key = j * kTcKeys + row;
+                    if (key >= zero_from || !((pm >> (row / BS)) & 1)) {
+                        uint4* z = reinterpret_cast<uint4*>(sv + h * KV_HALF + row * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kv_full[st]);
+            }
+            if (++st == p.stages) {
+                st = 0;
+                ++round;
+            }
+        }
+        // every load issued has landed before the CTA may exit (earlier
+        // tiles of a slot were consumed before the slot was refilled)
+        if (lane == 0)
             for (int j = max(0, issued - p.stages); j < issued; ++j)
                 mbar_wait(&kv_full[j % p.stages], (j / p.stages) & 1, p.errors);
-        }
         __syncwarp();
-    } else if (warp == 8) {
-        // ================= MMA issuer =================
+    } else if (warp == 8 || warp == 10) {
+        // ================= MMA issuer of query tile t =================
+        const int t = warp == 8 ? 0 : 1;
+        const int ntt = ntiles(t);
         if (lane == 0) {
             const uint32_t id_s = tc_idesc<T>(kTcRows, kTcKeys, 0);
             const uint32_t id_o = tc_idesc<T>(kTcRows, D, 1);
-            // S_tj = Q_t K_j^T for every query tile that needs key tile j
+            // Descriptors of Q tile t, K and V of slot 0; other operands add
+            // their byte offset >> 4 to the start-address field (shared
+            // addresses stay below 2^18, so the 14-bit field never carries).
+            const uint64_t dq = tc_desc_sw128(smem_addr(sQ + t * Q_BYTES), 16, 1024);
+            const uint64_t dk = tc_desc_sw128(smem_addr(sKV), 16, 1024);
+            const uint64_t dv = tc_desc_sw128(smem_addr(sKV + KV_BYTES), KV_HALF, 1024);
+            constexpr uint32_t SLOT16 = (2 * KV_BYTES) >> 4;
+            const uint32_t base = tmem + t * TILE_COLS;      // O of tile t, then its S buffers
+            int s_st = 0;          // slot of the next tile whose S is issued
+            uint32_t s_ph = 0;     // and the phase of its kv_full
+            // S_tj = Q_t K_j^T into S buffer j & 1
             auto issue_s = [&](int j) -> bool {
-                const int st = j % p.stages;
-                if (!mbar_wait(&kv_full[st], (j / p.stages) & 1, p.errors)) return false;
+                if (!mbar_wait(&kv_full[s_st], s_ph, p.errors)) return false;
                 tc_fence_after();
-                const uint32_t kb = smem_addr(sKV + (size_t)st * 2 * KV_BYTES);
+                const uint64_t kd = dk + (uint64_t)(s_st * SLOT16);
+                const uint32_t d = base + S_COL + (j & 1) * kTcKeys;
 #pragma unroll
-                for (int t = 0; t < kTcQTiles; ++t) {
-                    if (j >= nt[t]) continue;
-                    const uint32_t qb = smem_addr(sQ + t * Q_BYTES);
-                    const uint32_t d = tmem + t * TILE_COLS + S_COL + (j & 1) * kTcKeys;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const int h = ks / 4, kin = ks % 4;
-                        tc_mma(d, tc_desc_sw128(qb + h * Q_HALF + kin * 32, 16, 1024),
-                               tc_desc_sw128(kb + h * KV_HALF + kin * 32, 16, 1024), id_s,
-                               ks > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&s_full[t * 2 + (j & 1)]);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t qo = ((ks / 4) * Q_HALF + (ks % 4) * 32) >> 4;
+                    const uint32_t ko = ((ks / 4) * KV_HALF + (ks % 4) * 32) >> 4;
+                    tc_mma(d, dq + qo, kd + ko, id_s, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[t * 2 + (j & 1)]);
+                if (++s_st == p.stages) {
+                    s_st = 0;
+                    s_ph ^= 1u;
                 }
                 return true;
             };
-            bool ok = mbar_wait(q_full, 0, p.errors);
-            for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = issue_s(j);
+            bool ok = ntt == 0 || mbar_wait(q_full, 0, p.errors);
+            for (int j = 0; ok && j < 2 && j < ntt; ++j) ok = issue_s(j);
+            int v_st = 0, v_round = 0;     // slot of tile j, times the ring wrapped
             for (int j = 0; ok && j < n_tiles; ++j) {
-                const int st = j % p.stages;
-                const uint32_t ph = (j >> 1) & 1;
-                // where V rows get zeroed, both groups finish writing before
-                // any P V of the tile reads V
-                const bool zero = needs_zero(j);
-                if (zero) {
-#pragma unroll
-                    for (int t = 0; t < kTcQTiles; ++t)
-                        if (j < nt[t] && !mbar_wait(&p_full[t * 2 + (j & 1)], ph, p.errors))
-                            ok = false;
-                    if (!ok) break;
-                }
-                const uint32_t vb = smem_addr(sKV + (size_t)st * 2 * KV_BYTES + KV_BYTES);
-#pragma unroll
-                for (int t = 0; t < kTcQTiles; ++t) {
-                    if (j >= nt[t]) continue;
-                    if (!zero && !mbar_wait(&p_full[t * 2 + (j & 1)], ph, p.errors)) {
+                if (j < ntt) {
+                    if (!mbar_wait(&p_full[t * 2 + (j & 1)], (j >> 1) & 1, p.errors)) {
                         ok = false;
                         break;
                     }
+                    // O_t += P_tj V_j (hi part, then lo part; P in tensor memory)
                     tc_fence_after();
-                    const uint32_t base = tmem + t * TILE_COLS;
+                    const uint64_t vd = dv + (uint64_t)(v_st * SLOT16);
                     const uint32_t pa = base + S_COL + (j & 1) * kTcKeys;
 #pragma unroll
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
                         for (int ks = 0; ks < kTcKeys / 16; ++ks)
                             tc_mma_tmem_a(base, pa + part * (kTcKeys / 2) + ks * 8,
-                                          tc_desc_sw128(vb + ks * 16 * 128, KV_HALF, 1024), id_o,
+                                          vd + (uint64_t)((ks * 16 * 128) >> 4), id_o,
                                           (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
                     tc_commit(&o_done[t * 2 + (j & 1)]);
+                    tc_commit(&kv_free[v_st]);
+                    if (j + 2 < ntt) ok = issue_s(j + 2);
+                } else {
+                    // this tile's rows never see key tile j: release the slot
+                    // once it is loaded (keeps kv_free's phases in step)
+                    if (!mbar_wait(&kv_full[v_st], v_round & 1, p.errors)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive(&kv_free[v_st]);
                 }
-                if (!ok) break;
-                tc_commit(&kv_free[st]);
-                if (j + 2 < n_tiles) ok = issue_s(j + 2);
+                if (++v_st == p.stages) {
+                    v_st = 0;
+                    ++v_round;
+                }
             }
-            // every MMA complete before the tensor memory is released
-            tc_commit(fin);
-            mbar_wait(fin, 0, p.errors);
+            // every MMA of this issuer complete before the tensor memory is released
+            if (ntt > 0) {
+                tc_commit(&fin[t]);
+                mbar_wait(&fin[t], 0, p.errors);
+            }
         }
         __syncwarp();
     } else {
         // ================= softmax: group t, thread r owns row r of tile t =================
         const int t = warp >> 2;
         const int r = (warp & 3) * 32 + lane;            // tensor-memory lane
-        if (nt[t] > 0) {
+        if (ntiles(t) > 0) {
             const int tok = tok_lo + t * QT + r / G;
             const bool real = tok < q_len;
             const int pos = real ? first_pos + tok : -1;     // last key of this row
@@ -416,9 +464,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float sc = p.scale_log2;
             const bool pos_sc = sc > 0.f;                    // the usual case
             float m_used = -INFINITY;
-            float2 l2 = make_float2(0.f, 0.f);
+            float2 l4[4];                                  // row sum as 8 partial sums
+#pragma unroll
+            for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
             bool ok = true;
-            for (int j = 0; j < nt[t]; ++j) {
+            const int ntt = ntiles(t);
+            for (int j = 0; j < ntt; ++j) {
                 const int b = j & 1;
                 const bool w = mbar_wait(&s_full[t * 2 + b], (j >> 1) & 1, p.errors);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -433,22 +484,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // y: raw scores (scaled ones if the scale is not positive),
                 // -inf where a key is hidden from this row
                 float y[kTcKeys];
-                float mx = -INFINITY;
                 if (full && pos_sc) {
 #pragma unroll
-                    for (int c = 0; c < kTcKeys; ++c) {
-                        y[c] = __uint_as_float(sr[c]);
-                        mx = fmaxf(mx, y[c]);
-                    }
+                    for (int c = 0; c < kTcKeys; ++c) y[c] = __uint_as_float(sr[c]);
                 } else {
 #pragma unroll
                     for (int c = 0; c < kTcKeys; ++c) {
                         const bool keep = key0 + c <= pos && ((pm >> (c / BS)) & 1);
                         const float v = pos_sc ? __uint_as_float(sr[c]) : __uint_as_float(sr[c]) * sc;
                         y[c] = keep ? v : -INFINITY;
-                        mx = fmaxf(mx, y[c]);
                     }
                 }
+                // row maximum as 8 independent chains
+                float m8[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) m8[c] = y[c];
+#pragma unroll
+                for (int c = 8; c < kTcKeys; ++c) m8[c & 7] = fmaxf(m8[c & 7], y[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 const float a = pos_sc ? sc : 1.f;           // exponent = y * a - m
                 const float tmax = mx * a;
                 const bool first = m_used == -INFINITY;
@@ -485,7 +539,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const bool w2 = mbar_wait(&o_done[t * 2 + b], ((j - 2) >> 1) & 1, p.errors);
                     if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
                 }
-                l2 = __fmul2_rn(l2, make_float2(alpha, alpha));
+                l4[0] = __fmul2_rn(l4[0], make_float2(alpha, alpha));
+                l4[1] = __fmul2_rn(l4[1], make_float2(alpha, alpha));
+                l4[2] = __fmul2_rn(l4[2], make_float2(alpha, alpha));
+                l4[3] = __fmul2_rn(l4[3], make_float2(alpha, alpha));
                 const float mu = m_used == -INFINITY ? 0.f : m_used;
                 const float2 a2 = make_float2(a, a), nmu2 = make_float2(-mu, -mu);
                 const float2 neg1 = make_float2(-1.f, -1.f);
@@ -496,39 +553,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < kTcKeys / 2; ++i) {
                     const float2 e = __ffma2_rn(make_float2(y[2 * i], y[2 * i + 1]), a2, nmu2);
                     const float2 pv = make_float2(exp2f(e.x), exp2f(e.y));
-                    l2 = __fadd2_rn(l2, pv);
+                    l4[i & 3] = __fadd2_rn(l4[i & 3], pv);
                     ph[i] = pack2<T>(pv.x, pv.y);
                     const float2 lo = __ffma2_rn(unpack2<T>(ph[i]), neg1, pv);
                     pl[i] = pack2<T>(lo.x, lo.y);
                 }
                 tc_st32(t_lane + S_COL + b * kTcKeys, ph);
                 tc_st32(t_lane + S_COL + b * kTcKeys + 32, pl);
-                if (needs_zero(j)) {
-                    const int st = j % p.stages;
-                    const bool w3 = mbar_wait(&kv_full[st], (j / p.stages) & 1, p.errors);
-                    if (!__all_sync(0xffffffffu, w3)) { ok = false; break; }
-                    unsigned char* sv = sKV + (size_t)st * 2 * KV_BYTES + KV_BYTES;
-                    for (int idx = r; idx < kTcKeys * HALVES; idx += kTcRows) {
-                        const int row = idx % kTcKeys, h = idx / kTcKeys;
-                        const int key = key0 + row;
-                        if (key >= zero_from || !((pm >> (row / BS)) & 1)) {
-                            uint4* z = reinterpret_cast<uint4*>(sv + h * KV_HALF + row * 128);
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                    }
-                    fence_proxy_async_smem();
-                }
                 tc_wait_st();
                 tc_fence_before();
                 mbar_arrive(&p_full[t * 2 + b]);
             }
             // ---- O / L of this row
-            const int jl = nt[t] - 1;
+            const int jl = ntt - 1;
             const bool w4 = ok && mbar_wait(&o_done[t * 2 + (jl & 1)], (jl >> 1) & 1, p.errors);
             if (__all_sync(0xffffffffu, w4)) {
                 tc_fence_after();
-                const float l = l2.x + l2.y;
+                const float2 la = __fadd2_rn(l4[0], l4[1]), lb = __fadd2_rn(l4[2], l4[3]);
+                const float l = (la.x + lb.x) + (la.y + lb.y);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 const int qh = kvh * G + r % G;
 #pragma unroll 1
