@@ -201,8 +201,9 @@ PKV_API pkv_status paged_attn_decode_noalloc(void* out, pkv_dtype out_dtype, con
  * written) and flagged PKV_DEVERR_CONTEXT.  Tensor cores: query tokens x
  * query heads of one kv head form the tile rows: on tcgen05, two tiles of
  * 128 rows per CTA with S, P and O in tensor memory, when max_q_len x group
- * >= 128 (and total_q >= 128 / group); else 16 rows per warp on mma.sync.
- * The environment variable PKV_MQ_TC=0/1 forces one where it applies.
+ * >= 16 (groups of 4 and 8) or >= 48 (groups of 1 and 2), and total_q >=
+ * 128 / group; else 16 rows per warp on mma.sync.  The environment
+ * variable PKV_MQ_TC=0/1 forces one where it applies.
  */
 PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const void* q,
                                           const int32_t* q_start, int total_q, int max_q_len,

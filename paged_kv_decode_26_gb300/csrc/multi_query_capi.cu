@@ -80,12 +80,17 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
     const int map_blocks = num_blocks > 0 ? num_blocks : 1;
 
     // tcgen05 path: two query tiles of 128 rows (128/G tokens x G heads) per
-    // CTA.  Chosen when the longest chunk fills at least one such tile;
-    // PKV_MQ_TC=0/1 forces it off/on where it applies.
+    // CTA; PKV_MQ_TC=0/1 forces it off/on where it applies.
     {
         const int tc_tokens = pkv::kTcRows / G;
+        // Measured crossover (GB300): with groups of 4 the tcgen05 kernel wins
+        // from 4-token chunks (16 rows); with groups of 1 the mma.sync kernel
+        // wins up to 32 tokens and tcgen05 from 48.
         int want = env_int("PKV_MQ_TC", -1);
-        if (want < 0) want = (long long)max_q_len * G >= pkv::kTcRows ? 1 : 0;
+        if (want < 0) {
+            const long long rows = (long long)max_q_len * G;
+            want = (G >= 4 ? rows >= 16 : rows >= 48) ? 1 : 0;
+        }
         int stages = env_int("PKV_MQ_TC_STAGES", head_dim == 64 ? 6 : 4);
         stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
         while (stages > 2 && pkv::multi_query_tc_smem_bytes(head_dim, stages, max_pages) >

@@ -5,7 +5,11 @@ Tolerance (attention output vs the fp64 oracle, N(0,1) inputs):
   * max |err| <= 4e-3 and mean |err| <= 5e-4, where an element above 4e-3
     is accepted only if it is rounding-limited: |oracle| >= 2 (where one
     half-ulp of bf16 is 7.8e-3) and |err| <= half an ulp of the output type
-    at |oracle| + 1e-5;
+    at |oracle| + 1e-5; likewise the mean bound is rounding-limited where
+    the correctly rounded oracle itself exceeds it (rows that see a handful
+    of keys, e.g. the first tokens of a prefill from scratch, have |O| near
+    |V| and a bf16 mean rounding error near 5e-4): then the bound is that
+    rounded oracle's own mean error + 10 % (reported as mean_bound);
   * and, tighter, every element is within one ulp of the oracle rounded to
     the output type plus 2e-6 absolute (fp32 output: |err| <= 2e-5 +
     1e-5 |oracle|), which bounds the fp32 accumulation error of the kernel
@@ -63,6 +67,8 @@ def attention_errors(got: torch.Tensor, ref: np.ndarray, out_dtype: torch.dtype,
             aw = abs_weighted() if callable(abs_weighted) else abs_weighted
             beyond = np.abs(g - r) > bound + _SPLIT[kv_dtype] * np.asarray(aw)
         stats["beyond_one_ulp"] = int(beyond.sum())
+        rounded_mean = float(np.abs(r - ref).mean()) if ref.size else 0.0
+        stats["mean_bound"] = max(MEAN_ABS, 1.1 * rounded_mean)
         if beyond.any():
             i = np.unravel_index(np.argmax(np.abs(g - r) * beyond), g.shape)
             stats["worst"] = {"index": [int(x) for x in i], "got": float(g[i]),
@@ -85,7 +91,7 @@ def assert_attention_close(got, ref, out_dtype, what="", abs_weighted=None,
     st = attention_errors(got, ref, out_dtype, abs_weighted, kv_dtype)
     assert st["finite"], f"{what}: non-finite output"
     assert st["violations"] == 0, f"{what}: {st}"
-    assert st["mean_abs"] <= MEAN_ABS, f"{what}: {st}"
+    assert st["mean_abs"] <= st.get("mean_bound", MEAN_ABS), f"{what}: {st}"
     assert st["beyond_one_ulp"] == 0, f"{what}: {st}"
     return st
 

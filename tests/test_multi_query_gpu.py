@@ -218,3 +218,51 @@ def _oracle_skip_missing(case, q, qs, abs_v=False):
             sc = sc.masked_fill(~visible, float("-inf"))
             out[a:b, h] = torch.softmax(sc, 1) @ V[:, h // G]
     return out.numpy()
+
+
+# ------------------------------------------------- full sizes (sampled)
+
+def _oracle_rows(case, q, qs, s, a, b):
+    """Oracle rows a..b-1 of sequence s's chunk.  Causal attention of a row
+    only depends on the keys up to its position, so rows a..b-1 of a q_len
+    chunk over n keys are the whole (b - a)-row chunk over the first
+    n - q_len + b keys."""
+    q0, q1 = int(qs[s]), int(qs[s + 1])
+    n = int(case.context_lens[s])
+    sub_q = q[q0 + a:q0 + b]
+    sub_qs = torch.tensor([0, b - a], dtype=torch.int32)
+    sub_len = torch.tensor([n - (q1 - q0) + b], dtype=torch.int32)
+    return orc.multi_query(sub_q, case.k_pool, case.v_pool, case.block_tables[s:s + 1],
+                           sub_len, sub_qs, case.scale)
+
+
+@pytest.mark.parametrize("config,k", [(2, 4), (3, 4), (4, 2)])
+def test_full_size_sampled(pkv, config, k):
+    """The stated workload at full size with a 256-token chunk per sequence,
+    in the launch the multi-query benchmark times (the tcgen05 kernel),
+    checked on sampled sequences: the first rows, rows across the boundary
+    between CTAs (or query tiles), the last rows; every row finite and
+    within max |V|."""
+    import concurrent.futures as cf
+    case = wl.make_case(config)
+    q, qs = wl.multi_query_inputs(case, ("const", 256))
+    got = _run(pkv, case, q, qs)
+    assert pkv.device_errors(clear=True) == 0
+    G = case.H // case.Hk
+    edge = 128 if G == 1 else 2 * (128 // G)       # first token of the second CTA or tile
+    seqs = wl.sampled_seqs(case, k)
+    jobs = []
+    for s in seqs:
+        ql = int(qs[s + 1] - qs[s])
+        for a, b in ((0, 16), (max(0, edge - 8), min(ql, edge + 8)), (max(0, ql - 16), ql)):
+            if b > a:
+                jobs.append((s, a, b))
+    with cf.ThreadPoolExecutor(max_workers=8) as ex:
+        refs = list(ex.map(lambda j: _oracle_rows(case, q, qs, *j), jobs))
+    for (s, a, b), ref in zip(jobs, refs):
+        q0 = int(qs[s])
+        assert_attention_close(got[q0 + a:q0 + b], ref, case.out_dtype,
+                               f"config {config} seq {s} rows {a}..{b}")
+    g = got.float()
+    assert torch.isfinite(g).all()
+    assert g.abs().max() <= case.v_pool[torch.isfinite(case.v_pool.float())].float().abs().max() + 1e-2
