@@ -311,7 +311,24 @@ def build_replicas(args, rank, dev, pkv, wl, torch, np):
         "lens": torch.cat([r["lens_h"] for r in reps]).pin_memory(),
         "slots": torch.cat([r["slots_h"] for r in reps]).pin_memory(),
     }
-    devb = {k: v.to(dev) for k, v in host.items()}
+    # One pinned staging buffer and one device buffer hold every per-step
+    # input (256-byte aligned sections), so a step's inputs cross in one copy.
+    offs, total = {}, 0
+    for k, v in host.items():
+        nbytes = v.numel() * v.element_size()
+        offs[k] = (total, nbytes)
+        total = (total + nbytes + 255) // 256 * 256
+    hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+    devb = {}
+    for k in list(host):
+        o, nbytes = offs[k]
+        hv = hbuf[o:o + nbytes].view(host[k].dtype).view(host[k].shape)
+        hv.copy_(host[k])
+        host[k] = hv
+        devb[k] = dbuf[o:o + nbytes].view(hv.dtype).view(hv.shape)
+    dbuf.copy_(hbuf)
+    host["inputs"], devb["inputs"] = hbuf, dbuf
     c0 = reps[0]["case"]
     out_all = torch.empty(R * S, c0.H, c0.D, dtype=c0.out_dtype, device=dev)
     host["out"] = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
@@ -669,13 +686,11 @@ def main():
                      "matches_host_manager": bool(same)}
 
     # ---- end to end through the public API with host buffers
-    h2d_bytes = sum(host[k].numel() * host[k].element_size()
-                    for k in ("q", "k_new", "v_new", "bt", "lens", "slots"))
+    h2d_bytes = host["inputs"].numel()        # the staging buffer, copied whole
     d2h_bytes = host["out"].numel() * host["out"].element_size()
 
     def e2e_step():
-        for k in ("q", "k_new", "v_new", "bt", "lens", "slots"):
-            devb[k].copy_(host[k], non_blocking=True)
+        devb["inputs"].copy_(host["inputs"], non_blocking=True)
         run_step()
         host["out"].copy_(devb["out"], non_blocking=True)
         stream.synchronize()

@@ -16,9 +16,17 @@ from ._lib import check, lib
 _DT = {torch.float16: _lib.PKV_F16, torch.bfloat16: _lib.PKV_BF16, torch.float32: _lib.PKV_F32}
 
 
+# The current stream's raw handle without building a Stream object (a few
+# microseconds per call); the public call where torch lacks the shortcut.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_ptr(stream: Optional[torch.cuda.Stream]):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return C.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return C.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:
+        return C.c_void_p(_raw_stream(torch.cuda.current_device()))
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _ptr(t: Optional[torch.Tensor]):
