@@ -2,8 +2,9 @@
 // sequence over the paged KV cache on Blackwell's 5th-generation tensor
 // cores (tcgen05: MMAs issued by one thread from shared-memory descriptors,
 // fp32 accumulators in tensor memory), sm_103a.  Same operation, inputs and
-// outputs as paged_multi_query_kernel; chosen when a CTA's 128 query rows
-// are well filled.
+// outputs as paged_multi_query_kernel; taken for chunks of at least 48 rows
+// (tokens x group, groups of 1 and 2) or 16 rows (groups of 4 and 8), where
+// it measured faster.
 //
 // Pages followed (cited by title and section):
 //   [SWAP]   "vLLM 中 FlashAttention 与 KVCache 交换机制深度解析": FlashAttention
