@@ -266,3 +266,27 @@ def test_full_size_sampled(pkv, config, k):
     g = got.float()
     assert torch.isfinite(g).all()
     assert g.abs().max() <= case.v_pool[torch.isfinite(case.v_pool.float())].float().abs().max() + 1e-2
+
+
+@pytest.mark.parametrize("H,Hk", [(8, 8), (16, 4)])
+def test_tc_tile_boundaries(pkv, monkeypatch, H, Hk):
+    """Chunk lengths around the 128-row query tile and the 256-row CTA span
+    (one token short, exact, one over), contexts shorter than one 64-key
+    tile and contexts ending at, just before and just after a key-tile
+    boundary; the whole-context prefill among them."""
+    monkeypatch.setenv("PKV_MQ_TC", "1")
+    G = H // Hk
+    qt = 128 // G                                   # tokens per query tile
+    q_lens = [1, qt - 1, qt, qt + 1, 2 * qt - 1, 2 * qt, 2 * qt + 1, 3 * qt + 5]
+    lens = [max(q, n) for q, n in zip(q_lens, [63, 64, 65, 127, 128, 129, 300, 512])]
+    lens = [min(n, 1000) for n in lens]
+    case = wl.make_case(2, S=len(lens), lens_override=lens, H=H, Hk=Hk, D=128, poison=True,
+                        seed=G)
+    rng = np.random.default_rng(G)
+    ql = np.minimum(np.array(q_lens), np.array(lens))
+    qs = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    qs[1:] = torch.from_numpy(np.cumsum(ql).astype(np.int32))
+    q = torch.from_numpy(rng.standard_normal((int(qs[-1]), H, 128))).to(case.dtype)
+    got = _run(pkv, case, q, qs)
+    _close(got, _oracle(case, q, qs), case, q, qs, what=f"{H}/{Hk}")
+    assert pkv.device_errors(clear=True) == 0
