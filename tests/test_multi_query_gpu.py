@@ -290,3 +290,23 @@ def test_tc_tile_boundaries(pkv, monkeypatch, H, Hk):
     got = _run(pkv, case, q, qs)
     _close(got, _oracle(case, q, qs), case, q, qs, what=f"{H}/{Hk}")
     assert pkv.device_errors(clear=True) == 0
+
+
+def test_tc_bad_q_start_is_flagged(pkv, monkeypatch):
+    """The tcgen05 kernel skips and flags a sequence whose chunk is longer
+    than its context, and still answers the others."""
+    monkeypatch.setenv("PKV_MQ_TC", "1")
+    case = wl.make_case(2, S=3, lens_override=[40, 90, 70], H=16, Hk=2, D=128,
+                        out_dtype=torch.float32)
+    q, qs = wl.multi_query_inputs(case, ("const", 24))     # 72 rows >= 16 tokens per tile
+    bad = qs.clone()
+    bad[1] = 50                        # sequence 0 would own 50 rows of a 40-token context
+    out = torch.zeros(q.shape[0], case.H, case.D, dtype=torch.float32, device="cuda")
+    pkv.paged_attn_multi_query(out, q.cuda(), bad.cuda(), case.k_pool.cuda(), case.v_pool.cuda(),
+                               case.block_tables.cuda(), case.context_lens.cuda(), case.scale,
+                               50, 90)
+    assert pkv.device_errors(clear=True) & 0x2
+    # sequence 2 (rows 50..71 of the bad layout are sequence 1's; sequence 2 keeps its rows)
+    ref = _oracle(case, q, qs)
+    s2 = slice(int(qs[2]), int(qs[3]))
+    assert_attention_close(out[s2], ref[s2], torch.float32, "sequence 2")
