@@ -4,9 +4,11 @@
 Default workload (N=1): LLaMA-7B-shaped single-layer decode -- 64 sequences,
 32 heads MHA, head_dim 128, block size 16, context lengths U[512, 4096],
 bf16 K/V, physical blocks shuffled across a pool of the needed blocks + 10 %.
-One step = kv_append of one new token per sequence (into its last page, the
-slot of a freshly allocated block where the page was full) followed by
-paged_attn_decode over the context including that token.  The metric is KV
+One step = the append of one new token per sequence (into its last page, the
+slot of a freshly allocated block where the page was full) followed by the
+decode over the context including that token, in one call
+(paged_attn_decode_append: the decode CTA of each sequence's last split
+writes the token's rows before it loads the pages).  The metric is KV
 bytes read per second (logical K+V bytes of every sequence's context) and
 sequence-steps per second.
 
@@ -466,8 +468,11 @@ def main():
             side.wait_event(fork)
             with torch.cuda.stream(side):
                 swaps(r)
-        pkv.kv_append(r["k_pool"], r["v_pool"], r["k_new"], r["v_new"], r["slots"])
-        decode(r)
+        # append the step's token and decode, in one launch
+        pkv.paged_attn_decode_append(r["out"], r["q"], r["k_pool"], r["v_pool"], r["bt"],
+                                     r["lens"], case.scale, r["max_ctx"], r["k_new"],
+                                     r["v_new"], r["slots"], split_tokens=args.split,
+                                     workspace=r["ws"])
         if with_swaps:
             join = torch.cuda.Event()
             join.record(side)
@@ -493,7 +498,7 @@ def main():
                      r["bt"].numel() * 4 + S * 4)
         split_r = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B,
                                                         r["max_ctx"])
-        launches_per_step += 2 + (1 if (r["max_ctx"] + split_r - 1) // split_r > 1 else 0) + \
+        launches_per_step += 1 + (1 if (r["max_ctx"] + split_r - 1) // split_r > 1 else 0) + \
             (2 if with_swaps else 0)
     split_used = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B,
                                                        reps[0]["max_ctx"])
@@ -751,7 +756,7 @@ def main():
         "kv_bytes_per_step_all_gpus": total_kv,
         "config": {
             "workload": name,
-            "step": "kv_append (1 token/seq) + paged_attn_decode" +
+            "step": "paged_attn_decode_append (append 1 token/seq, then decode: one call)" +
                     (" + swap_blocks_kv D2D and pinned-H2D on a side stream, overlapped"
                      if with_swaps else ""),
             "replicas_per_gpu": R,

@@ -144,6 +144,27 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * paged_attn_decode_append -- kv_append followed by paged_attn_decode, in
+ * one launch: the decode CTA of each sequence's last split first writes
+ * k_new[s] and v_new[s] ([num_seqs, n_kv_heads, head_dim] of kv_dtype,
+ * 16-byte aligned) into pool row slot_mapping[s] (int64 [num_seqs], 8-byte
+ * aligned; -1 skips, a slot outside the pool is skipped and flagged
+ * PKV_DEVERR_SLOT) for its kv heads, then decodes.  context_lens already
+ * counts the appended token ([SWAP] serving loop: append, then attend; the
+ * host allocator's append_slots gives both).  Same outputs and pool bytes
+ * as the two calls, provided no other sequence of the call reads the page
+ * holding a slot (true once shared pages are copied on write), since the
+ * other sequences' CTAs do not wait for the append.  Other arguments as
+ * paged_attn_decode.
+ */
+PKV_API pkv_status paged_attn_decode_append(
+    void* out, pkv_dtype out_dtype, const void* q, void* k_pool, void* v_pool, pkv_dtype kv_dtype,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int n_heads, int n_kv_heads, int head_dim, int block_size, int num_blocks,
+    float scale, int max_context_len, int split_tokens, void* workspace, size_t workspace_bytes,
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, void* stream);
+
+/*
  * paged_attn_decode_noalloc -- paged_attn_decode for callers that cannot
  * allocate device memory.  The pages have no counterpart: this is an
  * interface addition of this library.

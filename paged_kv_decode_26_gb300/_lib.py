@@ -33,6 +33,8 @@ SIGNATURES = {
     "pkv_decode_split_tokens": (_i, [_i, _i, _i, _i, _i, _i]),
     "paged_attn_decode": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i, _i, _f,
                                _i, _i, _p, _sz, _p]),
+    "paged_attn_decode_append": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i,
+                                      _i, _f, _i, _i, _p, _sz, _p, _p, _p, _p]),
     "paged_attn_decode_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i,
                                        _i, _f, _i, _i, _p]),
     "paged_attn_multi_query": (_i, [_p, _i, _p, _p, _i, _i, _p, _p, _i, _p, _i, _p, _i, _i, _i,

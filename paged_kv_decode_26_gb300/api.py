@@ -95,6 +95,45 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     return out
 
 
+def paged_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                             v_pool: torch.Tensor, block_tables: torch.Tensor,
+                             context_lens: torch.Tensor, scale: float, max_context_len: int,
+                             k_new: torch.Tensor, v_new: torch.Tensor,
+                             slot_mapping: torch.Tensor, split_tokens: int = 0,
+                             workspace: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """kv_append(k_pool, v_pool, k_new, v_new, slot_mapping) then
+    paged_attn_decode(...) in one launch; context_lens counts the appended
+    token.  No other sequence of the call may read a page that holds a slot."""
+    for name, t in (("out", out), ("q", q), ("k_pool", k_pool), ("v_pool", v_pool),
+                    ("block_tables", block_tables), ("context_lens", context_lens),
+                    ("k_new", k_new), ("v_new", v_new), ("slot_mapping", slot_mapping)):
+        _need_cuda(name, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    S, H, D = q.shape
+    nb, B, Hk, D2 = k_pool.shape
+    if (D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != (S, H, D)
+            or q.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype
+            or block_tables.dim() != 2 or block_tables.shape[0] != S
+            or context_lens.shape != (S,) or tuple(k_new.shape) != (S, Hk, D)
+            or k_new.shape != v_new.shape or k_new.dtype != k_pool.dtype
+            or v_new.dtype != k_pool.dtype or slot_mapping.shape != (S,)):
+        raise ValueError("inconsistent shapes or dtypes")
+    if workspace is None:
+        workspace = alloc_decode_workspace(q, k_pool, max_context_len, split_tokens)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().paged_attn_decode_append(
+        _ptr(out), _DT[out.dtype], _ptr(q), _ptr(k_pool), _ptr(v_pool), _DT[k_pool.dtype],
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S, H, Hk, D, B, nb,
+        float(scale), int(max_context_len), int(split_tokens), _ptr(workspace), ws_bytes,
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _stream_ptr(stream))
+    check(st, "paged_attn_decode_append")
+    return out
+
+
 def paged_attn_multi_query(out: torch.Tensor, q: torch.Tensor, q_start: torch.Tensor,
                            k_pool: torch.Tensor, v_pool: torch.Tensor,
                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,

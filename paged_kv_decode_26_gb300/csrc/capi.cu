@@ -377,13 +377,19 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
     return workspace_bytes_for(num_seqs, n_heads, head_dim, c, nullptr);
 }
 
-PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void* q,
-                                     const void* k_pool, const void* v_pool, pkv_dtype kv_dtype,
-                                     const int32_t* block_tables, int max_blocks_per_seq,
-                                     const int32_t* context_lens, int num_seqs, int n_heads,
-                                     int n_kv_heads, int head_dim, int block_size, int num_blocks,
-                                     float scale, int max_context_len, int split_tokens,
-                                     void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// paged_attn_decode, with the append of paged_attn_decode_append fused in
+// when slot_mapping is not NULL.
+pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void* k_pool,
+                       const void* v_pool, pkv_dtype kv_dtype, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                       int n_heads, int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                       float scale, int max_context_len, int split_tokens, void* workspace,
+                       size_t workspace_bytes, const void* k_new, const void* v_new,
+                       const int64_t* slot_mapping, void* stream) {
     // ---- host-side validation (nothing is launched on failure)
     if (num_seqs < 0) return invalid("num_seqs < 0");
     if (num_seqs > 65535) return unsupported("more than 65535 sequences per call");
@@ -462,6 +468,11 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
     p.ws_o = need ? static_cast<float*>(workspace) : nullptr;
     p.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off) : nullptr;
     p.errors = dev->errors;
+    p.k_pool = const_cast<void*>(k_pool);
+    p.v_pool = const_cast<void*>(v_pool);
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_mapping = slot_mapping;
 
     L.grid = dim3((unsigned)c.max_splits, (unsigned)(n_kv_heads / c.hpc), (unsigned)num_seqs);
     L.block = dim3((unsigned)c.threads);
@@ -502,6 +513,40 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     }
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void* q,
+                                     const void* k_pool, const void* v_pool, pkv_dtype kv_dtype,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int n_heads,
+                                     int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                                     float scale, int max_context_len, int split_tokens,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(out, out_dtype, q, k_pool, v_pool, kv_dtype, block_tables,
+                       max_blocks_per_seq, context_lens, num_seqs, n_heads, n_kv_heads, head_dim,
+                       block_size, num_blocks, scale, max_context_len, split_tokens, workspace,
+                       workspace_bytes, nullptr, nullptr, nullptr, stream);
+}
+
+PKV_API pkv_status paged_attn_decode_append(
+    void* out, pkv_dtype out_dtype, const void* q, void* k_pool, void* v_pool, pkv_dtype kv_dtype,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int n_heads, int n_kv_heads, int head_dim, int block_size, int num_blocks,
+    float scale, int max_context_len, int split_tokens, void* workspace, size_t workspace_bytes,
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping))
+        return invalid("k_new, v_new and slot_mapping are required");
+    if (!aligned16(k_new) || !aligned16(v_new) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return invalid("k_new and v_new must be 16-byte aligned, slot_mapping 8-byte aligned");
+    return decode_impl(out, out_dtype, q, k_pool, v_pool, kv_dtype, block_tables,
+                       max_blocks_per_seq, context_lens, num_seqs, n_heads, n_kv_heads, head_dim,
+                       block_size, num_blocks, scale, max_context_len, split_tokens, workspace,
+                       workspace_bytes, k_new, v_new, slot_mapping, stream);
 }
 
 PKV_API pkv_status kv_append(void* k_pool, void* v_pool, const void* k_new, const void* v_new,

@@ -64,7 +64,46 @@ struct DecodeParams {
     float* ws_o;   // [num_seqs, n_heads, max_splits, D]
     float* ws_ml;  // [num_seqs, n_heads, max_splits, 2]
     unsigned int* errors;
+    // Fused append (paged_attn_decode_append; NULL slot_mapping: none):
+    // row k_new[s] / v_new[s] ([num_seqs, n_kv_heads, D]) goes to pool row
+    // slot_mapping[s] before the decode reads the context.
+    void* k_pool;
+    void* v_pool;
+    const void* k_new;
+    const void* v_new;
+    const int64_t* slot_mapping;
 };
+
+// Fused append: the CTA of a sequence's last split writes the new token's K
+// and V rows for its kv heads (hg * HPC ...) into pool row slot_mapping[s]
+// (skipped for -1, flagged when outside the pool), then makes the stores
+// visible to the TMA loads that follow the CTA barrier.  The last split is
+// the only one whose pages hold the new token's position (splits are
+// page-aligned), so no other CTA of the sequence reads that row.
+template <int D, int BS, typename T>
+__device__ __forceinline__ void fused_append(const DecodeParams& p, int s, int hg, int HPC,
+                                             bool last_split) {
+    if (p.slot_mapping == nullptr || !last_split) return;
+    const int64_t slot = p.slot_mapping[s];
+    if (slot < 0) return;
+    if (slot >= (int64_t)p.num_blocks * BS) {
+        if (threadIdx.x == 0 && hg == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
+        return;
+    }
+    constexpr int VEC = 16 / (int)sizeof(T);           // elements per 16-byte vector
+    const int per_row = HPC * D / VEC;                  // vectors of this CTA's heads
+    const size_t row = (size_t)p.n_kv_heads * D;        // elements of one token row
+    const size_t off_new = (size_t)s * row + (size_t)hg * HPC * D;
+    const size_t off_pool = (size_t)slot * row + (size_t)hg * HPC * D;
+    for (int i = threadIdx.x; i < 2 * per_row; i += blockDim.x) {
+        const bool is_v = i >= per_row;
+        const int j = (is_v ? i - per_row : i) * VEC;
+        const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) + off_new + j;
+        T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) + off_pool + j;
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // Shared-memory bytes of one CTA (must match the carve-up in the kernel).
 // The ring doubles as the buffer of the end-of-CTA merge between the WPT
@@ -223,6 +262,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
         s_bid[i] = b;
     }
+    fused_append<D, BS, T>(p, s, hg, HPC, split == n_splits - 1);
     if (threadIdx.x == 0) {
         for (int st = 0; st < p.stages; ++st) {
             mbar_init(&full[st], 1);

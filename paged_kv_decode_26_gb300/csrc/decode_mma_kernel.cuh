@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
         }
         s_bid[i] = b;
     }
+    fused_append<D, BS, T>(p, s, hg, HPC, split == n_splits - 1);
     if (threadIdx.x == 0) {
         for (int st = 0; st < p.stages; ++st) {
             mbar_init(&full[st], 1);

@@ -237,3 +237,63 @@ def test_full_size_sampled(lib, config, k):
     assert torch.isfinite(g).all()
     assert g.abs().max() <= case.v_pool.float().abs().max() + 1e-2
     _no_device_errors(lib)
+
+
+# ------------------------------------------------- fused append + decode
+
+@pytest.mark.parametrize("config,split", [(1, 0), (2, 0), (2, 64), (3, 0), (5, 0)])
+def test_decode_append_equals_two_calls(lib, config, split):
+    """paged_attn_decode_append gives the pools and the output of
+    kv_append followed by paged_attn_decode, bit for bit (the same kernels'
+    arithmetic), including sequences whose slot is -1 and a slot outside the
+    pool (skipped and flagged by both)."""
+    import paged_kv_decode_26_gb300 as pkv
+    extra = {"d2d_pairs": 8, "h2d_pairs": 8, "host_pool_blocks": 16} if config == 5 else {}
+    case = wl.make_case(config, S=8 if config != 1 else None, poison=True, seed=config + 40,
+                        **extra)
+    S = case.S
+    bm = pkv.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)
+    bt = case.block_tables.clone()
+    need = int(((case.context_lens + 1 + case.B - 1) // case.B).max())
+    if need > bt.shape[1]:
+        bt = torch.cat([bt, torch.full((S, need - bt.shape[1]), -1, dtype=torch.int32)], 1)
+    lens = case.context_lens.clone()
+    slots = torch.empty(S, dtype=torch.int64)
+    bm.append_slots(bt, lens, slots)
+    gen = torch.Generator().manual_seed(config)
+    k_new = torch.randn(S, case.Hk, case.D, generator=gen).to(case.dtype)
+    v_new = torch.randn(S, case.Hk, case.D, generator=gen).to(case.dtype)
+    slots_used = slots.clone()
+    # sequence 0 appends nothing; sequence 2's slot lies outside the pool
+    # (skipped and flagged): neither context counts the new token
+    for s_, bad in ((0, -1), (2, case.num_blocks * case.B + 5)):
+        if s_ < S and int(slots[s_]) >= 0:
+            slots_used[s_] = bad
+            lens[s_] -= 1
+    max_ctx = int(lens.max())
+    d = {k: v.cuda() for k, v in (("q", case.q), ("bt", bt), ("lens", lens),
+                                  ("slots", slots_used), ("kn", k_new), ("vn", v_new))}
+    results = []
+    for fused in (False, True):
+        kp, vp = case.k_pool.cuda(), case.v_pool.cuda()
+        out = torch.zeros(S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+        if fused:
+            pkv.paged_attn_decode_append(out, d["q"], kp, vp, d["bt"], d["lens"], case.scale,
+                                         max_ctx, d["kn"], d["vn"], d["slots"],
+                                         split_tokens=split)
+        else:
+            pkv.kv_append(kp, vp, d["kn"], d["vn"], d["slots"])
+            pkv.paged_attn_decode(out, d["q"], kp, vp, d["bt"], d["lens"], case.scale, max_ctx,
+                                  split_tokens=split)
+        torch.cuda.synchronize()
+        flags = pkv.device_errors(clear=True)
+        assert (flags & 0x4) == (0x4 if S > 2 and int(slots[2]) >= 0 else 0)
+        results.append((out.cpu(), kp.cpu(), vp.cpu()))
+    (o1, k1, v1), (o2, k2, v2) = results
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+    iv = torch.int16 if o1.element_size() == 2 else torch.int32
+    assert torch.equal(o1.view(iv), o2.view(iv))
+    # and against the oracle for the appended state
+    ref = _oracle(case, lens=lens, tables=bt, k=k1, v=v1)
+    assert_attention_close(o2, ref, case.out_dtype, f"config {config}")

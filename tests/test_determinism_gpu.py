@@ -1,0 +1,60 @@
+"""Repeated calls on the same inputs give bit-identical outputs: the
+kernels reduce in a fixed order (no atomics on data, split partials merged
+in split order, tensor-core products issued in a fixed sequence)."""
+import pytest
+import torch
+
+from paged_kv_decode_26_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_decode_26_gb300 import build
+    build.build()
+    import paged_kv_decode_26_gb300 as m
+    m.device_errors(clear=True)
+    return m
+
+
+@pytest.mark.parametrize("config,split", [(2, 0), (2, 64), (3, 0), (1, 0)])
+def test_decode_repeats_bitwise(pkv, config, split):
+    case = wl.make_case(config, S=8 if config != 1 else None, poison=True)
+    d = {k: getattr(case, k).cuda() for k in ("q", "k_pool", "v_pool", "block_tables",
+                                            "context_lens")}
+    outs = []
+    for _ in range(5):
+        out = torch.empty(case.S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+        pkv.paged_attn_decode(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"],
+                              d["context_lens"], case.scale, case.max_context_len,
+                              split_tokens=split)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16) if o.element_size() == 2 else o.view(torch.int32),
+                           outs[0].view(torch.int16) if o.element_size() == 2
+                           else outs[0].view(torch.int32))
+    assert pkv.device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("mode", ["0", "1"])
+def test_multi_query_repeats_bitwise(pkv, monkeypatch, mode):
+    monkeypatch.setenv("PKV_MQ_TC", mode)
+    case = wl.make_case(3, S=6, lens=("uniform", 200, 900), poison=True, seed=4)
+    q, qs = wl.multi_query_inputs(case, ("uniform", 60, 300), seed=5)
+    args = [q.cuda(), qs.cuda(), case.k_pool.cuda(), case.v_pool.cuda(),
+            case.block_tables.cuda(), case.context_lens.cuda()]
+    max_q = int((qs[1:] - qs[:-1]).max())
+    outs = []
+    for _ in range(5):
+        out = torch.empty(q.shape[0], case.H, case.D, dtype=case.out_dtype, device="cuda")
+        pkv.paged_attn_multi_query(out, *args[:2], *args[2:], case.scale, max_q,
+                                   case.max_context_len)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert pkv.device_errors(clear=True) == 0
