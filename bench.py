@@ -62,6 +62,9 @@ def parse_args():
                     help="replay each step as one CUDA graph")
     ap.add_argument("--replicas", type=int, default=1,
                     help="independent copies of the workload (own pools) per GPU, one graph")
+    ap.add_argument("--batched", action="store_true",
+                    help="run the replicas as one batched launch (pkv_decode_batched_plan once, "
+                         "paged_attn_decode_batched per step) instead of a graph")
     ap.add_argument("--multi-query", type=int, default=0,
                     help="time paged_attn_multi_query with this many new tokens per sequence")
     ap.add_argument("--graph-streams", type=int, default=32,
@@ -446,7 +449,9 @@ def main():
     S = case.S
     with_swaps = case.d2d_pairs is not None
     stream = torch.cuda.current_stream()
-    use_graph = args.graph or R > 1
+    use_graph = (args.graph or R > 1) and not args.batched
+    if args.batched and with_swaps:
+        raise SystemExit("--batched does not cover the block copies of the continuous workload")
 
     def decode(r):
         pkv.paged_attn_decode(r["out"], r["q"], r["k_pool"], r["v_pool"], r["bt"], r["lens"],
@@ -502,6 +507,13 @@ def main():
             (2 if with_swaps else 0)
     split_used = args.split or pkv.decode_split_tokens(S, case.H, case.Hk, case.D, case.B,
                                                        reps[0]["max_ctx"])
+    if args.batched:
+        # one launch (and one merge if any context splits) for all replicas
+        split_b = args.split or pkv.decode_split_tokens(R * S, case.H, case.Hk, case.D, case.B,
+                                                        max(r["max_ctx"] for r in reps))
+        split_used = split_b
+        launches_per_step = 1 + (1 if any((r["max_ctx"] + split_b - 1) // split_b > 1
+                                          for r in reps) else 0)
     decode_alg_bytes = kv_unique + io_bytes       # shared prefix rows counted once
     bb = case.B * case.Hk * case.D * es
     swap_bytes = 0
@@ -539,7 +551,25 @@ def main():
             join.record(b)
             cap.wait_event(join)
 
-    if use_graph:
+    if args.batched:
+        # every replica is one problem of a single batched launch
+        max_ctx_all = max(r["max_ctx"] for r in reps)
+
+        def problem(r, append):
+            d = dict(out=r["out"], q=r["q"], k_pool=r["k_pool"], v_pool=r["v_pool"],
+                     block_tables=r["bt"], context_lens=r["lens"])
+            if append:
+                d.update(k_new=r["k_new"], v_new=r["v_new"], slot_mapping=r["slots"])
+            return d
+        batch_step = pkv.DecodeBatch([problem(r, True) for r in reps], case.scale, max_ctx_all,
+                                     split_tokens=args.split)
+        batch_dec = pkv.DecodeBatch([problem(r, False) for r in reps], case.scale, max_ctx_all,
+                                    split_tokens=args.split)
+        run_step, run_decode = batch_step.run, batch_dec.run
+        for _ in range(3):
+            run_step()
+        torch.cuda.synchronize()
+    elif use_graph:
         g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_step):
             fan_out(step_one)
@@ -760,7 +790,9 @@ def main():
                     (" + swap_blocks_kv D2D and pinned-H2D on a side stream, overlapped"
                      if with_swaps else ""),
             "replicas_per_gpu": R,
-            "launch": (f"one CUDA graph per step, replicas on {min(args.graph_streams, R)} "
+            "launch": ("one batched launch per step for all replicas "
+                       "(paged_attn_decode_batched)" if args.batched else
+                       f"one CUDA graph per step, replicas on {min(args.graph_streams, R)} "
                        "parallel branches" if use_graph else "eager"),
             "num_seqs_per_gpu": R * S,
             "kv_bytes_per_step_per_gpu": kv_read,

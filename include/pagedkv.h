@@ -165,6 +165,64 @@ PKV_API pkv_status paged_attn_decode_append(
     const void* k_new, const void* v_new, const int64_t* slot_mapping, void* stream);
 
 /*
+ * Batched decode -- many independent decode problems (each with its own
+ * K/V pools, block tables, lengths, queries and outputs, and optionally a
+ * fused append) in one launch.  The problems share the head counts,
+ * head_dim, block_size and dtypes.  Plan once, run many times:
+ * pkv_decode_batched_plan writes every problem's TMA maps and parameters
+ * into the caller's workspace; paged_attn_decode_batched then launches from
+ * it.  A plan stays valid while the problems' buffers stay at the same
+ * addresses and every context stays within max_context_len; their contents
+ * (queries, tables, lengths, pools, new rows) may change between runs.
+ * Each problem computes exactly what paged_attn_decode (or, with
+ * slot_mapping, paged_attn_decode_append) computes for it.
+ */
+typedef struct {
+    void* out;                    /* device [num_seqs, n_heads, head_dim] of out_dtype */
+    const void* q;                /* device [num_seqs, n_heads, head_dim] of kv_dtype */
+    void* k_pool;                 /* device [num_blocks, block_size, n_kv_heads, head_dim] */
+    void* v_pool;
+    const int32_t* block_tables;  /* device int32 [num_seqs, max_blocks_per_seq] */
+    const int32_t* context_lens;  /* device int32 [num_seqs] */
+    const void* k_new;            /* fused append: device [num_seqs, n_kv_heads, head_dim], */
+    const void* v_new;            /*   16-byte aligned, with slot_mapping; else NULL */
+    const int64_t* slot_mapping;  /* device int64 [num_seqs] (-1 skips), or NULL: no append */
+    int num_seqs;
+    int num_blocks;
+    int max_blocks_per_seq;
+} pkv_decode_problem;
+
+/* Opaque launch plan, filled by pkv_decode_batched_plan (caller-owned). */
+typedef struct {
+    uint64_t opaque[16];
+} pkv_decode_plan;
+
+/* Workspace bytes a batch needs (descriptors, offsets, split partials). */
+PKV_API size_t pkv_decode_batched_workspace_bytes(const pkv_decode_problem* problems,
+                                                  int num_problems, int n_heads, int n_kv_heads,
+                                                  int head_dim, int block_size,
+                                                  int max_context_len, int split_tokens);
+
+/*
+ * Validates the problems (host-side, as paged_attn_decode does), chooses
+ * one launch shape for all of them and copies their descriptors into the
+ * workspace (device, 256-byte aligned, >= pkv_decode_batched_workspace_bytes)
+ * with cudaMemcpyAsync on `stream` from library-owned host memory (the call
+ * returns once the copy is staged; it is not meant for a timed loop).
+ * problems is a host array; at most 65535 sequences in total.
+ */
+PKV_API pkv_status pkv_decode_batched_plan(pkv_decode_plan* plan,
+                                           const pkv_decode_problem* problems, int num_problems,
+                                           pkv_dtype out_dtype, pkv_dtype kv_dtype, int n_heads,
+                                           int n_kv_heads, int head_dim, int block_size,
+                                           float scale, int max_context_len, int split_tokens,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Runs a planned batch on `stream` (one decode launch, plus the split merge
+ * when a context is longer than one split). */
+PKV_API pkv_status paged_attn_decode_batched(const pkv_decode_plan* plan, void* stream);
+
+/*
  * paged_attn_decode_noalloc -- paged_attn_decode for callers that cannot
  * allocate device memory.  The pages have no counterpart: this is an
  * interface addition of this library.

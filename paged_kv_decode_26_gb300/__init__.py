@@ -4,7 +4,8 @@ C ABI: include/pagedkv.h, implemented by libpagedkv.so (CUDA, sm_103a).
 This package holds the CUDA sources (csrc/), the in-tree build, a thin torch
 binding with the same entry-point names, and the seeded workload generator.
 """
-from .api import (BlockManager, DeviceBlockManager, alloc_decode_workspace, decode_split_tokens,
+from .api import (BlockManager, DecodeBatch, DeviceBlockManager, alloc_decode_workspace,
+                  decode_split_tokens,
                   decode_workspace_bytes, device_errors, kv_append, paged_attn_decode,
                   paged_attn_decode_append, paged_attn_multi_query,
                   swap_blocks, swap_blocks_kv)
@@ -12,4 +13,4 @@ from ._lib import PagedKVError, lib
 
 __all__ = ["paged_attn_decode", "paged_attn_decode_append", "paged_attn_multi_query", "kv_append", "swap_blocks", "swap_blocks_kv", "decode_workspace_bytes",
            "decode_split_tokens", "alloc_decode_workspace", "device_errors", "BlockManager", "DeviceBlockManager",
-           "PagedKVError", "lib"]
+           "DecodeBatch", "PagedKVError", "lib"]

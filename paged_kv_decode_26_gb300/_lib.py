@@ -35,6 +35,10 @@ SIGNATURES = {
                                _i, _i, _p, _sz, _p]),
     "paged_attn_decode_append": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i,
                                       _i, _f, _i, _i, _p, _sz, _p, _p, _p, _p]),
+    "pkv_decode_batched_workspace_bytes": (_sz, [_p, _i, _i, _i, _i, _i, _i, _i]),
+    "pkv_decode_batched_plan": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p, _sz,
+                                     _p]),
+    "paged_attn_decode_batched": (_i, [_p, _p]),
     "paged_attn_decode_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i,
                                        _i, _f, _i, _i, _p]),
     "paged_attn_multi_query": (_i, [_p, _i, _p, _p, _i, _i, _p, _p, _i, _p, _i, _p, _i, _i, _i,

@@ -134,6 +134,85 @@ def paged_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.T
     return out
 
 
+class _Problem(C.Structure):
+    """pkv_decode_problem of include/pagedkv.h."""
+    _fields_ = [("out", C.c_void_p), ("q", C.c_void_p), ("k_pool", C.c_void_p),
+                ("v_pool", C.c_void_p), ("block_tables", C.c_void_p),
+                ("context_lens", C.c_void_p), ("k_new", C.c_void_p), ("v_new", C.c_void_p),
+                ("slot_mapping", C.c_void_p), ("num_seqs", C.c_int), ("num_blocks", C.c_int),
+                ("max_blocks_per_seq", C.c_int)]
+
+
+class _Plan(C.Structure):
+    _fields_ = [("opaque", C.c_uint64 * 16)]
+
+
+class DecodeBatch:
+    """Independent decode problems (each with its own pools, tables, lengths,
+    queries and outputs, optionally a fused append) planned once and run in
+    one launch.  `problems` is a list of dicts with the keys out, q, k_pool,
+    v_pool, block_tables, context_lens and optionally k_new, v_new,
+    slot_mapping (as paged_attn_decode_append).  The plan stays valid while
+    those tensors keep their storage and every context stays within
+    max_context_len; run() reads their current contents."""
+
+    def __init__(self, problems, scale: float, max_context_len: int, split_tokens: int = 0,
+                 stream: Optional[torch.cuda.Stream] = None):
+        if not problems:
+            raise ValueError("no problems")
+        ref = problems[0]
+        _, H, D = ref["q"].shape
+        _, B, Hk, _ = ref["k_pool"].shape
+        kv_dt, out_dt = ref["k_pool"].dtype, ref["out"].dtype
+        arr = (_Problem * len(problems))()
+        for i, pr in enumerate(problems):
+            for name in ("out", "q", "k_pool", "v_pool", "block_tables", "context_lens"):
+                _need_cuda(name, pr[name])
+            q, kp = pr["q"], pr["k_pool"]
+            S = q.shape[0]
+            if (tuple(q.shape[1:]) != (H, D) or tuple(kp.shape[1:]) != (B, Hk, D)
+                    or pr["v_pool"].shape != kp.shape or tuple(pr["out"].shape) != (S, H, D)
+                    or q.dtype != kv_dt or kp.dtype != kv_dt or pr["v_pool"].dtype != kv_dt
+                    or pr["out"].dtype != out_dt
+                    or pr["block_tables"].dtype != torch.int32
+                    or pr["context_lens"].dtype != torch.int32
+                    or pr["block_tables"].shape[0] != S or pr["context_lens"].shape != (S,)):
+                raise ValueError(f"problem {i}: inconsistent shapes or dtypes")
+            sm = pr.get("slot_mapping")
+            if sm is not None:
+                for name in ("k_new", "v_new", "slot_mapping"):
+                    _need_cuda(name, pr[name])
+                if (sm.dtype != torch.int64 or sm.shape != (S,)
+                        or tuple(pr["k_new"].shape) != (S, Hk, D)
+                        or pr["v_new"].shape != pr["k_new"].shape
+                        or pr["k_new"].dtype != kv_dt or pr["v_new"].dtype != kv_dt):
+                    raise ValueError(f"problem {i}: inconsistent append rows")
+            arr[i] = _Problem(pr["out"].data_ptr(), q.data_ptr(), kp.data_ptr(),
+                              pr["v_pool"].data_ptr(), pr["block_tables"].data_ptr(),
+                              pr["context_lens"].data_ptr(),
+                              pr["k_new"].data_ptr() if sm is not None else None,
+                              pr["v_new"].data_ptr() if sm is not None else None,
+                              sm.data_ptr() if sm is not None else None, S, kp.shape[0],
+                              pr["block_tables"].shape[1])
+        self._problems = list(problems)      # keeps the tensors alive
+        ws_bytes = int(lib().pkv_decode_batched_workspace_bytes(
+            C.addressof(arr), len(problems), H, Hk, D, B, int(max_context_len),
+            int(split_tokens)))
+        if ws_bytes == 0:
+            raise ValueError("unsupported batch (head counts, head_dim, block size)")
+        self.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=ref["q"].device)
+        self._plan = _Plan()
+        st = lib().pkv_decode_batched_plan(
+            C.addressof(self._plan), C.addressof(arr), len(problems), _DT[out_dt], _DT[kv_dt], H,
+            Hk, D, B, float(scale), int(max_context_len), int(split_tokens),
+            _ptr(self.workspace), ws_bytes, _stream_ptr(stream))
+        check(st, "pkv_decode_batched_plan")
+
+    def run(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        check(lib().paged_attn_decode_batched(C.addressof(self._plan), _stream_ptr(stream)),
+              "paged_attn_decode_batched")
+
+
 def paged_attn_multi_query(out: torch.Tensor, q: torch.Tensor, q_start: torch.Tensor,
                            k_pool: torch.Tensor, v_pool: torch.Tensor,
                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,

@@ -12,9 +12,11 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "capi_host.h"
 #include "copy_kernels.cuh"
+#include "decode_batched.cuh"
 #include "decode_launch.h"
 
 // ----------------------------------------------------------------- errors
@@ -547,6 +549,267 @@ PKV_API pkv_status paged_attn_decode_append(
                        max_blocks_per_seq, context_lens, num_seqs, n_heads, n_kv_heads, head_dim,
                        block_size, num_blocks, scale, max_context_len, split_tokens, workspace,
                        workspace_bytes, k_new, v_new, slot_mapping, stream);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------ batched decode
+
+namespace {
+
+constexpr uint32_t kPlanMagic = 0x504b5642u;
+
+// What a plan remembers (inside the caller's pkv_decode_plan).
+struct BatchPlan {
+    uint32_t magic;
+    int num_problems;
+    int total_seqs;
+    int n_heads;
+    int head_dim;
+    int block_size;
+    int kv_dtype;
+    int mma;
+    int qpw;
+    int groups;       // kv-head groups per sequence (n_kv_heads / heads per CTA)
+    int max_splits;
+    int threads;
+    size_t smem;
+    char* workspace;
+    size_t seq_off;
+};
+static_assert(sizeof(BatchPlan) <= sizeof(pkv_decode_plan), "pkv_decode_plan is too small");
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace of a batch: the problems' descriptors, the sequence offsets,
+// then each problem's split partials (O, then (M, L)) when contexts split.
+struct BatchLayout {
+    size_t seq_off;
+    size_t parts_off;
+    size_t total;
+};
+
+BatchLayout batch_layout(const pkv_decode_problem* problems, int num_problems, int n_heads,
+                         int head_dim, const DecodeConfig& c) {
+    BatchLayout l;
+    l.seq_off = align256((size_t)num_problems * sizeof(pkv::BatchedProblem));
+    l.parts_off = l.seq_off + align256((size_t)(num_problems + 1) * sizeof(int));
+    size_t t = l.parts_off;
+    if (c.max_splits > 1)
+        for (int i = 0; i < num_problems; ++i) {
+            const size_t units =
+                (size_t)std::max(problems[i].num_seqs, 0) * n_heads * c.max_splits;
+            t += align256(units * head_dim * sizeof(float)) + align256(units * 2 * sizeof(float));
+        }
+    l.total = t;
+    return l;
+}
+
+long long total_seqs_of(const pkv_decode_problem* problems, int num_problems) {
+    long long t = 0;
+    for (int i = 0; i < num_problems; ++i) t += std::max(problems[i].num_seqs, 0);
+    return t;
+}
+
+}  // namespace
+
+extern "C" {
+
+PKV_API size_t pkv_decode_batched_workspace_bytes(const pkv_decode_problem* problems,
+                                                  int num_problems, int n_heads, int n_kv_heads,
+                                                  int head_dim, int block_size,
+                                                  int max_context_len, int split_tokens) {
+    if (num_problems < 0 || (num_problems > 0 && !problems) ||
+        !supported_shape(n_heads, n_kv_heads, head_dim, block_size) || max_context_len < 0)
+        return 0;
+    DeviceInfo* dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return 0;
+    const long long total = total_seqs_of(problems, num_problems);
+    DecodeConfig c;
+    if (make_config((int)std::min(total, 65535LL), n_heads, n_kv_heads, head_dim, block_size,
+                    max_context_len, split_tokens, dev->sm_count, &c) != PKV_OK)
+        return 0;
+    return batch_layout(problems, num_problems, n_heads, head_dim, c).total;
+}
+
+PKV_API pkv_status pkv_decode_batched_plan(pkv_decode_plan* plan,
+                                           const pkv_decode_problem* problems, int num_problems,
+                                           pkv_dtype out_dtype, pkv_dtype kv_dtype, int n_heads,
+                                           int n_kv_heads, int head_dim, int block_size,
+                                           float scale, int max_context_len, int split_tokens,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (!plan) return invalid("plan is NULL");
+    std::memset(plan, 0, sizeof(*plan));
+    if (num_problems < 0 || (num_problems > 0 && !problems)) return invalid("problems");
+    if (kv_dtype != PKV_BF16 && kv_dtype != PKV_F16) return unsupported("kv_dtype must be F16 or BF16");
+    if (out_dtype != PKV_BF16 && out_dtype != PKV_F16 && out_dtype != PKV_F32)
+        return invalid("out_dtype");
+    if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size))
+        return unsupported("head_dim 64/128, block_size 16/32, group 1/2/4/8");
+    if (max_context_len < 0) return invalid("max_context_len < 0");
+    if (!std::isfinite(scale)) return invalid("scale is not finite");
+    const long long total = total_seqs_of(problems, num_problems);
+    if (total > 65535) return unsupported("more than 65535 sequences per batch");
+    for (int i = 0; i < num_problems; ++i) {
+        const pkv_decode_problem& q = problems[i];
+        if (q.num_seqs < 0 || q.num_blocks < 0) return invalid("problem sizes");
+        if (q.num_seqs == 0) continue;
+        if (q.max_blocks_per_seq <= 0) return invalid("max_blocks_per_seq must be positive");
+        if (!q.out || !q.q || !q.block_tables || !q.context_lens)
+            return invalid("a problem's required pointer is NULL");
+        if (q.num_blocks > 0 && (!q.k_pool || !q.v_pool)) return invalid("a problem's pool is NULL");
+        if (!aligned16(q.out) || !aligned16(q.q) || !aligned16(q.k_pool) || !aligned16(q.v_pool))
+            return invalid("out, q, k_pool and v_pool must be 16-byte aligned");
+        if (q.slot_mapping &&
+            (!q.k_new || !q.v_new || !aligned16(q.k_new) || !aligned16(q.v_new) ||
+             (reinterpret_cast<uintptr_t>(q.slot_mapping) & 7u)))
+            return invalid("a problem's append rows are NULL or misaligned");
+    }
+    DeviceInfo* dev = nullptr;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DecodeConfig c;
+    pkv_status st = make_config((int)std::max(total, 1LL), n_heads, n_kv_heads, head_dim,
+                                block_size, max_context_len, split_tokens, dev->sm_count, &c);
+    if (st != PKV_OK) return st;
+    if (c.smem > (size_t)dev->smem_optin) return unsupported("shared memory of this configuration");
+    if (c.max_splits > 65535) return unsupported("more than 65535 splits per sequence");
+    const BatchLayout lay = batch_layout(problems, num_problems, n_heads, head_dim, c);
+    if (!workspace || workspace_bytes < lay.total) {
+        set_detail("%s", "workspace smaller than pkv_decode_batched_workspace_bytes()");
+        return PKV_ERR_WORKSPACE;
+    }
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return invalid("workspace must be 256-byte aligned");
+
+    char* ws = static_cast<char*>(workspace);
+    std::vector<pkv::BatchedProblem> hp((size_t)num_problems);
+    std::vector<int> seq_begin((size_t)num_problems + 1, 0);
+    size_t part = lay.parts_off;
+    const int cap_tokens =
+        (int)std::min(0x7fffffffLL, (long long)c.max_splits * c.split_tokens);
+    for (int i = 0; i < num_problems; ++i) {
+        const pkv_decode_problem& q = problems[i];
+        pkv::BatchedProblem& b = hp[(size_t)i];
+        std::memset(&b, 0, sizeof(b));
+        seq_begin[(size_t)i + 1] = seq_begin[(size_t)i] + std::max(q.num_seqs, 0);
+        // an empty pool (or problem) still gets well-formed maps; no block id
+        // passes the kernel's range check then, so nothing is loaded
+        const void* kb = q.num_blocks > 0 ? q.k_pool : (q.q ? q.q : workspace);
+        const void* vb = q.num_blocks > 0 ? q.v_pool : (q.q ? q.q : workspace);
+        const int mb = q.num_blocks > 0 ? q.num_blocks : 1;
+        if ((e = encode_pool_map(&b.tm_k, kb, kv_dtype, mb, block_size, n_kv_heads, head_dim,
+                                 c.hpc, c.mma)) != cudaSuccess ||
+            (e = encode_pool_map(&b.tm_v, vb, kv_dtype, mb, block_size, n_kv_heads, head_dim,
+                                 c.hpc, c.mma)) != cudaSuccess)
+            return cuda_fail(e);
+        pkv::DecodeParams& p = b.p;
+        p.out = q.out;
+        p.out_dtype = out_dtype;
+        p.q = q.q;
+        p.block_tables = q.block_tables;
+        p.max_blocks_per_seq = std::max(q.max_blocks_per_seq, 1);
+        p.context_lens = q.context_lens;
+        p.num_seqs = q.num_seqs;
+        p.n_heads = n_heads;
+        p.n_kv_heads = n_kv_heads;
+        p.group = n_heads / n_kv_heads;
+        p.num_blocks = q.num_blocks;
+        p.scale_log2 = scale * 1.4426950408889634f;
+        p.split_tokens = c.split_tokens;
+        p.max_splits = c.max_splits;
+        p.heads_per_cta = c.hpc;
+        p.warps_per_kv = c.wpk;
+        p.warps_per_tok = c.wpt;
+        p.stages = c.stages;
+        p.max_pages_per_split = c.max_pages;
+        p.errors = dev->errors;
+        p.k_pool = q.k_pool;
+        p.v_pool = q.v_pool;
+        p.k_new = q.k_new;
+        p.v_new = q.v_new;
+        p.slot_mapping = q.slot_mapping;
+        if (c.max_splits > 1) {
+            const size_t units = (size_t)std::max(q.num_seqs, 0) * n_heads * c.max_splits;
+            p.ws_o = reinterpret_cast<float*>(ws + part);
+            part += align256(units * head_dim * sizeof(float));
+            p.ws_ml = reinterpret_cast<float*>(ws + part);
+            part += align256(units * 2 * sizeof(float));
+        }
+        pkv::ReduceParams& r = b.r;
+        r.out = q.out;
+        r.out_dtype = out_dtype;
+        r.context_lens = q.context_lens;
+        r.num_seqs = q.num_seqs;
+        r.n_heads = n_heads;
+        r.split_tokens = c.split_tokens;
+        r.max_splits = c.max_splits;
+        r.cap_tokens = (int)std::min((long long)p.max_blocks_per_seq * block_size,
+                                     (long long)cap_tokens);
+        r.ws_o = p.ws_o;
+        r.ws_ml = p.ws_ml;
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (num_problems > 0) {
+        if ((e = cudaMemcpyAsync(ws, hp.data(), hp.size() * sizeof(pkv::BatchedProblem),
+                                 cudaMemcpyHostToDevice, cs)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(ws + lay.seq_off, seq_begin.data(),
+                                 seq_begin.size() * sizeof(int), cudaMemcpyHostToDevice, cs)) !=
+                cudaSuccess)
+            return cuda_fail(e);
+    }
+    BatchPlan* bp = reinterpret_cast<BatchPlan*>(plan);
+    bp->magic = kPlanMagic;
+    bp->num_problems = num_problems;
+    bp->total_seqs = (int)total;
+    bp->n_heads = n_heads;
+    bp->head_dim = head_dim;
+    bp->block_size = block_size;
+    bp->kv_dtype = kv_dtype;
+    bp->mma = c.mma ? 1 : 0;
+    bp->qpw = c.qpw;
+    bp->groups = n_kv_heads / c.hpc;
+    bp->max_splits = c.max_splits;
+    bp->threads = c.threads;
+    bp->smem = c.smem;
+    bp->workspace = ws;
+    bp->seq_off = lay.seq_off;
+    return PKV_OK;
+}
+
+PKV_API pkv_status paged_attn_decode_batched(const pkv_decode_plan* plan, void* stream) {
+    const BatchPlan* bp = reinterpret_cast<const BatchPlan*>(plan);
+    if (!bp || bp->magic != kPlanMagic) return invalid("not a plan from pkv_decode_batched_plan");
+    if (bp->total_seqs == 0) return PKV_OK;
+    pkv::BatchedLaunch L;
+    L.probs = reinterpret_cast<const pkv::BatchedProblem*>(bp->workspace);
+    L.seq_begin = reinterpret_cast<const int*>(bp->workspace + bp->seq_off);
+    L.num_problems = bp->num_problems;
+    L.grid = dim3((unsigned)bp->max_splits, (unsigned)bp->groups, (unsigned)bp->total_seqs);
+    L.block = dim3((unsigned)bp->threads);
+    L.smem_bytes = bp->smem;
+    L.stream = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (bp->mma)
+        e = bp->kv_dtype == PKV_BF16
+                ? pkv::launch_decode_mma_batched_bf16(bp->head_dim, bp->block_size, L)
+                : pkv::launch_decode_mma_batched_f16(bp->head_dim, bp->block_size, L);
+    else
+        e = bp->kv_dtype == PKV_BF16
+                ? pkv::launch_decode_batched_bf16(bp->head_dim, bp->block_size, bp->qpw, L)
+                : pkv::launch_decode_batched_f16(bp->head_dim, bp->block_size, bp->qpw, L);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (bp->max_splits > 1) {
+        const unsigned units = (unsigned)bp->total_seqs * (unsigned)bp->n_heads;
+        const dim3 grid((units + 3) / 4);
+        if (bp->head_dim == 128)
+            pkv::paged_decode_batched_reduce_kernel<128><<<grid, 128, 0, L.stream>>>(
+                L.probs, L.seq_begin, L.num_problems, bp->n_heads);
+        else
+            pkv::paged_decode_batched_reduce_kernel<64><<<grid, 128, 0, L.stream>>>(
+                L.probs, L.seq_begin, L.num_problems, bp->n_heads);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    }
+    return PKV_OK;
 }
 
 PKV_API pkv_status kv_append(void* k_pool, void* v_pool, const void* k_new, const void* v_new,

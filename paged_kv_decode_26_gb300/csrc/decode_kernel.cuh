@@ -196,10 +196,11 @@ __device__ __forceinline__ void consumer_sync(int n_threads) {
 
 // ------------------------------------------------------------ the kernel
 
+// One CTA's work: (sequence s, kv-head group hg, context split `split`) of
+// the problem described by p, its K/V pools seen through tm_k / tm_v.
 template <int D, int BS, int QPW, typename T>
-__global__ void __launch_bounds__(kMaxThreads, 1)
-    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+__device__ __forceinline__ void decode_cta(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                           const DecodeParams& p, int split, int hg, int s) {
     constexpr int LPR = D / 8;                   // lanes per K/V row (8 dims each)
     constexpr int TPI = 32 / LPR;                // rows per warp iteration
     constexpr int IPC = kChunk / TPI;            // iterations per 16-token chunk
@@ -212,9 +213,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
     extern __shared__ __align__(128) unsigned char smem[];
 
-    const int split = blockIdx.x;
-    const int hg = blockIdx.y;
-    const int s = blockIdx.z;
     const int HPC = p.heads_per_cta;
     const int per_sub = HPC * p.warps_per_kv;   // consumer warps per page
     const int n_cons = per_sub * p.warps_per_tok;
@@ -280,8 +278,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (warp == 0) {
         // ================= producer =================
         if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
+            prefetch_tensormap(tm_k);
+            prefetch_tensormap(tm_v);
             const uint64_t policy = l2_policy_evict_first();
             int i = 0;
             for (; i < n_pages; ++i) {
@@ -297,8 +295,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 if (b >= 0) {
                     unsigned char* dst = tiles + (size_t)st * 2 * tile_bytes;
                     mbar_arrive_expect_tx(&full[st], 2 * tile_bytes);
-                    tma_load_4d(dst, &tm_k, &full[st], 0, hg * HPC, 0, b, policy);
-                    tma_load_4d(dst + tile_bytes, &tm_v, &full[st], 0, hg * HPC, 0, b, policy);
+                    tma_load_4d(dst, tm_k, &full[st], 0, hg * HPC, 0, b, policy);
+                    tma_load_4d(dst + tile_bytes, tm_v, &full[st], 0, hg * HPC, 0, b, policy);
                 } else {
                     mbar_arrive(&full[st]);
                 }
@@ -571,6 +569,14 @@ __device__ __forceinline__ void store_row(void* base, size_t elem_off, int out_d
     }
 }
 
+template <int D, int BS, int QPW, typename T>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ DecodeParams p) {
+    decode_cta<D, BS, QPW, T>(&tm_k, &tm_v, p, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
 // ------------------------------------------------------------ split merge
 
 struct ReduceParams {
@@ -589,10 +595,8 @@ struct ReduceParams {
 // One warp per (sequence, query head): merges the partial states of its
 // splits, O = sum_k w_k O_k / sum_k w_k with w_k = L_k 2^{M_k - M*}.
 template <int D>
-__global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const ReduceParams p) {
+__device__ __forceinline__ void reduce_unit(const ReduceParams& p, int unit, int lane) {
     constexpr int DL = D / 32;
-    const int unit = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
     if (unit >= p.num_seqs * p.n_heads) return;
     const int s = unit / p.n_heads;
     int n = p.context_lens[s];
@@ -638,6 +642,11 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const ReducePa
 #pragma unroll
     for (int d = 0; d < DL; ++d) v[d] = acc[d] * inv;
     store_row<DL>(p.out, (size_t)unit * D + lane * DL, p.out_dtype, v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const __grid_constant__ ReduceParams p) {
+    reduce_unit<D>(p, blockIdx.x * 4 + (threadIdx.x >> 5), threadIdx.x & 31);
 }
 
 }  // namespace pkv

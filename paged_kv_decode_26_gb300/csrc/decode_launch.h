@@ -45,6 +45,24 @@ cudaError_t launch_multi_query_f16(int D, int BS, const MultiQueryLaunch& L);
 cudaError_t launch_multi_query_tc_bf16(int D, int BS, const MultiQueryLaunch& L);
 cudaError_t launch_multi_query_tc_f16(int D, int BS, const MultiQueryLaunch& L);
 
+struct BatchedProblem;
+
+struct BatchedLaunch {
+    const BatchedProblem* probs;   // device [num_problems]
+    const int* seq_begin;          // device [num_problems + 1]
+    int num_problems;
+    dim3 grid;
+    dim3 block;
+    size_t smem_bytes;
+    cudaStream_t stream;
+};
+
+// Launch paged_decode_batched_kernel<D, BS, QPW, T> / the tensor-core variant.
+cudaError_t launch_decode_batched_bf16(int D, int BS, int QPW, const BatchedLaunch& L);
+cudaError_t launch_decode_batched_f16(int D, int BS, int QPW, const BatchedLaunch& L);
+cudaError_t launch_decode_mma_batched_bf16(int D, int BS, const BatchedLaunch& L);
+cudaError_t launch_decode_mma_batched_f16(int D, int BS, const BatchedLaunch& L);
+
 // Raise a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask, size_t bytes);
 

@@ -101,10 +101,10 @@ __device__ __forceinline__ uint32_t swz(int t, int c) {
     return (uint32_t)(t * 128 + ((c ^ (t & 7)) << 4));
 }
 
+// One CTA's work (sequence s, kv-head group hg, split) of the problem p.
 template <int D, int BS, typename T>
-__global__ void __launch_bounds__(kMmaMaxThreads, 1)
-    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+__device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                               const DecodeParams& p, int split, int hg, int s) {
     constexpr int HALVES = D / 64;        // 128-byte boxes per token row
     constexpr int KSTEPS = D / 16;        // k-steps of the score MMA
     constexpr int NT = D / 8;             // n-tiles of the P V MMA
@@ -113,9 +113,6 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
 
-    const int split = blockIdx.x;
-    const int hg = blockIdx.y;
-    const int s = blockIdx.z;
     const int HPC = p.heads_per_cta;
     const int G = p.group;
     if ((int)blockDim.x != 32 * (1 + HPC) || G > 8 || p.warps_per_tok != 1) {
@@ -174,8 +171,8 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     if (warp == 0) {
         // ================= producer =================
         if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
+            prefetch_tensormap(tm_k);
+            prefetch_tensormap(tm_v);
             const uint64_t policy = l2_policy_evict_first();
             int i = 0;
             for (; i < n_pages; ++i) {
@@ -194,9 +191,9 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                     for (int hh = 0; hh < HPC; ++hh) {
                         const int row = (hg * HPC + hh) * HALVES;
                         for (int h = 0; h < HALVES; ++h) {
-                            tma_load_4d(dst + hh * head_bytes + h * BOX, &tm_k, &full[st], 0,
+                            tma_load_4d(dst + hh * head_bytes + h * BOX, tm_k, &full[st], 0,
                                         row + h, 0, b, policy);
-                            tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, &tm_v,
+                            tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, tm_v,
                                         &full[st], 0, row + h, 0, b, policy);
                         }
                     }
@@ -385,6 +382,14 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
             mbar_wait(&full[st], (last / p.stages) & 1, p.errors);
         }
     }
+}
+
+template <int D, int BS, typename T>
+__global__ void __launch_bounds__(kMmaMaxThreads, 1)
+    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ DecodeParams p) {
+    decode_mma_cta<D, BS, T>(&tm_k, &tm_v, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 }  // namespace pkv
