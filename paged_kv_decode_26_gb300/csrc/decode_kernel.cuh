@@ -72,6 +72,9 @@ struct DecodeParams {
     const void* k_new;
     const void* v_new;
     const int64_t* slot_mapping;
+    // 1: CTAs take their (split, head group, sequence) from the dense unit
+    // list of dense_unit() instead of their grid coordinates.
+    int dense;
 };
 
 // Fused append: the CTA of a sequence's last split writes the new token's K
@@ -569,12 +572,139 @@ __device__ __forceinline__ void store_row(void* base, size_t elem_off, int out_d
     }
 }
 
+// ------------------------------------------------------------ dense order
+
+// The grid holds one CTA per (split, kv-head group, sequence) of the longest
+// context, but a sequence of n tokens has only max(1, ceil(n / split_tokens))
+// splits.  Taken in grid order, the CTAs of missing splits sit between the
+// working ones; each holds an SM slot for the time it takes to read its
+// context length, and the dispatcher waits for slots.  With p.dense, CTA u
+// (in grid order, the head group fastest) takes the u-th entry of a dense
+// list instead: every sequence's full splits (sequence by sequence), then
+// every sequence's shorter last split.  The CTAs without an entry all come at
+// the end of the grid and the short units run in the tail.  Lengths are
+// clamped as decode_cta clamps them.  Uses the first 136 bytes of dynamic
+// shared memory before decode_cta does; returns false for a CTA without work.
+template <int BS>
+__device__ __forceinline__ bool dense_unit(const DecodeParams& p, int& split, int& hg, int& s) {
+    extern __shared__ __align__(16) int dense_scratch[];
+    int* s_full = dense_scratch;          // per-warp sums of full splits
+    int* s_last = dense_scratch + 16;     // per-warp sums of short last splits
+    int* s_pick = dense_scratch + 32;     // (sequence, split) of this CTA
+    const int groups = (int)gridDim.y;
+    const long long u =
+        blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+    hg = (int)(u % groups);
+    const long long want = u / groups;
+    const int S = p.num_seqs;
+    const int nt = (int)blockDim.x;
+    const int per = (S + nt - 1) / nt;
+    const int lo = min(S, (int)threadIdx.x * per);
+    const int hi = min(S, lo + per);
+    const int st = p.split_tokens;
+    const int cap = min(p.max_blocks_per_seq * BS, p.max_splits * st);
+    int f = 0, r = 0;  // full splits and short last splits of this thread's sequences
+    for (int i = lo; i < hi; ++i) {
+        int n = p.context_lens[i];
+        n = n < 0 ? 0 : (n > cap ? cap : n);
+        f += n / st;
+        r += (n == 0 || n % st != 0) ? 1 : 0;
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int fi = f, ri = r;  // inclusive scans within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, fi, d);
+        const int b = __shfl_up_sync(0xffffffffu, ri, d);
+        if (lane >= d) {
+            fi += a;
+            ri += b;
+        }
+    }
+    if (lane == 31) {
+        s_full[w] = fi;
+        s_last[w] = ri;
+    }
+    if (threadIdx.x == 0) s_pick[0] = -1;
+    __syncthreads();
+    int fo = fi - f, ro = ri - r, F = 0, R = 0;
+    for (int k = 0; k < (nt >> 5); ++k) {
+        const int a = s_full[k], b = s_last[k];
+        if (k < w) {
+            fo += a;
+            ro += b;
+        }
+        F += a;
+        R += b;
+    }
+    if (want < F) {
+        if (want >= fo && want < fo + f) {
+            int cum = fo;
+            for (int i = lo; i < hi; ++i) {
+                int n = p.context_lens[i];
+                n = n < 0 ? 0 : (n > cap ? cap : n);
+                if (want < cum + n / st) {
+                    s_pick[0] = i;
+                    s_pick[1] = (int)(want - cum);
+                    break;
+                }
+                cum += n / st;
+            }
+        }
+    } else if (want - F < R) {
+        const int t = (int)(want - F);
+        if (t >= ro && t < ro + r) {
+            int cum = ro;
+            for (int i = lo; i < hi; ++i) {
+                int n = p.context_lens[i];
+                n = n < 0 ? 0 : (n > cap ? cap : n);
+                if (n == 0 || n % st != 0) {
+                    if (t == cum) {
+                        s_pick[0] = i;
+                        s_pick[1] = n / st;
+                        break;
+                    }
+                    ++cum;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // The scratch lies in the ring, which only TMA writes, and only after
+    // the CTA barrier that follows the mbarrier setup: no barrier is needed
+    // between these reads and the kernel body.
+    s = s_pick[0];
+    split = s_pick[1];
+    return s >= 0;
+}
+
+// The CTA's (split, head group, sequence): dense list (p.dense == 1), grid
+// order with the head group fastest (2), or the grid coordinates (0).
+template <int BS>
+__device__ __forceinline__ bool decode_unit(const DecodeParams& p, int& split, int& hg, int& s) {
+    split = blockIdx.x;
+    hg = blockIdx.y;
+    s = blockIdx.z;
+    if (p.dense == 1) return dense_unit<BS>(p, split, hg, s);
+    if (p.dense == 2) {
+        const long long u =
+            blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+        hg = (int)(u % gridDim.y);
+        const long long rest = u / gridDim.y;
+        split = (int)(rest % gridDim.x);
+        s = (int)(rest / gridDim.x);
+    }
+    return true;
+}
+
 template <int D, int BS, int QPW, typename T>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ DecodeParams p) {
-    decode_cta<D, BS, QPW, T>(&tm_k, &tm_v, p, blockIdx.x, blockIdx.y, blockIdx.z);
+    int split, hg, s;
+    if (!decode_unit<BS>(p, split, hg, s)) return;
+    decode_cta<D, BS, QPW, T>(&tm_k, &tm_v, p, split, hg, s);
 }
 
 // ------------------------------------------------------------ split merge

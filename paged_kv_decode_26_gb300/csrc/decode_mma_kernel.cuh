@@ -389,7 +389,9 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ DecodeParams p) {
-    decode_mma_cta<D, BS, T>(&tm_k, &tm_v, p, blockIdx.x, blockIdx.y, blockIdx.z);
+    int split, hg, s;
+    if (!decode_unit<BS>(p, split, hg, s)) return;
+    decode_mma_cta<D, BS, T>(&tm_k, &tm_v, p, split, hg, s);
 }
 
 }  // namespace pkv

@@ -58,3 +58,36 @@ def test_multi_query_repeats_bitwise(pkv, monkeypatch, mode):
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
     assert pkv.device_errors(clear=True) == 0
+
+
+def _bits(o):
+    return o.view(torch.int16) if o.element_size() == 2 else o.view(torch.int32)
+
+
+@pytest.mark.parametrize("config,S,split,lens", [
+    (2, 40, 64, None),                                   # MHA consumer, many splits
+    (3, 24, 0, None),                                    # GQA tensor-core consumer
+    (4, 5, 256, [0, 1, 256, 257, 4000]),                 # block size 32, exact multiples
+    (2, 70, 16, [0] * 30 + [16 * k + 3 for k in range(40)]),  # many empty contexts
+])
+def test_dense_order_matches_grid_order(pkv, monkeypatch, config, S, split, lens):
+    """CTAs taking units from the dense list (full splits first, short last
+    splits after) or in grid order with the head group fastest compute the
+    same partials as CTAs taking them by grid coordinates: the outputs agree
+    bit for bit."""
+    over = {"pool_extra": 0.5} if config == 4 else {}
+    case = wl.make_case(config, S=S, poison=True, seed=11, lens_override=lens, **over)
+    d = {k: getattr(case, k).cuda() for k in ("q", "k_pool", "v_pool", "block_tables",
+                                            "context_lens")}
+    outs = {}
+    for mode in ("0", "1", "2"):
+        monkeypatch.setenv("PKV_DECODE_DENSE", mode)
+        out = torch.empty(case.S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+        pkv.paged_attn_decode(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"],
+                              d["context_lens"], case.scale, case.max_context_len,
+                              split_tokens=split)
+        outs[mode] = out
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(outs["0"]), _bits(outs["1"]))
+    assert torch.equal(_bits(outs["0"]), _bits(outs["2"]))
+    assert pkv.device_errors(clear=True) == 0
