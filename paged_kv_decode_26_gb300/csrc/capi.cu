@@ -258,6 +258,27 @@ int auto_split_tokens(int num_seqs, int n_kv_heads, int hpc, int block_size, int
     return split;
 }
 
+// The split merge's launch: 128 threads per CTA, allowed to start while the
+// decode kernel before it on the stream still runs (the decode CTAs signal
+// at their start, the merge waits for the decode grid's completion and
+// memory before it reads a partial), which hides the kernel boundary.
+// PKV_DECODE_PDL=0 launches it plainly after the decode kernel.
+struct DependentLaunch {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    DependentLaunch(dim3 grid, cudaStream_t stream) {
+        std::memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = env_int("PKV_DECODE_PDL", 1) != 0 ? 1 : 0;
+    }
+};
+
 // How decode CTAs find their work unit (DecodeParams::dense).  With 16 or
 // more splits of the longest context, the dense list: where most contexts are
 // shorter, most grid CTAs have no split, and placing them after the working
@@ -539,12 +560,10 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
         r.ws_o = p.ws_o;
         r.ws_ml = p.ws_ml;
         const unsigned units = (unsigned)num_seqs * (unsigned)n_heads;
-        const dim3 grid((units + 3) / 4);
-        if (head_dim == 128)
-            pkv::paged_decode_reduce_kernel<128><<<grid, 128, 0, L.stream>>>(r);
-        else
-            pkv::paged_decode_reduce_kernel<64><<<grid, 128, 0, L.stream>>>(r);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        DependentLaunch dl(dim3((units + 3) / 4), L.stream);
+        e = head_dim == 128 ? cudaLaunchKernelEx(&dl.cfg, pkv::paged_decode_reduce_kernel<128>, r)
+                            : cudaLaunchKernelEx(&dl.cfg, pkv::paged_decode_reduce_kernel<64>, r);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return PKV_OK;
 }
@@ -833,14 +852,15 @@ PKV_API pkv_status paged_attn_decode_batched(const pkv_decode_plan* plan, void* 
     if (e != cudaSuccess) return cuda_fail(e);
     if (bp->max_splits > 1) {
         const unsigned units = (unsigned)bp->total_seqs * (unsigned)bp->n_heads;
-        const dim3 grid((units + 3) / 4);
-        if (bp->head_dim == 128)
-            pkv::paged_decode_batched_reduce_kernel<128><<<grid, 128, 0, L.stream>>>(
-                L.probs, L.seq_begin, L.num_problems, bp->n_heads);
-        else
-            pkv::paged_decode_batched_reduce_kernel<64><<<grid, 128, 0, L.stream>>>(
-                L.probs, L.seq_begin, L.num_problems, bp->n_heads);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        DependentLaunch dl(dim3((units + 3) / 4), L.stream);
+        const pkv::BatchedProblem* probs = L.probs;
+        const int* seq_begin = L.seq_begin;
+        e = bp->head_dim == 128
+                ? cudaLaunchKernelEx(&dl.cfg, pkv::paged_decode_batched_reduce_kernel<128>, probs,
+                                     seq_begin, L.num_problems, bp->n_heads)
+                : cudaLaunchKernelEx(&dl.cfg, pkv::paged_decode_batched_reduce_kernel<64>, probs,
+                                     seq_begin, L.num_problems, bp->n_heads);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return PKV_OK;
 }

@@ -39,6 +39,7 @@ template <int D, int BS, int QPW, typename T>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_batched_kernel(const BatchedProblem* __restrict__ probs,
                                 const int* __restrict__ seq_begin, int num_problems) {
+    launch_dependents();
     const int z = blockIdx.z;
     const int i = problem_of(seq_begin, num_problems, z);
     const BatchedProblem& b = probs[i];
@@ -49,6 +50,7 @@ template <int D, int BS, typename T>
 __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     paged_decode_mma_batched_kernel(const BatchedProblem* __restrict__ probs,
                                     const int* __restrict__ seq_begin, int num_problems) {
+    launch_dependents();
     const int z = blockIdx.z;
     const int i = problem_of(seq_begin, num_problems, z);
     const BatchedProblem& b = probs[i];
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(128)
     paged_decode_batched_reduce_kernel(const BatchedProblem* __restrict__ probs,
                                        const int* __restrict__ seq_begin, int num_problems,
                                        int n_heads) {
+    dependency_wait();  // the decode kernel's partials (launched as its dependent)
     const int unit = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int z = unit / n_heads;
     if (z >= seq_begin[num_problems]) return;

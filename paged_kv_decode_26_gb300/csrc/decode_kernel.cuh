@@ -702,6 +702,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ DecodeParams p) {
+    launch_dependents();  // the split merge may start its CTAs (they wait)
     int split, hg, s;
     if (!decode_unit<BS>(p, split, hg, s)) return;
     decode_cta<D, BS, QPW, T>(&tm_k, &tm_v, p, split, hg, s);
@@ -776,6 +777,7 @@ __device__ __forceinline__ void reduce_unit(const ReduceParams& p, int unit, int
 
 template <int D>
 __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const __grid_constant__ ReduceParams p) {
+    dependency_wait();  // the decode kernel's partials (launched as its dependent)
     reduce_unit<D>(p, blockIdx.x * 4 + (threadIdx.x >> 5), threadIdx.x & 31);
 }
 

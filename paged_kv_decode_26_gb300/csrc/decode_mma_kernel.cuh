@@ -389,6 +389,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ DecodeParams p) {
+    launch_dependents();  // the split merge may start its CTAs (they wait)
     int split, hg, s;
     if (!decode_unit<BS>(p, split, hg, s)) return;
     decode_mma_cta<D, BS, T>(&tm_k, &tm_v, p, split, hg, s);

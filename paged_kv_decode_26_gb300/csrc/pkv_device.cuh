@@ -29,6 +29,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ------------------------------------------------- dependent launches
+// A kernel launched after this one with programmatic stream serialization
+// may start once every CTA here has called launch_dependents (or exited);
+// it must call dependency_wait before it reads anything this kernel writes.
+// Without such a launch both are no-ops.
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
