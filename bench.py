@@ -457,31 +457,34 @@ def main():
         pkv.paged_attn_decode(r["out"], r["q"], r["k_pool"], r["v_pool"], r["bt"], r["lens"],
                               case.scale, r["max_ctx"], split_tokens=args.split, workspace=r["ws"])
 
-    def swaps(r):
-        pkv.swap_blocks_kv(r["k_pool"], r["v_pool"], r["k_pool"], r["v_pool"], r["d2d"])
-        pkv.swap_blocks_kv(r["k_pool"], r["v_pool"], r["hk"], r["hv"], r["h2d"])
-
     # The block copies of the continuous-batching step touch only blocks
     # that neither the append nor the decode uses (free targets, read-only
-    # sources), so they run on a side stream, overlapped with the decode.
-    side = torch.cuda.Stream() if with_swaps else None
+    # sources), and the two copies have disjoint targets and the host copy
+    # writes no source of the device copy: each runs on its own side stream,
+    # overlapped with the decode and with each other (the step is then bound
+    # by the pinned-host copy alone).
+    side = (torch.cuda.Stream(), torch.cuda.Stream()) if with_swaps else None
 
     def step_one(r):
         if with_swaps:
             fork = torch.cuda.Event()
             fork.record(torch.cuda.current_stream())
-            side.wait_event(fork)
-            with torch.cuda.stream(side):
-                swaps(r)
+            for st in side:
+                st.wait_event(fork)
+            with torch.cuda.stream(side[0]):
+                pkv.swap_blocks_kv(r["k_pool"], r["v_pool"], r["hk"], r["hv"], r["h2d"])
+            with torch.cuda.stream(side[1]):
+                pkv.swap_blocks_kv(r["k_pool"], r["v_pool"], r["k_pool"], r["v_pool"], r["d2d"])
         # append the step's token and decode, in one launch
         pkv.paged_attn_decode_append(r["out"], r["q"], r["k_pool"], r["v_pool"], r["bt"],
                                      r["lens"], case.scale, r["max_ctx"], r["k_new"],
                                      r["v_new"], r["slots"], split_tokens=args.split,
                                      workspace=r["ws"])
         if with_swaps:
-            join = torch.cuda.Event()
-            join.record(side)
-            torch.cuda.current_stream().wait_event(join)
+            for st in side:
+                join = torch.cuda.Event()
+                join.record(st)
+                torch.cuda.current_stream().wait_event(join)
 
     def step_eager():
         for r in reps:
@@ -787,7 +790,7 @@ def main():
         "config": {
             "workload": name,
             "step": "paged_attn_decode_append (append 1 token/seq, then decode: one call)" +
-                    (" + swap_blocks_kv D2D and pinned-H2D on a side stream, overlapped"
+                    (" + swap_blocks_kv D2D and pinned-H2D on two side streams, overlapped"
                      if with_swaps else ""),
             "replicas_per_gpu": R,
             "launch": ("one batched launch per step for all replicas "
