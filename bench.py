@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--split", type=int, default=0, help="split_tokens (0 = automatic)")
     ap.add_argument("--seqs", type=int, default=0,
                     help="override the number of sequences (smaller cases for profiling)")
+    ap.add_argument("--lens", default="",
+                    help="override the context-length mix (profiling cases), e.g. "
+                         "const:32768, uniform:512:4096, loguniform:128:32768")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--graph", action="store_true",
                     help="replay each step as one CUDA graph")
@@ -168,10 +171,10 @@ def gpu_id_for_smi(torch, dev: int) -> str:
         return str(dev)
 
 
-def workload_name(case, config) -> str:
+def workload_name(case, config, lens_override: str = "") -> str:
     from paged_kv_decode_26_gb300 import workloads as wl
     spec = wl.CONFIGS[config]
-    lens = spec["lens"]
+    lens = tuple(lens_override.split(":")) if lens_override else spec["lens"]
     return (f"{case.name}: {case.S} seqs, {case.H} q / {case.Hk} kv heads, d={case.D}, "
             f"block_size={case.B}, lens {lens[0]}{list(lens[1:])}, "
             f"{str(case.dtype).replace('torch.', '')} K/V, {case.num_blocks} pool blocks, seed {case.seed}")
@@ -246,7 +249,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_name(case, args.config)},
+            "config": {"workload": workload_name(case, args.config, args.lens)},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -286,6 +289,9 @@ def build_replicas(args, rank, dev, pkv, wl, torch, np):
     extra = {"pool_extra": 0.01} if args.config == 4 else {}
     if args.seqs:
         extra["S"] = args.seqs
+    if args.lens:
+        kind, *nums = args.lens.split(":")
+        extra["lens"] = (kind, *[float(x) if "." in x else int(x) for x in nums])
     reps = []
     for r in range(R):
         seed = rank_seed(args.config, rank, r)
@@ -405,7 +411,7 @@ def run_multi_query(args):
     print(json.dumps({
         "metric": "paged multi-query attention TFLOP/s (causal chunk per sequence)",
         "value": tflops, "unit": "TFLOP/s", "ms_per_call": ms, "steps": args.steps,
-        "config": {"workload": workload_name(case, args.config), "q_len": args.multi_query,
+        "config": {"workload": workload_name(case, args.config, args.lens), "q_len": args.multi_query,
                    "query_rows": int(qs[-1]), "keys_attended": keys},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "peak_kind": "measured cuBLAS bf16 burst "
@@ -768,7 +774,7 @@ def main():
         return
 
     peak, peak_kind = measured_peak()
-    name = workload_name(case, args.config)
+    name = workload_name(case, args.config, args.lens)
     value = job_gbs(total_kv, ms)
     achieved = decode_alg_bytes / (dec_ms / 1e3) / 1e9
     logical_gbs = (kv_read + io_bytes) / (dec_ms / 1e3) / 1e9

@@ -362,8 +362,13 @@ cudaError_t ensure_smem_limit(const void* kernel, unsigned long long* done_mask,
     int optin = 0;
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
         return e;
-    if (bytes > (size_t)optin) return cudaErrorInvalidValue;
-    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin)))
+    // The per-block limit covers the kernel's static shared memory too.
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kernel))) return e;
+    const size_t dyn_max = (size_t)optin > fa.sharedSizeBytes ? optin - fa.sharedSizeBytes : 0;
+    if (bytes > dyn_max) return cudaErrorInvalidValue;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)dyn_max)))
         return e;
     __atomic_fetch_or(done_mask, bit, __ATOMIC_RELEASE);
     return cudaSuccess;
