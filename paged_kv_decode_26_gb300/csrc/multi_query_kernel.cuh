@@ -45,6 +45,9 @@ struct MultiQueryParams {
     int stages;
     int max_pages;      // block ids prefetched per CTA (ceil(max_context_len / B))
     unsigned int* errors;
+    // tcgen05 kernel: 0 = CTAs take sequences in index order; else num_seqs,
+    // and CTAs take them longest context first (see longest_first).
+    int lpt_seqs;
 };
 
 inline size_t multi_query_smem_bytes(int D, int BS, int elem_bytes, int stages, int max_pages) {

@@ -156,11 +156,47 @@ __device__ __forceinline__ void tc_wait_st() {
 
 // Shared memory of one CTA: 1 KB alignment slack, the two Q tiles, the K/V
 // ring, barriers, block ids, one word.
-inline size_t multi_query_tc_smem_bytes(int D, int stages, int max_pages) {
+inline size_t multi_query_tc_smem_bytes(int D, int stages, int max_pages, int lpt_seqs = 0) {
     const size_t q = (size_t)kTcQTiles * kTcRows * D * 2;
     const size_t kv = (size_t)stages * 2 * kTcKeys * D * 2;
     return 1024 + q + kv + (size_t)(3 * stages + 15) * sizeof(uint64_t) +
-           (size_t)max_pages * sizeof(int) + sizeof(int);
+           (size_t)max_pages * sizeof(int) + sizeof(int) +
+           (lpt_seqs > 0 ? (size_t)(lpt_seqs + 1) * sizeof(int) : 0);
+}
+
+// Longest context first.  A CTA's work grows with its sequence's context,
+// and with lengths spread over orders of magnitude the longest sequences'
+// CTAs, dispatched in index order, can start last and form the tail.  With
+// p.lpt_seqs the sequences are ranked by context length (ties: lower index
+// first) and CTA u (grid order) takes the sequence of rank u / (kv heads x
+// query tiles), the kv head fastest and the query tiles from the last (the
+// one that sees the most keys).  s_len: p.lpt_seqs + 1 ints of shared
+// memory that nothing else uses.
+__device__ __forceinline__ void longest_first(const MultiQueryParams& p, int* s_len, int& tile,
+                                              int& kvh, int& s) {
+    const int S = p.lpt_seqs;
+    int* s_pick = s_len + S;
+    const long long u =
+        blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+    const int per_seq = (int)(gridDim.x * gridDim.y);
+    const int r = (int)(u / per_seq);
+    const int rem = (int)(u % per_seq);
+    kvh = rem % (int)gridDim.y;
+    tile = (int)gridDim.x - 1 - rem / (int)gridDim.y;
+    for (int i = threadIdx.x; i < S; i += blockDim.x) s_len[i] = p.context_lens[i];
+    __syncthreads();
+    // the ranks are a permutation of 0 .. S-1: exactly one sequence has rank r
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+        const int ni = s_len[i];
+        int rank = 0;
+        for (int j = 0; j < S; ++j) {
+            const int nj = s_len[j];
+            rank += (nj > ni || (nj == ni && j < i)) ? 1 : 0;
+        }
+        if (rank == r) *s_pick = i;
+    }
+    __syncthreads();
+    s = *s_pick;
 }
 
 template <int D, int BS, typename T>
@@ -183,14 +219,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
 
-    const int tile = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int s = blockIdx.z;
     const int G = p.group;
     if (blockDim.x != kTcThreads || G < 1 || G > 8 || kTcRows % G != 0 || p.stages < 2) {
         if (threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONFIG);
         return;
     }
+
+    // ---- shared memory (1024-byte aligned for the swizzle)
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    unsigned char* sQ = sm;                                         // 2 x HALVES x [128 x 128 B]
+    unsigned char* sKV = sQ + kTcQTiles * Q_BYTES;                  // stages x (K, V)
+    uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + (size_t)p.stages * 2 * KV_BYTES);
+    uint64_t* kv_free = kv_full + p.stages;      // [stages]: both issuers done with the slot
+    uint64_t* kv_land = kv_free + p.stages;      // [stages]: loads landed (tiles to zero)
+    uint64_t* q_full = kv_land + p.stages;
+    uint64_t* s_full = q_full + 1;               // [tile][buffer]: S ready
+    uint64_t* p_full = s_full + 4;               // [tile][buffer]: P written (128 arrivals)
+    uint64_t* o_done = p_full + 4;               // [tile][parity of key tile]: P V done
+    uint64_t* fin = o_done + 4;                  // [tile]: every MMA of the tile's issuer done
+    int* s_bid = reinterpret_cast<int*>(fin + 2);
+    int* s_tmem = s_bid + p.max_pages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int tile = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    if (p.lpt_seqs > 0) longest_first(p, s_tmem + 1, tile, kvh, s);
     const int QT = kTcRows / G;                  // query tokens per query tile
     const int qs0 = p.q_start[s], qs1 = p.q_start[s + 1];
     const int n = p.context_lens[s];
@@ -213,23 +266,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n_keys = first_pos + min(q_len, tok_lo + kTcQTiles * QT);
     const int n_pages = (n_keys + BS - 1) / BS;
     const int zero_from = min(n, n_pages * BS);      // V rows from here on are zeroed
-
-    // ---- shared memory (1024-byte aligned for the swizzle)
-    const uint32_t raw = smem_addr(smem_raw);
-    unsigned char* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    unsigned char* sQ = sm;                                         // 2 x HALVES x [128 x 128 B]
-    unsigned char* sKV = sQ + kTcQTiles * Q_BYTES;                  // stages x (K, V)
-    uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + (size_t)p.stages * 2 * KV_BYTES);
-    uint64_t* kv_free = kv_full + p.stages;      // [stages]: both issuers done with the slot
-    uint64_t* kv_land = kv_free + p.stages;      // [stages]: loads landed (tiles to zero)
-    uint64_t* q_full = kv_land + p.stages;
-    uint64_t* s_full = q_full + 1;               // [tile][buffer]: S ready
-    uint64_t* p_full = s_full + 4;               // [tile][buffer]: P written (128 arrivals)
-    uint64_t* o_done = p_full + 4;               // [tile][parity of key tile]: P V done
-    uint64_t* fin = o_done + 4;                  // [tile]: every MMA of the tile's issuer done
-    int* s_bid = reinterpret_cast<int*>(fin + 2);
-    int* s_tmem = s_bid + p.max_pages;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     int missing = 0;
     for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {

@@ -91,3 +91,27 @@ def test_dense_order_matches_grid_order(pkv, monkeypatch, config, S, split, lens
     assert torch.equal(_bits(outs["0"]), _bits(outs["1"]))
     assert torch.equal(_bits(outs["0"]), _bits(outs["2"]))
     assert pkv.device_errors(clear=True) == 0
+
+
+def test_multi_query_longest_first_matches_index_order(pkv, monkeypatch):
+    """The tcgen05 multi-query kernel's CTAs taking sequences longest context
+    first compute what CTAs taking them in index order compute: bit for bit,
+    with lengths spread over orders of magnitude, equal lengths (the tie
+    order) and several query tiles per sequence."""
+    monkeypatch.setenv("PKV_MQ_TC", "1")
+    lens = [900, 150, 4000, 150, 2600, 300, 4000, 700, 1200, 260]
+    case = wl.make_case(3, S=len(lens), lens_override=lens, poison=True, seed=13)
+    q, qs = wl.multi_query_inputs(case, ("uniform", 100, 600), seed=14)
+    args = [q.cuda(), qs.cuda(), case.k_pool.cuda(), case.v_pool.cuda(),
+            case.block_tables.cuda(), case.context_lens.cuda()]
+    max_q = int((qs[1:] - qs[:-1]).max())
+    outs = {}
+    for mode in ("0", "1"):
+        monkeypatch.setenv("PKV_MQ_LPT", mode)
+        out = torch.empty(q.shape[0], case.H, case.D, dtype=case.out_dtype, device="cuda")
+        pkv.paged_attn_multi_query(out, *args[:2], *args[2:], case.scale, max_q,
+                                   case.max_context_len)
+        outs[mode] = out
+    torch.cuda.synchronize()
+    assert torch.equal(outs["0"].view(torch.int16), outs["1"].view(torch.int16))
+    assert pkv.device_errors(clear=True) == 0
