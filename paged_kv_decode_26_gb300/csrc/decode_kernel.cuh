@@ -750,22 +750,40 @@ __device__ __forceinline__ void reduce_unit(const ReduceParams& p, int unit, int
 #pragma unroll
     for (int d = 0; d < DL; ++d) acc[d] = 0.f;
     float wsum = 0.f;
-    for (int k = 0; k < n_splits; ++k) {
-        const float2 v = ml[k];
-        if (!(v.y > 0.f)) continue;
-        const float w = v.y * exp2f(v.x - mx);
-        wsum += w;
-        const float* ok = os + (size_t)k * D + lane * DL;
-        if constexpr (DL == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(ok);
-            acc[0] = fmaf(w, x.x, acc[0]);
-            acc[1] = fmaf(w, x.y, acc[1]);
-            acc[2] = fmaf(w, x.z, acc[2]);
-            acc[3] = fmaf(w, x.w, acc[3]);
-        } else {
-            const float2 x = *reinterpret_cast<const float2*>(ok);
-            acc[0] = fmaf(w, x.x, acc[0]);
-            acc[1] = fmaf(w, x.y, acc[1]);
+    // Splits in batches of RB: the batch's loads are all issued before its
+    // accumulation, so a warp waits one memory round trip per batch rather
+    // than per split; the accumulation order (k ascending) is unchanged.
+    constexpr int RB = 8;
+    for (int k0 = 0; k0 < n_splits; k0 += RB) {
+        float2 mlv[RB];
+        float x[RB][DL];
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+            const int k = k0 + u;
+            mlv[u] = make_float2(0.f, 0.f);
+            if (k < n_splits) {
+                mlv[u] = ml[k];
+                const float* ok = os + (size_t)k * D + lane * DL;
+                if constexpr (DL == 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(ok);
+                    x[u][0] = t.x;
+                    x[u][1] = t.y;
+                    x[u][2] = t.z;
+                    x[u][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2*>(ok);
+                    x[u][0] = t.x;
+                    x[u][1] = t.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+            if (k0 + u >= n_splits || !(mlv[u].y > 0.f)) continue;
+            const float w = mlv[u].y * exp2f(mlv[u].x - mx);
+            wsum += w;
+#pragma unroll
+            for (int d = 0; d < DL; ++d) acc[d] = fmaf(w, x[u][d], acc[d]);
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
