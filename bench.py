@@ -81,10 +81,16 @@ def parse_args():
 # ------------------------------------------------------------------ helpers
 
 def kernel_source_hash() -> str:
+    """Digest of the decode kernel's code: its sources with comments and
+    whitespace removed, so that a comment edit keeps the committed traffic
+    figure valid while any change to the code itself invalidates it."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -72,8 +72,9 @@ struct DecodeParams {
     const void* k_new;
     const void* v_new;
     const int64_t* slot_mapping;
-    // 1: CTAs take their (split, head group, sequence) from the dense unit
-    // list of dense_unit() instead of their grid coordinates.
+    // How a CTA finds its (split, head group, sequence): 0 = its grid
+    // coordinates, 1 = the dense unit list (dense_unit), 2 = grid order
+    // with the head group fastest (decode_unit).
     int dense;
 };
 
@@ -578,7 +579,7 @@ __device__ __forceinline__ void store_row(void* base, size_t elem_off, int out_d
 // context, but a sequence of n tokens has only max(1, ceil(n / split_tokens))
 // splits.  Taken in grid order, the CTAs of missing splits sit between the
 // working ones; each holds an SM slot for the time it takes to read its
-// context length, and the dispatcher waits for slots.  With p.dense, CTA u
+// context length, and the dispatcher waits for slots.  With p.dense == 1, CTA u
 // (in grid order, the head group fastest) takes the u-th entry of a dense
 // list instead: every sequence's full splits (sequence by sequence), then
 // every sequence's shorter last split.  The CTAs without an entry all come at
