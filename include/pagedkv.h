@@ -95,7 +95,14 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
                                           int head_dim, int block_size, int max_context_len,
                                           int split_tokens);
 
-/* The split length (tokens per work unit) the automatic choice takes. */
+/*
+ * The split length (tokens per work unit) the automatic choice takes, for
+ * the current device: 512 tokens; 1024 when max_context_len is 8192 or more
+ * and there are at most 2 x SMs (sequence, kv-head group) units; the whole
+ * context (no split, no merge) when the units fill the SMs 16 times over;
+ * rounded to whole blocks and capped at the context.  Returns 0 for an
+ * unsupported shape.
+ */
 PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, int head_dim,
                                     int block_size, int max_context_len);
 
