@@ -32,6 +32,11 @@
  *     index is skipped (never dereferenced) and recorded in the device error
  *     word read by pkv_device_errors().
  *   - Launch failures return PKV_ERR_CUDA (cudaGetLastError after launch).
+ *   - Per-device facts (the device error word's address, the SM count, the
+ *     no-alloc scratch address) are looked up on a device's first call and
+ *     kept for the life of the process.  They do not survive
+ *     cudaDeviceReset: a process that resets a device must not call the
+ *     library on that device again.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -77,6 +82,43 @@ PKV_API const char* pkv_last_error_detail(void);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 PKV_API int pkv_version(void);
+
+/*
+ * Launch-shape overrides, for tests and tuning sweeps only.  The library
+ * picks every launch shape by itself (the values measured best on GB300);
+ * nothing but pkv_set_tuning changes that choice (no environment variable
+ * is read).  A knob holds PKV_TUNE_AUTO (the automatic choice) until set.
+ * Knobs are process-wide and apply to every later call on every thread;
+ * out-of-range values are clamped or ignored by the call that reads them,
+ * never let through to a kernel.  No page has a counterpart.
+ */
+#define PKV_TUNE_AUTO (-2147483647 - 1)
+typedef enum pkv_tune_knob {
+    PKV_TUNE_DECODE_MMA = 0,      /* 0/1: tensor-core decode consumer off/on (groups >= 2) */
+    PKV_TUNE_DECODE_HPC = 1,      /* kv heads per decode CTA */
+    PKV_TUNE_DECODE_STAGES = 2,   /* decode ring depth, 2..8 */
+    PKV_TUNE_DECODE_WPT = 3,      /* decode warps taking turns on a head's pages */
+    PKV_TUNE_DECODE_QPW = 4,      /* query heads per CUDA-core consumer warp, 1/2/4 */
+    PKV_TUNE_DECODE_SPLIT = 5,    /* automatic split length, tokens */
+    PKV_TUNE_DECODE_ORDER = 6,    /* 0 grid order, 1 dense unit list, 2 head group fastest */
+    PKV_TUNE_DECODE_PDL = 7,      /* 0: launch the split merge without programmatic overlap */
+    PKV_TUNE_MQ_TC = 8,           /* 0/1: multi-query on mma.sync / tcgen05 */
+    PKV_TUNE_MQ_TC_STAGES = 9,    /* tcgen05 multi-query ring depth */
+    PKV_TUNE_MQ_LPT = 10,         /* 0/1: multi-query longest-context-first order off/on */
+    PKV_TUNE_MQ_STAGES = 11,      /* mma.sync multi-query ring depth */
+    PKV_TUNE_SWAP_BULK = 12,      /* 0: device-to-device block copy by 16-byte loads and stores */
+    PKV_TUNE_SWAP_CHUNK = 13,     /* bulk block copy: bytes per copy (multiple of 16) */
+    PKV_TUNE_SWAP_STAGES = 14,    /* bulk block copy: copies in flight per CTA, 2..8 */
+    PKV_TUNE_SWAP_CTAS = 15,      /* bulk block copy: CTAs per SM */
+    PKV_TUNE_COUNT = 16
+} pkv_tune_knob;
+
+/* Set one knob (value PKV_TUNE_AUTO restores the automatic choice).
+ * PKV_ERR_INVALID for an unknown knob. */
+PKV_API pkv_status pkv_set_tuning(int knob, int value);
+
+/* Current value of a knob (PKV_TUNE_AUTO when unset or unknown). */
+PKV_API int pkv_get_tuning(int knob);
 
 /*
  * Device error word of the current device: OR of PKV_DEVERR_* bits set by
@@ -250,7 +292,9 @@ PKV_API pkv_status paged_attn_decode_batched(const pkv_decode_plan* plan, void* 
  *     kernels may overlap on the GPU (different streams without ordering)
  *     race on it.
  *   - The first call on each device looks up the array's device address;
- *     make that first call before any stream capture begins.
+ *     make that first call before any stream capture begins.  The address
+ *     is kept for the life of the process and does not survive
+ *     cudaDeviceReset (see the conventions at the top of this header).
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 PKV_API pkv_status paged_attn_decode_noalloc(void* out, pkv_dtype out_dtype, const void* q,
@@ -288,8 +332,7 @@ PKV_API pkv_status paged_attn_decode_noalloc(void* out, pkv_dtype out_dtype, con
  * query heads of one kv head form the tile rows: on tcgen05, two tiles of
  * 128 rows per CTA with S, P and O in tensor memory, when max_q_len x group
  * >= 16 (groups of 4 and 8) or >= 48 (groups of 1 and 2), and total_q >=
- * 128 / group; else 16 rows per warp on mma.sync.  The environment
- * variable PKV_MQ_TC=0/1 forces one where it applies.
+ * 128 / group; else 16 rows per warp on mma.sync.
  */
 PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const void* q,
                                           const int32_t* q_start, int total_q, int max_q_len,

@@ -22,12 +22,21 @@ DEVERR_SLOT = 0x4
 DEVERR_PAIR = 0x8
 DEVERR_TIMEOUT = 0x10
 
+# Launch-shape override knobs (pkv_tune_knob), by lower-case name.
+TUNE_AUTO = -2147483648
+TUNE_KNOBS = {name: i for i, name in enumerate(
+    ["decode_mma", "decode_hpc", "decode_stages", "decode_wpt", "decode_qpw", "decode_split",
+     "decode_order", "decode_pdl", "mq_tc", "mq_tc_stages", "mq_lpt", "mq_stages", "swap_bulk",
+     "swap_chunk", "swap_stages", "swap_ctas"])}
+
 # Every symbol include/pagedkv.h declares, with (restype, argtypes).
 _p, _i, _i32, _i64, _sz, _f = C.c_void_p, C.c_int, C.c_int32, C.c_int64, C.c_size_t, C.c_float
 SIGNATURES = {
     "pkv_status_string": (C.c_char_p, [_i]),
     "pkv_last_error_detail": (C.c_char_p, []),
     "pkv_version": (_i, []),
+    "pkv_set_tuning": (_i, [_i, _i]),
+    "pkv_get_tuning": (_i, [_i]),
     "pkv_device_errors": (_i, [C.POINTER(C.c_uint32), _i]),
     "pkv_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "pkv_decode_split_tokens": (_i, [_i, _i, _i, _i, _i, _i]),

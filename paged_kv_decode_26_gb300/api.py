@@ -40,6 +40,29 @@ def _need_cuda(name: str, t: torch.Tensor):
         raise ValueError(f"{name} must be contiguous")
 
 
+def set_tuning(**knobs) -> None:
+    """Override launch shapes for tests and tuning sweeps, e.g.
+    ``set_tuning(decode_hpc=2, mq_tc=0)``; a value of None restores the
+    automatic choice.  Names: the pkv_tune_knob names of pagedkv.h in lower
+    case without the PKV_TUNE_ prefix.  Process-wide."""
+    for name, value in knobs.items():
+        if name not in _lib.TUNE_KNOBS:
+            raise ValueError(f"unknown tuning knob {name!r}")
+        v = _lib.TUNE_AUTO if value is None else int(value)
+        check(lib().pkv_set_tuning(_lib.TUNE_KNOBS[name], v), "pkv_set_tuning")
+
+
+def get_tuning(name: str) -> Optional[int]:
+    """Current override of one knob, None when it holds the automatic choice."""
+    v = int(lib().pkv_get_tuning(_lib.TUNE_KNOBS[name]))
+    return None if v == _lib.TUNE_AUTO else v
+
+
+def reset_tuning() -> None:
+    """Every knob back to the automatic choice."""
+    set_tuning(**{name: None for name in _lib.TUNE_KNOBS})
+
+
 def decode_workspace_bytes(num_seqs: int, n_heads: int, n_kv_heads: int, head_dim: int,
                            block_size: int, max_context_len: int, split_tokens: int = 0) -> int:
     return int(lib().pkv_decode_workspace_bytes(num_seqs, n_heads, n_kv_heads, head_dim,

@@ -97,10 +97,28 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int env_int(const char* name, int fallback) {
-    const char* v = std::getenv(name);
-    if (!v || !*v) return fallback;
-    return std::atoi(v);
+std::atomic<int> g_tuning[PKV_TUNE_COUNT] = {};
+std::once_flag g_tuning_once;
+
+void tuning_init() {
+    std::call_once(g_tuning_once, [] {
+        for (auto& k : g_tuning) k.store(PKV_TUNE_AUTO, std::memory_order_relaxed);
+    });
+}
+
+int tuning(pkv_tune_knob knob, int fallback) {
+    tuning_init();
+    const int v = g_tuning[knob].load(std::memory_order_relaxed);
+    return v == PKV_TUNE_AUTO ? fallback : v;
+}
+
+bool tuned(pkv_tune_knob knob) {
+    tuning_init();
+    return g_tuning[knob].load(std::memory_order_relaxed) != PKV_TUNE_AUTO;
+}
+
+bool table_tokens_fit(int max_blocks_per_seq, int block_size) {
+    return (long long)max_blocks_per_seq * block_size <= 0x7fffffffLL;
 }
 
 bool supported_shape(int n_heads, int n_kv_heads, int head_dim, int block_size) {
@@ -182,14 +200,15 @@ constexpr int kDenseMaxSeqs = 1024;
 // 1 KB contiguous per token row and 32 KB (block size 16) or 64 KB (block
 // size 32) per stage.  Three stages keep two CTAs (block size 16) or one CTA
 // (block size 32) resident per SM with ~192 KB of loads in flight per SM,
-// which measured best on GB300 for both block sizes.  PKV_DECODE_HPC,
-// _STAGES, _WPT and _QPW override the choice (for tuning sweeps).
+// which measured best on GB300 for both block sizes.  The knobs
+// PKV_TUNE_DECODE_HPC, _STAGES, _WPT and _QPW override the choice (for
+// tuning sweeps).
 void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size, int hpc_target,
                       DecodeConfig* c) {
     const int G = n_heads / n_kv_heads;
     // Groups of four or more query heads per kv head make each page a small
     // dense contraction: the tensor-core consumer takes them.
-    c->mma = env_int("PKV_DECODE_MMA", G >= 4 ? 1 : 0) != 0 && G >= 2;
+    c->mma = tuning(PKV_TUNE_DECODE_MMA, G >= 4 ? 1 : 0) != 0 && G >= 2;
     if (c->mma) {
         c->qpw = G;
         c->wpk = 1;
@@ -200,12 +219,12 @@ void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size,
         for (int h = 1; h <= n_kv_heads; ++h)
             if (n_kv_heads % h == 0 && h <= target && h <= pkv::kMmaMaxWarps) hpc = h;
         c->hpc = hpc;
-        const int stages = env_int("PKV_DECODE_STAGES", 3);
+        const int stages = tuning(PKV_TUNE_DECODE_STAGES, 3);
         c->stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
         c->threads = 32 * (1 + c->hpc);
         return;
     }
-    int qpw = env_int("PKV_DECODE_QPW", G < 4 ? G : 4);
+    int qpw = tuning(PKV_TUNE_DECODE_QPW, G < 4 ? G : 4);
     if (qpw < 1 || qpw > 4 || (qpw & (qpw - 1)) || G % qpw) qpw = G < 4 ? G : 4;
     c->qpw = qpw;
     c->wpk = G / c->qpw;
@@ -215,11 +234,11 @@ void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size,
     for (int h = 1; h <= n_kv_heads; ++h)
         if (n_kv_heads % h == 0 && h <= target && h * c->wpk <= pkv::kMaxConsumerWarps) hpc = h;
     c->hpc = hpc;
-    int stages = env_int("PKV_DECODE_STAGES", 3);
+    int stages = tuning(PKV_TUNE_DECODE_STAGES, 3);
     c->stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
     // Optionally let several warps take turns on the pages of a kv head
     // (merged in shared memory at the end of the CTA).
-    int wpt = env_int("PKV_DECODE_WPT", 1);
+    int wpt = tuning(PKV_TUNE_DECODE_WPT, 1);
     if (wpt < 1) wpt = 1;
     while (wpt > 1 && c->hpc * c->wpk * wpt > pkv::kMaxConsumerWarps) --wpt;
     c->wpt = wpt;
@@ -235,7 +254,7 @@ void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size,
 
 void shape_config(int n_heads, int n_kv_heads, int head_dim, int block_size, DecodeConfig* c) {
     shape_config_hpc(n_heads, n_kv_heads, head_dim, block_size,
-                     env_int("PKV_DECODE_HPC", 512 / head_dim), c);
+                     tuning(PKV_TUNE_DECODE_HPC, 512 / head_dim), c);
 }
 
 int auto_split_tokens(int num_seqs, int n_kv_heads, int hpc, int block_size, int max_context_len,
@@ -247,7 +266,7 @@ int auto_split_tokens(int num_seqs, int n_kv_heads, int hpc, int block_size, int
     const int base = max_context_len >= kLongContextTokens && units <= 2LL * sms
                          ? kLongSplitTokens
                          : kDefaultSplitTokens;
-    int split = env_int("PKV_DECODE_SPLIT", base);
+    int split = tuning(PKV_TUNE_DECODE_SPLIT, base);
     split = (split + block_size - 1) / block_size * block_size;
     if (split <= 0) split = base;
     // Enough (sequence, head-group) units to fill the GPU many times over
@@ -262,7 +281,7 @@ int auto_split_tokens(int num_seqs, int n_kv_heads, int hpc, int block_size, int
 // decode kernel before it on the stream still runs (the decode CTAs signal
 // at their start, the merge waits for the decode grid's completion and
 // memory before it reads a partial), which hides the kernel boundary.
-// PKV_DECODE_PDL=0 launches it plainly after the decode kernel.
+// The PKV_TUNE_DECODE_PDL knob set to 0 launches it plainly after the decode kernel.
 struct DependentLaunch {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
@@ -275,7 +294,7 @@ struct DependentLaunch {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = env_int("PKV_DECODE_PDL", 1) != 0 ? 1 : 0;
+        cfg.numAttrs = tuning(PKV_TUNE_DECODE_PDL, 1) != 0 ? 1 : 0;
     }
 };
 
@@ -287,10 +306,10 @@ struct DependentLaunch {
 // slices of a block together (a 32K-token MHA decode: 1.231 instead of 1.269
 // ms).  Fewer splits: grid order (the dense list's scan of the lengths in
 // every CTA then costs more than it saves: 4K-token MHA 0.346 vs 0.341 ms).
-// PKV_DECODE_DENSE = 0, 1 or 2 (grid order with the head group fastest)
-// forces one order.
+// The PKV_TUNE_DECODE_ORDER knob (0, 1, or 2 = grid order with the head
+// group fastest) forces one order.
 int cta_order(int max_splits, int num_seqs) {
-    const int forced = env_int("PKV_DECODE_DENSE", -1);
+    const int forced = tuning(PKV_TUNE_DECODE_ORDER, -1);
     if (forced >= 0 && forced <= 2) return forced;
     return max_splits >= 16 && num_seqs <= kDenseMaxSeqs ? 1 : 0;
 }
@@ -301,7 +320,7 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
     // Too few (sequence, head-group) units to occupy the SMs: two kv heads per
     // CTA give more, shorter CTAs (measured on the tiny workload, 4 sequences
     // x 8 kv heads: 12.6 us per call instead of 14.8 us with 8 heads per CTA).
-    if (!std::getenv("PKV_DECODE_HPC") && c->hpc > 2 &&
+    if (!tuned(PKV_TUNE_DECODE_HPC) && c->hpc > 2 &&
         (long long)num_seqs * (n_kv_heads / c->hpc) < (sm_count > 0 ? sm_count : 1)) {
         DecodeConfig narrow;
         shape_config_hpc(n_heads, n_kv_heads, head_dim, block_size, 2, &narrow);
@@ -394,7 +413,20 @@ PKV_API const char* pkv_status_string(pkv_status status) {
 
 PKV_API const char* pkv_last_error_detail(void) { return t_detail; }
 
-PKV_API int pkv_version(void) { return 100; }
+PKV_API int pkv_version(void) { return 200; }
+
+PKV_API pkv_status pkv_set_tuning(int knob, int value) {
+    if (knob < 0 || knob >= PKV_TUNE_COUNT) return invalid("unknown tuning knob");
+    tuning_init();
+    g_tuning[knob].store(value, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
+PKV_API int pkv_get_tuning(int knob) {
+    if (knob < 0 || knob >= PKV_TUNE_COUNT) return PKV_TUNE_AUTO;
+    tuning_init();
+    return g_tuning[knob].load(std::memory_order_relaxed);
+}
 
 PKV_API pkv_status pkv_device_errors(uint32_t* flags, int clear) {
     if (!flags) return invalid("flags is NULL");
@@ -461,6 +493,8 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
         return unsupported("head_dim 64/128, block_size 16/32, group 1/2/4/8");
     if (num_blocks < 0) return invalid("num_blocks < 0");
     if (max_blocks_per_seq <= 0) return invalid("max_blocks_per_seq must be positive");
+    if (!table_tokens_fit(max_blocks_per_seq, block_size))
+        return unsupported("max_blocks_per_seq * block_size exceeds 2^31 - 1 tokens");
     if (max_context_len < 0) return invalid("max_context_len < 0");
     if (!std::isfinite(scale)) return invalid("scale is not finite");
     if (num_seqs == 0) return PKV_OK;
@@ -480,6 +514,10 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
                                 max_context_len, split_tokens, dev->sm_count, &c);
     if (st != PKV_OK) return st;
     if (c.smem > (size_t)dev->smem_optin) return unsupported("shared memory of this configuration");
+    // The kernels clamp a context to min(table tokens, splits x split
+    // length) in 32-bit arithmetic: both products must fit.
+    if ((long long)c.max_splits * c.split_tokens > 0x7fffffffLL)
+        return unsupported("max_context_len too close to 2^31 - 1 tokens for this split length");
     size_t ml_off = 0;
     const size_t need = workspace_bytes_for(num_seqs, n_heads, head_dim, c, &ml_off);
     if (need > 0) {
@@ -730,6 +768,11 @@ PKV_API pkv_status pkv_decode_batched_plan(pkv_decode_plan* plan,
     if (st != PKV_OK) return st;
     if (c.smem > (size_t)dev->smem_optin) return unsupported("shared memory of this configuration");
     if (c.max_splits > 65535) return unsupported("more than 65535 splits per sequence");
+    if ((long long)c.max_splits * c.split_tokens > 0x7fffffffLL)
+        return unsupported("max_context_len too close to 2^31 - 1 tokens for this split length");
+    for (int i = 0; i < num_problems; ++i)
+        if (!table_tokens_fit(std::max(problems[i].max_blocks_per_seq, 1), block_size))
+            return unsupported("max_blocks_per_seq * block_size exceeds 2^31 - 1 tokens");
     const BatchLayout lay = batch_layout(problems, num_problems, n_heads, head_dim, c);
     if (!workspace || workspace_bytes < lay.total) {
         set_detail("%s", "workspace smaller than pkv_decode_batched_workspace_bytes()");
@@ -911,6 +954,27 @@ PKV_API pkv_status kv_append(void* k_pool, void* v_pool, const void* k_new, cons
 
 namespace {
 
+// Device memory of the current device on both sides of every pool: the bulk
+// copy engine path.  A source in pinned host memory (or on another device)
+// takes the 16-byte load/store kernel, which reaches it through unified
+// addressing.  The PKV_TUNE_SWAP_BULK knob set to 0 forces that kernel.
+bool use_bulk_copy(void* const* dst_pools, const void* const* src_pools, int n_pools) {
+    if (tuning(PKV_TUNE_SWAP_BULK, 1) == 0) return false;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    for (int k = 0; k < n_pools; ++k) {
+        for (const void* ptr : {static_cast<const void*>(dst_pools[k]), src_pools[k]}) {
+            cudaPointerAttributes a;
+            if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return false;
+            }
+            if (a.type != cudaMemoryTypeDevice || a.device != dev) return false;
+        }
+    }
+    return true;
+}
+
 pkv_status launch_swap(void* const* dst_pools, const void* const* src_pools, int n_pools,
                        size_t block_bytes, const int64_t* pairs, int n_pairs,
                        int64_t num_src_blocks, int64_t num_dst_blocks, void* stream) {
@@ -931,6 +995,40 @@ pkv_status launch_swap(void* const* dst_pools, const void* const* src_pools, int
     DeviceInfo* dev = nullptr;
     cudaError_t e = device_info(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (use_bulk_copy(dst_pools, src_pools, n_pools)) {
+        pkv::BulkSwapParams p;
+        p.pools = pools;
+        p.pairs = pairs;
+        p.n_pairs = n_pairs;
+        p.num_src = num_src_blocks;
+        p.num_dst = num_dst_blocks;
+        p.block_bytes = block_bytes;
+        // One bulk copy moves a chunk of up to 32 KB (a whole block of the
+        // 16-token, 8-head, d = 128 bf16 pools); three chunks in flight per
+        // CTA and two CTAs per SM keep ~192 KB per SM moving.
+        long long chunk = tuning(PKV_TUNE_SWAP_CHUNK, 32768);
+        chunk = std::max(16LL, std::min(chunk, 65536LL)) / 16 * 16;
+        if ((unsigned long long)chunk > block_bytes) chunk = (long long)block_bytes;
+        int stages = std::max(2, std::min(tuning(PKV_TUNE_SWAP_STAGES, 3), pkv::kMaxBulkStages));
+        while (stages > 2 && (size_t)stages * chunk > (size_t)dev->smem_optin - 4096) --stages;
+        const int ctas = std::max(1, std::min(tuning(PKV_TUNE_SWAP_CTAS, 2), 32));
+        p.chunk_bytes = (uint32_t)chunk;
+        p.chunks = (int)((block_bytes + chunk - 1) / chunk);
+        p.n_pools = n_pools;
+        p.stages = stages;
+        p.errors = dev->errors;
+        const size_t smem = (size_t)stages * chunk;
+        static unsigned long long smem_done = 0;
+        if ((e = pkv::ensure_smem_limit((const void*)pkv::swap_blocks_bulk_kernel, &smem_done,
+                                        smem)) != cudaSuccess)
+            return cuda_fail(e);
+        const long long items = (long long)n_pairs * n_pools * p.chunks;
+        const long long grid = std::min(items, (long long)dev->sm_count * ctas);
+        pkv::swap_blocks_bulk_kernel<<<(unsigned)grid, 32, smem,
+                                       static_cast<cudaStream_t>(stream)>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        return PKV_OK;
+    }
     const dim3 grid((unsigned)std::min<long long>(n_pairs, 1LL << 20), (unsigned)n_pools);
     pkv::swap_blocks_kernel<<<grid, pkv::kSwapThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         pools, (int64_t)(block_bytes / 16), pairs, n_pairs, num_src_blocks, num_dst_blocks,

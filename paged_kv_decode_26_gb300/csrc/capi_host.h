@@ -29,8 +29,15 @@ cudaError_t device_info(DeviceInfo** out);
 
 bool aligned16(const void* p);
 
-// Integer from the environment (tuning overrides), `fallback` if unset.
-int env_int(const char* name, int fallback);
+// Value of a launch-shape override (pkv_set_tuning), `fallback` while the
+// knob holds PKV_TUNE_AUTO.
+int tuning(pkv_tune_knob knob, int fallback);
+// Whether the knob was set.
+bool tuned(pkv_tune_knob knob);
+
+// Tokens a block-table row can address (max_blocks_per_seq * block_size)
+// fit the kernels' 32-bit token arithmetic.
+bool table_tokens_fit(int max_blocks_per_seq, int block_size);
 
 // head_dim 64/128, block_size 16/32, group 1/2/4/8.
 bool supported_shape(int n_heads, int n_kv_heads, int head_dim, int block_size);

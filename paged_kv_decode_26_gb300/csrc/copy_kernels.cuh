@@ -11,9 +11,11 @@
 //     FlashAttention与KVCache优化解析", "Swap Blocks 机制": Key and Value caches
 //     copied by separate calls.
 //
-// Both move 16-byte vectors; a row of one token (all kv heads) and a whole
-// block are contiguous in the [num_blocks, B, Hk, D] pool, so every warp
-// access is a fully coalesced 512-byte run.
+// A row of one token (all kv heads) and a whole block are contiguous in the
+// [num_blocks, B, Hk, D] pool.  The append moves 16-byte vectors (every
+// warp access a coalesced 512-byte run); the block copy between device
+// pools moves whole blocks with bulk copies through shared memory, and
+// from pinned host memory with 16-byte vectors.
 #pragma once
 
 #include "pkv_device.cuh"
@@ -45,6 +47,7 @@ __global__ void __launch_bounds__(256)
 }
 
 constexpr int kSwapThreads = 256;
+constexpr int kMaxBulkStages = 8;
 constexpr int kSwapUnroll = 8;
 
 // Up to two caches (Key and Value) copied by one launch with the same pairs.
@@ -86,6 +89,190 @@ __global__ void __launch_bounds__(kSwapThreads)
                 if (e < block_vec) __stcs(d + e, r[u]);
             }
         }
+    }
+}
+
+// ------------------------------------------------------- bulk block copy
+//
+// swap_blocks between two device pools through the copy engine of each SM
+// (cp.async.bulk): a block (or a chunk of it) moves global -> shared with
+// one bulk load that completes on an mbarrier, then shared -> global with
+// one bulk store; no thread touches the bytes.  One warp per CTA: its lanes
+// look up the pairs of the CTA's items in batches, then lane 0 keeps
+// `stages` chunks in flight: the store of chunk n is issued as soon as its
+// load lands, and the slot of chunk n - 1 is refilled with chunk n - 1 +
+// stages once that chunk's store has finished reading it.  The grid is a
+// whole number of CTAs per SM; CTA b takes a contiguous range of the
+// (pair, cache, chunk) items, so the ranges differ by one item at most.
+
+constexpr int kBulkBatch = 128;   // item descriptors looked up at once
+
+struct BulkSwapParams {
+    SwapPools pools;
+    const int64_t* pairs;
+    int64_t n_pairs;
+    int64_t num_src;
+    int64_t num_dst;
+    uint64_t block_bytes;
+    uint32_t chunk_bytes;   // multiple of 16; the last chunk of a block may be shorter
+    int chunks;             // per block
+    int n_pools;
+    int stages;
+    unsigned int* errors;
+};
+
+struct BulkItem {
+    const char* src;
+    char* dst;
+    uint32_t bytes;   // 0: skipped pair
+};
+
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes,
+                                           uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+            reinterpret_cast<uint64_t>(dst)),
+        "r"(smem_addr(src_smem)), "r"(bytes), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Every bulk store group but the newest `1` has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Every bulk store group has completed (its writes are performed).
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(32)
+    swap_blocks_bulk_kernel(const BulkSwapParams p) {
+    extern __shared__ __align__(128) unsigned char bulk_smem[];
+    __shared__ __align__(8) uint64_t full[kMaxBulkStages];
+    __shared__ BulkItem items[kBulkBatch];
+    const int lane = threadIdx.x;
+    const int S = p.stages;
+    if (S < 2 || S > kMaxBulkStages) {
+        if (lane == 0) raise_error(p.errors, PKV_DEVERR_CONFIG);
+        return;
+    }
+    const int64_t per_pair = (int64_t)p.n_pools * p.chunks;
+    const int64_t total = p.n_pairs * per_pair;
+    const int64_t begin = total * blockIdx.x / gridDim.x;
+    const int64_t end = total * (blockIdx.x + 1) / gridDim.x;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const uint64_t policy = l2_policy_evict_first();
+    uint32_t phase_bits = 0;   // lane 0: parity of each slot's next wait
+    bool ok = true;
+    for (int64_t b0 = begin; b0 < end && ok; b0 += kBulkBatch) {
+        const int nb = (int)(end - b0 < kBulkBatch ? end - b0 : kBulkBatch);
+        // ---- look up the batch's pairs (all lanes)
+        for (int t = lane; t < nb; t += 32) {
+            const int64_t u = b0 + t;
+            const int64_t k = u / per_pair;
+            const int r = (int)(u - k * per_pair);
+            const int pool = r / p.chunks;
+            const int c = r - pool * p.chunks;
+            const int64_t i = p.pairs[2 * k];
+            const int64_t j = p.pairs[2 * k + 1];
+            BulkItem it;
+            it.src = nullptr;
+            it.dst = nullptr;
+            it.bytes = 0;
+            if (i >= 0 && j >= 0) {
+                if (i >= p.num_src || j >= p.num_dst) {
+                    if (pool == 0 && c == 0) raise_error(p.errors, PKV_DEVERR_PAIR);
+                } else {
+                    const uint64_t off = (uint64_t)c * p.chunk_bytes;
+                    const uint64_t left = p.block_bytes - off;
+                    it.bytes = (uint32_t)(left < p.chunk_bytes ? left : p.chunk_bytes);
+                    it.src = reinterpret_cast<const char*>(p.pools.src[pool]) +
+                             (uint64_t)i * p.block_bytes + off;
+                    it.dst = reinterpret_cast<char*>(p.pools.dst[pool]) +
+                             (uint64_t)j * p.block_bytes + off;
+                }
+            }
+            items[t] = it;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            // ---- pipeline over the batch: slot n % S holds item n
+            const int pre = nb < S ? nb : S;
+            for (int n = 0; n < pre; ++n) {
+                if (items[n].bytes) {
+                    mbar_arrive_expect_tx(&full[n], items[n].bytes);
+                    bulk_load(bulk_smem + (size_t)n * p.chunk_bytes, items[n].src, items[n].bytes,
+                              &full[n], policy);
+                } else {
+                    mbar_arrive(&full[n]);
+                }
+            }
+            int n = 0;
+            for (; n < nb; ++n) {
+                const int slot = n % S;
+                if (!mbar_wait(&full[slot], (phase_bits >> slot) & 1u, p.errors)) {
+                    ok = false;
+                    break;
+                }
+                phase_bits ^= 1u << slot;
+                if (items[n].bytes) {
+                    fence_proxy_async_smem();
+                    bulk_store(items[n].dst, bulk_smem + (size_t)slot * p.chunk_bytes,
+                               items[n].bytes, policy);
+                }
+                bulk_commit();
+                // refill the slot of item n - 1 with item n - 1 + S once the
+                // store of item n - 1 has read it
+                const int m = n - 1 + S;
+                if (n >= 1 && m < nb) {
+                    bulk_wait_read_all_but_one();
+                    const int ms = m % S;
+                    if (items[m].bytes) {
+                        mbar_arrive_expect_tx(&full[ms], items[m].bytes);
+                        bulk_load(bulk_smem + (size_t)ms * p.chunk_bytes, items[m].src,
+                                  items[m].bytes, &full[ms], policy);
+                    } else {
+                        mbar_arrive(&full[ms]);
+                    }
+                }
+            }
+            if (!ok) {
+                // item n never landed: wait once more (bounded) for it and
+                // for the loads issued after it, so that no copy still
+                // writes shared memory when the CTA leaves
+                const int issued = min(nb, S + max(0, n - 1));
+                for (int q = n; q < issued; ++q) {
+                    const int slot = q % S;
+                    if (!mbar_wait(&full[slot], (phase_bits >> slot) & 1u, p.errors)) break;
+                    phase_bits ^= 1u << slot;
+                }
+            }
+            bulk_wait_all();
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        __syncwarp();
     }
 }
 

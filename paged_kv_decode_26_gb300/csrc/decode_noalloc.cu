@@ -25,7 +25,9 @@
 //     last call's contents.
 //   * The first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress) with that device current; make that first call
-//     before any stream capture begins.
+//     before any stream capture begins.  The address is cached for the life
+//     of the process: it does not survive cudaDeviceReset, after which the
+//     library must not be called on that device again.
 #include <mutex>
 
 #include "../../include/pagedkv.h"

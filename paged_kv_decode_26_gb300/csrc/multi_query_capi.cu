@@ -65,6 +65,8 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
     if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size))
         return unsupported("head_dim 64/128, block_size 16/32, group 1/2/4/8");
     if (num_blocks < 0 || max_blocks_per_seq <= 0) return invalid("pool / table sizes");
+    if (!table_tokens_fit(max_blocks_per_seq, block_size))
+        return unsupported("max_blocks_per_seq * block_size exceeds 2^31 - 1 tokens");
     if (!std::isfinite(scale)) return invalid("scale is not finite");
     if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
     if (!out || !q || !q_start || !block_tables || !context_lens) return invalid("NULL pointer");
@@ -85,18 +87,18 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
     const int map_blocks = num_blocks > 0 ? num_blocks : 1;
 
     // tcgen05 path: two query tiles of 128 rows (128/G tokens x G heads) per
-    // CTA; PKV_MQ_TC=0/1 forces it off/on where it applies.
+    // CTA; the PKV_TUNE_MQ_TC knob forces it off/on where it applies.
     {
         const int tc_tokens = pkv::kTcRows / G;
         // Measured crossover (GB300): with groups of 4 the tcgen05 kernel wins
         // from 4-token chunks (16 rows); with groups of 1 the mma.sync kernel
         // wins up to 32 tokens and tcgen05 from 48.
-        int want = env_int("PKV_MQ_TC", -1);
+        int want = tuning(PKV_TUNE_MQ_TC, -1);
         if (want < 0) {
             const long long rows = (long long)max_q_len * G;
             want = (G >= 4 ? rows >= 16 : rows >= 48) ? 1 : 0;
         }
-        int stages = env_int("PKV_MQ_TC_STAGES", head_dim == 64 ? 6 : 4);
+        int stages = tuning(PKV_TUNE_MQ_TC_STAGES, head_dim == 64 ? 6 : 4);
         stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
         // Longest context first (see longest_first) for batches small enough
         // to rank in every CTA, and only with contexts of 8K tokens or more:
@@ -104,8 +106,8 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
         // nothing hides it), which long CTAs absorb.  GB300, 256-token
         // chunks: log-uniform [128, 32768] contexts 3.409 -> 3.215 ms;
         // uniform [512, 4096] 0.729 -> 0.744 ms, hence the threshold.
-        // PKV_MQ_LPT = 0 / 1 forces index order / longest first.
-        const int lpt_env = env_int("PKV_MQ_LPT", -1);
+        // The PKV_TUNE_MQ_LPT knob (0 / 1) forces index order / longest first.
+        const int lpt_env = tuning(PKV_TUNE_MQ_LPT, -1);
         const bool lpt_on = lpt_env >= 0 ? lpt_env != 0 : max_context_len >= kLptMinContext;
         const int lpt = lpt_on && num_seqs <= kLptMaxSeqs ? num_seqs : 0;
         while (stages > 2 && pkv::multi_query_tc_smem_bytes(head_dim, stages, max_pages, lpt) >
@@ -160,7 +162,7 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
     const int qt = 16 / G;  // query tokens per warp
     int warps = (max_q_len + qt - 1) / qt;
     warps = warps < 1 ? 1 : (warps > 4 ? 4 : warps);
-    int stages = env_int("PKV_MQ_STAGES", 4);
+    int stages = tuning(PKV_TUNE_MQ_STAGES, 4);
     stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
     pkv::MultiQueryLaunch L;
     std::memset(&L, 0, sizeof(L));

@@ -23,3 +23,12 @@ def load_golden(name):
 @pytest.fixture(scope="session")
 def golden():
     return load_golden
+
+
+@pytest.fixture
+def tuning():
+    """Launch-shape overrides of the library (pkv_set_tuning) for one test:
+    ``tuning(decode_hpc=2)``; every knob is back to automatic afterwards."""
+    import paged_kv_decode_26_gb300 as pkv
+    yield pkv.set_tuning
+    pkv.reset_tuning()

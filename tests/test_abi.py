@@ -96,6 +96,7 @@ def _decode(L, **kw):
     (dict(q=NULL), 1),
     (dict(bt=NULL), 1),
     (dict(out=C.c_void_p(4104)), 1),   # 8-byte aligned only
+    (dict(mb=1 << 27, B=32), 2),       # 2^32 tokens per table row: beyond int32 tokens
 ])
 def test_decode_rejects_invalid_arguments(L, kw, code):
     assert _decode(L, **kw) == code
@@ -168,3 +169,45 @@ def test_multi_query_rejects_invalid_arguments(L):
     assert mq(mc=1000) == 1          # beyond the block table (4 blocks of 16)
     assert mq(out=C.c_void_p(4104)) == 1
     assert mq(T=0) == 0 and mq(S=0) == 0
+
+
+def test_tuning_knobs_are_explicit_and_not_read_from_the_environment(L):
+    """Launch shapes change only through pkv_set_tuning: an environment
+    variable of the old tuning names has no effect; a knob set and reset
+    round-trips; an unknown knob is refused."""
+    import paged_kv_decode_26_gb300 as pkv
+    from paged_kv_decode_26_gb300 import _lib
+    pkv.reset_tuning()
+    base = pkv.decode_split_tokens(1, 8, 8, 128, 16, 4097)
+    assert base == 512
+    old = os.environ.get("PKV_DECODE_SPLIT")
+    os.environ["PKV_DECODE_SPLIT"] = "2048"
+    try:
+        assert pkv.decode_split_tokens(1, 8, 8, 128, 16, 4097) == base
+    finally:
+        if old is None:
+            del os.environ["PKV_DECODE_SPLIT"]
+        else:
+            os.environ["PKV_DECODE_SPLIT"] = old
+    try:
+        pkv.set_tuning(decode_split=2048)
+        assert pkv.get_tuning("decode_split") == 2048
+        assert pkv.decode_split_tokens(1, 8, 8, 128, 16, 4097) == 2048
+    finally:
+        pkv.reset_tuning()
+    assert pkv.get_tuning("decode_split") is None
+    assert pkv.decode_split_tokens(1, 8, 8, 128, 16, 4097) == base
+    assert L.pkv_set_tuning(_lib.TUNE_KNOBS["swap_ctas"] + 1, 3) == 1     # PKV_ERR_INVALID
+    assert L.pkv_set_tuning(-1, 3) == 1
+    assert L.pkv_get_tuning(99) == _lib.TUNE_AUTO
+    with pytest.raises(ValueError):
+        pkv.set_tuning(no_such_knob=1)
+
+
+def test_tuning_knob_names_match_the_header():
+    from paged_kv_decode_26_gb300 import _lib
+    text = open(HEADER).read()
+    enum = dict((m.group(1).lower(), int(m.group(2)))
+                for m in re.finditer(r"PKV_TUNE_(\w+)\s*=\s*(\d+)", text))
+    count = enum.pop("count")
+    assert enum == _lib.TUNE_KNOBS and count == len(enum)

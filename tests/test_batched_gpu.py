@@ -41,8 +41,8 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("H,Hk,split", [(8, 8, 64), (8, 8, 512), (16, 4, 64), (16, 4, 0)])
-def test_batched_equals_single_calls(pkv, monkeypatch, H, Hk, split):
-    monkeypatch.setenv("PKV_DECODE_HPC", "2")     # one launch shape for both ways
+def test_batched_equals_single_calls(pkv, tuning, H, Hk, split):
+    tuning(decode_hpc="2")     # one launch shape for both ways
     sizes = [3, 0, 5, 1, 4]
     cases = _problems(2, sizes, H, Hk, seed=H + split)
     max_ctx = max(int(c.context_lens.max()) for c in cases if c is not None)
@@ -80,10 +80,10 @@ def test_batched_equals_single_calls(pkv, monkeypatch, H, Hk, split):
         assert_attention_close(pr["out"], oracle, c.out_dtype)
 
 
-def test_batched_append_and_rerun(pkv, monkeypatch):
+def test_batched_append_and_rerun(pkv, tuning):
     """Problems with a fused append and problems without in one batch; a
     second run reads the buffers' new contents (queries changed)."""
-    monkeypatch.setenv("PKV_DECODE_HPC", "2")
+    tuning(decode_hpc="2")
     H, Hk, D = 16, 4, 128
     cases = [wl.make_case(2, S=S, lens=("uniform", 20, 200), H=H, Hk=Hk, D=D, seed=70 + i)
              for i, S in enumerate([4, 6, 2])]

@@ -72,6 +72,64 @@ def test_swap_sizes_and_untouched_bytes(lib, block_bytes):
     assert lib.device_errors() == 0
 
 
+@pytest.mark.parametrize("block_bytes,n", [(16, 300), (48, 23), (4096, 100), (40976, 23),
+                                          (131072, 9)])
+@pytest.mark.parametrize("knobs", [
+    {},                                                    # automatic launch shape
+    {"swap_chunk": 16, "swap_stages": 2, "swap_ctas": 1},  # many chunks, several batches per CTA
+    {"swap_chunk": 4096, "swap_stages": 8, "swap_ctas": 4},
+    {"swap_chunk": 65536, "swap_stages": 8},               # stages cut to fit shared memory
+    {"swap_chunk": 24, "swap_stages": 3},                  # rounded down to 16 bytes
+    {"swap_bulk": 0},                                      # 16-byte load/store kernel
+], ids=lambda k: ",".join(f"{a[5:]}={b}" for a, b in k.items()) or "auto")
+def test_swap_bulk_launch_shapes(lib, tuning, knobs, block_bytes, n):
+    """The bulk-copy kernel (device pools on both sides) for every chunk size
+    (a block in one copy, in several, with a shorter last chunk), ring depth
+    and CTAs per SM, with skipped and out-of-range pairs, bit-exact against
+    the oracle's loop, K and V in one launch and the untouched bytes kept."""
+    tuning(**knobs)
+    rng = np.random.default_rng(block_bytes + n)
+    ns, nd = n + 9, n + 13
+    src = [torch.from_numpy(rng.integers(0, 255, size=(ns, block_bytes), dtype=np.uint8))
+           for _ in range(2)]
+    dst = [torch.from_numpy(rng.integers(0, 255, size=(nd, block_bytes), dtype=np.uint8))
+           for _ in range(2)]
+    si = rng.choice(ns, n, replace=False)
+    di = rng.choice(nd, n, replace=False)
+    pairs = torch.from_numpy(np.stack([si, di], 1).astype(np.int64))
+    pairs[min(3, n - 1)] = torch.tensor([-1, int(di[min(3, n - 1)])])
+    d = [x.cuda() for x in dst]
+    s = [x.cuda() for x in src]
+    lib.swap_blocks_kv(d[0], d[1], s[0], s[1], pairs.cuda())
+    torch.cuda.synchronize()
+    for k in range(2):
+        orc.swap_blocks(dst[k], src[k], pairs)
+        assert torch.equal(d[k].cpu(), dst[k])
+    assert lib.device_errors() == 0
+    bad = pairs.clone()
+    bad[0, 0] = ns                                         # source past its pool
+    before = [x.clone() for x in d]
+    lib.swap_blocks(d[0], s[0], bad.cuda())
+    assert lib.device_errors(clear=True) & 0x8
+    orc.swap_blocks(before[0], s[0], bad)
+    assert torch.equal(d[0], before[0])
+
+
+def test_swap_within_one_pool(lib):
+    """Device-to-device inside one pool (disjoint sources and targets), as
+    the copy-on-write and defragmentation moves use it."""
+    case = wl.make_case(5, S=32, lens=("uniform", 16, 64), d2d_pairs=200, h2d_pairs=4,
+                        host_pool_blocks=8)
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    pairs = case.d2d_pairs
+    lib.swap_blocks_kv(dk, dv, dk, dv, pairs.cuda())
+    rk, rv = case.k_pool.clone(), case.v_pool.clone()
+    orc.swap_blocks(rk, rk.clone(), pairs)
+    orc.swap_blocks(rv, rv.clone(), pairs)
+    assert torch.equal(_bits(dk.cpu()), _bits(rk)) and torch.equal(_bits(dv.cpu()), _bits(rv))
+    assert lib.device_errors() == 0
+
+
 def test_swap_from_pinned_host(lib):
     case = wl.make_case(5, S=8, lens=("uniform", 16, 64), d2d_pairs=4, h2d_pairs=32,
                         host_pool_blocks=64)

@@ -75,23 +75,22 @@ def test_shape_matrix(lib, D, B, H, Hk, dtype, out_dtype):
     _no_device_errors(lib)
 
 
-@pytest.mark.parametrize("env", [
-    {"PKV_DECODE_WPT": "2"},
-    {"PKV_DECODE_WPT": "2", "PKV_DECODE_STAGES": "4"},
-    {"PKV_DECODE_WPT": "4", "PKV_DECODE_HPC": "2"},
-    {"PKV_DECODE_HPC": "1", "PKV_DECODE_STAGES": "6"},
-    {"PKV_DECODE_HPC": "2", "PKV_DECODE_STAGES": "2"},
-    {"PKV_DECODE_QPW": "2"},
-    {"PKV_DECODE_QPW": "1", "PKV_DECODE_HPC": "2"},
-    {"PKV_DECODE_MMA": "0"},
-    {"PKV_DECODE_MMA": "1", "PKV_DECODE_HPC": "2", "PKV_DECODE_STAGES": "4"},
-], ids=lambda e: ",".join(f"{k[11:]}={v}" for k, v in e.items()))
+@pytest.mark.parametrize("knobs", [
+    {"decode_wpt": 2},
+    {"decode_wpt": 2, "decode_stages": 4},
+    {"decode_wpt": 4, "decode_hpc": 2},
+    {"decode_hpc": 1, "decode_stages": 6},
+    {"decode_hpc": 2, "decode_stages": 2},
+    {"decode_qpw": 2},
+    {"decode_qpw": 1, "decode_hpc": 2},
+    {"decode_mma": 0},
+    {"decode_mma": 1, "decode_hpc": 2, "decode_stages": 4},
+], ids=lambda e: ",".join(f"{k[7:]}={v}" for k, v in e.items()))
 @pytest.mark.parametrize("config", [1, 2, 3, 4])
-def test_launch_configurations(lib, monkeypatch, config, env):
+def test_launch_configurations(lib, tuning, config, knobs):
     """Every tuning choice of the launch (kv heads per CTA, ring depth, warps
     taking turns on pages, query heads per warp) computes the same result."""
-    for k, v in env.items():
-        monkeypatch.setenv(k, v)
+    tuning(**knobs)
     case = wl.make_case(config, poison=True, **SMALL[config])
     for split in (0, 2 * case.B * 4):
         try:
@@ -99,8 +98,8 @@ def test_launch_configurations(lib, monkeypatch, config, env):
         except lib.PagedKVError as e:
             # a combination whose ring does not fit in shared memory is refused
             assert e.status == 2 and "shared memory" in str(e)
-            pytest.skip(f"{env} does not fit: {e}")
-        assert_attention_close(got, _oracle(case), case.out_dtype, f"{env} split {split}")
+            pytest.skip(f"{knobs} does not fit: {e}")
+        assert_attention_close(got, _oracle(case), case.out_dtype, f"{knobs} split {split}")
     _no_device_errors(lib)
 
 
@@ -109,10 +108,10 @@ def test_launch_configurations(lib, monkeypatch, config, env):
 @pytest.mark.parametrize("H,Hk", [(8, 4), (16, 4), (32, 4)])
 @pytest.mark.parametrize("dtype,out_dtype", [(torch.bfloat16, torch.bfloat16),
                                              (torch.float16, torch.float32)])
-def test_grouped_heads_both_paths(lib, monkeypatch, mma, D, B, H, Hk, dtype, out_dtype):
+def test_grouped_heads_both_paths(lib, tuning, mma, D, B, H, Hk, dtype, out_dtype):
     """Query-head groups of 2, 4 and 8 on the CUDA-core and the tensor-core
     consumer, ragged tails and NaN padding included."""
-    monkeypatch.setenv("PKV_DECODE_MMA", mma)
+    tuning(decode_mma=mma)
     case = wl.make_case(3, S=4, lens=("uniform", 1, 400), H=H, Hk=Hk, D=D, B=B, dtype=dtype,
                         out_dtype=out_dtype, share_blocks=2, poison=True, seed=H + D + B)
     for split in (0, 2 * B):

@@ -41,8 +41,8 @@ def test_decode_repeats_bitwise(pkv, config, split):
 
 
 @pytest.mark.parametrize("mode", ["0", "1"])
-def test_multi_query_repeats_bitwise(pkv, monkeypatch, mode):
-    monkeypatch.setenv("PKV_MQ_TC", mode)
+def test_multi_query_repeats_bitwise(pkv, tuning, mode):
+    tuning(mq_tc=mode)
     case = wl.make_case(3, S=6, lens=("uniform", 200, 900), poison=True, seed=4)
     q, qs = wl.multi_query_inputs(case, ("uniform", 60, 300), seed=5)
     args = [q.cuda(), qs.cuda(), case.k_pool.cuda(), case.v_pool.cuda(),
@@ -70,7 +70,7 @@ def _bits(o):
     (4, 5, 256, [0, 1, 256, 257, 4000]),                 # block size 32, exact multiples
     (2, 70, 16, [0] * 30 + [16 * k + 3 for k in range(40)]),  # many empty contexts
 ])
-def test_dense_order_matches_grid_order(pkv, monkeypatch, config, S, split, lens):
+def test_dense_order_matches_grid_order(pkv, tuning, config, S, split, lens):
     """CTAs taking units from the dense list (full splits first, short last
     splits after) or in grid order with the head group fastest compute the
     same partials as CTAs taking them by grid coordinates: the outputs agree
@@ -81,7 +81,7 @@ def test_dense_order_matches_grid_order(pkv, monkeypatch, config, S, split, lens
                                             "context_lens")}
     outs = {}
     for mode in ("0", "1", "2"):
-        monkeypatch.setenv("PKV_DECODE_DENSE", mode)
+        tuning(decode_order=mode)
         out = torch.empty(case.S, case.H, case.D, dtype=case.out_dtype, device="cuda")
         pkv.paged_attn_decode(out, d["q"], d["k_pool"], d["v_pool"], d["block_tables"],
                               d["context_lens"], case.scale, case.max_context_len,
@@ -93,12 +93,12 @@ def test_dense_order_matches_grid_order(pkv, monkeypatch, config, S, split, lens
     assert pkv.device_errors(clear=True) == 0
 
 
-def test_multi_query_longest_first_matches_index_order(pkv, monkeypatch):
+def test_multi_query_longest_first_matches_index_order(pkv, tuning):
     """The tcgen05 multi-query kernel's CTAs taking sequences longest context
     first compute what CTAs taking them in index order compute: bit for bit,
     with lengths spread over orders of magnitude, equal lengths (the tie
     order) and several query tiles per sequence."""
-    monkeypatch.setenv("PKV_MQ_TC", "1")
+    tuning(mq_tc="1")
     lens = [900, 150, 4000, 150, 2600, 300, 4000, 700, 1200, 260]
     case = wl.make_case(3, S=len(lens), lens_override=lens, poison=True, seed=13)
     q, qs = wl.multi_query_inputs(case, ("uniform", 100, 600), seed=14)
@@ -107,7 +107,7 @@ def test_multi_query_longest_first_matches_index_order(pkv, monkeypatch):
     max_q = int((qs[1:] - qs[:-1]).max())
     outs = {}
     for mode in ("0", "1"):
-        monkeypatch.setenv("PKV_MQ_LPT", mode)
+        tuning(mq_lpt=mode)
         out = torch.empty(q.shape[0], case.H, case.D, dtype=case.out_dtype, device="cuda")
         pkv.paged_attn_multi_query(out, *args[:2], *args[2:], case.scale, max_q,
                                    case.max_context_len)

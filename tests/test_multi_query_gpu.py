@@ -4,7 +4,7 @@ context, for query-head groups 1-8, head dims 64/128, block sizes 16/32,
 fp16/bf16 inputs, speculative-sized and prefill-sized chunks, ragged pages
 and NaN padding.  Both kernels are covered: the mma.sync kernel (16 rows
 per warp) and the tcgen05 kernel (128 rows per CTA), selected through
-PKV_MQ_TC."""
+the library's mq_tc tuning knob."""
 import numpy as np
 import pytest
 import torch
@@ -50,10 +50,10 @@ def _close(got, ref, case, q, qs, out_dtype=None, what=""):
 
 
 @pytest.fixture(params=["mma", "tc"])
-def path(request, monkeypatch):
+def path(request, tuning):
     """Forces one multi-query kernel (the tcgen05 one needs at least 128/G
     query rows in the call; smaller calls take the mma.sync kernel)."""
-    monkeypatch.setenv("PKV_MQ_TC", "1" if request.param == "tc" else "0")
+    tuning(mq_tc="1" if request.param == "tc" else "0")
     return request.param
 
 
@@ -127,11 +127,11 @@ def _oracle(case, q, qs):
 
 @pytest.mark.parametrize("D,B", [(128, 16), (64, 32), (128, 32), (64, 16)])
 @pytest.mark.parametrize("H,Hk", [(8, 8), (8, 4), (32, 4), (16, 8)])
-def test_tc_several_tiles_ragged(pkv, monkeypatch, D, B, H, Hk):
+def test_tc_several_tiles_ragged(pkv, tuning, D, B, H, Hk):
     """Chunks of 100-400 tokens: several 128-row tiles per (sequence, kv
     head) with a ragged last tile, contexts of many 64-key tiles with a
     ragged last tile, shared pages and NaN in every row outside a context."""
-    monkeypatch.setenv("PKV_MQ_TC", "1")
+    tuning(mq_tc="1")
     case = wl.make_case(2, S=4, lens=("uniform", 150, 700), H=H, Hk=Hk, D=D, B=B, share_blocks=3,
                         poison=True, seed=D * B + H)
     q, qs = wl.multi_query_inputs(case, ("uniform", 100, 400), seed=H * Hk)
@@ -141,11 +141,11 @@ def test_tc_several_tiles_ragged(pkv, monkeypatch, D, B, H, Hk):
 
 
 @pytest.mark.parametrize("gain", [8.0, 40.0])
-def test_tc_rescale_of_wide_scores(pkv, monkeypatch, gain):
+def test_tc_rescale_of_wide_scores(pkv, tuning, gain):
     """Queries scaled up so that scores spread over tens of binary orders:
     the running maximum of a row grows by more than 2^8 from one key tile to
     the next, which takes the kernel's O-rescaling branch."""
-    monkeypatch.setenv("PKV_MQ_TC", "1")
+    tuning(mq_tc="1")
     case = wl.make_case(2, S=3, lens=("uniform", 300, 600), H=8, Hk=2, D=128,
                         out_dtype=torch.float32, poison=True, seed=5)
     q, qs = wl.multi_query_inputs(case, ("uniform", 150, 300), seed=6)
@@ -155,10 +155,10 @@ def test_tc_rescale_of_wide_scores(pkv, monkeypatch, gain):
     assert pkv.device_errors(clear=True) == 0
 
 
-def test_tc_increasing_scores(pkv, monkeypatch):
+def test_tc_increasing_scores(pkv, tuning):
     """Key t scores t * c against every query, so each new key tile raises
     every row's maximum (rescale on every tile once the growth passes 2^8)."""
-    monkeypatch.setenv("PKV_MQ_TC", "1")
+    tuning(mq_tc="1")
     case = wl.make_case(2, S=2, lens_override=[640, 517], H=4, Hk=1, D=64,
                         out_dtype=torch.float32, poison=True, seed=9)
     k = case.k_pool.float()
@@ -174,7 +174,7 @@ def test_tc_increasing_scores(pkv, monkeypatch):
     assert pkv.device_errors(clear=True) == 0
 
 
-def test_tc_missing_pages_are_skipped(pkv, monkeypatch):
+def test_tc_missing_pages_are_skipped(pkv, tuning):
     """A block id of -1 inside a context (a page the table does not hold)
     is skipped like in the mma.sync kernel, and flagged."""
     case = wl.make_case(2, S=3, lens_override=[400, 300, 260], H=8, Hk=4, D=128,
@@ -186,12 +186,12 @@ def test_tc_missing_pages_are_skipped(pkv, monkeypatch):
     case.block_tables = bt
     outs = {}
     for mode in ("0", "1"):
-        monkeypatch.setenv("PKV_MQ_TC", mode)
+        tuning(mq_tc=mode)
         outs[mode] = _run(pkv, case, q, qs)
         assert pkv.device_errors(clear=True) & 0x1
     ref = _oracle_skip_missing(case, q, qs)
     for mode, got in outs.items():
-        assert_attention_close(got, ref, torch.float32, f"PKV_MQ_TC={mode}",
+        assert_attention_close(got, ref, torch.float32, f"mq_tc={mode}",
                                abs_weighted=lambda: _oracle_skip_missing(case, q, qs, True),
                                kv_dtype=case.dtype)
 
@@ -269,12 +269,12 @@ def test_full_size_sampled(pkv, config, k):
 
 
 @pytest.mark.parametrize("H,Hk", [(8, 8), (16, 4)])
-def test_tc_tile_boundaries(pkv, monkeypatch, H, Hk):
+def test_tc_tile_boundaries(pkv, tuning, H, Hk):
     """Chunk lengths around the 128-row query tile and the 256-row CTA span
     (one token short, exact, one over), contexts shorter than one 64-key
     tile and contexts ending at, just before and just after a key-tile
     boundary; the whole-context prefill among them."""
-    monkeypatch.setenv("PKV_MQ_TC", "1")
+    tuning(mq_tc="1")
     G = H // Hk
     qt = 128 // G                                   # tokens per query tile
     q_lens = [1, qt - 1, qt, qt + 1, 2 * qt - 1, 2 * qt, 2 * qt + 1, 3 * qt + 5]
@@ -292,10 +292,10 @@ def test_tc_tile_boundaries(pkv, monkeypatch, H, Hk):
     assert pkv.device_errors(clear=True) == 0
 
 
-def test_tc_bad_q_start_is_flagged(pkv, monkeypatch):
+def test_tc_bad_q_start_is_flagged(pkv, tuning):
     """The tcgen05 kernel skips and flags a sequence whose chunk is longer
     than its context, and still answers the others."""
-    monkeypatch.setenv("PKV_MQ_TC", "1")
+    tuning(mq_tc="1")
     case = wl.make_case(2, S=3, lens_override=[40, 90, 70], H=16, Hk=2, D=128,
                         out_dtype=torch.float32)
     q, qs = wl.multi_query_inputs(case, ("const", 24))     # 72 rows >= 16 tokens per tile
