@@ -1,204 +1,185 @@
-"""Plain-Python restatement of the block allocator and scheduler that the page
-"大模型长文本推理基座从 FlashAttention 硬件加速机制到 vLLM 核心 PagedAttention
-显存物理布局深度剖析" gives in its section 三 (PhysicalBlock, KVBlockManager,
-BlockTable, PagedAttentionScheduler), used as the oracle for the library's
-native block manager.
+"""Block allocator rules of paged KV caching, restated as plain functions over
+a reference-count list; the oracle for the library's native block manager
+(host and device).
 
 TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
 benchmark's CPU-baseline leg, never by the product path.
 
-The page's text lost several operators in extraction.  Readings taken (the
-only ones the surrounding code and its comments support):
-  * ``is_free``: ``ref_count == 0``;
-  * ``allocate``: ``free_blocks.pop(0)`` then ``ref_count = 1``;
-  * ``free``: ``if ref_count > 0: ref_count -= 1``; when it reaches 0 the id
-    goes back to the free list, which is kept sorted so that the lowest id
-    is handed out first;
-  * ``add_reference``: ``ref_count += 1``;
-  * ``register_request``: ``ceil(prompt_len / block_size)`` blocks;
-  * ``append_token``: a new block when ``num_allocated_tokens % block_size ==
-    0``, then ``num_allocated_tokens += 1``; an empty pool makes the append
-    fail (return False) without changing the table.
+The rules, as the page "大模型长文本推理基座从 FlashAttention 硬件加速机制到
+vLLM 核心 PagedAttention 显存物理布局深度剖析" states them in its section 二.2
+(logical blocks of 16 tokens mapped to physical blocks by a block table)
+and section 三 (a pool of physical blocks with reference counts; a request
+gets blocks for its prompt, one more each time its last block is full, and
+gives them back when it finishes):
 
-Parity: pinned by the page's own walkthrough (tests/golden/allocator_walkthrough.json).
+  R1  The pool holds ids 0 .. N-1.  Each id carries a reference count; an id
+      whose count is 0 is free.
+  R2  Taking a block hands out the lowest free id and sets its count to 1
+      (the page keeps its free list sorted and takes the first entry).  With
+      no free id the take fails.
+  R3  Dropping a reference lowers a held id's count by one; at 0 the id is
+      free again (a free id stays free).
+  R4  Sharing a held block (a common prompt prefix, a forked request) adds a
+      reference.  Sharing a free id is refused (the page's code would allow
+      it while leaving the id in its free list; that state is never valid).
+  R5  A request of n tokens holds ceil(n / B) blocks.  Its token number n
+      (0-based) needs a new block exactly when n mod B == 0; if the take
+      fails the token is not added and the request is unchanged.
+  R6  Token n of a request lives at row n mod B of its logical block n div B,
+      i.e. at flat slot table[n div B] * B + n mod B of the pool.
+
+Here a pool is a list of reference counts; a request is its table (list of
+physical ids) and its token count.  Readings where the extracted page text
+is garbled (lost comparison and update operators) are listed in the repo's
+design notes; the two-request walkthrough of section 三 pins the result
+(tests/golden/allocator_walkthrough.json).
 """
 from __future__ import annotations
 
 
-class OutOfBlocks(MemoryError):
-    """Raised by ``allocate`` when no physical block is free (the page raises
-    MemoryError with a "CUDA Out of Memory" message)."""
+# ------------------------------------------------------------------ pool
+
+def make_pool(num_blocks: int, free_ids=None) -> list[int]:
+    """R1: reference counts of a pool of num_blocks ids.  With free_ids
+    given, the ids not listed start held once (a pool already in use)."""
+    if free_ids is None:
+        return [0] * num_blocks
+    refs = [1] * num_blocks
+    for b in free_ids:
+        refs[int(b)] = 0
+    return refs
 
 
-class PhysicalBlock:
-    def __init__(self, block_id: int, block_size: int = 16):
-        self.block_id = block_id
-        self.block_size = block_size
-        self.ref_count = 0
-
-    def is_free(self) -> bool:
-        return self.ref_count == 0
+def free_list(refs) -> list[int]:
+    """The free ids in increasing order (the order R2 hands them out)."""
+    return [b for b, r in enumerate(refs) if r == 0]
 
 
-class KVBlockManager:
-    def __init__(self, num_blocks: int, block_size: int = 16, free_ids=None):
-        self.block_size = block_size
-        self.gpu_blocks = [PhysicalBlock(i, block_size) for i in range(num_blocks)]
-        if free_ids is None:
-            self.free_blocks = list(range(num_blocks))
-        else:
-            # A pool that starts part-used: ids not listed are held once.
-            self.free_blocks = sorted(int(i) for i in free_ids)
-            held = set(range(num_blocks)) - set(self.free_blocks)
-            for i in held:
-                self.gpu_blocks[i].ref_count = 1
-
-    def allocate(self) -> int:
-        if not self.free_blocks:
-            raise OutOfBlocks("CUDA Out of Memory: No free physical blocks available in pool!")
-        block_id = self.free_blocks.pop(0)
-        self.gpu_blocks[block_id].ref_count = 1
-        return block_id
-
-    def free(self, block_id: int) -> None:
-        block = self.gpu_blocks[block_id]
-        if block.ref_count > 0:
-            block.ref_count -= 1
-            if block.ref_count == 0:
-                self.free_blocks.append(block_id)
-                self.free_blocks.sort()
-
-    def add_reference(self, block_id: int) -> None:
-        self.gpu_blocks[block_id].ref_count += 1
-
-    def get_free_blocks_count(self) -> int:
-        return len(self.free_blocks)
+def take_block(refs):
+    """R2: the lowest free id, now held once; None if every id is held."""
+    for b, r in enumerate(refs):
+        if r == 0:
+            refs[b] = 1
+            return b
+    return None
 
 
-class BlockTable:
-    def __init__(self, request_id):
-        self.request_id = request_id
-        self.physical_block_ids: list[int] = []
-        self.num_allocated_tokens = 0
+def drop_reference(refs, b: int) -> None:
+    """R3: one reference fewer on block b (nothing happens to a free id)."""
+    if refs[b] > 0:
+        refs[b] -= 1
 
 
-class PagedAttentionScheduler:
-    def __init__(self, num_blocks: int = 10, block_size: int = 16, free_ids=None):
-        self.manager = KVBlockManager(num_blocks, block_size, free_ids)
-        self.block_size = block_size
-        self.active_requests: dict = {}
+def share_block(refs, b: int) -> None:
+    """R4: one reference more on the held block b."""
+    if refs[b] <= 0:
+        raise ValueError(f"block {b} is free and cannot be shared")
+    refs[b] += 1
 
-    def register_request(self, request_id, prompt_len: int) -> BlockTable:
-        table = BlockTable(request_id)
-        required_blocks = (prompt_len + self.block_size - 1) // self.block_size
-        for _ in range(required_blocks):
-            table.physical_block_ids.append(self.manager.allocate())
-        table.num_allocated_tokens = prompt_len
-        self.active_requests[request_id] = table
-        return table
 
-    def adopt(self, request_id, block_ids, num_tokens: int) -> BlockTable:
-        """Install an existing table (blocks already held) without allocating;
-        used to start from a generated cache state."""
-        table = BlockTable(request_id)
-        table.physical_block_ids = [int(b) for b in block_ids]
-        table.num_allocated_tokens = int(num_tokens)
-        self.active_requests[request_id] = table
-        return table
+# -------------------------------------------------------------- requests
 
-    def append_token(self, request_id) -> bool:
-        table = self.active_requests.get(request_id)
-        if not table:
-            return False
-        current_tokens = table.num_allocated_tokens
-        if current_tokens % self.block_size == 0:
-            try:
-                new_block_id = self.manager.allocate()
-            except OutOfBlocks:
-                return False
-            table.physical_block_ids.append(new_block_id)
-        table.num_allocated_tokens += 1
-        return True
+def blocks_needed(num_tokens: int, block_size: int) -> int:
+    """R5: blocks a request of num_tokens tokens holds."""
+    return -(-num_tokens // block_size)
 
-    def finish_request(self, request_id) -> None:
-        table = self.active_requests.pop(request_id, None)
-        if table:
-            for block_id in table.physical_block_ids:
-                self.manager.free(block_id)
+
+def admit(refs, num_tokens: int, block_size: int):
+    """A new request with a prompt of num_tokens tokens: its table of
+    blocks_needed blocks taken one after another (R2), or None when the
+    pool runs out (the blocks taken so far are given back)."""
+    table = []
+    for _ in range(blocks_needed(num_tokens, block_size)):
+        b = take_block(refs)
+        if b is None:
+            for t in table:
+                drop_reference(refs, t)
+            return None
+        table.append(b)
+    return table
+
+
+def slot_of(table, n: int, block_size: int) -> int:
+    """R6: flat pool slot of token n."""
+    return table[n // block_size] * block_size + n % block_size
+
+
+def add_token(refs, table, num_tokens: int, block_size: int):
+    """R5 for one request: returns (slot of the new token, new token count),
+    or (-1, num_tokens) when a new block was needed and none was free.
+    `table` grows in place when a block is opened."""
+    if num_tokens % block_size == 0:
+        b = take_block(refs)
+        if b is None:
+            return -1, num_tokens
+        table.append(b)
+    return slot_of(table, num_tokens, block_size), num_tokens + 1
+
+
+def release(refs, table) -> None:
+    """A finished request gives back one reference on each of its blocks."""
+    for b in table:
+        drop_reference(refs, b)
+
+
+# ------------------------------------------------------- one decode step
+
+def append_slots(tables, context_lens, block_size: int, free_ids, num_blocks: int):
+    """One decode step's append for every sequence, in sequence order: each
+    sequence gets one new token (add_token), starting from a pool whose free
+    ids are `free_ids` and whose other ids are held once.
+
+    Returns (new_tables, new_lens, slots, free_ids_after); a sequence whose
+    append failed has slot -1 and keeps its table and length."""
+    refs = make_pool(num_blocks, free_ids)
+    new_tables = [[int(b) for b in t] for t in tables]
+    new_lens, slots = [], []
+    for table, n in zip(new_tables, context_lens):
+        slot, n_after = add_token(refs, table, int(n), block_size)
+        slots.append(slot)
+        new_lens.append(n_after)
+    return new_tables, new_lens, slots, free_list(refs)
 
 
 def append_slots_cow(tables, context_lens, block_size: int, free_ids, num_blocks: int,
                      ref_counts):
     """append_slots with copy-on-write ([LAYOUT] section 四.2): several
-    requests may point at one physical block (ref_count > 1).  The page
-    says only a request that writes its own next token into such a block
-    triggers the copy: it gets a freshly allocated private block holding a
-    copy of the shared one, and drops its reference to the shared block.
+    requests may point at one physical block (count > 1), and a request
+    that writes its next token into such a shared block first gets a
+    private copy: a newly taken block that replaces the shared one in its
+    table, the shared block losing that reference.
 
-    Readings: the copy happens when the token's page is an existing shared
-    block (a partly filled last page; a full page opens a new block as in
-    append_token).  ref_counts gives the starting count of every block
-    (free ids have 0).  Returns (new_tables, new_lens, slots, copy_pairs,
-    free_after, ref_after); copy_pairs lists (shared block, private block)
-    in sequence order, for the caller to copy before writing.
-    """
-    mgr = KVBlockManager(num_blocks, block_size, free_ids)
-    for b in range(num_blocks):
-        mgr.gpu_blocks[b].ref_count = int(ref_counts[b])
-    tables = [list(map(int, t)) for t in tables]
-    lens = [int(n) for n in context_lens]
-    slots, pairs = [], []
-    for s in range(len(tables)):
-        n = lens[s]
+    Readings: the copy happens only when the token's page is an existing
+    block held more than once (a partly filled last page); a token that
+    starts a page opens a new block as in add_token.  ref_counts gives every
+    block's starting count (free ids 0; free_ids must list exactly those).
+    Returns (new_tables, new_lens, slots, copy_pairs, free_after, ref_after);
+    copy_pairs lists (shared block, private block) in sequence order, for
+    the caller to copy before the tokens are written."""
+    refs = [int(r) for r in ref_counts]
+    assert free_list(refs) == sorted(int(b) for b in free_ids)
+    assert len(refs) == num_blocks
+    new_tables = [[int(b) for b in t] for t in tables]
+    new_lens, slots, pairs = [], [], []
+    for table, n in zip(new_tables, context_lens):
+        n = int(n)
         j = n // block_size
-        if n % block_size == 0:
-            try:
-                tables[s].append(mgr.allocate())
-            except OutOfBlocks:
+        if n % block_size != 0 and refs[table[j]] > 1:
+            private = take_block(refs)
+            if private is None:
                 slots.append(-1)
+                new_lens.append(n)
                 continue
-        else:
-            b = tables[s][j]
-            if mgr.gpu_blocks[b].ref_count > 1:
-                try:
-                    nb = mgr.allocate()
-                except OutOfBlocks:
-                    slots.append(-1)
-                    continue
-                mgr.free(b)
-                tables[s][j] = nb
-                pairs.append((b, nb))
-        slots.append(tables[s][j] * block_size + n % block_size)
-        lens[s] = n + 1
-    refs = [blk.ref_count for blk in mgr.gpu_blocks]
-    return tables, lens, slots, pairs, list(mgr.free_blocks), refs
+            pairs.append((table[j], private))
+            drop_reference(refs, table[j])
+            table[j] = private
+        slot, n_after = add_token(refs, table, n, block_size)
+        slots.append(slot)
+        new_lens.append(n_after)
+    return new_tables, new_lens, slots, pairs, free_list(refs), refs
 
 
-def append_slots(tables, context_lens, block_size: int, free_ids, num_blocks: int):
-    """One decode step's append for every sequence, in sequence order: each
-    sequence gets one new token through ``append_token`` (a new block from the
-    free list when its last page is full) and the flat slot that token is
-    written to, ``table[n // B] * B + n % B`` for its old length n.  A
-    sequence whose append fails gets slot -1.
-
-    Returns (new_tables (list of lists), new_lens, slots, free_ids_after).
-    """
-    sch = PagedAttentionScheduler(num_blocks, block_size, free_ids)
-    for s, (ids, n) in enumerate(zip(tables, context_lens)):
-        sch.adopt(s, ids, n)
-    slots = []
-    for s in range(len(tables)):
-        n = sch.active_requests[s].num_allocated_tokens
-        ok = sch.append_token(s)
-        if not ok:
-            slots.append(-1)
-            continue
-        ids = sch.active_requests[s].physical_block_ids
-        slots.append(ids[n // block_size] * block_size + n % block_size)
-    new_tables = [list(sch.active_requests[s].physical_block_ids) for s in range(len(tables))]
-    new_lens = [sch.active_requests[s].num_allocated_tokens for s in range(len(tables))]
-    return new_tables, new_lens, slots, list(sch.manager.free_blocks)
-
+# ----------------------------------------------------- defragmentation
 
 def defrag_plan(ref_counts):
     """Defragmentation by block copies ("vLLM 中 FlashAttention 与 KVCache 交换

@@ -1,11 +1,12 @@
 """The library's native block manager against the oracle's restatement of the
-pages' allocator: the walkthrough, random operation sequences, and the
+pages' allocator rules: the walkthrough, random operation sequences, and the
 per-step append bookkeeping, all bit-exact.  CPU only (host code)."""
 import numpy as np
 import pytest
 import torch
 
-from oracle.block_manager import KVBlockManager, OutOfBlocks, append_slots
+from oracle import block_manager as obm
+from oracle.block_manager import append_slots
 from paged_kv_decode_26_gb300 import workloads as wl
 
 
@@ -53,16 +54,13 @@ def test_random_operation_sequences_match_oracle(pkv):
     rng = np.random.default_rng(17)
     for trial in range(20):
         nb = int(rng.integers(1, 200))
-        ref = KVBlockManager(nb, 16)
+        refs = obm.make_pool(nb)
         bm = pkv.BlockManager(nb, 16)
         held = []
         for _ in range(400):
             op = rng.integers(0, 3)
             if op == 0:
-                try:
-                    a = ref.allocate()
-                except OutOfBlocks:
-                    a = None
+                a = obm.take_block(refs)
                 if a is None:
                     with pytest.raises(pkv.PagedKVError):
                         bm.allocate()
@@ -71,17 +69,17 @@ def test_random_operation_sequences_match_oracle(pkv):
                     held.append(a)
             elif op == 1 and held:
                 b = held.pop(int(rng.integers(len(held))))
-                ref.free(b)
+                obm.drop_reference(refs, b)
                 bm.free(b)
             elif op == 2 and held:
                 b = held[int(rng.integers(len(held)))]
-                ref.add_reference(b)
+                obm.share_block(refs, b)
                 bm.add_reference(b)
                 held.append(b)
-            assert bm.free_count() == ref.get_free_blocks_count()
-        assert bm.free_ids() == ref.free_blocks
+            assert bm.free_count() == len(obm.free_list(refs))
+        assert bm.free_ids() == obm.free_list(refs)
         for b in range(nb):
-            assert bm.ref_count(b) == ref.gpu_blocks[b].ref_count
+            assert bm.ref_count(b) == refs[b]
 
 
 def test_add_reference_of_free_block_is_rejected(pkv):

@@ -9,7 +9,8 @@ import scipy.special
 import torch
 
 from oracle import oracle as orc
-from oracle.block_manager import PagedAttentionScheduler, append_slots
+from oracle import block_manager as bm
+from oracle.block_manager import append_slots
 from paged_kv_decode_26_gb300 import workloads as wl
 
 
@@ -374,41 +375,91 @@ def test_kv_append_rejects_slot_past_pool():
 # ---------------------------------------------------------- allocator
 
 def test_allocator_walkthrough(golden):
+    """The two-request walkthrough of [LAYOUT] section 三: register A (20
+    tokens) and B (10), append 13 tokens to A, finish B."""
     g = golden("allocator_walkthrough.json")
-    sch = PagedAttentionScheduler(num_blocks=g["num_blocks"], block_size=g["block_size"])
-    assert sch.manager.get_free_blocks_count() == g["free_at_start"]
-    a = sch.register_request("req_A", g["req_A"]["prompt_len"])
-    b = sch.register_request("req_B", g["req_B"]["prompt_len"])
-    assert a.physical_block_ids == g["req_A"]["blocks"]
-    assert b.physical_block_ids == g["req_B"]["blocks"]
-    assert sch.manager.get_free_blocks_count() == g["free_after_register"]
+    B = g["block_size"]
+    refs = bm.make_pool(g["num_blocks"])
+    assert len(bm.free_list(refs)) == g["free_at_start"]
+    a = bm.admit(refs, g["req_A"]["prompt_len"], B)
+    b = bm.admit(refs, g["req_B"]["prompt_len"], B)
+    assert a == g["req_A"]["blocks"] and b == g["req_B"]["blocks"]
+    assert len(bm.free_list(refs)) == g["free_after_register"]
+    n = g["req_A"]["prompt_len"]
     opened_at = None
     for i in range(g["appends_A"]):
-        before = len(a.physical_block_ids)
-        assert sch.append_token("req_A")
-        if len(a.physical_block_ids) > before:
+        before = len(a)
+        slot, n_new = bm.add_token(refs, a, n, B)
+        assert slot >= 0 and n_new == n + 1
+        assert slot == a[n // B] * B + n % B
+        n = n_new
+        if len(a) > before:
             assert opened_at is None
             opened_at = i + 1
     assert opened_at == g["new_block_on_append_number"]
-    assert a.physical_block_ids == g["A_blocks_after_appends"]
-    assert a.num_allocated_tokens == g["A_tokens_after_appends"]
-    assert sch.manager.get_free_blocks_count() == g["free_after_appends"]
-    sch.finish_request("req_B")
-    assert sch.manager.get_free_blocks_count() == g["free_after_finish_B"]
-    assert sch.manager.free_blocks == g["free_list_after_finish_B"]
+    assert a[-1] == g["new_block_id"]
+    assert a == g["A_blocks_after_appends"]
+    assert n == g["A_tokens_after_appends"]
+    assert len(bm.free_list(refs)) == g["free_after_appends"]
+    bm.release(refs, b)
+    assert len(bm.free_list(refs)) == g["free_after_finish_B"]
+    assert bm.free_list(refs) == g["free_list_after_finish_B"]
 
 
 def test_allocator_refcount_and_exhaustion():
-    sch = PagedAttentionScheduler(num_blocks=2, block_size=4)
-    t = sch.register_request("x", 8)
-    assert t.physical_block_ids == [0, 1]
-    assert not sch.append_token("x")          # page full, pool empty: fails
-    assert t.num_allocated_tokens == 8 and t.physical_block_ids == [0, 1]
-    sch.manager.add_reference(0)              # a second holder of block 0
-    sch.finish_request("x")
-    assert sch.manager.free_blocks == [1]     # block 0 still referenced once
-    sch.manager.free(0)
-    assert sch.manager.free_blocks == [0, 1]
+    refs = bm.make_pool(2)
+    t = bm.admit(refs, 8, 4)
+    assert t == [0, 1]
+    assert bm.add_token(refs, t, 8, 4) == (-1, 8)   # page full, pool empty: fails
+    assert t == [0, 1]
+    assert bm.admit(refs, 1, 4) is None
+    bm.share_block(refs, 0)                          # a second holder of block 0
+    bm.release(refs, t)
+    assert bm.free_list(refs) == [1]                 # block 0 still referenced once
+    bm.drop_reference(refs, 0)
+    assert bm.free_list(refs) == [0, 1]
+    bm.drop_reference(refs, 0)                       # a free id stays free
+    assert refs == [0, 0]
+    with pytest.raises(ValueError):
+        bm.share_block(refs, 1)                      # a free id cannot be shared
+
+
+def test_admit_gives_back_a_partial_allocation():
+    refs = bm.make_pool(5, free_ids=[1, 3, 4])
+    assert bm.admit(refs, 4 * 16, 16) is None       # needs 4 of 3 free
+    assert bm.free_list(refs) == [1, 3, 4]
+    assert bm.admit(refs, 33, 16) == [1, 3, 4]
+
+
+def test_allocator_against_brute_force_lowest_free():
+    """Random takes, shares and drops against a recount from scratch: the
+    free list is exactly the ids whose count is 0, and every take returns
+    the minimum of that set."""
+    rng = np.random.default_rng(3)
+    for _ in range(30):
+        nb = int(rng.integers(1, 40))
+        refs = bm.make_pool(nb)
+        held = []
+        for _ in range(300):
+            op = int(rng.integers(0, 3))
+            if op == 0:
+                free_before = [b for b in range(nb) if refs[b] == 0]
+                b = bm.take_block(refs)
+                if free_before:
+                    assert b == min(free_before) and refs[b] == 1
+                    held.append(b)
+                else:
+                    assert b is None
+            elif op == 1 and held:
+                b = held.pop(int(rng.integers(len(held))))
+                bm.drop_reference(refs, b)
+            elif op == 2 and held:
+                b = held[int(rng.integers(len(held)))]
+                bm.share_block(refs, b)
+                held.append(b)
+            counts = [held.count(b) for b in range(nb)]
+            assert refs == counts
+            assert bm.free_list(refs) == [b for b in range(nb) if counts[b] == 0]
 
 
 def test_append_slots_page_boundary():

@@ -1,8 +1,11 @@
-"""Each plausible mistake planted in a copy of the oracle's C source must make
-the oracle's pin suite (tests/test_oracle.py) fail -- evidence that the pins
-pin the arithmetic, not just exercise it.  CPU only: the mutants are compiled
-with gcc into a temporary directory; the committed oracle is untouched."""
+"""Each plausible mistake planted in a copy of the oracle (its C source, or
+its Python allocator rules) must make the oracle's pin suite
+(tests/test_oracle.py) fail -- evidence that the pins pin the arithmetic and
+the rules, not just exercise them.  CPU only: C mutants are compiled with
+gcc into a temporary directory, Python mutants run from a temporary copy of
+the tree; the committed oracle is untouched."""
 import os
+import shutil
 import subprocess
 import sys
 
@@ -58,3 +61,52 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
                           os.path.join(ROOT, "tests", "test_oracle.py")],
                          cwd=ROOT, env=env, capture_output=True, text=True)
     assert res.returncode != 0, f"the pins did not catch: {name}\n{res.stdout[-2000:]}"
+
+
+BM_SRC = os.path.join(ROOT, "oracle", "block_manager.py")
+
+# (name, exact source text, planted replacement) in oracle/block_manager.py
+PY_MUTANTS = [
+    ("highest free id first", "    for b, r in enumerate(refs):\n        if r == 0:\n            refs[b] = 1",
+     "    for b, r in reversed(list(enumerate(refs))):\n        if r == 0:\n            refs[b] = 1"),
+    ("page opened at n mod B == 1", "    if num_tokens % block_size == 0:\n        b = take_block(refs)",
+     "    if num_tokens % block_size == 1:\n        b = take_block(refs)"),
+    ("dropped reference never freed", "        refs[b] -= 1", "        refs[b] -= 0"),
+    ("token row shifted", "    return table[n // block_size] * block_size + n % block_size",
+     "    return table[n // block_size] * block_size + (n + 1) % block_size"),
+]
+
+
+def _copy_tree(dst):
+    ignore = shutil.ignore_patterns("_build", "__pycache__", "*.so", "*.o", "csrc")
+    for d in ("oracle", "tests", "paged_kv_decode_26_gb300"):
+        shutil.copytree(os.path.join(ROOT, d), os.path.join(dst, d), ignore=ignore)
+    shutil.copy(os.path.join(ROOT, "pytest.ini"), dst)
+
+
+@pytest.mark.parametrize("name,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_pins_catch_planted_allocator_mistake(tmp_path, name, old, new):
+    from oracle import build as ob
+    src = open(BM_SRC).read()
+    assert src.count(old) == 1, f"mutation site for '{name}' not found: update the mutant list"
+    _copy_tree(str(tmp_path))
+    with open(os.path.join(str(tmp_path), "oracle", "block_manager.py"), "w") as f:
+        f.write(src.replace(old, new))
+    env = dict(os.environ, PKV_ORACLE_LIB=ob.build())
+    res = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                          os.path.join("tests", "test_oracle.py")],
+                         cwd=str(tmp_path), env=env, capture_output=True, text=True)
+    assert res.returncode != 0, f"the pins did not catch: {name}\n{res.stdout[-2000:]}"
+    assert "passed" in res.stdout or "failed" in res.stdout, res.stdout[-2000:]
+
+
+def test_unmutated_copy_passes(tmp_path):
+    """The copied tree itself passes the pins (so a mutant's failure is the
+    mutant's)."""
+    from oracle import build as ob
+    _copy_tree(str(tmp_path))
+    env = dict(os.environ, PKV_ORACLE_LIB=ob.build())
+    res = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                          os.path.join("tests", "test_oracle.py")],
+                         cwd=str(tmp_path), env=env, capture_output=True, text=True)
+    assert res.returncode == 0, res.stdout[-3000:]
