@@ -108,11 +108,11 @@ def test_swap_bulk_launch_shapes(lib, tuning, knobs, block_bytes, n):
     assert lib.device_errors() == 0
     bad = pairs.clone()
     bad[0, 0] = ns                                         # source past its pool
-    before = [x.clone() for x in d]
+    expect = dst[0].clone()
     lib.swap_blocks(d[0], s[0], bad.cuda())
     assert lib.device_errors(clear=True) & 0x8
-    orc.swap_blocks(before[0], s[0], bad)
-    assert torch.equal(d[0], before[0])
+    assert orc.swap_blocks(expect, src[0], bad) == 1
+    assert torch.equal(d[0].cpu(), expect)
 
 
 def test_swap_within_one_pool(lib):
