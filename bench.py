@@ -73,8 +73,10 @@ def parse_args():
     ap.add_argument("--graph-streams", type=int, default=32,
                     help="parallel branches of the replica graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=12.0,
-                    help="seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other stated workloads after the headline one")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds (wall) of threaded oracle work for the CPU baseline")
     return ap.parse_args()
 
 
@@ -188,75 +190,81 @@ def workload_name(case, config, lens_override: str = "") -> str:
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sample_seconds(case, lens, tables, budget_s):
-    """Run the oracle on whole sequences (all heads) of the step until about
-    `budget_s` seconds of CPU work; returns (kv_bytes, seconds, n_seqs)."""
-    from oracle import oracle as orc
-    row = case.Hk * case.D * 2 * 2
-    done_bytes, t_total, n = 0, 0.0, 0
-    order = list(range(case.S))
-    while t_total < budget_s and n < len(order):
-        s = order[n]
+def oracle_step_seconds(case, lens, tables, budget_s, threads=None):
+    """The fp64 oracle on the whole decode step of `case` (every sequence,
+    every head), threaded over the host cores (oracle.parallel), repeated
+    while the total stays under about `budget_s` seconds of wall time.
+    Returns (kv_bytes per run, seconds per run, runs, threads); the bytes are
+    the logical K+V bytes of the step, the unit of the GPU figures."""
+    from oracle import parallel
+    threads = threads or parallel.host_threads()
+    import torch
+    row = case.Hk * case.D * case.k_pool.element_size() * 2
+    kv = int(lens.to(torch.int64).sum()) * row
+    times = []
+    while True:
         t0 = time.perf_counter()
-        orc.decode_two_pass(case.q, case.k_pool, case.v_pool, tables, lens, case.scale,
-                            seq_ids=[s])
-        t_total += time.perf_counter() - t0
-        done_bytes += int(lens[s]) * row
-        n += 1
-    return done_bytes, t_total, n
+        parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, tables, lens, case.scale,
+                                 threads=threads)
+        times.append(time.perf_counter() - t0)
+        if sum(times) + times[-1] > budget_s or len(times) >= 50:
+            break
+    return kv, statistics.median(times), len(times), threads
 
 
 def run_reference(args):
-    """The reference arm: the fp64 oracle timed on the host cores, each step a
-    bounded sample (a few heads of one sequence) of the same workload."""
+    """The reference arm: the fp64 oracle timed on the host cores (threaded
+    over sequences and heads), each step the whole decode step of the
+    workload, or an equal share of its sequences when K + W whole steps
+    would not end within about two minutes."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import torch
     from oracle import build as ob
-    from oracle import oracle as orc
+    from oracle import parallel
     from paged_kv_decode_26_gb300 import workloads as wl
     ob.build()
-    torch.set_num_threads(1)
-    case = wl.make_case(args.config)
+    threads = parallel.host_threads()
+    case = wl.make_case(args.config, **({"pool_extra": 0.01} if args.config == 4 else {}))
     lens = case.context_lens
-    # choose the per-step sample: h heads of the longest-running sequence
-    s = int(torch.argmax(lens))
-    heads = case.H
+    row = case.Hk * case.D * case.k_pool.element_size() * 2
     t0 = time.perf_counter()
-    orc.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables, lens, case.scale,
-                        seq_ids=[s])
-    t_seq = time.perf_counter() - t0
-    budget = 90.0 / max(1, args.steps + args.warmup)
-    h = max(1, min(heads, int(heads * budget / max(t_seq, 1e-6))))
-    G = case.H // case.Hk
-    hk = max(1, h // G)
-    h = hk * G
-    # compact sub-case: the sequence's blocks, the first hk kv heads
-    nb = (int(lens[s]) + case.B - 1) // case.B
-    ids = case.block_tables[s, :nb].long()
-    k_sub = case.k_pool[ids][:, :, :hk].contiguous()
-    v_sub = case.v_pool[ids][:, :, :hk].contiguous()
-    q_sub = case.q[s:s + 1, :h].contiguous()
-    bt_sub = torch.arange(nb, dtype=torch.int32).view(1, nb)
-    l_sub = lens[s:s + 1].clone()
-    step_bytes = int(lens[s]) * hk * case.D * 2 * 2
-    for _ in range(args.warmup):
-        orc.decode_two_pass(q_sub, k_sub, v_sub, bt_sub, l_sub, case.scale)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        orc.decode_two_pass(q_sub, k_sub, v_sub, bt_sub, l_sub, case.scale)
-    dt = time.perf_counter() - t0
-    ms = dt / max(1, args.steps) * 1e3
-    value = step_bytes / (ms / 1e3) / 1e9
-    sample = (f"per step: sequence {s} ({int(lens[s])} tokens), {h} of {case.H} query heads "
-              f"({hk} kv heads), fp64 two-pass oracle, single thread")
+    parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables, lens,
+                             case.scale, threads=threads)
+    t_full = time.perf_counter() - t0
+    n_runs = max(1, args.steps + args.warmup)
+    frac = min(1.0, 120.0 / (n_runs * max(t_full, 1e-6)))
+    n_seq = max(1, int(round(case.S * frac)))
+    # every step takes the next n_seq sequences (cyclically), so the steps
+    # together cover the workload's length mix
+    order = list(range(case.S))
+
+    def seqs_of(i):
+        return [order[(i * n_seq + k) % case.S] for k in range(n_seq)]
+
+    for i in range(args.warmup):
+        parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables, lens,
+                                 case.scale, seq_ids=seqs_of(i), threads=threads)
+    total_b, total_t = 0, 0.0
+    for i in range(args.steps):
+        sel = seqs_of(args.warmup + i)
+        t0 = time.perf_counter()
+        parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables, lens,
+                                 case.scale, seq_ids=sel, threads=threads)
+        total_t += time.perf_counter() - t0
+        total_b += int(lens[sel].to(torch.int64).sum()) * row
+    ms = total_t / max(1, args.steps) * 1e3
+    value = total_b / max(total_t, 1e-9) / 1e9
+    sample = (f"per step: {n_seq} of {case.S} sequences of the step (all {case.H} heads), "
+              f"fp64 two-pass oracle on {threads} host threads" +
+              ("" if n_seq == case.S else "; consecutive steps take consecutive sequences"))
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(case, args.config, args.lens)},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -426,34 +434,16 @@ def run_multi_query(args):
         "dtype": "bf16 in, f32 accumulate"}), flush=True)
 
 
-def main():
-    args = parse_args()
-    if args.impl == "reference":
-        run_reference(args)
-        return
-    if args.multi_query:
-        run_multi_query(args)
-        return
-
+def measure(args, rank, world, dev, pkv, wl, *, full):
+    """Times one workload (args.config, args.replicas, args.batched, ...):
+    the step, then the decode call alone; with `full` also the clock record,
+    the end-to-end step through the public API and (continuous-batching
+    workload) the device-side allocation.  The block copies of the
+    continuous-batching workload are timed either way.  Returns a dict of
+    figures; rank 0 holds the job-wide ones."""
     import numpy as np
     import torch
     import torch.distributed as dist
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    from paged_kv_decode_26_gb300 import build as lib_build
-    if rank == 0:
-        lib_build.build()
-    if world > 1:
-        dist.barrier()
-    import paged_kv_decode_26_gb300 as pkv
-    from paged_kv_decode_26_gb300 import workloads as wl
 
     reps, host, devb = build_replicas(args, rank, dev, pkv, wl, torch, np)
     R = len(reps)
@@ -598,9 +588,10 @@ def main():
     else:
         run_step, run_decode = step_eager, decode_eager
 
-    sampler = ClockSampler(gpu_id_for_smi(torch, local))
-    sampler.start()
-    time.sleep(0.3)
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev.index or 0)) if full else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     step_events = [(ev(), ev()) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
@@ -624,12 +615,14 @@ def main():
         ms = t_start.elapsed_time(t_end) / max(1, args.steps)
     if world > 1:
         dist.barrier()
-    # keep the GPU under the same load until the sampler has ~1.5 s of samples
-    while time.perf_counter() - wall0 < 1.5:
-        for _ in range(20):
-            run_step()
-        torch.cuda.synchronize()
-    clocks = sampler.stop()
+    clocks = None
+    if sampler:
+        # keep the GPU under the same load until the sampler has ~1.5 s of samples
+        while time.perf_counter() - wall0 < 1.5:
+            for _ in range(20):
+                run_step()
+            torch.cuda.synchronize()
+        clocks = sampler.stop()
 
     # ---- the decode call alone (the dominant kernel), timed per launch
     dec_events = [(ev(), ev()) for _ in range(args.steps)]
@@ -696,12 +689,13 @@ def main():
             "timing": "median of per-call CUDA events, L2 flushed before each; "
                       "K and V in one swap_blocks_kv launch",
         }
+        del src_d, dst_d, src_h, dst_h
 
     # ---- the step's allocation on the device (continuous-batching workload):
     # pkv_device_append_slots from the pre-step state, restored before each
     # timed call
     dev_alloc = None
-    if with_swaps and rank == 0:
+    if full and with_swaps and rank == 0:
         r0 = reps[0]
         c0 = r0["case"]
         refs = torch.zeros(c0.num_blocks, dtype=torch.int32)
@@ -736,118 +730,221 @@ def main():
                      "matches_host_manager": bool(same)}
 
     # ---- end to end through the public API with host buffers
-    h2d_bytes = host["inputs"].numel()        # the staging buffer, copied whole
-    d2h_bytes = host["out"].numel() * host["out"].element_size()
+    e2e = None
+    if full:
+        h2d_bytes = host["inputs"].numel()        # the staging buffer, copied whole
+        d2h_bytes = host["out"].numel() * host["out"].element_size()
 
-    def e2e_step():
-        devb["inputs"].copy_(host["inputs"], non_blocking=True)
-        run_step()
-        host["out"].copy_(devb["out"], non_blocking=True)
-        stream.synchronize()
+        def e2e_step():
+            devb["inputs"].copy_(host["inputs"], non_blocking=True)
+            run_step()
+            host["out"].copy_(devb["out"], non_blocking=True)
+            stream.synchronize()
 
-    for _ in range(3):
-        e2e_step()
-    n_e2e = max(1, min(args.e2e_steps, args.steps))
+        for _ in range(3):
+            e2e_step()
+        n_e2e = max(1, min(args.e2e_steps, args.steps))
+        if world > 1:
+            dist.barrier()
+        e2e_times = []
+        for i in range(n_e2e):
+            if flush_mode:
+                flush_buf.fill_(i & 255)
+            a, b = ev(), ev()
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            torch.cuda.synchronize()
+            e2e_times.append(a.elapsed_time(b))
+        e2e_ms = statistics.mean(e2e_times)
+        e2e_ms, = reduce_over_ranks([e2e_ms], "max", dist, world, dev)
+        e2e = {"value": job_gbs(total_kv, e2e_ms), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "ms_per_step": e2e_ms, "steps": n_e2e}
+
+    return dict(case=case, reps=reps, R=R, S=S, ms=ms, dec_ms=dec_ms, kv_read=kv_read,
+                kv_unique=kv_unique, io_bytes=io_bytes, total_kv=total_kv,
+                decode_alg_bytes=decode_alg_bytes, split_used=split_used,
+                launches_per_step=launches_per_step, flush_mode=flush_mode, use_graph=use_graph,
+                with_swaps=with_swaps, swap_bytes=swap_bytes, swap=swap, dev_alloc=dev_alloc,
+                clocks=clocks, e2e=e2e)
+
+
+def release(res):
+    """Drops a measured workload's device and pinned buffers."""
+    import gc
+    import torch
+    res.pop("reps", None)
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+# Other stated workloads measured after the headline one, each as
+# (label, config, replicas, batched).  The tiny workload reads 0.9 MB per
+# step, so it is reported per launch and as 1100 independent problems in
+# one batched launch (~1 GB of distinct pools per step).
+PER_CONFIG = [("tiny_per_launch", 1, 1, False), ("tiny_batched_x1100", 1, 1100, True),
+              ("gqa_prefix", 3, 1, False), ("long_context", 4, 1, False),
+              ("continuous", 5, 1, False)]
+
+
+def per_config_entry(args, res, peak, cpu_budget):
+    """Summary of one extra workload: decode GB/s and roofline fraction,
+    step GB/s, sequence-steps per second, and the threaded oracle's GB/s on
+    the same inputs (one replica's whole step)."""
+    case = res["case"]
+    dec_gbs = res["decode_alg_bytes"] / (res["dec_ms"] / 1e3) / 1e9
+    e = {"workload": workload_name(case, args.config),
+         "replicas": res["R"], "launch": ("batched" if args.batched else
+                                          "graph" if res["use_graph"] else "eager"),
+         "decode_ms": res["dec_ms"], "decode_gbs": dec_gbs,
+         "roofline_frac": dec_gbs / peak,
+         "decode_bytes": res["decode_alg_bytes"],
+         "step_ms": res["ms"], "step_gbs": job_gbs(res["total_kv"], res["ms"]),
+         "seq_steps_per_s": res["R"] * res["S"] / (res["ms"] / 1e3),
+         "split_tokens": res["split_used"],
+         "l2": "flushed before every step" if res["flush_mode"] else "inputs larger than L2"}
+    if res["swap"]:
+        e["swap_blocks"] = res["swap"]
+    if cpu_budget > 0:
+        r0 = res["reps"][0]
+        kv, secs, runs, thr = oracle_step_seconds(case, r0["lens_h"], r0["bt_h"], cpu_budget)
+        e["oracle"] = {"gbs": kv / secs / 1e9, "threads": thr, "runs": runs,
+                       "sample": "one replica's whole step, fp64 two-pass oracle"}
+    return e
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if args.multi_query:
+        run_multi_query(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_decode_26_gb300 import build as lib_build
+    if rank == 0:
+        lib_build.build()
     if world > 1:
         dist.barrier()
-    e2e_times = []
-    for i in range(n_e2e):
-        if flush_mode:
-            flush_buf.fill_(i & 255)
-        a, b = ev(), ev()
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_times.append(a.elapsed_time(b))
-    e2e_ms = statistics.mean(e2e_times)
-    e2e_ms, = reduce_over_ranks([e2e_ms], "max", dist, world, dev)
+    import paged_kv_decode_26_gb300 as pkv
+    from paged_kv_decode_26_gb300 import workloads as wl
 
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
+    res = measure(args, rank, world, dev, pkv, wl, full=True)
+    case, R, S = res["case"], res["R"], res["S"]
+
+    # ---- CPU baseline: the oracle on the step (rank 0, N=1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import build as ob
         ob.build()
-        b, secs, nseq = oracle_sample_seconds(case, reps[0]["lens_h"], reps[0]["bt_h"],
-                                              args.cpu_budget)
-        cpu = {"value": b / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{nseq} of {S} sequences of the step (all {case.H} heads, "
-                         f"{b / 1e6:.1f} MB of K/V), fp64 two-pass oracle, single thread"}
-
-    if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
-        return
+        r0 = res["reps"][0]
+        kv, secs, runs, thr = oracle_step_seconds(case, r0["lens_h"], r0["bt_h"],
+                                                  args.cpu_budget)
+        cpu = {"value": kv / secs / 1e9, "unit": "GB/s", "cores": thr, "kind": "oracle",
+               "sample": f"the whole step ({S} sequences, all {case.H} heads, "
+                         f"{kv / 1e6:.1f} MB of K/V), fp64 two-pass oracle threaded over "
+                         f"{thr} host threads, median of {runs} runs"}
 
     peak, peak_kind = measured_peak()
     name = workload_name(case, args.config, args.lens)
-    value = job_gbs(total_kv, ms)
-    achieved = decode_alg_bytes / (dec_ms / 1e3) / 1e9
-    logical_gbs = (kv_read + io_bytes) / (dec_ms / 1e3) / 1e9
-    line = {
-        "metric": METRIC,
-        "value": value,
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": ms,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f32",
-        "data": "synthetic",
-        "seq_steps_per_s": R * S * world / (ms / 1e3),
-        "kv_bytes_per_step_all_gpus": total_kv,
-        "config": {
-            "workload": name,
-            "step": "paged_attn_decode_append (append 1 token/seq, then decode: one call)" +
-                    (" + swap_blocks_kv D2D and pinned-H2D on two side streams, overlapped"
-                     if with_swaps else ""),
-            "replicas_per_gpu": R,
-            "launch": ("one batched launch per step for all replicas "
-                       "(paged_attn_decode_batched)" if args.batched else
-                       f"one CUDA graph per step, replicas on {min(args.graph_streams, R)} "
-                       "parallel branches" if use_graph else "eager"),
-            "num_seqs_per_gpu": R * S,
-            "kv_bytes_per_step_per_gpu": kv_read,
-            "kv_unique_bytes_per_step_per_gpu": kv_unique,
-            "split_tokens": split_used,
-            "storage_dtype": str(case.dtype).replace("torch.", ""),
-            "out_dtype": str(case.out_dtype).replace("torch.", ""),
-            "l2": ("inputs larger than L2 (%.2f GB of K/V vs 129 MB), no flush" % (kv_read / 1e9)
-                   if not flush_mode else
-                   "L2 flushed (512 MB write) before every step, outside the timed events"),
-            "parallelism": f"replicas x{world} (sequences per GPU independent)",
-        },
-        "roofline": {
-            "bound": "hbm",
-            "achieved": achieved,
-            "peak": peak,
+    value = job_gbs(res["total_kv"], res["ms"])
+    achieved = res["decode_alg_bytes"] / (res["dec_ms"] / 1e3) / 1e9
+    logical_gbs = (res["kv_read"] + res["io_bytes"]) / (res["dec_ms"] / 1e3) / 1e9
+    line = None
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
             "unit": "GB/s",
-            "frac": achieved / peak,
-            "traffic": committed_traffic(name) if R == 1 else None,
-            "kernel": "paged_attn_decode (decode kernel + split merge), CUDA events per call" +
-                      (" (all replicas, one graph)" if use_graph else ""),
-            "bytes": "unique K/V rows read (shared prefix rows once) + q + out + tables",
-            "logical_gbs": logical_gbs,
-            "algorithmic_bytes_per_launch": decode_alg_bytes,
-            "ms_per_launch": dec_ms,
-            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6.8 TB/s",
-        },
-        "clocks": clocks,
-        "e2e": {"value": job_gbs(total_kv, e2e_ms), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-                "ms_per_step": e2e_ms, "steps": n_e2e},
-        "gpu_launches": launches_per_step * args.steps,
-        "cpu_baseline": cpu,
-    }
-    if with_swaps:
-        line["config"]["swap_bytes_per_step"] = swap_bytes
-        line["swap_blocks"] = swap
-        line["device_append_slots"] = dev_alloc
-    print(json.dumps(line), flush=True)
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": res["ms"],
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "seq_steps_per_s": R * S * world / (res["ms"] / 1e3),
+            "kv_bytes_per_step_all_gpus": res["total_kv"],
+            "config": {
+                "workload": name,
+                "step": "paged_attn_decode_append (append 1 token/seq, then decode: one call)" +
+                        (" + swap_blocks_kv D2D and pinned-H2D on two side streams, overlapped"
+                         if res["with_swaps"] else ""),
+                "replicas_per_gpu": R,
+                "launch": ("one batched launch per step for all replicas "
+                           "(paged_attn_decode_batched)" if args.batched else
+                           f"one CUDA graph per step, replicas on {min(args.graph_streams, R)} "
+                           "parallel branches" if res["use_graph"] else "eager"),
+                "num_seqs_per_gpu": R * S,
+                "kv_bytes_per_step_per_gpu": res["kv_read"],
+                "kv_unique_bytes_per_step_per_gpu": res["kv_unique"],
+                "split_tokens": res["split_used"],
+                "storage_dtype": str(case.dtype).replace("torch.", ""),
+                "out_dtype": str(case.out_dtype).replace("torch.", ""),
+                "l2": ("inputs larger than L2 (%.2f GB of K/V vs 129 MB), no flush"
+                       % (res["kv_read"] / 1e9) if not res["flush_mode"] else
+                       "L2 flushed (512 MB write) before every step, outside the timed events"),
+                "parallelism": f"replicas x{world} (sequences per GPU independent)",
+            },
+            "roofline": {
+                "bound": "hbm",
+                "achieved": achieved,
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": committed_traffic(name) if R == 1 else None,
+                "kernel": "paged_attn_decode (decode kernel + split merge), CUDA events per call" +
+                          (" (all replicas, one graph)" if res["use_graph"] else ""),
+                "bytes": "unique K/V rows read (shared prefix rows once) + q + out + tables",
+                "logical_gbs": logical_gbs,
+                "algorithmic_bytes_per_launch": res["decode_alg_bytes"],
+                "ms_per_launch": res["dec_ms"],
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+            },
+            "clocks": res["clocks"],
+            "e2e": res["e2e"],
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "cpu_baseline": cpu,
+        }
+        if res["with_swaps"]:
+            line["config"]["swap_bytes_per_step"] = res["swap_bytes"]
+            line["swap_blocks"] = res["swap"]
+            line["device_append_slots"] = res["dev_alloc"]
+    release(res)
+
+    # ---- the other stated workloads (single GPU, headline workload only)
+    if world == 1 and not args.no_per_config and args.config == 2 and not args.seqs \
+            and not args.lens and R == 1 and not args.batched and not args.graph:
+        per = {}
+        for label, cfg, reps_n, batched in PER_CONFIG:
+            sub = argparse.Namespace(**vars(args))
+            sub.config, sub.replicas, sub.batched, sub.graph = cfg, reps_n, batched, False
+            sub.split = 0
+            sub.steps = min(args.steps, 200)
+            r = measure(sub, rank, world, dev, pkv, wl, full=False)
+            per[label] = per_config_entry(sub, r, peak,
+                                          0.0 if args.no_cpu_baseline else min(args.cpu_budget,
+                                                                               6.0))
+            release(r)
+        line["per_config"] = per
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 

@@ -118,7 +118,7 @@ def test_swap_bulk_launch_shapes(lib, tuning, knobs, block_bytes, n):
 def test_swap_within_one_pool(lib):
     """Device-to-device inside one pool (disjoint sources and targets), as
     the copy-on-write and defragmentation moves use it."""
-    case = wl.make_case(5, S=32, lens=("uniform", 16, 64), d2d_pairs=200, h2d_pairs=4,
+    case = wl.make_case(5, S=256, lens=("uniform", 16, 64), d2d_pairs=200, h2d_pairs=4,
                         host_pool_blocks=8)
     dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
     pairs = case.d2d_pairs

@@ -561,3 +561,25 @@ def test_multi_query_matches_torch_sdpa_causal():
                                                                scale=0.25)
         np.testing.assert_allclose(got[int(qs[s]):int(qs[s + 1])], ref.permute(1, 0, 2).numpy(),
                                    rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------- threaded oracle driver
+
+@pytest.mark.parametrize("threads", [1, 3, 16])
+@pytest.mark.parametrize("H,Hk", [(8, 8), (8, 2)])
+def test_threaded_oracle_equals_one_call(threads, H, Hk):
+    """The thread-pool driver (whole sequences, or sequences cut into kv-head
+    ranges over compact pools) gives the single call's result exactly,
+    empty contexts and NaN padding included."""
+    from oracle import parallel
+    case = wl.make_case(3, S=5, lens_override=[0, 70, 1, 33, 200], H=H, Hk=Hk, D=64,
+                        share_blocks=2, poison=True, seed=H + Hk + threads)
+    ref = orc.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
+                              case.context_lens, case.scale)
+    got = parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
+                                   case.context_lens, case.scale, threads=threads)
+    assert np.array_equal(got, ref)
+    sub = parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
+                                   case.context_lens, case.scale, seq_ids=[4, 1],
+                                   threads=threads)
+    assert np.array_equal(sub, ref[[4, 1]])
