@@ -526,9 +526,16 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
         n_d2d, n_h2d = case.d2d_pairs.shape[0], case.h2d_pairs.shape[0]
         swap_bytes = R * 2 * 2 * bb * (n_d2d + n_h2d)
     # Workloads whose bytes fit in L2 are timed step by step with an L2
-    # flush (a 512 MB write) between steps, outside the timed events.
+    # flush between steps, outside the timed events: a read of a 512 MB
+    # buffer, which leaves the L2 holding clean lines of that buffer only (a
+    # flush by writing would leave dirty lines whose write-back the timed
+    # step would pay for).
     flush_mode = with_swaps or kv_read < 4 * L2_BYTES
-    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush_mode else None
+    flush_buf = torch.zeros(512 * 1024 * 1024 // 8, dtype=torch.int64, device=dev) \
+        if flush_mode else None
+
+    def flush_l2():
+        flush_buf.sum()
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -599,7 +606,7 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
     wall0 = time.perf_counter()
     if flush_mode:
         for i in range(args.steps):
-            flush_buf.fill_(i & 255)
+            flush_l2()
             step_events[i][0].record(stream)
             run_step()
             step_events[i][1].record(stream)
@@ -628,7 +635,7 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
     dec_events = [(ev(), ev()) for _ in range(args.steps)]
     for i in range(args.steps):
         if flush_mode:
-            flush_buf.fill_(i & 255)
+            flush_l2()
         dec_events[i][0].record(stream)
         run_decode()
         dec_events[i][1].record(stream)
@@ -663,7 +670,7 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
                               dst_d.copy_(src_d, non_blocking=True)), d2d_ref_t),
                     (lambda: (dst_h.copy_(src_h, non_blocking=True),
                               dst_h.copy_(src_h, non_blocking=True)), h2d_ref_t)):
-                flush_buf.fill_(i & 255)
+                flush_l2()
                 a, b = ev(), ev()
                 a.record(stream)
                 fn()
@@ -674,7 +681,36 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
         moved_d2d, moved_h2d = 2 * n_d2d * bb, 2 * n_h2d * bb       # K and V
         d2d_ms, h2d_ms = statistics.median(d2d_t), statistics.median(h2d_t)
         d2d_ref_ms, h2d_ref_ms = statistics.median(d2d_ref_t), statistics.median(h2d_ref_t)
+        # the asymptote: 8192 pairs of the same block size (1 GB moved)
+        n_big = 8192
+        big_k = torch.empty(2 * n_big, bb, dtype=torch.uint8, device=dev)
+        big_v = torch.empty(2 * n_big, bb, dtype=torch.uint8, device=dev)
+        perm = torch.randperm(2 * n_big, generator=torch.Generator().manual_seed(5))
+        big_pairs = torch.stack([perm[:n_big], perm[n_big:]], 1).to(dev)
+        big_src = torch.empty(2 * n_big * bb, dtype=torch.uint8, device=dev)
+        big_dst = torch.empty_like(big_src)
+        big_t, big_ref_t = [], []
+        for i in range(20):
+            for fn, acc in ((lambda: pkv.swap_blocks_kv(big_k, big_v, big_k, big_v, big_pairs),
+                             big_t),
+                            (lambda: big_dst.copy_(big_src, non_blocking=True), big_ref_t)):
+                flush_l2()
+                a, b = ev(), ev()
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                acc.append(a.elapsed_time(b))
+        big_ms, big_ref_ms = statistics.median(big_t), statistics.median(big_ref_t)
+        moved_big = 2 * 2 * n_big * bb                             # K and V, read + write
+        del big_k, big_v, big_src, big_dst
         swap = {
+            "d2d_8192_pairs": {"pairs": n_big, "block_bytes": bb, "ms_k_and_v": big_ms,
+                               "gbs_read_write": moved_big / (big_ms / 1e3) / 1e9,
+                               "vs_measured_copy_peak":
+                                   moved_big / (big_ms / 1e3) / 1e9 / peak_copy,
+                               "contiguous_copy_same_bytes_gbs_read_write":
+                                   moved_big / (big_ref_ms / 1e3) / 1e9},
             "d2d": {"pairs": n_d2d, "block_bytes": bb, "ms_k_and_v": d2d_ms,
                     "gbs_read_write": 2 * moved_d2d / (d2d_ms / 1e3) / 1e9,
                     "vs_measured_copy_peak": 2 * moved_d2d / (d2d_ms / 1e3) / 1e9 / peak_copy,
@@ -686,7 +722,7 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
                     "gbs": moved_h2d / (h2d_ms / 1e3) / 1e9,
                     "memcpy_h2d_same_bytes_gbs": moved_h2d / (h2d_ref_ms / 1e3) / 1e9,
                     "vs_memcpy": h2d_ref_ms / h2d_ms},
-            "timing": "median of per-call CUDA events, L2 flushed before each; "
+            "timing": "median of per-call CUDA events, L2 flushed (512 MB read) before each; "
                       "K and V in one swap_blocks_kv launch",
         }
         del src_d, dst_d, src_h, dst_h
@@ -749,7 +785,7 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
         e2e_times = []
         for i in range(n_e2e):
             if flush_mode:
-                flush_buf.fill_(i & 255)
+                flush_l2()
             a, b = ev(), ev()
             a.record(stream)
             e2e_step()
@@ -898,7 +934,7 @@ def main():
                 "out_dtype": str(case.out_dtype).replace("torch.", ""),
                 "l2": ("inputs larger than L2 (%.2f GB of K/V vs 129 MB), no flush"
                        % (res["kv_read"] / 1e9) if not res["flush_mode"] else
-                       "L2 flushed (512 MB write) before every step, outside the timed events"),
+                       "L2 flushed (512 MB read) before every step, outside the timed events"),
                 "parallelism": f"replicas x{world} (sequences per GPU independent)",
             },
             "roofline": {

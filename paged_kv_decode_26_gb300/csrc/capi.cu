@@ -1016,6 +1016,7 @@ pkv_status launch_swap(void* const* dst_pools, const void* const* src_pools, int
         p.chunks = (int)((block_bytes + chunk - 1) / chunk);
         p.n_pools = n_pools;
         p.stages = stages;
+        p.hint = tuning(PKV_TUNE_SWAP_HINT, 1) != 0 ? 1 : 0;
         p.errors = dev->errors;
         const size_t smem = (size_t)stages * chunk;
         static unsigned long long smem_done = 0;

@@ -118,6 +118,7 @@ struct BulkSwapParams {
     int chunks;             // per block
     int n_pools;
     int stages;
+    int hint;               // 1: loads and stores carry the L2 evict-first hint
     unsigned int* errors;
 };
 
@@ -143,6 +144,23 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint
             reinterpret_cast<uint64_t>(dst)),
         "r"(smem_addr(src_smem)), "r"(bytes), "l"(policy)
         : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_plain(void* dst_smem, const void* src, uint32_t bytes,
+                                                uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store_plain(void* dst, const void* src_smem,
+                                                 uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_addr(src_smem)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() {
@@ -223,8 +241,12 @@ __global__ void __launch_bounds__(32)
             for (int n = 0; n < pre; ++n) {
                 if (items[n].bytes) {
                     mbar_arrive_expect_tx(&full[n], items[n].bytes);
-                    bulk_load(bulk_smem + (size_t)n * p.chunk_bytes, items[n].src, items[n].bytes,
-                              &full[n], policy);
+                    if (p.hint)
+                        bulk_load(bulk_smem + (size_t)n * p.chunk_bytes, items[n].src,
+                                  items[n].bytes, &full[n], policy);
+                    else
+                        bulk_load_plain(bulk_smem + (size_t)n * p.chunk_bytes, items[n].src,
+                                        items[n].bytes, &full[n]);
                 } else {
                     mbar_arrive(&full[n]);
                 }
@@ -239,8 +261,12 @@ __global__ void __launch_bounds__(32)
                 phase_bits ^= 1u << slot;
                 if (items[n].bytes) {
                     fence_proxy_async_smem();
-                    bulk_store(items[n].dst, bulk_smem + (size_t)slot * p.chunk_bytes,
-                               items[n].bytes, policy);
+                    if (p.hint)
+                        bulk_store(items[n].dst, bulk_smem + (size_t)slot * p.chunk_bytes,
+                                   items[n].bytes, policy);
+                    else
+                        bulk_store_plain(items[n].dst, bulk_smem + (size_t)slot * p.chunk_bytes,
+                                         items[n].bytes);
                 }
                 bulk_commit();
                 // refill the slot of item n - 1 with item n - 1 + S once the
@@ -251,8 +277,12 @@ __global__ void __launch_bounds__(32)
                     const int ms = m % S;
                     if (items[m].bytes) {
                         mbar_arrive_expect_tx(&full[ms], items[m].bytes);
-                        bulk_load(bulk_smem + (size_t)ms * p.chunk_bytes, items[m].src,
-                                  items[m].bytes, &full[ms], policy);
+                        if (p.hint)
+                            bulk_load(bulk_smem + (size_t)ms * p.chunk_bytes, items[m].src,
+                                      items[m].bytes, &full[ms], policy);
+                        else
+                            bulk_load_plain(bulk_smem + (size_t)ms * p.chunk_bytes, items[m].src,
+                                            items[m].bytes, &full[ms]);
                     } else {
                         mbar_arrive(&full[ms]);
                     }

@@ -197,7 +197,7 @@ def test_tuning_knobs_are_explicit_and_not_read_from_the_environment(L):
         pkv.reset_tuning()
     assert pkv.get_tuning("decode_split") is None
     assert pkv.decode_split_tokens(1, 8, 8, 128, 16, 4097) == base
-    assert L.pkv_set_tuning(_lib.TUNE_KNOBS["swap_ctas"] + 1, 3) == 1     # PKV_ERR_INVALID
+    assert L.pkv_set_tuning(len(_lib.TUNE_KNOBS), 3) == 1         # PKV_ERR_INVALID
     assert L.pkv_set_tuning(-1, 3) == 1
     assert L.pkv_get_tuning(99) == _lib.TUNE_AUTO
     with pytest.raises(ValueError):

@@ -80,6 +80,7 @@ def test_swap_sizes_and_untouched_bytes(lib, block_bytes):
     {"swap_chunk": 4096, "swap_stages": 8, "swap_ctas": 4},
     {"swap_chunk": 65536, "swap_stages": 8},               # stages cut to fit shared memory
     {"swap_chunk": 24, "swap_stages": 3},                  # rounded down to 16 bytes
+    {"swap_hint": 0, "swap_chunk": 8192},                  # no L2 cache hints
     {"swap_bulk": 0},                                      # 16-byte load/store kernel
 ], ids=lambda k: ",".join(f"{a[5:]}={b}" for a, b in k.items()) or "auto")
 def test_swap_bulk_launch_shapes(lib, tuning, knobs, block_bytes, n):
