@@ -111,7 +111,8 @@ typedef enum pkv_tune_knob {
     PKV_TUNE_SWAP_STAGES = 14,    /* bulk block copy: copies in flight per CTA, 2..8 */
     PKV_TUNE_SWAP_CTAS = 15,      /* bulk block copy: CTAs per SM */
     PKV_TUNE_SWAP_HINT = 16,      /* bulk block copy L2 hint: 0 none, 1 evict-first */
-    PKV_TUNE_COUNT = 17
+    PKV_TUNE_DECODE_STREAM = 17,  /* 0/1: tensor-core decode by resident CTAs streaming units */
+    PKV_TUNE_COUNT = 18
 } pkv_tune_knob;
 
 /* Set one knob (value PKV_TUNE_AUTO restores the automatic choice).

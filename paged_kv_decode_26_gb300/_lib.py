@@ -27,7 +27,7 @@ TUNE_AUTO = -2147483648
 TUNE_KNOBS = {name: i for i, name in enumerate(
     ["decode_mma", "decode_hpc", "decode_stages", "decode_wpt", "decode_qpw", "decode_split",
      "decode_order", "decode_pdl", "mq_tc", "mq_tc_stages", "mq_lpt", "mq_stages", "swap_bulk",
-     "swap_chunk", "swap_stages", "swap_ctas", "swap_hint"])}
+     "swap_chunk", "swap_stages", "swap_ctas", "swap_hint", "decode_stream"])}
 
 # Every symbol include/pagedkv.h declares, with (restype, argtypes).
 _p, _i, _i32, _i64, _sz, _f = C.c_void_p, C.c_int, C.c_int32, C.c_int64, C.c_size_t, C.c_float

@@ -18,6 +18,7 @@
 #include "copy_kernels.cuh"
 #include "decode_batched.cuh"
 #include "decode_launch.h"
+#include "decode_stream_kernel.cuh"
 
 // ----------------------------------------------------------------- errors
 
@@ -472,6 +473,27 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
 
 namespace {
 
+// Whether the tensor-core decode runs as resident CTAs streaming the work
+// units (paged_decode_mma_stream_kernel) instead of one CTA per unit, and
+// that kernel's shared memory.  It needs the tensor-core consumer, at most
+// kStreamMaxSeqs sequences (their lengths live in shared memory) and page
+// counts that fit 32 bits.  The PKV_TUNE_DECODE_STREAM knob chooses; by
+// default it is off.
+bool use_stream(const DecodeConfig& c, int num_seqs, int n_kv_heads, int head_dim,
+                int block_size, int max_context_len, pkv_dtype kv_dtype, int group,
+                const DeviceInfo* dev, size_t* smem) {
+    if (!c.mma || c.wpt != 1 || num_seqs > pkv::kStreamMaxSeqs) return false;
+    if (tuning(PKV_TUNE_DECODE_STREAM, 0) == 0) return false;
+    const long long pages = ((long long)max_context_len + block_size - 1) / block_size;
+    if ((long long)num_seqs * n_kv_heads * pages > 0x7fffffffLL) return false;
+    (void)kv_dtype;
+    const size_t bytes = pkv::decode_stream_smem_bytes(head_dim, block_size, group, 2, c.hpc,
+                                                       c.stages, c.max_pages, num_seqs);
+    if (bytes > (size_t)dev->smem_optin) return false;
+    *smem = bytes;
+    return true;
+}
+
 // paged_attn_decode, with the append of paged_attn_decode_append fused in
 // when slot_mapping is not NULL.
 pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void* k_pool,
@@ -576,9 +598,14 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
     L.block = dim3((unsigned)c.threads);
     L.smem_bytes = c.smem;
     L.stream = static_cast<cudaStream_t>(stream);
+    L.sm_count = dev->sm_count;
     if (c.max_splits > 65535 * 1024) return unsupported("context too long for the grid");
 
-    if (c.mma)
+    if (use_stream(c, num_seqs, n_kv_heads, head_dim, block_size, max_context_len, kv_dtype,
+                   n_heads / n_kv_heads, dev, &L.smem_bytes))
+        e = kv_dtype == PKV_BF16 ? pkv::launch_decode_stream_bf16(head_dim, block_size, L)
+                                 : pkv::launch_decode_stream_f16(head_dim, block_size, L);
+    else if (c.mma)
         e = kv_dtype == PKV_BF16 ? pkv::launch_decode_mma_bf16(head_dim, block_size, L)
                                  : pkv::launch_decode_mma_f16(head_dim, block_size, L);
     else

@@ -3,4 +3,5 @@
 #define PKV_FN launch_decode_bf16
 #define PKV_MMA_FN launch_decode_mma_bf16
 #define PKV_MQ_FN launch_multi_query_bf16
+#define PKV_STREAM_FN launch_decode_stream_bf16
 #include "decode_inst.inc"

@@ -1,0 +1,527 @@
+// decode_stream_kernel.cuh -- paged single-query attention for grouped-query
+// heads on the tensor cores, one CTA streaming many work units (sm_103a).
+// Same inputs, outputs and arithmetic per unit as paged_decode_mma_kernel.
+//
+// Pages followed (cited by title and section):
+//   [SWAP]   "vLLM 中 FlashAttention 与 KVCache 交换机制深度解析": the attention
+//            formula, Tiling + Kernel Fusion + the OnlineSoftmax recurrence,
+//            MQA/GQA by indexing.
+//   [LAYOUT] "大模型长文本推理基座从 FlashAttention 硬件加速机制到 vLLM 核心
+//            PagedAttention 显存物理布局深度剖析", section 二.2: block table.
+//
+// Why: with many short contexts (a continuous-batching step: most sequences
+// hold 1-4 pages), a CTA per (sequence, head group, split) spends its life on
+// one dependent chain -- context length, block ids, page loads, a few pages
+// of work -- and the SMs wait on latency instead of streaming HBM.  Here a
+// grid of resident CTAs covers the work instead: the units (sequence s,
+// split k, head group h) are laid out one after another, each weighing its
+// page count, and CTA c takes the units that start in the c-th equal share
+// of the total pages.  Its producer warp walks those units in order and
+// keeps the page ring full across unit boundaries: while the consumers
+// finish one unit's pages, the next unit's block ids are looked up and its
+// pages (and its query rows) are already loading.  Each ring slot carries a
+// small record of the unit it belongs to; a consumer starts a unit (query
+// fragments from the slot, fresh state) on the unit's first page and writes
+// its output (or split partial) after the last.  A record with no pages
+// ends the stream.  Sequences with an empty context get their zero rows
+// from the CTA whose share holds their (empty) place in the layout.
+#pragma once
+
+#include "decode_mma_kernel.cuh"
+
+namespace pkv {
+
+constexpr int kStreamMaxSeqs = 2048;   // context lengths held in shared memory
+
+// What the producer tells the consumers about the page in one ring slot.
+struct StreamSlot {
+    int s;          // sequence (-1: end of the stream)
+    int hg;         // kv-head group
+    int split;      // split of the sequence
+    int page;       // page of the unit (0 = first: query rows in the slot)
+    int n_pages;    // pages of the unit
+    int n_splits;   // splits of the sequence
+    int tok_begin;  // first token of the unit
+    int tok_end;    // one past its last token
+    int valid;      // the page's block id was in range (else the page is skipped)
+};
+
+// Shared memory of one CTA (must match the carve-up in the kernel): 1 KB
+// alignment slack, the ring of K/V pages, the query rows of each slot,
+// barriers, slot records, block ids of one unit, the clamped lengths and
+// their page prefix sums, a few words.
+inline size_t decode_stream_smem_bytes(int D, int BS, int G, int elem_bytes, int hpc,
+                                       int stages, int max_pages_per_split, int num_seqs) {
+    const size_t ring = (size_t)stages * 2 * hpc * D * BS * elem_bytes;
+    const size_t qs = (size_t)stages * hpc * G * D * elem_bytes;
+    return 1024 + ring + qs + (size_t)stages * 2 * sizeof(uint64_t) +
+           (size_t)stages * sizeof(StreamSlot) + (size_t)max_pages_per_split * sizeof(int) +
+           (size_t)(2 * num_seqs + 2) * sizeof(int) + 8 * sizeof(int);
+}
+
+__device__ __forceinline__ void bulk_load_q(void* dst_smem, const void* src, uint32_t bytes,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+template <int D, int BS, typename T>
+__global__ void __launch_bounds__(kMmaMaxThreads, 1)
+    paged_decode_mma_stream_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                   const __grid_constant__ CUtensorMap tm_v,
+                                   const __grid_constant__ DecodeParams p) {
+    constexpr int HALVES = D / 64;        // 128-byte boxes per token row
+    constexpr int KSTEPS = D / 16;        // k-steps of the score MMA
+    constexpr int NT = D / 8;             // n-tiles of the P V MMA
+    constexpr uint32_t BOX = BS * 128;    // bytes of one [BS x 64] box
+    static_assert(BS % 16 == 0 && D % 64 == 0, "shape");
+
+    launch_dependents();  // the split merge may start its CTAs (they wait)
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+
+    const int HPC = p.heads_per_cta;
+    const int G = p.group;
+    const int S = p.num_seqs;
+    const int stages = p.stages;
+    const int PPS = p.split_tokens / BS;   // pages per full split
+    if ((int)blockDim.x != 32 * (1 + HPC) || G > 8 || p.warps_per_tok != 1 || S > kStreamMaxSeqs ||
+        stages < 2 || stages > 16 || PPS > p.max_pages_per_split || PPS < 1) {
+        if (threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONFIG);
+        return;
+    }
+    const int HG = p.n_kv_heads / HPC;
+
+    // ---- shared memory
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    unsigned char* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t head_bytes = HALVES * BOX;              // one kv head's K (or V) page
+    const uint32_t stage_bytes = 2 * HPC * head_bytes;     // K then V for HPC heads
+    const uint32_t q_bytes = (uint32_t)(HPC * G * D * sizeof(T));   // query rows of a unit
+    unsigned char* ring = smem;
+    unsigned char* qbuf = ring + (size_t)stages * stage_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(qbuf + (size_t)stages * q_bytes);
+    uint64_t* empty = full + stages;
+    StreamSlot* slot = reinterpret_cast<StreamSlot*>(empty + stages);
+    int* s_bid = reinterpret_cast<int*>(slot + stages);
+    int* s_len = s_bid + p.max_pages_per_split;      // clamped context lengths [S]
+    int* s_pref = s_len + S;                         // page prefix sums [S + 1]
+    int* s_var = s_pref + S + 1;                     // first sequence, abort, issued, warp sums
+
+    const int cap = min(p.max_blocks_per_seq * BS, p.max_splits * p.split_tokens);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- layout of the work: W_s = HG x pages of sequence s, prefix sums
+    // (one pass: each thread a contiguous run of sequences, then a scan of
+    // the per-thread sums through warp shuffles and shared memory)
+    {
+        const int nt = (int)blockDim.x;
+        const int per = (S + nt - 1) / nt;
+        const int lo = min(S, (int)threadIdx.x * per);
+        const int hi = min(S, lo + per);
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) {
+            int n = p.context_lens[i];
+            if (n < 0 || n > cap) {
+                if (blockIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONTEXT);
+                n = n < 0 ? 0 : cap;
+            }
+            s_len[i] = n;
+            sum += HG * ((n + BS - 1) / BS);
+        }
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += a;
+        }
+        __shared__ int warp_tot[kMmaMaxWarps + 1];
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int before = incl - sum;
+        for (int w = 0; w < warp; ++w) before += warp_tot[w];
+        int run = before;
+        for (int i = lo; i < hi; ++i) {
+            s_pref[i] = run;
+            run += HG * ((s_len[i] + BS - 1) / BS);
+        }
+        if (threadIdx.x == nt - 1) s_pref[S] = run;
+        __syncthreads();
+    }
+    const long long P = s_pref[S];
+    const long long C = gridDim.x;
+    const long long P0 = P * blockIdx.x / C;
+    const long long P1 = P * (blockIdx.x + 1) / C;
+    const bool last_cta = blockIdx.x == gridDim.x - 1;
+
+    // ---- empty contexts: zero rows, written by the CTA whose share holds
+    // the sequence's place (the last CTA for places at the very end)
+    for (int i = threadIdx.x; i < S * HG; i += blockDim.x) {
+        const int s = i / HG;
+        if (s_len[s] != 0) continue;
+        const long long at = s_pref[s];
+        if (!((at >= P0 && at < P1) || (at >= P && last_cta))) continue;
+        const int hg = i - s * HG;
+        if (p.slot_mapping != nullptr) {
+            // an append into an empty context (its length not counting the
+            // token) still writes the row, as the per-unit kernels do
+            const int64_t slot_row = p.slot_mapping[s];
+            if (slot_row >= (int64_t)p.num_blocks * BS) {
+                if (hg == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
+            } else if (slot_row >= 0) {
+                constexpr int VEC = 16 / (int)sizeof(T);
+                const size_t row = (size_t)p.n_kv_heads * D;
+                const size_t off_new = (size_t)s * row + (size_t)hg * HPC * D;
+                const size_t off_pool = (size_t)slot_row * row + (size_t)hg * HPC * D;
+                for (int j = 0; j < HPC * D; j += VEC) {
+                    *reinterpret_cast<uint4*>(static_cast<T*>(p.k_pool) + off_pool + j) =
+                        *reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + off_new + j);
+                    *reinterpret_cast<uint4*>(static_cast<T*>(p.v_pool) + off_pool + j) =
+                        *reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + off_new + j);
+                }
+            }
+        }
+        const int q0 = hg * HPC * G;
+        for (int qh = q0; qh < q0 + HPC * G; ++qh) {
+            const size_t e = ((size_t)s * p.n_heads + qh) * D;
+            if (p.out_dtype == PKV_F32) {
+                float* o = reinterpret_cast<float*>(p.out) + e;
+                for (int d = 0; d < D; ++d) o[d] = 0.f;
+            } else {
+                uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + e;
+                for (int d = 0; d < D; ++d) o[d] = 0;
+            }
+        }
+    }
+
+    // first sequence whose pages reach into [P0, P1): the last s with
+    // pref[s] <= P0 (binary search; sequences of no pages are skipped later)
+    if (threadIdx.x == 0) {
+        int a = 0, b = S - 1, f = 0;
+        while (a <= b) {
+            const int m = (a + b) >> 1;
+            if ((long long)s_pref[m] <= P0) {
+                f = m;
+                a = m + 1;
+            } else {
+                b = m - 1;
+            }
+        }
+        s_var[0] = f;
+        s_var[1] = 0;   // abort
+        s_var[2] = 0;   // slots issued
+        for (int st = 0; st < stages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], HPC);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    volatile int* s_abort = s_var + 1;
+
+    if (warp == 0) {
+        // ================= producer =================
+        const uint64_t policy = l2_policy_evict_first();
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        int g = 0;             // slots issued so far
+        bool stop = false;
+        for (int s = s_var[0]; s < S && !stop; ++s) {
+            const long long Ps = s_pref[s];
+            if (Ps >= P1) break;
+            const int n = s_len[s];
+            if (n == 0) continue;
+            const int np = (n + BS - 1) / BS;
+            const int n_splits = max(1, (n + p.split_tokens - 1) / p.split_tokens);
+            for (int k = 0; k < n_splits && !stop; ++k) {
+                const int npk = min(PPS, np - k * PPS);
+                for (int hg = 0; hg < HG && !stop; ++hg) {
+                    const long long start = Ps + (long long)HG * k * PPS + (long long)hg * npk;
+                    if (start < P0) continue;
+                    if (start >= P1) {
+                        stop = true;
+                        break;
+                    }
+                    // ---- the unit's block ids (whole warp)
+                    const int page0 = k * PPS;
+                    for (int i = lane; i < npk; i += 32) {
+                        int b = p.block_tables[(size_t)s * p.max_blocks_per_seq + page0 + i];
+                        if (b < 0 || b >= p.num_blocks) {
+                            raise_error(p.errors, PKV_DEVERR_BLOCK_ID);
+                            b = -1;
+                        }
+                        s_bid[i] = b;
+                    }
+                    // ---- fused append: the last split's unit writes the new
+                    // token's rows of its heads before any of its pages load
+                    if (p.slot_mapping != nullptr && k == n_splits - 1) {
+                        const int64_t slot_row = p.slot_mapping[s];
+                        if (slot_row >= 0 && slot_row < (int64_t)p.num_blocks * BS) {
+                            constexpr int VEC = 16 / (int)sizeof(T);
+                            const int per_row = HPC * D / VEC;
+                            const size_t row = (size_t)p.n_kv_heads * D;
+                            const size_t off_new = (size_t)s * row + (size_t)hg * HPC * D;
+                            const size_t off_pool = (size_t)slot_row * row + (size_t)hg * HPC * D;
+                            for (int i = lane; i < 2 * per_row; i += 32) {
+                                const bool is_v = i >= per_row;
+                                const int j = (is_v ? i - per_row : i) * VEC;
+                                const T* src =
+                                    static_cast<const T*>(is_v ? p.v_new : p.k_new) + off_new + j;
+                                T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) + off_pool + j;
+                                *reinterpret_cast<uint4*>(dst) =
+                                    *reinterpret_cast<const uint4*>(src);
+                            }
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                        } else if (slot_row >= 0 && hg == 0 && lane == 0) {
+                            raise_error(p.errors, PKV_DEVERR_SLOT);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        const int tok_begin = k * p.split_tokens;
+                        const int tok_end = min(n, tok_begin + p.split_tokens);
+                        const T* qsrc = reinterpret_cast<const T*>(p.q) +
+                                        ((size_t)s * p.n_heads + (size_t)hg * HPC * G) * D;
+                        for (int i = 0; i < npk; ++i, ++g) {
+                            const int st = g % stages;
+                            if (g >= stages &&
+                                !mbar_wait(&empty[st], ((g / stages) - 1) & 1, p.errors)) {
+                                *s_abort = 1;
+                                stop = true;
+                                break;
+                            }
+                            if (*s_abort) {
+                                stop = true;
+                                break;
+                            }
+                            const int b = s_bid[i];
+                            StreamSlot& r = slot[st];
+                            r.s = s;
+                            r.hg = hg;
+                            r.split = k;
+                            r.page = i;
+                            r.n_pages = npk;
+                            r.n_splits = n_splits;
+                            r.tok_begin = tok_begin;
+                            r.tok_end = tok_end;
+                            r.valid = b >= 0;
+                            const uint32_t bytes = (b >= 0 ? stage_bytes : 0u) + (i == 0 ? q_bytes : 0u);
+                            if (bytes == 0) {
+                                mbar_arrive(&full[st]);
+                                continue;
+                            }
+                            mbar_arrive_expect_tx(&full[st], bytes);
+                            if (i == 0)
+                                bulk_load_q(qbuf + (size_t)st * q_bytes, qsrc, q_bytes, &full[st],
+                                            policy);
+                            if (b >= 0) {
+                                unsigned char* dst = ring + (size_t)st * stage_bytes;
+                                for (int hh = 0; hh < HPC; ++hh) {
+                                    const int row = (hg * HPC + hh) * HALVES;
+                                    for (int h = 0; h < HALVES; ++h) {
+                                        tma_load_4d(dst + hh * head_bytes + h * BOX, &tm_k,
+                                                    &full[st], 0, row + h, 0, b, policy);
+                                        tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, &tm_v,
+                                                    &full[st], 0, row + h, 0, b, policy);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+                    __syncwarp();
+                }
+            }
+        }
+        // ---- end of the stream: a record without pages
+        if (lane == 0 && !*s_abort) {
+            const int st = g % stages;
+            if (g < stages || mbar_wait(&empty[st], ((g / stages) - 1) & 1, p.errors)) {
+                slot[st].s = -1;
+                mbar_arrive(&full[st]);
+                ++g;
+            } else {
+                *s_abort = 1;
+            }
+        }
+        if (lane == 0) s_var[2] = g;
+        __syncwarp();
+    } else {
+        // ================= consumers: one warp per kv head =================
+        const int kv_local = warp - 1;
+        const int gid = lane >> 2;     // fragment row (query head) of this lane
+        const int tig = lane & 3;      // pair of columns of this lane
+        const bool row_real = gid < G;
+        const int mat = lane >> 3;
+        const int mrow = lane & 7;
+        const int k_tok = (mat >> 1) * 8 + mrow;
+        const int k_dc = mat & 1;
+        const int v_tok = (mat & 1) * 8 + mrow;
+        const int v_dc = mat >> 1;
+
+        uint32_t qa[KSTEPS][4];
+        float o[NT][4];
+        float m_row = -INFINITY, l_part = 0.f;
+        for (int g = 0;; ++g) {
+            const int st = g % stages;
+            if (!mbar_wait(&full[st], (g / stages) & 1, p.errors)) {
+                *s_abort = 1;
+                break;
+            }
+            const StreamSlot r = slot[st];
+            if (r.s < 0) break;
+            if (r.page == 0) {
+                // query rows of this unit's kv head: rows = query heads
+                const T* qrow = reinterpret_cast<const T*>(qbuf + (size_t)st * q_bytes) +
+                                ((size_t)kv_local * G + (row_real ? gid : 0)) * D;
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    const uint32_t lo = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + tig * 2);
+                    const uint32_t hi =
+                        *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + tig * 2);
+                    qa[ks][0] = row_real ? lo : 0u;
+                    qa[ks][1] = 0u;
+                    qa[ks][2] = row_real ? hi : 0u;
+                    qa[ks][3] = 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+                m_row = -INFINITY;
+                l_part = 0.f;
+            }
+            if (r.valid) {
+                const uint32_t kbase = smem_addr(ring + (size_t)st * stage_bytes +
+                                                 kv_local * head_bytes);
+                const uint32_t vbase = smem_addr(ring + (size_t)st * stage_bytes +
+                                                 (HPC + kv_local) * head_bytes);
+                const int page_tok = r.tok_begin + r.page * BS;
+#pragma unroll
+                for (int ch = 0; ch < BS / 16; ++ch) {
+                    const int valid = min(16, r.tok_end - (page_tok + ch * 16));
+                    if (valid <= 0) break;
+                    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int ks = 0; ks < KSTEPS; ++ks) {
+                        const int h = ks / 4;
+                        const int c = (ks % 4) * 2 + k_dc;
+                        const int t = ch * 16 + k_tok;
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kbase + h * BOX + swz(t, c), b0, b1, b2, b3);
+                        mma16816<T>(sc[0], qa[ks], b0, b1);
+                        mma16816<T>(sc[1], qa[ks], b2, b3);
+                    }
+                    float x[4];
+                    x[0] = sc[0][0] * p.scale_log2;
+                    x[1] = sc[0][1] * p.scale_log2;
+                    x[2] = sc[1][0] * p.scale_log2;
+                    x[3] = sc[1][1] * p.scale_log2;
+                    if (tig * 2 >= valid) x[0] = -INFINITY;
+                    if (tig * 2 + 1 >= valid) x[1] = -INFINITY;
+                    if (8 + tig * 2 >= valid) x[2] = -INFINITY;
+                    if (8 + tig * 2 + 1 >= valid) x[3] = -INFINITY;
+                    float cmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
+                    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
+                    const float m_new = fmaxf(m_row, cmax);
+                    const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+                    const float alpha = exp2f(m_row - mu);
+                    m_row = m_new;
+                    const float p0 = exp2f(x[0] - mu), p1 = exp2f(x[1] - mu);
+                    const float p2 = exp2f(x[2] - mu), p3 = exp2f(x[3] - mu);
+                    l_part = l_part * alpha + ((p0 + p1) + (p2 + p3));
+                    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+                    if (valid < 16) {
+                        vm0 = (tig * 2 < valid ? 0x0000ffffu : 0u) |
+                              (tig * 2 + 1 < valid ? 0xffff0000u : 0u);
+                        vm1 = (8 + tig * 2 < valid ? 0x0000ffffu : 0u) |
+                              (8 + tig * 2 + 1 < valid ? 0xffff0000u : 0u);
+                    }
+                    uint32_t pa[4], pl[4];
+                    pa[0] = pack2<T>(p0, p1);
+                    pa[2] = pack2<T>(p2, p3);
+                    {
+                        const float2 h01 = unpack2<T>(pa[0]), h23 = unpack2<T>(pa[2]);
+                        pl[0] = pack2<T>(p0 - h01.x, p1 - h01.y);
+                        pl[2] = pack2<T>(p2 - h23.x, p3 - h23.y);
+                    }
+                    pa[1] = pa[3] = pl[1] = pl[3] = 0u;
+#pragma unroll
+                    for (int j = 0; j < NT; j += 2) {
+                        o[j][0] *= alpha;
+                        o[j][1] *= alpha;
+                        o[j + 1][0] *= alpha;
+                        o[j + 1][1] *= alpha;
+                        const int h = j / 8;
+                        const int c = (j % 8) + v_dc;
+                        const int t = ch * 16 + v_tok;
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_trans(vbase + h * BOX + swz(t, c), b0, b1, b2, b3);
+                        b0 &= vm0;
+                        b1 &= vm1;
+                        b2 &= vm0;
+                        b3 &= vm1;
+                        mma16816<T>(o[j], pa, b0, b1);
+                        mma16816<T>(o[j + 1], pa, b2, b3);
+                        mma16816<T>(o[j], pl, b0, b1);
+                        mma16816<T>(o[j + 1], pl, b2, b3);
+                    }
+                }
+            }
+            if (r.page == r.n_pages - 1) {
+                // ---- the unit's output (or split partial)
+                float l_row = l_part;
+                l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
+                l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+                if (row_real) {
+                    const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+                    const int qh = (r.hg * HPC + kv_local) * G + gid;
+                    if (r.n_splits == 1) {
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) {
+                            const size_t e = ((size_t)r.s * p.n_heads + qh) * D + j * 8 + tig * 2;
+                            if (p.out_dtype == PKV_F32) {
+                                *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.out) + e) =
+                                    make_float2(o[j][0] * inv, o[j][1] * inv);
+                            } else {
+                                *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) +
+                                                             e) =
+                                    pack_out(o[j][0] * inv, o[j][1] * inv, p.out_dtype);
+                            }
+                        }
+                    } else {
+                        const size_t unit =
+                            ((size_t)r.s * p.n_heads + qh) * p.max_splits + r.split;
+#pragma unroll
+                        for (int j = 0; j < NT; ++j)
+                            *reinterpret_cast<float2*>(p.ws_o + unit * D + j * 8 + tig * 2) =
+                                make_float2(o[j][0] * inv, o[j][1] * inv);
+                        if (tig == 0)
+                            *reinterpret_cast<float2*>(p.ws_ml + unit * 2) =
+                                make_float2(m_row, l_row);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+    }
+
+    __syncthreads();
+    if (*s_abort && threadIdx.x == 0) {
+        // loads still in flight land before the CTA's shared memory goes away
+        const int issued = s_var[2];
+        for (int st = 0; st < stages && st < issued; ++st) {
+            const int last = st + ((issued - 1 - st) / stages) * stages;
+            mbar_wait(&full[st], (last / stages) & 1, p.errors);
+        }
+    }
+}
+
+}  // namespace pkv
