@@ -106,7 +106,7 @@ typedef enum pkv_tune_knob {
     PKV_TUNE_MQ_TC_STAGES = 9,    /* tcgen05 multi-query ring depth */
     PKV_TUNE_MQ_LPT = 10,         /* 0/1: multi-query longest-context-first order off/on */
     PKV_TUNE_MQ_STAGES = 11,      /* mma.sync multi-query ring depth */
-    PKV_TUNE_SWAP_BULK = 12,      /* 0: device-to-device block copy by 16-byte loads and stores */
+    PKV_TUNE_SWAP_BULK = 12,      /* 1: device-to-device block copy by bulk copies (default 0) */
     PKV_TUNE_SWAP_CHUNK = 13,     /* bulk block copy: bytes per copy (multiple of 16) */
     PKV_TUNE_SWAP_STAGES = 14,    /* bulk block copy: copies in flight per CTA, 2..8 */
     PKV_TUNE_SWAP_CTAS = 15,      /* bulk block copy: CTAs per SM */

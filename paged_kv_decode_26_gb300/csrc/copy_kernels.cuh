@@ -12,10 +12,12 @@
 //     copied by separate calls.
 //
 // A row of one token (all kv heads) and a whole block are contiguous in the
-// [num_blocks, B, Hk, D] pool.  The append moves 16-byte vectors (every
-// warp access a coalesced 512-byte run); the block copy between device
-// pools moves whole blocks with bulk copies through shared memory, and
-// from pinned host memory with 16-byte vectors.
+// [num_blocks, B, Hk, D] pool.  The append and the block copy move 16-byte
+// vectors (every warp access a coalesced 512-byte run; a pinned-host source
+// is reached through unified addressing).  A second block-copy kernel
+// moves whole blocks between device pools with bulk copies through shared
+// memory; it measured a few percent behind the vector kernel on GB300 and
+// runs only when asked for (see capi.cu).
 #pragma once
 
 #include "pkv_device.cuh"

@@ -75,19 +75,20 @@ def test_swap_sizes_and_untouched_bytes(lib, block_bytes):
 @pytest.mark.parametrize("block_bytes,n", [(16, 300), (48, 23), (4096, 100), (40976, 23),
                                           (131072, 9)])
 @pytest.mark.parametrize("knobs", [
-    {},                                                    # automatic launch shape
-    {"swap_chunk": 16, "swap_stages": 2, "swap_ctas": 1},  # many chunks, several batches per CTA
-    {"swap_chunk": 4096, "swap_stages": 8, "swap_ctas": 4},
-    {"swap_chunk": 65536, "swap_stages": 8},               # stages cut to fit shared memory
-    {"swap_chunk": 24, "swap_stages": 3},                  # rounded down to 16 bytes
-    {"swap_hint": 0, "swap_chunk": 8192},                  # no L2 cache hints
-    {"swap_bulk": 0},                                      # 16-byte load/store kernel
-], ids=lambda k: ",".join(f"{a[5:]}={b}" for a, b in k.items()) or "auto")
+    {},                                                    # the default (16-byte loads/stores)
+    {"swap_bulk": 1},                                      # bulk copies, automatic launch shape
+    {"swap_bulk": 1, "swap_chunk": 16, "swap_stages": 2, "swap_ctas": 1},  # several batches per CTA
+    {"swap_bulk": 1, "swap_chunk": 4096, "swap_stages": 8, "swap_ctas": 4},
+    {"swap_bulk": 1, "swap_chunk": 65536, "swap_stages": 8},  # stages cut to fit shared memory
+    {"swap_bulk": 1, "swap_chunk": 24, "swap_stages": 3},  # rounded down to 16 bytes
+    {"swap_bulk": 1, "swap_hint": 0, "swap_chunk": 8192},  # no L2 cache hints
+], ids=lambda k: ",".join(f"{a[5:]}={b}" for a, b in k.items()) or "default")
 def test_swap_bulk_launch_shapes(lib, tuning, knobs, block_bytes, n):
-    """The bulk-copy kernel (device pools on both sides) for every chunk size
-    (a block in one copy, in several, with a shorter last chunk), ring depth
-    and CTAs per SM, with skipped and out-of-range pairs, bit-exact against
-    the oracle's loop, K and V in one launch and the untouched bytes kept."""
+    """Both device-to-device copy kernels: the 16-byte load/store one and the
+    bulk-copy one for every chunk size (a block in one copy, in several, with
+    a shorter last chunk), ring depth and CTAs per SM, with skipped and
+    out-of-range pairs, bit-exact against the oracle's loop, K and V in one
+    launch and the untouched bytes kept."""
     tuning(**knobs)
     rng = np.random.default_rng(block_bytes + n)
     ns, nd = n + 9, n + 13
