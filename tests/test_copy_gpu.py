@@ -237,11 +237,14 @@ def _continuous_oracle(case):
         bt[s, :len(row)] = torch.tensor(row, dtype=torch.int32)
     lens = torch.tensor(new_lens, dtype=torch.int32)
     out = orc.decode_two_pass(case.q, k, v, bt, lens, case.scale)
+    # sum_t w_t |V_t| on the appended state (the hi + lo weight term of the bound)
+    out_abs = lambda: orc.decode_two_pass(case.q, k0, v0.abs(), bt, lens, case.scale)  # noqa: E731
+    k0, v0 = k.clone(), v.clone()
     for pool in (k, v):
         assert orc.swap_blocks(pool, pool.clone(), case.d2d_pairs) == 0
     assert orc.swap_blocks(k, case.host_k_pool, case.h2d_pairs) == 0
     assert orc.swap_blocks(v, case.host_v_pool, case.h2d_pairs) == 0
-    return bt, lens, slots, out, k, v
+    return bt, lens, slots, out, k, v, out_abs
 
 
 @pytest.mark.parametrize("small", [True, False])
@@ -252,12 +255,13 @@ def test_continuous_batching_step(lib, small):
     else:
         case = wl.make_case(5)            # the stated workload at full size
     bt, lens, slots, out, k, v = _continuous_step(lib, case)
-    rbt, rlens, rslots, rout, rk, rv = _continuous_oracle(case)
+    rbt, rlens, rslots, rout, rk, rv, rabs = _continuous_oracle(case)
     assert slots.tolist() == rslots
     assert torch.equal(lens, rlens)
     assert torch.equal(bt, rbt)
     assert torch.equal(_bits(k), _bits(rk)) and torch.equal(_bits(v), _bits(rv))
-    assert_attention_close(out, rout, case.out_dtype, "continuous step")
+    assert_attention_close(out, rout, case.out_dtype, "continuous step", kv_dtype=case.dtype,
+                           abs_weighted=rabs)
     assert lib.device_errors() == 0
 
 

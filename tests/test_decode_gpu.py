@@ -33,6 +33,13 @@ def _oracle(case, seq_ids=None, lens=None, tables=None, k=None, v=None):
                                seq_ids=seq_ids)
 
 
+def _abs_v(case, **kw):
+    """sum_t w_t |V_t| per output element (the oracle's attention with |V|),
+    on demand: the tensor-core consumer's hi + lo weight rounding term of
+    the parity bound."""
+    return lambda: _oracle(case, **dict(kw, v=kw.get("v", case.v_pool).abs()))
+
+
 def _no_device_errors(pkv):
     assert pkv.device_errors(clear=True) == 0
 
@@ -56,7 +63,8 @@ def test_small_case_matches_oracle(lib, config, split):
         pytest.skip("split must be a multiple of the block size")
     got = run_decode(case, split_tokens=split)
     ref = _oracle(case)
-    assert_attention_close(got, ref, case.out_dtype, f"config {config} split {split}")
+    assert_attention_close(got, ref, case.out_dtype, f"config {config} split {split}",
+                           abs_weighted=_abs_v(case), kv_dtype=case.dtype)
     _no_device_errors(lib)
 
 
@@ -72,7 +80,8 @@ def test_shape_matrix(lib, D, B, H, Hk, dtype, out_dtype):
                         out_dtype=out_dtype, poison=True, seed=D + B + H + Hk)
     for split in (0, 4 * B):
         got = run_decode(case, split_tokens=split)
-        assert_attention_close(got, _oracle(case), out_dtype, f"{D} {B} {H}/{Hk} split {split}")
+        assert_attention_close(got, _oracle(case), out_dtype, f"{D} {B} {H}/{Hk} split {split}",
+                               abs_weighted=_abs_v(case), kv_dtype=dtype)
     _no_device_errors(lib)
 
 
@@ -100,7 +109,8 @@ def test_launch_configurations(lib, tuning, config, knobs):
             # a combination whose ring does not fit in shared memory is refused
             assert e.status == 2 and "shared memory" in str(e)
             pytest.skip(f"{knobs} does not fit: {e}")
-        assert_attention_close(got, _oracle(case), case.out_dtype, f"{knobs} split {split}")
+        assert_attention_close(got, _oracle(case), case.out_dtype, f"{knobs} split {split}",
+                               abs_weighted=_abs_v(case), kv_dtype=case.dtype)
     _no_device_errors(lib)
 
 
@@ -117,7 +127,8 @@ def test_grouped_heads_both_paths(lib, tuning, mma, D, B, H, Hk, dtype, out_dtyp
                         out_dtype=out_dtype, share_blocks=2, poison=True, seed=H + D + B)
     for split in (0, 2 * B):
         got = run_decode(case, split_tokens=split)
-        assert_attention_close(got, _oracle(case), out_dtype, f"mma={mma} split {split}")
+        assert_attention_close(got, _oracle(case), out_dtype, f"mma={mma} split {split}",
+                               abs_weighted=_abs_v(case), kv_dtype=dtype)
     _no_device_errors(lib)
 
 
@@ -286,7 +297,9 @@ def test_full_size_step_whole_output(lib, config):
     assert torch.equal(dv.cpu().view(torch.int16), v.view(torch.int16))
     del dk, dv
     ref = parallel.decode_two_pass(case.q, k, v, bt, lens, case.scale)
-    st = assert_attention_close(out, ref, case.out_dtype, f"config {config}")
+    st = assert_attention_close(
+        out, ref, case.out_dtype, f"config {config}", kv_dtype=case.dtype,
+        abs_weighted=lambda: parallel.decode_two_pass(case.q, k, v.abs(), bt, lens, case.scale))
     print(f"config {config}: {st['n']} elements, max |err| {st['max_abs']:.3g}, "
           f"mean {st['mean_abs']:.3g}, rounding-limited {st['rounding_limited']}")
 
@@ -348,4 +361,5 @@ def test_decode_append_equals_two_calls(lib, config, split):
     assert torch.equal(o1.view(iv), o2.view(iv))
     # and against the oracle for the appended state
     ref = _oracle(case, lens=lens, tables=bt, k=k1, v=v1)
-    assert_attention_close(o2, ref, case.out_dtype, f"config {config}")
+    assert_attention_close(o2, ref, case.out_dtype, f"config {config}", kv_dtype=case.dtype,
+                           abs_weighted=_abs_v(case, lens=lens, tables=bt, k=k1, v=v1))

@@ -31,6 +31,13 @@ def _bits(t):
         t.contiguous().view(torch.int32)
 
 
+def _abs_v(case):
+    """sum_t w_t |V_t| per output element, on demand (the tensor-core
+    consumer's hi + lo weight rounding term of the parity bound)."""
+    return lambda: parallel.decode_two_pass(case.q, case.k_pool, case.v_pool.abs(),
+                                            case.block_tables, case.context_lens, case.scale)
+
+
 def _both(lib, tuning, case, split, **kw):
     """(per-unit kernel output, stream kernel output) of one decode."""
     dev = to_device(case)
@@ -53,7 +60,8 @@ def test_stream_equals_per_unit_kernel(lib, tuning, D, B, H, Hk, split):
     assert torch.equal(_bits(a), _bits(b))
     ref = orc.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
                               case.context_lens, case.scale)
-    assert_attention_close(b, ref, case.out_dtype, f"D={D} B={B} {H}/{Hk} split {split}")
+    assert_attention_close(b, ref, case.out_dtype, f"D={D} B={B} {H}/{Hk} split {split}",
+                           abs_weighted=_abs_v(case), kv_dtype=case.dtype)
     assert lib.device_errors(clear=True) == 0
 
 
@@ -72,7 +80,8 @@ def test_stream_workload_mixes(lib, tuning, config, extra):
         assert torch.equal(_bits(a), _bits(b))
     ref = parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
                                    case.context_lens, case.scale)
-    assert_attention_close(b, ref, case.out_dtype, f"config {config}")
+    assert_attention_close(b, ref, case.out_dtype, f"config {config}",
+                           abs_weighted=_abs_v(case), kv_dtype=case.dtype)
     assert lib.device_errors(clear=True) == 0
 
 
@@ -120,7 +129,9 @@ def test_stream_fused_append_equals_two_calls(lib, tuning):
     assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
     assert torch.equal(_bits(o1), _bits(o2))
     ref = orc.decode_two_pass(case.q, k1, v1, bt, lens, case.scale)
-    assert_attention_close(o2, ref, case.out_dtype, "fused append")
+    assert_attention_close(o2, ref, case.out_dtype, "fused append", kv_dtype=case.dtype,
+                           abs_weighted=lambda: orc.decode_two_pass(case.q, k1, v1.abs(), bt,
+                                                                    lens, case.scale))
 
 
 def test_stream_bad_block_ids_are_flagged(lib, tuning):
@@ -139,4 +150,7 @@ def test_stream_bad_block_ids_are_flagged(lib, tuning):
     assert torch.equal(_bits(outs[0]), _bits(outs[1]))
     ref = orc.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
                               case.context_lens, case.scale, seq_ids=keep)
-    assert_attention_close(outs[1][keep], ref, case.out_dtype)
+    assert_attention_close(outs[1][keep], ref, case.out_dtype, kv_dtype=case.dtype,
+                           abs_weighted=lambda: orc.decode_two_pass(
+                               case.q, case.k_pool, case.v_pool.abs(), case.block_tables,
+                               case.context_lens, case.scale, seq_ids=keep))
