@@ -179,9 +179,19 @@ struct DecodeConfig {
     int max_pages;
     size_t smem;
     int threads;
+    bool stream;  // tensor-core decode by resident CTAs streaming the units
 };
 
 constexpr int kDefaultSplitTokens = 512;
+// Split length of the streaming decode when the caller leaves it to the
+// library: a CTA's share of the work is a few pages when contexts are short,
+// and a unit longer than that becomes the tail (one CTA works through it
+// alone), so units are kept short; the partials of the few long contexts
+// are merged as usual.
+constexpr int kStreamSplitTokens = 128;
+// The streaming decode is chosen (knob PKV_TUNE_DECODE_STREAM unset) for
+// tensor-core decodes whose longest context is at most this long.
+constexpr int kStreamMaxContext = 0;
 // Few (sequence, head-group) units with contexts of 8K tokens or more: every
 // unit is cut into many pieces anyway, and at 1024 tokens a piece the GPU stays
 // as full while each CTA pays its prologue and writes its partials half as
@@ -316,7 +326,8 @@ int cta_order(int max_splits, int num_seqs) {
 }
 
 pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, int block_size,
-                       int max_context_len, int split_tokens, int sm_count, DecodeConfig* c) {
+                       int max_context_len, int split_tokens, int sm_count, DecodeConfig* c,
+                       bool allow_stream = true, size_t smem_optin = 0) {
     shape_config(n_heads, n_kv_heads, head_dim, block_size, c);
     // Too few (sequence, head-group) units to occupy the SMs: two kv heads per
     // CTA give more, shorter CTAs (measured on the tiny workload, 4 sequences
@@ -327,9 +338,31 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
         shape_config_hpc(n_heads, n_kv_heads, head_dim, block_size, 2, &narrow);
         *c = narrow;
     }
+    // Streaming decode: the tensor-core consumer, at most kStreamMaxSeqs
+    // sequences (their lengths live in shared memory), 32-bit page counts.
+    const long long all_pages = (long long)num_seqs * n_kv_heads *
+                                (((long long)max_context_len + block_size - 1) / block_size);
+    const int stream_knob = tuning(PKV_TUNE_DECODE_STREAM, -1);
+    c->stream = allow_stream && c->mma && c->wpt == 1 && num_seqs <= pkv::kStreamMaxSeqs &&
+                all_pages <= 0x7fffffffLL &&
+                (stream_knob >= 0 ? stream_knob != 0 : max_context_len <= kStreamMaxContext);
+    if (c->stream) {
+        // its shared memory must fit (the per-unit kernel runs otherwise)
+        const int pages = split_tokens > 0 ? split_tokens / block_size
+                                           : (kStreamSplitTokens + block_size - 1) / block_size;
+        const size_t limit = smem_optin > 0 ? smem_optin : (size_t)227 * 1024;
+        if (pkv::decode_stream_smem_bytes(head_dim, block_size, n_heads / n_kv_heads, 2, c->hpc,
+                                          c->stages, pages, num_seqs) > limit)
+            c->stream = false;
+    }
     if (split_tokens == 0) {
-        split_tokens = auto_split_tokens(num_seqs, n_kv_heads, c->hpc, block_size,
-                                         max_context_len, sm_count);
+        split_tokens = c->stream && !tuned(PKV_TUNE_DECODE_SPLIT)
+                           ? std::min((max_context_len + block_size - 1) / block_size * block_size,
+                                      (kStreamSplitTokens + block_size - 1) / block_size *
+                                          block_size)
+                           : auto_split_tokens(num_seqs, n_kv_heads, c->hpc, block_size,
+                                               max_context_len, sm_count);
+        if (split_tokens <= 0) split_tokens = block_size;
     } else if (split_tokens < 0 || split_tokens % block_size) {
         return invalid("split_tokens must be a positive multiple of block_size (or 0)");
     }
@@ -344,6 +377,9 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
                                                   c->max_pages)
                      : pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc, c->wpk,
                                               c->wpt, c->stages, c->max_pages);
+    if (c->stream)
+        c->smem = pkv::decode_stream_smem_bytes(head_dim, block_size, n_heads / n_kv_heads, 2,
+                                                c->hpc, c->stages, c->max_pages, num_seqs);
     return PKV_OK;
 }
 
@@ -448,10 +484,10 @@ PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, i
                                     int block_size, int max_context_len) {
     if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size) || num_seqs < 0) return 0;
     DeviceInfo* d = nullptr;
-    const int sms = device_info(&d) == cudaSuccess ? d->sm_count : 0;
+    const bool ok = device_info(&d) == cudaSuccess;
     DecodeConfig c;
-    if (make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size, max_context_len, 0, sms,
-                    &c) != PKV_OK)
+    if (make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size, max_context_len, 0,
+                    ok ? d->sm_count : 0, &c, true, ok ? (size_t)d->smem_optin : 0) != PKV_OK)
         return 0;
     return c.split_tokens;
 }
@@ -461,10 +497,11 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
                                           int split_tokens) {
     if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size) || num_seqs < 0) return 0;
     DeviceInfo* d = nullptr;
-    const int sms = device_info(&d) == cudaSuccess ? d->sm_count : 0;
+    const bool ok = device_info(&d) == cudaSuccess;
     DecodeConfig c;
     if (make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size, max_context_len,
-                    split_tokens, sms, &c) != PKV_OK)
+                    split_tokens, ok ? d->sm_count : 0, &c, true,
+                    ok ? (size_t)d->smem_optin : 0) != PKV_OK)
         return 0;
     return workspace_bytes_for(num_seqs, n_heads, head_dim, c, nullptr);
 }
@@ -472,27 +509,6 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
 }  // extern "C"
 
 namespace {
-
-// Whether the tensor-core decode runs as resident CTAs streaming the work
-// units (paged_decode_mma_stream_kernel) instead of one CTA per unit, and
-// that kernel's shared memory.  It needs the tensor-core consumer, at most
-// kStreamMaxSeqs sequences (their lengths live in shared memory) and page
-// counts that fit 32 bits.  The PKV_TUNE_DECODE_STREAM knob chooses; by
-// default it is off.
-bool use_stream(const DecodeConfig& c, int num_seqs, int n_kv_heads, int head_dim,
-                int block_size, int max_context_len, pkv_dtype kv_dtype, int group,
-                const DeviceInfo* dev, size_t* smem) {
-    if (!c.mma || c.wpt != 1 || num_seqs > pkv::kStreamMaxSeqs) return false;
-    if (tuning(PKV_TUNE_DECODE_STREAM, 0) == 0) return false;
-    const long long pages = ((long long)max_context_len + block_size - 1) / block_size;
-    if ((long long)num_seqs * n_kv_heads * pages > 0x7fffffffLL) return false;
-    (void)kv_dtype;
-    const size_t bytes = pkv::decode_stream_smem_bytes(head_dim, block_size, group, 2, c.hpc,
-                                                       c.stages, c.max_pages, num_seqs);
-    if (bytes > (size_t)dev->smem_optin) return false;
-    *smem = bytes;
-    return true;
-}
 
 // paged_attn_decode, with the append of paged_attn_decode_append fused in
 // when slot_mapping is not NULL.
@@ -533,7 +549,8 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
 
     DecodeConfig c;
     pkv_status st = make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size,
-                                max_context_len, split_tokens, dev->sm_count, &c);
+                                max_context_len, split_tokens, dev->sm_count, &c, true,
+                                (size_t)dev->smem_optin);
     if (st != PKV_OK) return st;
     if (c.smem > (size_t)dev->smem_optin) return unsupported("shared memory of this configuration");
     // The kernels clamp a context to min(table tokens, splits x split
@@ -601,8 +618,7 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
     L.sm_count = dev->sm_count;
     if (c.max_splits > 65535 * 1024) return unsupported("context too long for the grid");
 
-    if (use_stream(c, num_seqs, n_kv_heads, head_dim, block_size, max_context_len, kv_dtype,
-                   n_heads / n_kv_heads, dev, &L.smem_bytes))
+    if (c.stream)
         e = kv_dtype == PKV_BF16 ? pkv::launch_decode_stream_bf16(head_dim, block_size, L)
                                  : pkv::launch_decode_stream_f16(head_dim, block_size, L);
     else if (c.mma)
@@ -748,7 +764,7 @@ PKV_API size_t pkv_decode_batched_workspace_bytes(const pkv_decode_problem* prob
     const long long total = total_seqs_of(problems, num_problems);
     DecodeConfig c;
     if (make_config((int)std::min(total, 65535LL), n_heads, n_kv_heads, head_dim, block_size,
-                    max_context_len, split_tokens, dev->sm_count, &c) != PKV_OK)
+                    max_context_len, split_tokens, dev->sm_count, &c, false) != PKV_OK)
         return 0;
     return batch_layout(problems, num_problems, n_heads, head_dim, c).total;
 }
@@ -791,7 +807,8 @@ PKV_API pkv_status pkv_decode_batched_plan(pkv_decode_plan* plan,
     if (e != cudaSuccess) return cuda_fail(e);
     DecodeConfig c;
     pkv_status st = make_config((int)std::max(total, 1LL), n_heads, n_kv_heads, head_dim,
-                                block_size, max_context_len, split_tokens, dev->sm_count, &c);
+                                block_size, max_context_len, split_tokens, dev->sm_count, &c,
+                                false);
     if (st != PKV_OK) return st;
     if (c.smem > (size_t)dev->smem_optin) return unsupported("shared memory of this configuration");
     if (c.max_splits > 65535) return unsupported("more than 65535 splits per sequence");

@@ -32,6 +32,19 @@
 namespace pkv {
 
 constexpr int kStreamMaxSeqs = 2048;   // context lengths held in shared memory
+constexpr int kStreamBatchUnits = 32;  // units whose block ids one lookup fetches
+constexpr int kStreamBatchPages = 128; // pages of one lookup (at least one split's)
+
+// A unit queued by the producer: sequence, split, head group, its pages and
+// where its block ids start in the batch buffer.
+struct StreamUnit {
+    int s;
+    int k;
+    int hg;
+    int npk;
+    int n_splits;
+    int first;
+};
 
 // What the producer tells the consumers about the page in one ring slot.
 struct StreamSlot {
@@ -54,9 +67,12 @@ inline size_t decode_stream_smem_bytes(int D, int BS, int G, int elem_bytes, int
                                        int stages, int max_pages_per_split, int num_seqs) {
     const size_t ring = (size_t)stages * 2 * hpc * D * BS * elem_bytes;
     const size_t qs = (size_t)stages * hpc * G * D * elem_bytes;
+    const int batch = max_pages_per_split > kStreamBatchPages ? max_pages_per_split
+                                                              : kStreamBatchPages;
     return 1024 + ring + qs + (size_t)stages * 2 * sizeof(uint64_t) +
-           (size_t)stages * sizeof(StreamSlot) + (size_t)max_pages_per_split * sizeof(int) +
-           (size_t)(2 * num_seqs + 2) * sizeof(int) + 8 * sizeof(int);
+           (size_t)stages * sizeof(StreamSlot) + kStreamBatchUnits * sizeof(StreamUnit) +
+           (size_t)batch * sizeof(int) + (size_t)(2 * num_seqs + 2) * sizeof(int) +
+           8 * sizeof(int);
 }
 
 __device__ __forceinline__ void bulk_load_q(void* dst_smem, const void* src, uint32_t bytes,
@@ -106,10 +122,11 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(qbuf + (size_t)stages * q_bytes);
     uint64_t* empty = full + stages;
     StreamSlot* slot = reinterpret_cast<StreamSlot*>(empty + stages);
-    int* s_bid = reinterpret_cast<int*>(slot + stages);
-    int* s_len = s_bid + p.max_pages_per_split;      // clamped context lengths [S]
+    StreamUnit* s_unitq = reinterpret_cast<StreamUnit*>(slot + stages);
+    int* s_bid = reinterpret_cast<int*>(s_unitq + kStreamBatchUnits);
+    int* s_len = s_bid + max(kStreamBatchPages, p.max_pages_per_split);   // clamped lengths [S]
     int* s_pref = s_len + S;                         // page prefix sums [S + 1]
-    int* s_var = s_pref + S + 1;                     // first sequence, abort, issued, warp sums
+    int* s_var = s_pref + S + 1;   // first sequence, abort, slots issued, queued units
 
     const int cap = min(p.max_blocks_per_seq * BS, p.max_splits * p.split_tokens);
     const int warp = threadIdx.x >> 5;
@@ -225,120 +242,169 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
 
     if (warp == 0) {
         // ================= producer =================
+        // Units are taken in batches: lane 0 queues the next units (up to
+        // kStreamBatchUnits, or until their pages would pass the batch's
+        // block-id buffer), the whole warp looks up all their block ids at
+        // once (one memory round trip per batch instead of one per unit) and
+        // writes the fused appends, then lane 0 issues every page.
         const uint64_t policy = l2_policy_evict_first();
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
         }
-        int g = 0;             // slots issued so far
-        bool stop = false;
-        for (int s = s_var[0]; s < S && !stop; ++s) {
-            const long long Ps = s_pref[s];
-            if (Ps >= P1) break;
-            const int n = s_len[s];
-            if (n == 0) continue;
-            const int np = (n + BS - 1) / BS;
-            const int n_splits = max(1, (n + p.split_tokens - 1) / p.split_tokens);
-            for (int k = 0; k < n_splits && !stop; ++k) {
-                const int npk = min(PPS, np - k * PPS);
-                for (int hg = 0; hg < HG && !stop; ++hg) {
-                    const long long start = Ps + (long long)HG * k * PPS + (long long)hg * npk;
-                    if (start < P0) continue;
-                    if (start >= P1) {
-                        stop = true;
+        const int cap_pages = max(kStreamBatchPages, PPS);
+        int g = 0;                          // slots issued so far (lane 0)
+        // walk cursor (lane 0): sequence, its place, split and head group
+        int cs = s_var[0], ck = 0, ch = 0;
+        bool done = false, stop = false;
+        while (!done && !stop) {
+            if (lane == 0) {
+                int nu = 0, np_batch = 0;
+                while (nu < kStreamBatchUnits && cs < S) {
+                    const long long Ps = s_pref[cs];
+                    if (Ps >= P1) {
+                        cs = S;
                         break;
                     }
-                    // ---- the unit's block ids (whole warp)
-                    const int page0 = k * PPS;
-                    for (int i = lane; i < npk; i += 32) {
-                        int b = p.block_tables[(size_t)s * p.max_blocks_per_seq + page0 + i];
-                        if (b < 0 || b >= p.num_blocks) {
-                            raise_error(p.errors, PKV_DEVERR_BLOCK_ID);
-                            b = -1;
-                        }
-                        s_bid[i] = b;
+                    const int n = s_len[cs];
+                    const int np = (n + BS - 1) / BS;
+                    const int n_splits = max(1, (n + p.split_tokens - 1) / p.split_tokens);
+                    if (n == 0 || ck >= n_splits) {
+                        ++cs;
+                        ck = ch = 0;
+                        continue;
                     }
-                    // ---- fused append: the last split's unit writes the new
-                    // token's rows of its heads before any of its pages load
-                    if (p.slot_mapping != nullptr && k == n_splits - 1) {
-                        const int64_t slot_row = p.slot_mapping[s];
-                        if (slot_row >= 0 && slot_row < (int64_t)p.num_blocks * BS) {
-                            constexpr int VEC = 16 / (int)sizeof(T);
-                            const int per_row = HPC * D / VEC;
-                            const size_t row = (size_t)p.n_kv_heads * D;
-                            const size_t off_new = (size_t)s * row + (size_t)hg * HPC * D;
-                            const size_t off_pool = (size_t)slot_row * row + (size_t)hg * HPC * D;
-                            for (int i = lane; i < 2 * per_row; i += 32) {
-                                const bool is_v = i >= per_row;
-                                const int j = (is_v ? i - per_row : i) * VEC;
-                                const T* src =
-                                    static_cast<const T*>(is_v ? p.v_new : p.k_new) + off_new + j;
-                                T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) + off_pool + j;
-                                *reinterpret_cast<uint4*>(dst) =
-                                    *reinterpret_cast<const uint4*>(src);
-                            }
-                            asm volatile("fence.proxy.async.global;" ::: "memory");
-                        } else if (slot_row >= 0 && hg == 0 && lane == 0) {
-                            raise_error(p.errors, PKV_DEVERR_SLOT);
-                        }
+                    const int npk = min(PPS, np - ck * PPS);
+                    const long long start = Ps + (long long)HG * ck * PPS + (long long)ch * npk;
+                    if (start >= P1) {
+                        cs = S;
+                        break;
                     }
-                    __syncwarp();
-                    if (lane == 0) {
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        const int tok_begin = k * p.split_tokens;
-                        const int tok_end = min(n, tok_begin + p.split_tokens);
-                        const T* qsrc = reinterpret_cast<const T*>(p.q) +
-                                        ((size_t)s * p.n_heads + (size_t)hg * HPC * G) * D;
-                        for (int i = 0; i < npk; ++i, ++g) {
-                            const int st = g % stages;
-                            if (g >= stages &&
-                                !mbar_wait(&empty[st], ((g / stages) - 1) & 1, p.errors)) {
-                                *s_abort = 1;
-                                stop = true;
-                                break;
-                            }
-                            if (*s_abort) {
-                                stop = true;
-                                break;
-                            }
-                            const int b = s_bid[i];
-                            StreamSlot& r = slot[st];
-                            r.s = s;
-                            r.hg = hg;
-                            r.split = k;
-                            r.page = i;
-                            r.n_pages = npk;
-                            r.n_splits = n_splits;
-                            r.tok_begin = tok_begin;
-                            r.tok_end = tok_end;
-                            r.valid = b >= 0;
-                            const uint32_t bytes = (b >= 0 ? stage_bytes : 0u) + (i == 0 ? q_bytes : 0u);
-                            if (bytes == 0) {
-                                mbar_arrive(&full[st]);
-                                continue;
-                            }
-                            mbar_arrive_expect_tx(&full[st], bytes);
-                            if (i == 0)
-                                bulk_load_q(qbuf + (size_t)st * q_bytes, qsrc, q_bytes, &full[st],
-                                            policy);
-                            if (b >= 0) {
-                                unsigned char* dst = ring + (size_t)st * stage_bytes;
-                                for (int hh = 0; hh < HPC; ++hh) {
-                                    const int row = (hg * HPC + hh) * HALVES;
-                                    for (int h = 0; h < HALVES; ++h) {
-                                        tma_load_4d(dst + hh * head_bytes + h * BOX, &tm_k,
-                                                    &full[st], 0, row + h, 0, b, policy);
-                                        tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, &tm_v,
-                                                    &full[st], 0, row + h, 0, b, policy);
-                                    }
+                    if (start >= P0) {
+                        if (np_batch + npk > cap_pages) break;   // the next batch takes it
+                        StreamUnit& u = s_unitq[nu++];
+                        u.s = cs;
+                        u.k = ck;
+                        u.hg = ch;
+                        u.npk = npk;
+                        u.n_splits = n_splits;
+                        u.first = np_batch;
+                        np_batch += npk;
+                    }
+                    if (++ch == HG) {
+                        ch = 0;
+                        ++ck;
+                    }
+                }
+                s_var[3] = nu;
+            }
+            __syncwarp();
+            const int nu = s_var[3];
+            if (nu == 0) {
+                done = true;
+                break;
+            }
+            // ---- block ids of every queued unit (all lanes, independent loads)
+            for (int ui = 0; ui < nu; ++ui) {
+                const StreamUnit u = s_unitq[ui];
+                const int* row = p.block_tables + (size_t)u.s * p.max_blocks_per_seq + u.k * PPS;
+                for (int i = lane; i < u.npk; i += 32) {
+                    int b = row[i];
+                    if (b < 0 || b >= p.num_blocks) {
+                        raise_error(p.errors, PKV_DEVERR_BLOCK_ID);
+                        b = -1;
+                    }
+                    s_bid[u.first + i] = b;
+                }
+            }
+            // ---- fused append: a last split's unit writes the new token's
+            // rows of its heads before any of its pages load
+            if (p.slot_mapping != nullptr) {
+                constexpr int VEC = 16 / (int)sizeof(T);
+                const int per_row = HPC * D / VEC;
+                const size_t row = (size_t)p.n_kv_heads * D;
+                for (int ui = 0; ui < nu; ++ui) {
+                    const StreamUnit u = s_unitq[ui];
+                    if (u.k != u.n_splits - 1) continue;
+                    const int64_t slot_row = p.slot_mapping[u.s];
+                    if (slot_row < 0) continue;
+                    if (slot_row >= (int64_t)p.num_blocks * BS) {
+                        if (u.hg == 0 && lane == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
+                        continue;
+                    }
+                    const size_t off_new = (size_t)u.s * row + (size_t)u.hg * HPC * D;
+                    const size_t off_pool = (size_t)slot_row * row + (size_t)u.hg * HPC * D;
+                    for (int i = lane; i < 2 * per_row; i += 32) {
+                        const bool is_v = i >= per_row;
+                        const int j = (is_v ? i - per_row : i) * VEC;
+                        const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) + off_new + j;
+                        T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) + off_pool + j;
+                        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+                    }
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            __syncwarp();
+            // ---- issue every page of the batch (lane 0)
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                for (int ui = 0; ui < nu && !stop; ++ui) {
+                    const StreamUnit u = s_unitq[ui];
+                    const int n = s_len[u.s];
+                    const int tok_begin = u.k * p.split_tokens;
+                    const int tok_end = min(n, tok_begin + p.split_tokens);
+                    const T* qsrc = reinterpret_cast<const T*>(p.q) +
+                                    ((size_t)u.s * p.n_heads + (size_t)u.hg * HPC * G) * D;
+                    for (int i = 0; i < u.npk; ++i, ++g) {
+                        const int st = g % stages;
+                        if (g >= stages &&
+                            !mbar_wait(&empty[st], ((g / stages) - 1) & 1, p.errors)) {
+                            *s_abort = 1;
+                            stop = true;
+                            break;
+                        }
+                        if (*s_abort) {
+                            stop = true;
+                            break;
+                        }
+                        const int b = s_bid[u.first + i];
+                        StreamSlot& r = slot[st];
+                        r.s = u.s;
+                        r.hg = u.hg;
+                        r.split = u.k;
+                        r.page = i;
+                        r.n_pages = u.npk;
+                        r.n_splits = u.n_splits;
+                        r.tok_begin = tok_begin;
+                        r.tok_end = tok_end;
+                        r.valid = b >= 0;
+                        const uint32_t bytes =
+                            (b >= 0 ? stage_bytes : 0u) + (i == 0 ? q_bytes : 0u);
+                        if (bytes == 0) {
+                            mbar_arrive(&full[st]);
+                            continue;
+                        }
+                        mbar_arrive_expect_tx(&full[st], bytes);
+                        if (i == 0)
+                            bulk_load_q(qbuf + (size_t)st * q_bytes, qsrc, q_bytes, &full[st],
+                                        policy);
+                        if (b >= 0) {
+                            unsigned char* dst = ring + (size_t)st * stage_bytes;
+                            for (int hh = 0; hh < HPC; ++hh) {
+                                const int hrow = (u.hg * HPC + hh) * HALVES;
+                                for (int h = 0; h < HALVES; ++h) {
+                                    tma_load_4d(dst + hh * head_bytes + h * BOX, &tm_k,
+                                                &full[st], 0, hrow + h, 0, b, policy);
+                                    tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, &tm_v,
+                                                &full[st], 0, hrow + h, 0, b, policy);
                                 }
                             }
                         }
                     }
-                    stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-                    __syncwarp();
                 }
             }
+            stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+            __syncwarp();
         }
         // ---- end of the stream: a record without pages
         if (lane == 0 && !*s_abort) {

@@ -39,13 +39,21 @@ def _abs_v(case):
 
 
 def _both(lib, tuning, case, split, **kw):
-    """(per-unit kernel output, stream kernel output) of one decode."""
+    """(per-unit kernel output, stream kernel output) of one decode with the
+    same split length (split 0: the stream kernel's automatic one, which the
+    per-unit kernel is then given explicitly), plus the stream kernel's
+    output with the automatic split."""
     dev = to_device(case)
+    tuning(decode_stream=1)
+    auto = run_decode(case, split_tokens=0, dev=dev, **kw)
+    if split == 0:
+        split = lib.decode_split_tokens(case.S, case.H, case.Hk, case.D, case.B,
+                                        int(case.context_lens.max()))
+    b = run_decode(case, split_tokens=split, dev=dev, **kw)
     tuning(decode_stream=0)
     a = run_decode(case, split_tokens=split, dev=dev, **kw)
-    tuning(decode_stream=1)
-    b = run_decode(case, split_tokens=split, dev=dev, **kw)
     torch.cuda.synchronize()
+    assert torch.equal(_bits(auto), _bits(b))
     return a, b
 
 
