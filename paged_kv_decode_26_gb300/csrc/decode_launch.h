@@ -33,6 +33,7 @@ cudaError_t launch_decode_stream_bf16(int D, int BS, const DecodeLaunch& L);
 cudaError_t launch_decode_stream_f16(int D, int BS, const DecodeLaunch& L);
 
 struct MultiQueryLaunch {
+    CUtensorMap tm_q;   // tcgen05 kernel only
     CUtensorMap tm_k;
     CUtensorMap tm_v;
     MultiQueryParams p;

@@ -20,6 +20,28 @@ namespace {
 constexpr int kLptMaxSeqs = 256;
 constexpr int kLptMinContext = 8192;
 
+// The queries [total_q, n_heads, D] as a 4-D tensor for the tcgen05
+// multi-query kernel: dims (64, D/64, n_heads, total_q), box (64, 1, G, 128/G)
+// with 128-byte swizzle, so one load per 64-element half brings the 128 rows
+// (token, head of the group) of a query tile as [128][64], K-major.
+cudaError_t encode_query_map(CUtensorMap* map, const void* q, pkv_dtype dt, int total_q,
+                             int n_heads, int head_dim, int group) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t es = 2;
+    cuuint64_t dims[4] = {64, (cuuint64_t)head_dim / 64, (cuuint64_t)n_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[3] = {64 * es, (cuuint64_t)head_dim * es,
+                             (cuuint64_t)n_heads * head_dim * es};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = encode(map, dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        4, const_cast<void*>(q), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 extern "C" {
@@ -76,7 +98,7 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
             const long long rows = (long long)max_q_len * G;
             want = (G >= 4 ? rows >= 16 : rows >= 48) ? 1 : 0;
         }
-        int stages = tuning(PKV_TUNE_MQ_TC_STAGES, head_dim == 64 ? 8 : 6);
+        int stages = tuning(PKV_TUNE_MQ_TC_STAGES, head_dim == 64 ? 6 : 4);
         stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
         // Longest context first (see longest_first) for batches small enough
         // to rank in every CTA, and only with contexts of 8K tokens or more:
@@ -95,6 +117,9 @@ PKV_API pkv_status paged_attn_multi_query(void* out, pkv_dtype out_dtype, const 
         if (want && total_q >= tc_tokens && smem <= (size_t)dev->smem_optin) {
             pkv::MultiQueryLaunch L;
             std::memset(&L, 0, sizeof(L));
+            if ((e = encode_query_map(&L.tm_q, q, kv_dtype, total_q, n_heads, head_dim, G)) !=
+                cudaSuccess)
+                return cuda_fail(e);
             if ((e = encode_pool_map(&L.tm_k, kmap_base, kv_dtype, map_blocks, block_size,
                                      n_kv_heads, head_dim, 1, true)) != cudaSuccess)
                 return cuda_fail(e);

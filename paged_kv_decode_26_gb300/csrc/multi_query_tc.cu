@@ -13,7 +13,7 @@ cudaError_t launch_tc(const MultiQueryLaunch& L) {
     cudaError_t e = ensure_smem_limit(fn, &done_mask, L.smem_bytes);
     if (e != cudaSuccess) return e;
     paged_multi_query_tc_kernel<D, BS, T>
-        <<<L.grid, L.block, L.smem_bytes, L.stream>>>(L.tm_k, L.tm_v, L.p);
+        <<<L.grid, L.block, L.smem_bytes, L.stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
     return cudaGetLastError();
 }
 

@@ -154,11 +154,12 @@ __device__ __forceinline__ void tc_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Shared memory of one CTA: 1 KB alignment slack, the K/V ring, barriers,
-// block ids, one word (and the ranking scratch of longest_first).
+// Shared memory of one CTA: 1 KB alignment slack, the two Q tiles, the K/V
+// ring, barriers, block ids, one word.
 inline size_t multi_query_tc_smem_bytes(int D, int stages, int max_pages, int lpt_seqs = 0) {
+    const size_t q = (size_t)kTcQTiles * kTcRows * D * 2;
     const size_t kv = (size_t)stages * 2 * kTcKeys * D * 2;
-    return 1024 + kv + (size_t)(3 * stages + 4 * kTcQTiles) * sizeof(uint64_t) +
+    return 1024 + q + kv + (size_t)(3 * stages + 15) * sizeof(uint64_t) +
            (size_t)max_pages * sizeof(int) + sizeof(int) +
            (lpt_seqs > 0 ? (size_t)(lpt_seqs + 1) * sizeof(int) : 0);
 }
@@ -200,20 +201,21 @@ __device__ __forceinline__ void longest_first(const MultiQueryParams& p, int* s_
 
 template <int D, int BS, typename T>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    paged_multi_query_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+    paged_multi_query_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                const __grid_constant__ CUtensorMap tm_k,
                                 const __grid_constant__ CUtensorMap tm_v,
                                 const MultiQueryParams p) {
     constexpr int HALVES = D / 64;
     constexpr int PAGES = kTcKeys / BS;                 // pages per key tile
     constexpr uint32_t KV_HALF = kTcKeys * 128;         // [64 keys x 64 elements]
     constexpr uint32_t KV_BYTES = HALVES * KV_HALF;     // one K (or V) tile
+    constexpr uint32_t Q_HALF = kTcRows * 128;          // [128 rows x 64 elements]
+    constexpr uint32_t Q_BYTES = HALVES * Q_HALF;       // one query tile
     constexpr uint32_t TMEM_COLS = 512;
-    constexpr uint32_t TILE_COLS = 256;                 // per query tile: O, Q, S
-    constexpr uint32_t O_COL = 0;                       // O: D fp32 columns
-    constexpr uint32_t Q_COL = D;                       // Q: D / 2 columns of 16-bit pairs
-    constexpr uint32_t S_COL = D + D / 2;               // S, then P over it: kTcKeys columns
+    constexpr uint32_t TILE_COLS = 256;                 // per query tile: O, then two S buffers
+    constexpr uint32_t S_COL = D;
     constexpr int ALL_PAGES = (1 << PAGES) - 1;
-    static_assert(kTcKeys % BS == 0 && D % 64 == 0 && S_COL + kTcKeys <= TILE_COLS, "shape");
+    static_assert(kTcKeys % BS == 0 && D % 64 == 0 && D + 2 * kTcKeys <= TILE_COLS, "shape");
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
 
@@ -226,15 +228,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- shared memory (1024-byte aligned for the swizzle)
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    unsigned char* sKV = sm;                                        // stages x (K, V)
+    unsigned char* sQ = sm;                                         // 2 x HALVES x [128 x 128 B]
+    unsigned char* sKV = sQ + kTcQTiles * Q_BYTES;                  // stages x (K, V)
     uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + (size_t)p.stages * 2 * KV_BYTES);
     uint64_t* kv_free = kv_full + p.stages;      // [stages]: both issuers done with the slot
     uint64_t* kv_land = kv_free + p.stages;      // [stages]: loads landed (tiles to zero)
-    uint64_t* q_ready = kv_land + p.stages;      // [tile]: Q rows in tensor memory (128 arrivals)
-    uint64_t* s_full = q_ready + kTcQTiles;      // [tile]: S ready
-    uint64_t* p_full = s_full + kTcQTiles;       // [tile]: P written (128 arrivals)
-    uint64_t* fin = p_full + kTcQTiles;          // [tile]: every MMA of the tile's issuer done
-    int* s_bid = reinterpret_cast<int*>(fin + kTcQTiles);
+    uint64_t* q_full = kv_land + p.stages;
+    uint64_t* s_full = q_full + 1;               // [tile][buffer]: S ready
+    uint64_t* p_full = s_full + 4;               // [tile][buffer]: P written (128 arrivals)
+    uint64_t* o_done = p_full + 4;               // [tile][parity of key tile]: P V done
+    uint64_t* fin = o_done + 4;                  // [tile]: every MMA of the tile's issuer done
+    int* s_bid = reinterpret_cast<int*>(fin + 2);
     int* s_tmem = s_bid + p.max_pages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -286,12 +290,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&kv_free[st], kTcQTiles);
             mbar_init(&kv_land[st], 1);
         }
-        for (int q = 0; q < kTcQTiles; ++q) {
-            mbar_init(&q_ready[q], kTcRows);
-            mbar_init(&s_full[q], 1);
-            mbar_init(&p_full[q], kTcRows);
-            mbar_init(&fin[q], 1);
+        mbar_init(q_full, 1);
+        for (int b = 0; b < 4; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], kTcRows);
+            mbar_init(&o_done[b], 1);
         }
+        mbar_init(&fin[0], 1);
+        mbar_init(&fin[1], 1);
         fence_barrier_init();
     }
     tc_fence_before();
@@ -323,8 +329,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 9) {
         // ================= TMA producer (the whole warp zeroes V rows) =================
         if (lane == 0) {
+            prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
+            uint32_t q_bytes = 0;
+#pragma unroll
+            for (int t = 0; t < kTcQTiles; ++t) q_bytes += ntiles(t) > 0 ? Q_BYTES : 0;
+            mbar_arrive_expect_tx(q_full, q_bytes);
+            const uint64_t once = l2_policy_evict_first();
+#pragma unroll
+            for (int t = 0; t < kTcQTiles; ++t) {
+                if (ntiles(t) == 0) continue;
+                for (int h = 0; h < HALVES; ++h)
+                    tma_load_4d(sQ + t * Q_BYTES + h * Q_HALF, &tm_q, q_full, 0, h, kvh * G,
+                                qs0 + tok_lo + t * QT, once);
+            }
         }
         const uint64_t keep = l2_policy_evict_normal();   // pages serve other query tiles
         int issued = 0;
@@ -392,68 +411,82 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp == 8 || warp == 10) {
         // ================= MMA issuer of query tile t =================
-        // Per key tile j: S = Q K_j^T (A = Q from tensor memory), then, once
-        // the softmax has written P over S, O += P V_j (A = P from tensor
-        // memory).  The next S reuses the columns of P: issued after this
-        // P V by the same thread, it runs after it.
         const int t = warp == 8 ? 0 : 1;
         const int ntt = ntiles(t);
         if (lane == 0) {
             const uint32_t id_s = tc_idesc<T>(kTcRows, kTcKeys, 0);
             const uint32_t id_o = tc_idesc<T>(kTcRows, D, 1);
-            // Descriptors of K and V of slot 0; other slots and k-steps add
+            // Descriptors of Q tile t, K and V of slot 0; other operands add
             // their byte offset >> 4 to the start-address field (shared
             // addresses stay below 2^18, so the 14-bit field never carries).
+            const uint64_t dq = tc_desc_sw128(smem_addr(sQ + t * Q_BYTES), 16, 1024);
             const uint64_t dk = tc_desc_sw128(smem_addr(sKV), 16, 1024);
             const uint64_t dv = tc_desc_sw128(smem_addr(sKV + KV_BYTES), KV_HALF, 1024);
             constexpr uint32_t SLOT16 = (2 * KV_BYTES) >> 4;
-            const uint32_t base = tmem + t * TILE_COLS;
-            bool ok = ntt == 0 || mbar_wait(&q_ready[t], 0, p.errors);
-            int st = 0, round = 0;         // slot of tile j, times the ring wrapped
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (!mbar_wait(&kv_full[st], round & 1, p.errors)) {
-                    ok = false;
-                    break;
-                }
-                if (j < ntt) {
-                    tc_fence_after();
-                    const uint64_t kd = dk + (uint64_t)(st * SLOT16);
+            const uint32_t base = tmem + t * TILE_COLS;      // O of tile t, then its S buffers
+            int s_st = 0;          // slot of the next tile whose S is issued
+            uint32_t s_ph = 0;     // and the phase of its kv_full
+            // S_tj = Q_t K_j^T into S buffer j & 1
+            auto issue_s = [&](int j) -> bool {
+                if (!mbar_wait(&kv_full[s_st], s_ph, p.errors)) return false;
+                tc_fence_after();
+                const uint64_t kd = dk + (uint64_t)(s_st * SLOT16);
+                const uint32_t d = base + S_COL + (j & 1) * kTcKeys;
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t ko = ((ks / 4) * KV_HALF + (ks % 4) * 32) >> 4;
-                        tc_mma_tmem_a(base + S_COL, base + Q_COL + ks * 8, kd + ko, id_s,
-                                      ks > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&s_full[t]);
-                    if (!mbar_wait(&p_full[t], j & 1, p.errors)) {
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t qo = ((ks / 4) * Q_HALF + (ks % 4) * 32) >> 4;
+                    const uint32_t ko = ((ks / 4) * KV_HALF + (ks % 4) * 32) >> 4;
+                    tc_mma(d, dq + qo, kd + ko, id_s, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[t * 2 + (j & 1)]);
+                if (++s_st == p.stages) {
+                    s_st = 0;
+                    s_ph ^= 1u;
+                }
+                return true;
+            };
+            bool ok = ntt == 0 || mbar_wait(q_full, 0, p.errors);
+            for (int j = 0; ok && j < 2 && j < ntt; ++j) ok = issue_s(j);
+            int v_st = 0, v_round = 0;     // slot of tile j, times the ring wrapped
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j < ntt) {
+                    if (!mbar_wait(&p_full[t * 2 + (j & 1)], (j >> 1) & 1, p.errors)) {
                         ok = false;
                         break;
                     }
                     // O_t += P_tj V_j (hi part, then lo part; P in tensor memory)
                     tc_fence_after();
-                    const uint64_t vd = dv + (uint64_t)(st * SLOT16);
+                    const uint64_t vd = dv + (uint64_t)(v_st * SLOT16);
+                    const uint32_t pa = base + S_COL + (j & 1) * kTcKeys;
 #pragma unroll
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
                         for (int ks = 0; ks < kTcKeys / 16; ++ks)
-                            tc_mma_tmem_a(base + O_COL, base + S_COL + part * (kTcKeys / 2) + ks * 8,
+                            tc_mma_tmem_a(base, pa + part * (kTcKeys / 2) + ks * 8,
                                           vd + (uint64_t)((ks * 16 * 128) >> 4), id_o,
                                           (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-                    tc_commit(&kv_free[st]);
+                    tc_commit(&o_done[t * 2 + (j & 1)]);
+                    tc_commit(&kv_free[v_st]);
+                    if (j + 2 < ntt) ok = issue_s(j + 2);
                 } else {
                     // this tile's rows never see key tile j: release the slot
-                    // (keeps kv_free's phases in step)
-                    mbar_arrive(&kv_free[st]);
+                    // once it is loaded (keeps kv_free's phases in step)
+                    if (!mbar_wait(&kv_full[v_st], v_round & 1, p.errors)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive(&kv_free[v_st]);
                 }
-                if (++st == p.stages) {
-                    st = 0;
-                    ++round;
+                if (++v_st == p.stages) {
+                    v_st = 0;
+                    ++v_round;
                 }
             }
-            // every MMA of this issuer complete before O is read and the
-            // tensor memory released
-            if (ntt > 0) tc_commit(&fin[t]);
-            if (ntt > 0 && ok) mbar_wait(&fin[t], 0, p.errors);
+            // every MMA of this issuer complete before the tensor memory is released
+            if (ntt > 0) {
+                tc_commit(&fin[t]);
+                mbar_wait(&fin[t], 0, p.errors);
+            }
         }
         __syncwarp();
     } else {
@@ -465,32 +498,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool real = tok < q_len;
             const int pos = real ? first_pos + tok : -1;     // last key of this row
             const uint32_t t_lane = tmem + t * TILE_COLS + ((uint32_t)((warp & 3) * 32) << 16);
-            const int qh = kvh * G + r % G;
-            // ---- this row of Q into tensor memory: element pairs (2c, 2c + 1)
-            // in column c, the A-operand layout of the score product
-            {
-                uint32_t qr[D / 2];
-                if (real) {
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        static_cast<const T*>(p.q) + ((size_t)(qs0 + tok) * p.n_heads + qh) * D);
-#pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
-                        const uint4 v = src[c];
-                        qr[4 * c] = v.x;
-                        qr[4 * c + 1] = v.y;
-                        qr[4 * c + 2] = v.z;
-                        qr[4 * c + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < D / 2; ++c) qr[c] = 0u;
-                }
-#pragma unroll
-                for (int c0 = 0; c0 < D / 2; c0 += 32) tc_st32(t_lane + Q_COL + c0, qr + c0);
-                tc_wait_st();
-                tc_fence_before();
-                mbar_arrive(&q_ready[t]);
-            }
             const float sc = p.scale_log2;
             const bool pos_sc = sc > 0.f;                    // the usual case
             float m_used = -INFINITY;
@@ -500,14 +507,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             const int ntt = ntiles(t);
             for (int j = 0; j < ntt; ++j) {
-                // S_j done: every earlier product of this tile's issuer (the
-                // P V of key tile j - 1 included) is done too
-                const bool w = mbar_wait(&s_full[t], j & 1, p.errors);
+                const int b = j & 1;
+                const bool w = mbar_wait(&s_full[t * 2 + b], (j >> 1) & 1, p.errors);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[kTcKeys];
-                tc_ld32(t_lane + S_COL, sr);
-                tc_ld32(t_lane + S_COL + 32, sr + 32);
+                tc_ld32(t_lane + S_COL + b * kTcKeys, sr);
+                tc_ld32(t_lane + S_COL + b * kTcKeys + 32, sr + 32);
                 tc_wait_ld();
                 const int key0 = j * kTcKeys;
                 const int pm = page_mask(j);
@@ -544,11 +550,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     m_used = tmax;
                 }
                 if (__any_sync(0xffffffffu, grow && !first)) {
-                    // O of this warp's rows (P V up to key tile j - 1, done)
+                    // O of this warp's rows holds P V up to key tile j-1 first
+                    const bool w2 = mbar_wait(&o_done[t * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1,
+                                              p.errors);
+                    if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t ov[32];
-                        tc_ld32(t_lane + O_COL + c0, ov);
+                        tc_ld32(t_lane + c0, ov);
                         tc_wait_ld();
                         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
@@ -558,8 +568,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             ov[c] = __float_as_uint(v.x);
                             ov[c + 1] = __float_as_uint(v.y);
                         }
-                        tc_st32(t_lane + O_COL + c0, ov);
+                        tc_st32(t_lane + c0, ov);
                     }
+                }
+                if (j >= 2) {
+                    // keeps this barrier's phases in step with the waits above
+                    const bool w2 = mbar_wait(&o_done[t * 2 + b], ((j - 2) >> 1) & 1, p.errors);
+                    if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
                 }
                 l4[0] = __fmul2_rn(l4[0], make_float2(alpha, alpha));
                 l4[1] = __fmul2_rn(l4[1], make_float2(alpha, alpha));
@@ -568,8 +583,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float mu = m_used == -INFINITY ? 0.f : m_used;
                 const float2 a2 = make_float2(a, a), nmu2 = make_float2(-mu, -mu);
                 const float2 neg1 = make_float2(-1.f, -1.f);
-                // P = 2^(y a - m) as hi + lo over the S columns just read: hi in
-                // [0, 32), lo in [32, 64), keys 2i and 2i+1 in column i
+                // P = 2^(y a - m) as hi + lo over the S buffer just read: hi in
+                // its columns [0, 32), lo in [32, 64), keys 2i and 2i+1 in column i
                 uint32_t ph[kTcKeys / 2], pl[kTcKeys / 2];
 #pragma unroll
                 for (int i = 0; i < kTcKeys / 2; ++i) {
@@ -580,23 +595,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const float2 lo = __ffma2_rn(unpack2<T>(ph[i]), neg1, pv);
                     pl[i] = pack2<T>(lo.x, lo.y);
                 }
-                tc_st32(t_lane + S_COL, ph);
-                tc_st32(t_lane + S_COL + 32, pl);
+                tc_st32(t_lane + S_COL + b * kTcKeys, ph);
+                tc_st32(t_lane + S_COL + b * kTcKeys + 32, pl);
                 tc_wait_st();
                 tc_fence_before();
-                mbar_arrive(&p_full[t]);
+                mbar_arrive(&p_full[t * 2 + b]);
             }
-            // ---- O / L of this row, once the last P V is done
-            const bool w4 = ok && mbar_wait(&fin[t], 0, p.errors);
+            // ---- O / L of this row
+            const int jl = ntt - 1;
+            const bool w4 = ok && mbar_wait(&o_done[t * 2 + (jl & 1)], (jl >> 1) & 1, p.errors);
             if (__all_sync(0xffffffffu, w4)) {
                 tc_fence_after();
                 const float2 la = __fadd2_rn(l4[0], l4[1]), lb = __fadd2_rn(l4[2], l4[3]);
                 const float l = (la.x + lb.x) + (la.y + lb.y);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int qh = kvh * G + r % G;
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t ov[32];
-                    tc_ld32(t_lane + O_COL + c0, ov);
+                    tc_ld32(t_lane + c0, ov);
                     tc_wait_ld();
                     if (!real) continue;
                     const size_t e = ((size_t)(qs0 + tok) * p.n_heads + qh) * D + c0;
