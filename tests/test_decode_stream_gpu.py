@@ -45,15 +45,17 @@ def _both(lib, tuning, case, split, **kw):
     output with the automatic split."""
     dev = to_device(case)
     tuning(decode_stream=1)
-    auto = run_decode(case, split_tokens=0, dev=dev, **kw)
+    auto = None
     if split == 0:
+        auto = run_decode(case, split_tokens=0, dev=dev, **kw)
         split = lib.decode_split_tokens(case.S, case.H, case.Hk, case.D, case.B,
                                         int(case.context_lens.max()))
     b = run_decode(case, split_tokens=split, dev=dev, **kw)
     tuning(decode_stream=0)
     a = run_decode(case, split_tokens=split, dev=dev, **kw)
     torch.cuda.synchronize()
-    assert torch.equal(_bits(auto), _bits(b))
+    if auto is not None:
+        assert torch.equal(_bits(auto), _bits(b))
     return a, b
 
 
