@@ -11,13 +11,18 @@
 //            PagedAttention 显存物理布局深度剖析", section 二.2: block table.
 //
 // With G query heads per kv head, one page of one kv head is a small dense
-// contraction: S = Q K^T is [G x 16 tokens x head_dim] and O += P V is
-// [G x head_dim x 16 tokens].  One warp per kv head computes both with
-// mma.sync m16n8k16 (bf16/fp16 in, fp32 accumulate), the G query heads
-// being rows 0..G-1 of the 16-row tile.  The scores' accumulator layout is
-// the A-operand layout of P, so P never leaves registers; P enters the P V
-// product as two 16-bit parts (hi + lo) so that its rounding stays at fp32
-// level.
+// contraction.  One warp per kv head computes it with mma.sync m16n8k16
+// (bf16/fp16 in, fp32 accumulate) with the tokens as the 16 rows and the
+// query heads as the 8 columns: S^T = K Q^T (A = 16 tokens x 16 dims of K,
+// B = Q^T, column n = query head n) and O^T += V^T P^T (A = 16 dims x 16
+// tokens of V, B = P^T).  A group of 4 then fills half of each product's
+// columns, a group of 8 all of them -- against a quarter / half with the
+// query heads as rows -- so a 16-token chunk costs head_dim/16 score
+// products and head_dim/16 x 2 value products.  The score accumulators hold
+// P^T by token rows; a lane needs it by head columns for the B operand of
+// the value product, which eight warp shuffles per chunk provide.  P enters
+// that product as two 16-bit parts (hi + lo) so that its rounding stays at
+// fp32 level.
 //
 // Staging: per page and kv head, K and V arrive as head_dim/64 TMA boxes of
 // [B tokens x 64 elements] with 128-byte swizzle: token t's 16-byte chunk c
@@ -101,13 +106,183 @@ __device__ __forceinline__ uint32_t swz(int t, int c) {
     return (uint32_t)(t * 128 + ((c ^ (t & 7)) << 4));
 }
 
+// Running state of one kv head's G query heads in one warp (lane = 4 gid +
+// tig): Q^T as B fragments, O^T accumulators (m-tile j: dims 16j..16j+15,
+// columns = query heads; this lane holds dims 16j + gid and 16j + gid + 8 of
+// heads 2 tig and 2 tig + 1), and the running maximum (log2 domain) and this
+// lane's share of the sum of heads 2 tig and 2 tig + 1.
+template <int D>
+struct MmaHeads {
+    uint32_t qb[D / 16][2];
+    float o[D / 16][4];
+    float m[2];
+    float l[2];
+};
+
+// Query rows qrow0 + h * D (h < G; the rest zero) as the B operand.
+template <int D, typename T>
+__device__ __forceinline__ void mma_heads_start(MmaHeads<D>& st, const T* qrow0, int G, int lane) {
+    const int gid = lane >> 2, tig = lane & 3;
+    const bool real = gid < G;
+    const T* qrow = qrow0 + (size_t)(real ? gid : 0) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t lo = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + tig * 2);
+        const uint32_t hi = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + tig * 2);
+        st.qb[ks][0] = real ? lo : 0u;
+        st.qb[ks][1] = real ? hi : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.f;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+}
+
+// One 16-token chunk (`valid` of its tokens inside the context, 1..16) of
+// one kv head's K and V, swizzled [rows x 128 B] boxes at kbase / vbase,
+// token rows t0 .. t0 + 15 of the boxes.
+template <int D, typename T>
+__device__ __forceinline__ void mma_heads_chunk(MmaHeads<D>& st, uint32_t kbase, uint32_t vbase,
+                                                uint32_t box_bytes, int t0, int valid,
+                                                float scale_log2, int lane) {
+    constexpr int KSTEPS = D / 16;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int mat = lane >> 3, mrow = lane & 7;
+    // ldmatrix matrices: K (tokens 0-7, c), (0-7, c+1), (8-15, c), (8-15, c+1);
+    // V transposed: (tokens 0-7, c), (8-15, c), (0-7, c+1), (8-15, c+1)
+    const int k_tok = t0 + (mat >> 1) * 8 + mrow, k_dc = mat & 1;
+    const int v_tok = t0 + (mat & 1) * 8 + mrow, v_dc = mat >> 1;
+
+    // ---- S^T = K Q^T: rows = tokens, columns = query heads
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int h = ks / 4;
+        const int c = (ks % 4) * 2 + k_dc;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + h * box_bytes + swz(k_tok, c), b0, b1, b2, b3);
+        const uint32_t a[4] = {b0, b2, b1, b3};
+        mma16816<T>(s, a, st.qb[ks][0], st.qb[ks][1]);
+    }
+    // this lane: tokens gid (s0, s1) and gid + 8 (s2, s3) of heads 2 tig, 2 tig + 1
+    const bool v0 = gid < valid, v1 = gid + 8 < valid;
+    const float x0 = v0 ? s[0] * scale_log2 : -INFINITY;
+    const float x1 = v0 ? s[1] * scale_log2 : -INFINITY;
+    const float x2 = v1 ? s[2] * scale_log2 : -INFINITY;
+    const float x3 = v1 ? s[3] * scale_log2 : -INFINITY;
+    float c0 = fmaxf(x0, x2), c1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, off));
+        c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, off));
+    }
+    const float mn0 = fmaxf(st.m[0], c0), mn1 = fmaxf(st.m[1], c1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(st.m[0] - mu0), al1 = exp2f(st.m[1] - mu1);
+    st.m[0] = mn0;
+    st.m[1] = mn1;
+    const float p0 = exp2f(x0 - mu0), p1 = exp2f(x1 - mu1);
+    const float p2 = exp2f(x2 - mu0), p3 = exp2f(x3 - mu1);
+    st.l[0] = st.l[0] * al0 + (p0 + p2);
+    st.l[1] = st.l[1] * al1 + (p1 + p3);
+    // P in two 16-bit parts (hi = round(p), lo = round(p - hi)), packed by
+    // token: (head 2 tig, head 2 tig + 1) of token gid and of token gid + 8
+    const uint32_t hA = pack2<T>(p0, p1), hB = pack2<T>(p2, p3);
+    const float2 fA = unpack2<T>(hA), fB = unpack2<T>(hB);
+    const uint32_t lA = pack2<T>(p0 - fA.x, p1 - fA.y), lB = pack2<T>(p2 - fB.x, p3 - fB.y);
+    // ---- P^T as the B operand: this lane (column = head gid) needs tokens
+    // 2 tig, 2 tig + 1 (k 0-7) and 2 tig + 8, 2 tig + 9 (k 8-15), which lanes
+    // 4 (2 tig) + gid / 2 and 4 (2 tig + 1) + gid / 2 hold (half gid % 2)
+    const int srcA = 4 * (2 * tig) + (gid >> 1), srcB = srcA + 4;
+    const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;   // the half of this lane's head
+    const uint32_t hAa = __shfl_sync(0xffffffffu, hA, srcA), hAb = __shfl_sync(0xffffffffu, hA, srcB);
+    const uint32_t hBa = __shfl_sync(0xffffffffu, hB, srcA), hBb = __shfl_sync(0xffffffffu, hB, srcB);
+    const uint32_t lAa = __shfl_sync(0xffffffffu, lA, srcA), lAb = __shfl_sync(0xffffffffu, lA, srcB);
+    const uint32_t lBa = __shfl_sync(0xffffffffu, lB, srcA), lBb = __shfl_sync(0xffffffffu, lB, srcB);
+    // (keys 2 tig, 2 tig + 1) -> low / high half of one register
+    const uint32_t bh0 = __byte_perm(hAa, hAb, sel);
+    const uint32_t bh1 = __byte_perm(hBa, hBb, sel);
+    const uint32_t bl0 = __byte_perm(lAa, lAb, sel);
+    const uint32_t bl1 = __byte_perm(lBa, lBb, sel);
+    // ---- O^T = O^T * alpha + V^T P^T; V rows past the context may hold
+    // anything (NaN included): P is 0 there, but 0 * NaN is not, so those
+    // rows are cleared in the A fragments (tokens 2 tig, 2 tig + 1 in a0/a1,
+    // 2 tig + 8, 2 tig + 9 in a2/a3)
+    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    if (valid < 16) {
+        vm0 = (tig * 2 < valid ? 0x0000ffffu : 0u) | (tig * 2 + 1 < valid ? 0xffff0000u : 0u);
+        vm1 = (8 + tig * 2 < valid ? 0x0000ffffu : 0u) | (8 + tig * 2 + 1 < valid ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+        st.o[j][0] *= al0;
+        st.o[j][1] *= al1;
+        st.o[j][2] *= al0;
+        st.o[j][3] *= al1;
+        const int h = j / 4;
+        const int c = (j % 4) * 2 + v_dc;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(vbase + h * box_bytes + swz(v_tok, c), b0, b1, b2, b3);
+        const uint32_t a[4] = {b0 & vm0, b2 & vm0, b1 & vm1, b3 & vm1};
+        mma16816<T>(st.o[j], a, bh0, bh1);
+        mma16816<T>(st.o[j], a, bl0, bl1);
+    }
+}
+
+// The unit's result: normalised rows of the real query heads qh0 .. qh0+G-1
+// to the output (one split) or to the split partials.
+template <int D>
+__device__ __forceinline__ void mma_heads_finish(const MmaHeads<D>& st, const DecodeParams& p,
+                                                 int s, int qh0, int G, int n_splits, int split,
+                                                 int lane) {
+    const int gid = lane >> 2, tig = lane & 3;
+    float l0 = st.l[0], l1 = st.l[1];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int hh = 2 * tig + e;
+        if (hh >= G) continue;
+        const float l = e ? l1 : l0;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int qh = qh0 + hh;
+        if (n_splits == 1) {
+            const size_t row = ((size_t)s * p.n_heads + qh) * D;
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                const float a = st.o[j][e] * inv, b = st.o[j][2 + e] * inv;
+                const size_t d0 = row + j * 16 + gid, d1 = d0 + 8;
+                if (p.out_dtype == PKV_F32) {
+                    reinterpret_cast<float*>(p.out)[d0] = a;
+                    reinterpret_cast<float*>(p.out)[d1] = b;
+                } else {
+                    const uint32_t w = pack_out(a, b, p.out_dtype);
+                    reinterpret_cast<uint16_t*>(p.out)[d0] = (uint16_t)(w & 0xffffu);
+                    reinterpret_cast<uint16_t*>(p.out)[d1] = (uint16_t)(w >> 16);
+                }
+            }
+        } else {
+            const size_t unit = ((size_t)s * p.n_heads + qh) * p.max_splits + split;
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                p.ws_o[unit * D + j * 16 + gid] = st.o[j][e] * inv;
+                p.ws_o[unit * D + j * 16 + gid + 8] = st.o[j][2 + e] * inv;
+            }
+            if (gid == 0)
+                *reinterpret_cast<float2*>(p.ws_ml + unit * 2) =
+                    make_float2(st.m[e], l);
+        }
+    }
+}
+
 // One CTA's work (sequence s, kv-head group hg, split) of the problem p.
 template <int D, int BS, typename T>
 __device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                                const DecodeParams& p, int split, int hg, int s) {
     constexpr int HALVES = D / 64;        // 128-byte boxes per token row
-    constexpr int KSTEPS = D / 16;        // k-steps of the score MMA
-    constexpr int NT = D / 8;             // n-tiles of the P V MMA
     constexpr uint32_t BOX = BS * 128;    // bytes of one [BS x 64] box
     static_assert(BS % 16 == 0 && D % 64 == 0, "shape");
 
@@ -208,170 +383,33 @@ __device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CU
         // ================= consumers: one warp per kv head =================
         const int kv_local = warp - 1;
         const int qh0 = (hg * HPC + kv_local) * G;
-        const int gid = lane >> 2;     // fragment row (query head) of this lane
-        const int tig = lane & 3;      // pair of columns of this lane
-        const bool row_real = gid < G;
-
-        // Q as the A operand: rows = query heads (rows >= G and 8..15 zero)
-        uint32_t qa[KSTEPS][4];
-        {
-            const T* qrow = reinterpret_cast<const T*>(p.q) +
-                            ((size_t)s * p.n_heads + qh0 + (row_real ? gid : 0)) * D;
-#pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                const uint32_t lo = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + tig * 2);
-                const uint32_t hi = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + tig * 2);
-                qa[ks][0] = row_real ? lo : 0u;
-                qa[ks][1] = 0u;
-                qa[ks][2] = row_real ? hi : 0u;
-                qa[ks][3] = 0u;
-            }
-        }
-
-        float o[NT][4];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-        float m_row = -INFINITY;   // running max of this lane's row
-        float l_part = 0.f;        // this lane's share of the row's sum
-
-        // ldmatrix row addresses (lane-dependent parts)
-        const int mat = lane >> 3;          // which 8x8 matrix this lane addresses
-        const int mrow = lane & 7;          // row inside it
-        // scores: matrices (tokens 0-7, c), (tokens 0-7, c+1), (8-15, c), (8-15, c+1)
-        const int k_tok = (mat >> 1) * 8 + mrow;
-        const int k_dc = mat & 1;
-        // P V: matrices (tokens 0-7, n), (8-15, n), (0-7, n+1), (8-15, n+1)
-        const int v_tok = (mat & 1) * 8 + mrow;
-        const int v_dc = mat >> 1;
-
+        MmaHeads<D> st;
+        mma_heads_start<D, T>(st, reinterpret_cast<const T*>(p.q) + ((size_t)s * p.n_heads + qh0) * D,
+                              G, lane);
         for (int i = 0; i < n_pages; ++i) {
-            const int st = i % p.stages;
-            if (!mbar_wait(&full[st], (i / p.stages) & 1, p.errors)) {
+            const int slot = i % p.stages;
+            if (!mbar_wait(&full[slot], (i / p.stages) & 1, p.errors)) {
                 atomicExch(s_abort, 1);
                 break;
             }
             if (s_bid[i] >= 0) {
-                const uint32_t kbase = smem_addr(ring + (size_t)st * stage_bytes +
+                const uint32_t kbase = smem_addr(ring + (size_t)slot * stage_bytes +
                                                  kv_local * head_bytes);
-                const uint32_t vbase = smem_addr(ring + (size_t)st * stage_bytes +
+                const uint32_t vbase = smem_addr(ring + (size_t)slot * stage_bytes +
                                                  (HPC + kv_local) * head_bytes);
                 const int page_tok = tok_begin + i * BS;
 #pragma unroll
                 for (int ch = 0; ch < BS / 16; ++ch) {
                     const int valid = min(16, tok_end - (page_tok + ch * 16));
                     if (valid <= 0) break;
-                    // ---- S = Q K^T for 16 tokens (two n-tiles of 8)
-                    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks) {
-                        const int h = ks / 4;                  // which 64-wide half
-                        const int c = (ks % 4) * 2 + k_dc;     // 16-byte chunk in the row
-                        const int t = ch * 16 + k_tok;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(kbase + h * BOX + swz(t, c), b0, b1, b2, b3);
-                        mma16816<T>(sc[0], qa[ks], b0, b1);
-                        mma16816<T>(sc[1], qa[ks], b2, b3);
-                    }
-                    // ---- online softmax on this lane's row (4 of its 16 scores)
-                    float x[4];
-                    x[0] = sc[0][0] * p.scale_log2;
-                    x[1] = sc[0][1] * p.scale_log2;
-                    x[2] = sc[1][0] * p.scale_log2;
-                    x[3] = sc[1][1] * p.scale_log2;
-                    if (tig * 2 >= valid) x[0] = -INFINITY;
-                    if (tig * 2 + 1 >= valid) x[1] = -INFINITY;
-                    if (8 + tig * 2 >= valid) x[2] = -INFINITY;
-                    if (8 + tig * 2 + 1 >= valid) x[3] = -INFINITY;
-                    float cmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
-                    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
-                    const float m_new = fmaxf(m_row, cmax);
-                    const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-                    const float alpha = exp2f(m_row - mu);
-                    m_row = m_new;
-                    const float p0 = exp2f(x[0] - mu), p1 = exp2f(x[1] - mu);
-                    const float p2 = exp2f(x[2] - mu), p3 = exp2f(x[3] - mu);
-                    l_part = l_part * alpha + ((p0 + p1) + (p2 + p3));
-                    // V rows past the context may hold anything (NaN included):
-                    // P is 0 there, but 0 * NaN is not, so those rows are
-                    // cleared in the B fragments of the last chunk.  Lane
-                    // fragments hold tokens 2*tig, 2*tig+1 (low / high half)
-                    // and 8 more in the second register.
-                    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-                    if (valid < 16) {
-                        vm0 = (tig * 2 < valid ? 0x0000ffffu : 0u) |
-                              (tig * 2 + 1 < valid ? 0xffff0000u : 0u);
-                        vm1 = (8 + tig * 2 < valid ? 0x0000ffffu : 0u) |
-                              (8 + tig * 2 + 1 < valid ? 0xffff0000u : 0u);
-                    }
-                    // P in two parts of the input type (hi = round(p), lo =
-                    // round(p - hi)): one 16-bit rounding of the weights would
-                    // cost ~2^-9 relative in O; hi + lo leaves ~2^-17.
-                    uint32_t pa[4], pl[4];
-                    pa[0] = pack2<T>(p0, p1);
-                    pa[2] = pack2<T>(p2, p3);
-                    {
-                        const float2 h01 = unpack2<T>(pa[0]), h23 = unpack2<T>(pa[2]);
-                        pl[0] = pack2<T>(p0 - h01.x, p1 - h01.y);
-                        pl[2] = pack2<T>(p2 - h23.x, p3 - h23.y);
-                    }
-                    pa[1] = pa[3] = pl[1] = pl[3] = 0u;
-                    // ---- O = O * alpha + P V (n-tiles of 8 dims, two per ldmatrix)
-#pragma unroll
-                    for (int j = 0; j < NT; j += 2) {
-                        o[j][0] *= alpha;
-                        o[j][1] *= alpha;
-                        o[j + 1][0] *= alpha;
-                        o[j + 1][1] *= alpha;
-                        const int h = j / 8;
-                        const int c = (j % 8) + v_dc;
-                        const int t = ch * 16 + v_tok;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_trans(vbase + h * BOX + swz(t, c), b0, b1, b2, b3);
-                        b0 &= vm0;
-                        b1 &= vm1;
-                        b2 &= vm0;
-                        b3 &= vm1;
-                        mma16816<T>(o[j], pa, b0, b1);
-                        mma16816<T>(o[j + 1], pa, b2, b3);
-                        mma16816<T>(o[j], pl, b0, b1);
-                        mma16816<T>(o[j + 1], pl, b2, b3);
-                    }
+                    mma_heads_chunk<D, T>(st, kbase, vbase, BOX, ch * 16, valid, p.scale_log2,
+                                          lane);
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            if (lane == 0) mbar_arrive(&empty[slot]);
         }
-
-        // ---- L of each row: the 4 lanes of a row hold its parts
-        float l_row = l_part;
-        l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
-        l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-        if (row_real) {
-            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-            const int qh = qh0 + gid;
-            if (n_splits == 1) {
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const size_t e = ((size_t)s * p.n_heads + qh) * D + j * 8 + tig * 2;
-                    if (p.out_dtype == PKV_F32) {
-                        *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.out) + e) =
-                            make_float2(o[j][0] * inv, o[j][1] * inv);
-                    } else {
-                        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + e) =
-                            pack_out(o[j][0] * inv, o[j][1] * inv, p.out_dtype);
-                    }
-                }
-            } else {
-                const size_t unit = ((size_t)s * p.n_heads + qh) * p.max_splits + split;
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-                    *reinterpret_cast<float2*>(p.ws_o + unit * D + j * 8 + tig * 2) =
-                        make_float2(o[j][0] * inv, o[j][1] * inv);
-                if (tig == 0)
-                    *reinterpret_cast<float2*>(p.ws_ml + unit * 2) = make_float2(m_row, l_row);
-            }
-        }
+        mma_heads_finish<D>(st, p, s, qh0, G, n_splits, split, lane);
     }
 
     __syncthreads();

@@ -90,8 +90,6 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                                    const __grid_constant__ CUtensorMap tm_v,
                                    const __grid_constant__ DecodeParams p) {
     constexpr int HALVES = D / 64;        // 128-byte boxes per token row
-    constexpr int KSTEPS = D / 16;        // k-steps of the score MMA
-    constexpr int NT = D / 8;             // n-tiles of the P V MMA
     constexpr uint32_t BOX = BS * 128;    // bytes of one [BS x 64] box
     static_assert(BS % 16 == 0 && D % 64 == 0, "shape");
 
@@ -422,160 +420,39 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     } else {
         // ================= consumers: one warp per kv head =================
         const int kv_local = warp - 1;
-        const int gid = lane >> 2;     // fragment row (query head) of this lane
-        const int tig = lane & 3;      // pair of columns of this lane
-        const bool row_real = gid < G;
-        const int mat = lane >> 3;
-        const int mrow = lane & 7;
-        const int k_tok = (mat >> 1) * 8 + mrow;
-        const int k_dc = mat & 1;
-        const int v_tok = (mat & 1) * 8 + mrow;
-        const int v_dc = mat >> 1;
-
-        uint32_t qa[KSTEPS][4];
-        float o[NT][4];
-        float m_row = -INFINITY, l_part = 0.f;
+        MmaHeads<D> st;
         for (int g = 0;; ++g) {
-            const int st = g % stages;
-            if (!mbar_wait(&full[st], (g / stages) & 1, p.errors)) {
+            const int slot_i = g % stages;
+            if (!mbar_wait(&full[slot_i], (g / stages) & 1, p.errors)) {
                 *s_abort = 1;
                 break;
             }
-            const StreamSlot r = slot[st];
+            const StreamSlot r = slot[slot_i];
             if (r.s < 0) break;
-            if (r.page == 0) {
-                // query rows of this unit's kv head: rows = query heads
-                const T* qrow = reinterpret_cast<const T*>(qbuf + (size_t)st * q_bytes) +
-                                ((size_t)kv_local * G + (row_real ? gid : 0)) * D;
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks) {
-                    const uint32_t lo = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + tig * 2);
-                    const uint32_t hi =
-                        *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + tig * 2);
-                    qa[ks][0] = row_real ? lo : 0u;
-                    qa[ks][1] = 0u;
-                    qa[ks][2] = row_real ? hi : 0u;
-                    qa[ks][3] = 0u;
-                }
-#pragma unroll
-                for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-                m_row = -INFINITY;
-                l_part = 0.f;
-            }
+            if (r.page == 0)
+                // query rows of this unit's kv head (loaded into the slot)
+                mma_heads_start<D, T>(st, reinterpret_cast<const T*>(qbuf + (size_t)slot_i * q_bytes) +
+                                              (size_t)kv_local * G * D,
+                                      G, lane);
             if (r.valid) {
-                const uint32_t kbase = smem_addr(ring + (size_t)st * stage_bytes +
+                const uint32_t kbase = smem_addr(ring + (size_t)slot_i * stage_bytes +
                                                  kv_local * head_bytes);
-                const uint32_t vbase = smem_addr(ring + (size_t)st * stage_bytes +
+                const uint32_t vbase = smem_addr(ring + (size_t)slot_i * stage_bytes +
                                                  (HPC + kv_local) * head_bytes);
                 const int page_tok = r.tok_begin + r.page * BS;
 #pragma unroll
                 for (int ch = 0; ch < BS / 16; ++ch) {
                     const int valid = min(16, r.tok_end - (page_tok + ch * 16));
                     if (valid <= 0) break;
-                    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks) {
-                        const int h = ks / 4;
-                        const int c = (ks % 4) * 2 + k_dc;
-                        const int t = ch * 16 + k_tok;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(kbase + h * BOX + swz(t, c), b0, b1, b2, b3);
-                        mma16816<T>(sc[0], qa[ks], b0, b1);
-                        mma16816<T>(sc[1], qa[ks], b2, b3);
-                    }
-                    float x[4];
-                    x[0] = sc[0][0] * p.scale_log2;
-                    x[1] = sc[0][1] * p.scale_log2;
-                    x[2] = sc[1][0] * p.scale_log2;
-                    x[3] = sc[1][1] * p.scale_log2;
-                    if (tig * 2 >= valid) x[0] = -INFINITY;
-                    if (tig * 2 + 1 >= valid) x[1] = -INFINITY;
-                    if (8 + tig * 2 >= valid) x[2] = -INFINITY;
-                    if (8 + tig * 2 + 1 >= valid) x[3] = -INFINITY;
-                    float cmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
-                    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
-                    const float m_new = fmaxf(m_row, cmax);
-                    const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-                    const float alpha = exp2f(m_row - mu);
-                    m_row = m_new;
-                    const float p0 = exp2f(x[0] - mu), p1 = exp2f(x[1] - mu);
-                    const float p2 = exp2f(x[2] - mu), p3 = exp2f(x[3] - mu);
-                    l_part = l_part * alpha + ((p0 + p1) + (p2 + p3));
-                    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-                    if (valid < 16) {
-                        vm0 = (tig * 2 < valid ? 0x0000ffffu : 0u) |
-                              (tig * 2 + 1 < valid ? 0xffff0000u : 0u);
-                        vm1 = (8 + tig * 2 < valid ? 0x0000ffffu : 0u) |
-                              (8 + tig * 2 + 1 < valid ? 0xffff0000u : 0u);
-                    }
-                    uint32_t pa[4], pl[4];
-                    pa[0] = pack2<T>(p0, p1);
-                    pa[2] = pack2<T>(p2, p3);
-                    {
-                        const float2 h01 = unpack2<T>(pa[0]), h23 = unpack2<T>(pa[2]);
-                        pl[0] = pack2<T>(p0 - h01.x, p1 - h01.y);
-                        pl[2] = pack2<T>(p2 - h23.x, p3 - h23.y);
-                    }
-                    pa[1] = pa[3] = pl[1] = pl[3] = 0u;
-#pragma unroll
-                    for (int j = 0; j < NT; j += 2) {
-                        o[j][0] *= alpha;
-                        o[j][1] *= alpha;
-                        o[j + 1][0] *= alpha;
-                        o[j + 1][1] *= alpha;
-                        const int h = j / 8;
-                        const int c = (j % 8) + v_dc;
-                        const int t = ch * 16 + v_tok;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_trans(vbase + h * BOX + swz(t, c), b0, b1, b2, b3);
-                        b0 &= vm0;
-                        b1 &= vm1;
-                        b2 &= vm0;
-                        b3 &= vm1;
-                        mma16816<T>(o[j], pa, b0, b1);
-                        mma16816<T>(o[j + 1], pa, b2, b3);
-                        mma16816<T>(o[j], pl, b0, b1);
-                        mma16816<T>(o[j + 1], pl, b2, b3);
-                    }
+                    mma_heads_chunk<D, T>(st, kbase, vbase, BOX, ch * 16, valid, p.scale_log2,
+                                          lane);
                 }
             }
-            if (r.page == r.n_pages - 1) {
-                // ---- the unit's output (or split partial)
-                float l_row = l_part;
-                l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
-                l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-                if (row_real) {
-                    const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-                    const int qh = (r.hg * HPC + kv_local) * G + gid;
-                    if (r.n_splits == 1) {
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            const size_t e = ((size_t)r.s * p.n_heads + qh) * D + j * 8 + tig * 2;
-                            if (p.out_dtype == PKV_F32) {
-                                *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.out) + e) =
-                                    make_float2(o[j][0] * inv, o[j][1] * inv);
-                            } else {
-                                *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) +
-                                                             e) =
-                                    pack_out(o[j][0] * inv, o[j][1] * inv, p.out_dtype);
-                            }
-                        }
-                    } else {
-                        const size_t unit =
-                            ((size_t)r.s * p.n_heads + qh) * p.max_splits + r.split;
-#pragma unroll
-                        for (int j = 0; j < NT; ++j)
-                            *reinterpret_cast<float2*>(p.ws_o + unit * D + j * 8 + tig * 2) =
-                                make_float2(o[j][0] * inv, o[j][1] * inv);
-                        if (tig == 0)
-                            *reinterpret_cast<float2*>(p.ws_ml + unit * 2) =
-                                make_float2(m_row, l_row);
-                    }
-                }
-            }
+            if (r.page == r.n_pages - 1)
+                mma_heads_finish<D>(st, p, r.s, (r.hg * HPC + kv_local) * G, G, r.n_splits,
+                                    r.split, lane);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            if (lane == 0) mbar_arrive(&empty[slot_i]);
         }
     }
 
