@@ -144,8 +144,10 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
  * the current device: 512 tokens; 1024 when max_context_len is 8192 or more
  * and there are at most 2 x SMs (sequence, kv-head group) units; the whole
  * context (no split, no merge) when the units fill the SMs 16 times over;
- * rounded to whole blocks and capped at the context.  Returns 0 for an
- * unsupported shape.
+ * 128 tokens when the decode streams its units through resident CTAs
+ * (groups of 4 or 8 query heads, at most 2048 sequences, max_context_len at
+ * most 1536: many short contexts); rounded to whole blocks and capped at the
+ * context.  Returns 0 for an unsupported shape.
  */
 PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, int head_dim,
                                     int block_size, int max_context_len);
@@ -162,7 +164,10 @@ PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, i
  * query head h reads KV head h / (n_heads / n_kv_heads).  Computed in one
  * pass per work unit with the [SWAP] OnlineSoftmax recurrence in fp32; long
  * contexts are cut into splits of split_tokens whose partial (M, L, O)
- * states are merged by the same recurrence in a second kernel.
+ * states are merged by the same recurrence in a second kernel.  A work unit
+ * is (sequence, group of kv heads, split): one CTA each, or, for groups of 4
+ * or 8 query heads with short contexts (see pkv_decode_split_tokens), a
+ * grid of resident CTAs that each stream an equal share of the units' pages.
  *
  *   out          device, [num_seqs, n_heads, head_dim] of out_dtype
  *                (F16, BF16 or F32), written completely.  A sequence with

@@ -190,8 +190,14 @@ constexpr int kDefaultSplitTokens = 512;
 // are merged as usual.
 constexpr int kStreamSplitTokens = 128;
 // The streaming decode is chosen (knob PKV_TUNE_DECODE_STREAM unset) for
-// tensor-core decodes whose longest context is at most this long.
-constexpr int kStreamMaxContext = 0;
+// tensor-core decodes whose longest context is at most this long, with a
+// two-page ring.  GB300, continuous-batching step (256 sequences, Pareto
+// lengths, longest 1234 tokens, 32 / 8 heads): 32.4 us per decode call
+// against 37.5 us one CTA per unit; with contexts up to 2048 tokens (128
+// sequences of U[256, 2048]) it loses (107 us against 87 us), and more so
+// at 32K tokens.
+constexpr int kStreamMaxContext = 1536;
+constexpr int kStreamStages = 2;
 // Few (sequence, head-group) units with contexts of 8K tokens or more: every
 // unit is cut into many pieces anyway, and at 1024 tokens a piece the GPU stays
 // as full while each CTA pays its prologue and writes its partials half as
@@ -348,12 +354,15 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
                 (stream_knob >= 0 ? stream_knob != 0 : max_context_len <= kStreamMaxContext);
     if (c->stream) {
         // its shared memory must fit (the per-unit kernel runs otherwise)
+        const int stages = tuned(PKV_TUNE_DECODE_STAGES) ? c->stages : kStreamStages;
         const int pages = split_tokens > 0 ? split_tokens / block_size
                                            : (kStreamSplitTokens + block_size - 1) / block_size;
         const size_t limit = smem_optin > 0 ? smem_optin : (size_t)227 * 1024;
         if (pkv::decode_stream_smem_bytes(head_dim, block_size, n_heads / n_kv_heads, 2, c->hpc,
-                                          c->stages, pages, num_seqs) > limit)
+                                          stages, pages, num_seqs) > limit)
             c->stream = false;
+        else
+            c->stages = stages;
     }
     if (split_tokens == 0) {
         split_tokens = c->stream && !tuned(PKV_TUNE_DECODE_SPLIT)
