@@ -423,7 +423,7 @@ __device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CU
 }
 
 template <int D, int BS, typename T>
-__global__ void __launch_bounds__(kMmaMaxThreads, 2)
+__global__ void __launch_bounds__(kMmaMaxThreads, 1)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ DecodeParams p) {

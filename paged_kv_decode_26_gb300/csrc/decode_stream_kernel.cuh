@@ -85,7 +85,7 @@ __device__ __forceinline__ void bulk_load_q(void* dst_smem, const void* src, uin
 }
 
 template <int D, int BS, typename T>
-__global__ void __launch_bounds__(kMmaMaxThreads, 2)
+__global__ void __launch_bounds__(kMmaMaxThreads, 1)
     paged_decode_mma_stream_kernel(const __grid_constant__ CUtensorMap tm_k,
                                    const __grid_constant__ CUtensorMap tm_v,
                                    const __grid_constant__ DecodeParams p) {
