@@ -16,8 +16,15 @@ Under torchrun each rank runs its own replica (own sequences, own pools):
 decode is data-parallel by sequence with no exchange, so scaling is weak and
 the value is the bytes all ranks read divided by the slowest rank's time.
 
---impl reference times the fp64 CPU oracle on a bounded sample of the same
-workload instead (the reference arm of this benchmark).
+--impl reference times the fp64 CPU oracle on the host cores instead (the
+reference arm of this benchmark): the same workload's whole step, or an
+equal share of its sequences when the run would take more than about two
+minutes.
+
+On one GPU with the default workload the line also carries `per_config`:
+the other stated workloads (tiny per launch and as 1100 problems in one
+batched launch, gqa_prefix, long_context, continuous with its block copies)
+measured the same way, each with the oracle's GB/s on the same inputs.
 
 Prints one JSON line (rank 0).
 """
