@@ -111,7 +111,8 @@ typedef enum pkv_tune_knob {
     PKV_TUNE_SWAP_STAGES = 14,    /* bulk block copy: copies in flight per CTA, 2..8 */
     PKV_TUNE_SWAP_CTAS = 15,      /* bulk block copy: CTAs per SM */
     PKV_TUNE_SWAP_HINT = 16,      /* bulk block copy L2 hint: 0 none, 1 evict-first */
-    PKV_TUNE_DECODE_STREAM = 17,  /* 0/1: tensor-core decode by resident CTAs streaming units */
+    PKV_TUNE_DECODE_STREAM = 17,  /* 0/1: tensor-core decode by resident CTAs taking equal
+                                     page shares (automatic split only) */
     PKV_TUNE_COUNT = 18
 } pkv_tune_knob;
 
@@ -133,7 +134,9 @@ PKV_API pkv_status pkv_device_errors(uint32_t* flags, int clear);
  * Workspace bytes paged_attn_decode needs for the given problem and split
  * length (split_tokens = 0 means the automatic choice; the same arguments
  * must then be passed to the decode call).  Returns 0 when no workspace is
- * needed (every sequence fits one split).
+ * needed (every sequence fits one split; for the streaming decode, every
+ * context fits one block).  The streaming decode's workspace holds two
+ * partial states per resident CTA and does not grow with num_seqs.
  */
 PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads,
                                           int head_dim, int block_size, int max_context_len,
@@ -144,10 +147,11 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
  * the current device: 512 tokens; 1024 when max_context_len is 8192 or more
  * and there are at most 2 x SMs (sequence, kv-head group) units; the whole
  * context (no split, no merge) when the units fill the SMs 16 times over;
- * 128 tokens when the decode streams its units through resident CTAs
- * (groups of 4 or 8 query heads, at most 2048 sequences, max_context_len at
- * most 1536: many short contexts); rounded to whole blocks and capped at the
- * context.  Returns 0 for an unsupported shape.
+ * the whole context when the decode streams through resident CTAs (groups
+ * of 4 or 8 query heads, at most 2048 sequences, max_context_len at most
+ * 1536: many short contexts), which cut the work at equal page shares
+ * instead of at splits; rounded to whole blocks and capped at the context.
+ * Returns 0 for an unsupported shape.
  */
 PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, int head_dim,
                                     int block_size, int max_context_len);
@@ -165,9 +169,12 @@ PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, i
  * pass per work unit with the [SWAP] OnlineSoftmax recurrence in fp32; long
  * contexts are cut into splits of split_tokens whose partial (M, L, O)
  * states are merged by the same recurrence in a second kernel.  A work unit
- * is (sequence, group of kv heads, split): one CTA each, or, for groups of 4
- * or 8 query heads with short contexts (see pkv_decode_split_tokens), a
- * grid of resident CTAs that each stream an equal share of the units' pages.
+ * is (sequence, group of kv heads, split), one CTA each.  For groups of 4 or
+ * 8 query heads with short contexts and split_tokens = 0 (see
+ * pkv_decode_split_tokens) a grid of resident CTAs runs instead, each taking
+ * an exactly equal share of all (sequence, kv-head group, block) positions;
+ * a context that a share boundary cuts leaves one partial state per CTA,
+ * merged by the same recurrence in a second kernel.
  *
  *   out          device, [num_seqs, n_heads, head_dim] of out_dtype
  *                (F16, BF16 or F32), written completely.  A sequence with
@@ -184,7 +191,8 @@ PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, i
  *   max_context_len  host-side upper bound of context_lens (sizes the grid;
  *                the metadata's max_decode_seq_len).  A longer context is
  *                clamped and flagged PKV_DEVERR_CONTEXT.
- *   split_tokens tokens per split (a multiple of block_size), 0 = automatic
+ *   split_tokens tokens per split (a multiple of block_size), 0 = automatic;
+ *                an explicit length always selects one CTA per unit
  *   workspace    device, >= pkv_decode_workspace_bytes(...) bytes, 256-byte
  *                aligned; may be NULL when that size is 0.  Scratch only:
  *                contents on entry are ignored.
@@ -201,8 +209,8 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
 
 /*
  * paged_attn_decode_append -- kv_append followed by paged_attn_decode, in
- * one launch: the decode CTA of each sequence's last split first writes
- * k_new[s] and v_new[s] ([num_seqs, n_kv_heads, head_dim] of kv_dtype,
+ * one launch: the decode CTA that reads each sequence's last block (of its
+ * last split, or of its streaming share) first writes k_new[s] and v_new[s] ([num_seqs, n_kv_heads, head_dim] of kv_dtype,
  * 16-byte aligned) into pool row slot_mapping[s] (int64 [num_seqs], 8-byte
  * aligned; -1 skips, a slot outside the pool is skipped and flagged
  * PKV_DEVERR_SLOT) for its kv heads, then decodes.  context_lens already

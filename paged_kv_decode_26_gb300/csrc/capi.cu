@@ -179,23 +179,19 @@ struct DecodeConfig {
     int max_pages;
     size_t smem;
     int threads;
-    bool stream;  // tensor-core decode by resident CTAs streaming the units
+    bool stream;      // tensor-core decode by resident CTAs streaming equal page shares
+    int stream_ctas;  // its grid is at most this many CTAs (sizes the workspace)
 };
 
 constexpr int kDefaultSplitTokens = 512;
-// Split length of the streaming decode when the caller leaves it to the
-// library: a CTA's share of the work is a few pages when contexts are short,
-// and a unit longer than that becomes the tail (one CTA works through it
-// alone), so units are kept short; the partials of the few long contexts
-// are merged as usual.
-constexpr int kStreamSplitTokens = 128;
 // The streaming decode is chosen (knob PKV_TUNE_DECODE_STREAM unset) for
-// tensor-core decodes whose longest context is at most this long, with a
-// two-page ring.  GB300, continuous-batching step (256 sequences, Pareto
-// lengths, longest 1234 tokens, 32 / 8 heads): 32.4 us per decode call
-// against 37.5 us one CTA per unit; with contexts up to 2048 tokens (128
-// sequences of U[256, 2048]) it loses (107 us against 87 us), and more so
-// at 32K tokens.
+// tensor-core decodes with the automatic split whose longest context is at
+// most this long, with a two-page ring.  GB300, decode call by CUDA events:
+// continuous-batching step (256 sequences, Pareto lengths, longest 1235
+// tokens, 32 / 8 heads) 25.6 us against 37.5 us one CTA per unit; with
+// longer contexts the per-unit kernel's three-page ring streams faster
+// (128 sequences of U[256, 2048] tokens: 96.9 against 86.7 us; 32K-token
+// log-uniform GQA: 431 against 398 us).
 constexpr int kStreamMaxContext = 1536;
 constexpr int kStreamStages = 2;
 // Few (sequence, head-group) units with contexts of 8K tokens or more: every
@@ -333,7 +329,7 @@ int cta_order(int max_splits, int num_seqs) {
 
 pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, int block_size,
                        int max_context_len, int split_tokens, int sm_count, DecodeConfig* c,
-                       bool allow_stream = true, size_t smem_optin = 0) {
+                       bool allow_stream = true, size_t smem_optin = 0, int smem_per_sm = 0) {
     shape_config(n_heads, n_kv_heads, head_dim, block_size, c);
     // Too few (sequence, head-group) units to occupy the SMs: two kv heads per
     // CTA give more, shorter CTAs (measured on the tiny workload, 4 sequences
@@ -344,64 +340,87 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
         shape_config_hpc(n_heads, n_kv_heads, head_dim, block_size, 2, &narrow);
         *c = narrow;
     }
-    // Streaming decode: the tensor-core consumer, at most kStreamMaxSeqs
-    // sequences (their lengths live in shared memory), 32-bit page counts.
-    const long long all_pages = (long long)num_seqs * n_kv_heads *
-                                (((long long)max_context_len + block_size - 1) / block_size);
+    // The whole longest context, in whole blocks.
+    const long long full = ((long long)(max_context_len > 0 ? max_context_len : 1) +
+                            block_size - 1) / block_size * block_size;
+    // Streaming decode: the tensor-core consumer with the automatic split, at
+    // most kStreamMaxSeqs sequences (their lengths live in shared memory),
+    // 32-bit positions.  It cuts no context into splits (the work is cut at
+    // the CTAs' shares instead), so the split length is the whole context.
+    const long long all_pages = (long long)num_seqs * n_kv_heads * (full / block_size);
     const int stream_knob = tuning(PKV_TUNE_DECODE_STREAM, -1);
-    c->stream = allow_stream && c->mma && c->wpt == 1 && num_seqs <= pkv::kStreamMaxSeqs &&
-                all_pages <= 0x7fffffffLL &&
+    c->stream = allow_stream && split_tokens == 0 && c->mma && c->wpt == 1 &&
+                num_seqs <= pkv::kStreamMaxSeqs && all_pages <= 0x7fffffffLL &&
+                full <= 0x7fffffffLL &&
                 (stream_knob >= 0 ? stream_knob != 0 : max_context_len <= kStreamMaxContext);
+    c->stream_ctas = 0;
     if (c->stream) {
         // its shared memory must fit (the per-unit kernel runs otherwise)
         const int stages = tuned(PKV_TUNE_DECODE_STAGES) ? c->stages : kStreamStages;
-        const int pages = split_tokens > 0 ? split_tokens / block_size
-                                           : (kStreamSplitTokens + block_size - 1) / block_size;
         const size_t limit = smem_optin > 0 ? smem_optin : (size_t)227 * 1024;
-        if (pkv::decode_stream_smem_bytes(head_dim, block_size, n_heads / n_kv_heads, 2, c->hpc,
-                                          stages, pages, num_seqs) > limit)
+        const size_t smem = pkv::decode_stream_smem_bytes(head_dim, block_size,
+                                                          n_heads / n_kv_heads, 2, c->hpc,
+                                                          stages, num_seqs);
+        if (smem > limit) {
             c->stream = false;
-        else
+        } else {
             c->stages = stages;
+            // an upper bound of the resident CTAs (shared memory alone)
+            const size_t per_sm_bytes =
+                smem_per_sm > 0 ? (size_t)smem_per_sm : (size_t)228 * 1024;
+            int per_sm = (int)(per_sm_bytes / smem);
+            per_sm = per_sm < 1 ? 1 : (per_sm > 32 ? 32 : per_sm);
+            c->stream_ctas = (sm_count > 0 ? sm_count : 1) * per_sm;
+        }
     }
     if (split_tokens == 0) {
-        split_tokens = c->stream && !tuned(PKV_TUNE_DECODE_SPLIT)
-                           ? std::min((max_context_len + block_size - 1) / block_size * block_size,
-                                      (kStreamSplitTokens + block_size - 1) / block_size *
-                                          block_size)
-                           : auto_split_tokens(num_seqs, n_kv_heads, c->hpc, block_size,
-                                               max_context_len, sm_count);
+        split_tokens = c->stream ? (int)full
+                                 : auto_split_tokens(num_seqs, n_kv_heads, c->hpc, block_size,
+                                                     max_context_len, sm_count);
         if (split_tokens <= 0) split_tokens = block_size;
     } else if (split_tokens < 0 || split_tokens % block_size) {
         return invalid("split_tokens must be a positive multiple of block_size (or 0)");
     }
-    if (split_tokens / block_size > kMaxPagesPerSplit)
+    if (!c->stream && split_tokens / block_size > kMaxPagesPerSplit)
         return invalid("split_tokens exceeds 4096 pages");
     c->split_tokens = split_tokens;
     const long long ms = ((long long)(max_context_len > 0 ? max_context_len : 0) + split_tokens - 1) /
                          split_tokens;
     c->max_splits = ms < 1 ? 1 : (int)ms;
     c->max_pages = split_tokens / block_size;
-    c->smem = c->mma ? pkv::decode_mma_smem_bytes(head_dim, block_size, 2, c->hpc, c->stages,
-                                                  c->max_pages)
-                     : pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc, c->wpk,
-                                              c->wpt, c->stages, c->max_pages);
     if (c->stream)
         c->smem = pkv::decode_stream_smem_bytes(head_dim, block_size, n_heads / n_kv_heads, 2,
-                                                c->hpc, c->stages, c->max_pages, num_seqs);
+                                                c->hpc, c->stages, num_seqs);
+    else
+        c->smem = c->mma ? pkv::decode_mma_smem_bytes(head_dim, block_size, 2, c->hpc, c->stages,
+                                                      c->max_pages)
+                         : pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc,
+                                                  c->wpk, c->wpt, c->stages, c->max_pages);
     return PKV_OK;
 }
 
 size_t workspace_bytes_for(int num_seqs, int n_heads, int head_dim, const DecodeConfig& c,
-                           size_t* ml_offset) {
-    if (c.max_splits <= 1) {
+                           size_t* ml_offset, size_t* desc_offset = nullptr) {
+    size_t units = 0;
+    if (c.stream) {
+        // a run of one page is never cut: no partial states
+        if (c.max_pages > 1)
+            units = pkv::decode_stream_partial_rows(c.stream_ctas, c.hpc, c.qpw);
+    } else if (c.max_splits > 1) {
+        units = (size_t)num_seqs * n_heads * c.max_splits;
+    }
+    if (units == 0) {
         if (ml_offset) *ml_offset = 0;
         return 0;
     }
-    const size_t units = (size_t)num_seqs * n_heads * c.max_splits;
     const size_t o_bytes = (units * head_dim * sizeof(float) + 255) / 256 * 256;
     if (ml_offset) *ml_offset = o_bytes;
-    return o_bytes + units * 2 * sizeof(float);
+    const size_t ml_bytes = units * 2 * sizeof(float);
+    if (!c.stream) return o_bytes + ml_bytes;
+    // then the boundary records (int4 per CTA), 16-byte aligned
+    const size_t desc_at = (o_bytes + ml_bytes + 15) / 16 * 16;
+    if (desc_offset) *desc_offset = desc_at;
+    return desc_at + (size_t)c.stream_ctas * 16;
 }
 
 }  // namespace
@@ -496,7 +515,8 @@ PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, i
     const bool ok = device_info(&d) == cudaSuccess;
     DecodeConfig c;
     if (make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size, max_context_len, 0,
-                    ok ? d->sm_count : 0, &c, true, ok ? (size_t)d->smem_optin : 0) != PKV_OK)
+                    ok ? d->sm_count : 0, &c, true, ok ? (size_t)d->smem_optin : 0,
+                    ok ? d->smem_per_sm : 0) != PKV_OK)
         return 0;
     return c.split_tokens;
 }
@@ -510,7 +530,7 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
     DecodeConfig c;
     if (make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size, max_context_len,
                     split_tokens, ok ? d->sm_count : 0, &c, true,
-                    ok ? (size_t)d->smem_optin : 0) != PKV_OK)
+                    ok ? (size_t)d->smem_optin : 0, ok ? d->smem_per_sm : 0) != PKV_OK)
         return 0;
     return workspace_bytes_for(num_seqs, n_heads, head_dim, c, nullptr);
 }
@@ -559,15 +579,15 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
     DecodeConfig c;
     pkv_status st = make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size,
                                 max_context_len, split_tokens, dev->sm_count, &c, true,
-                                (size_t)dev->smem_optin);
+                                (size_t)dev->smem_optin, dev->smem_per_sm);
     if (st != PKV_OK) return st;
     if (c.smem > (size_t)dev->smem_optin) return unsupported("shared memory of this configuration");
     // The kernels clamp a context to min(table tokens, splits x split
     // length) in 32-bit arithmetic: both products must fit.
     if ((long long)c.max_splits * c.split_tokens > 0x7fffffffLL)
         return unsupported("max_context_len too close to 2^31 - 1 tokens for this split length");
-    size_t ml_off = 0;
-    const size_t need = workspace_bytes_for(num_seqs, n_heads, head_dim, c, &ml_off);
+    size_t ml_off = 0, desc_off = 0;
+    const size_t need = workspace_bytes_for(num_seqs, n_heads, head_dim, c, &ml_off, &desc_off);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) {
             set_detail("%s", "workspace smaller than pkv_decode_workspace_bytes()");
@@ -612,6 +632,9 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
     p.max_pages_per_split = c.max_pages;
     p.ws_o = need ? static_cast<float*>(workspace) : nullptr;
     p.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off) : nullptr;
+    p.ws_desc = need && c.stream
+                    ? reinterpret_cast<int4*>(static_cast<char*>(workspace) + desc_off)
+                    : nullptr;
     p.errors = dev->errors;
     p.k_pool = const_cast<void*>(k_pool);
     p.v_pool = const_cast<void*>(v_pool);
@@ -625,11 +648,14 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
     L.smem_bytes = c.smem;
     L.stream = static_cast<cudaStream_t>(stream);
     L.sm_count = dev->sm_count;
+    L.max_ctas = c.stream_ctas;
     if (c.max_splits > 65535 * 1024) return unsupported("context too long for the grid");
 
+    int stream_ctas = 0;
     if (c.stream)
-        e = kv_dtype == PKV_BF16 ? pkv::launch_decode_stream_bf16(head_dim, block_size, L)
-                                 : pkv::launch_decode_stream_f16(head_dim, block_size, L);
+        e = kv_dtype == PKV_BF16
+                ? pkv::launch_decode_stream_bf16(head_dim, block_size, L, &stream_ctas)
+                : pkv::launch_decode_stream_f16(head_dim, block_size, L, &stream_ctas);
     else if (c.mma)
         e = kv_dtype == PKV_BF16 ? pkv::launch_decode_mma_bf16(head_dim, block_size, L)
                                  : pkv::launch_decode_mma_f16(head_dim, block_size, L);
@@ -638,7 +664,15 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
                                  : pkv::launch_decode_f16(head_dim, block_size, c.qpw, L);
     if (e != cudaSuccess) return cuda_fail(e);
 
-    if (c.max_splits > 1) {
+    if (c.stream && need > 0) {
+        // the runs cut by the stream decode's share boundaries
+        const unsigned rows = (unsigned)(c.hpc * (n_heads / n_kv_heads));
+        DependentLaunch dl(dim3((unsigned)stream_ctas, (rows + 3) / 4), L.stream);
+        e = head_dim == 128
+                ? cudaLaunchKernelEx(&dl.cfg, pkv::paged_decode_stream_merge_kernel<128>, p)
+                : cudaLaunchKernelEx(&dl.cfg, pkv::paged_decode_stream_merge_kernel<64>, p);
+        if (e != cudaSuccess) return cuda_fail(e);
+    } else if (c.max_splits > 1) {
         pkv::ReduceParams r;
         r.out = out;
         r.out_dtype = out_dtype;

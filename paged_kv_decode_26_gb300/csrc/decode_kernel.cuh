@@ -63,6 +63,7 @@ struct DecodeParams {
     int max_pages_per_split;
     float* ws_o;   // [num_seqs, n_heads, max_splits, D]
     float* ws_ml;  // [num_seqs, n_heads, max_splits, 2]
+    int4* ws_desc; // stream decode: the runs its share boundaries cut [grid] (see there)
     unsigned int* errors;
     // Fused append (paged_attn_decode_append; NULL slot_mapping: none):
     // row k_new[s] / v_new[s] ([num_seqs, n_kv_heads, D]) goes to pool row
@@ -724,24 +725,19 @@ struct ReduceParams {
     const float* ws_ml;
 };
 
-// One warp per (sequence, query head): merges the partial states of its
-// splits, O = sum_k w_k O_k / sum_k w_k with w_k = L_k 2^{M_k - M*}.
+// One warp merges n partial states of one (sequence, query head): state k
+// has its (M_k, L_k) at ml + k * ml_step floats and its normalised output
+// row at o + k * o_step floats.  O = sum_k w_k O_k / sum_k w_k with
+// w_k = L_k 2^{M_k - M*}, M* the largest M_k of a state with L_k > 0;
+// written to out (element offset out_off, out_dtype).
 template <int D>
-__device__ __forceinline__ void reduce_unit(const ReduceParams& p, int unit, int lane) {
+__device__ __forceinline__ void merge_states(const float* ml, size_t ml_step, const float* o,
+                                             size_t o_step, int n, void* out, size_t out_off,
+                                             int out_dtype, int lane) {
     constexpr int DL = D / 32;
-    if (unit >= p.num_seqs * p.n_heads) return;
-    const int s = unit / p.n_heads;
-    int n = p.context_lens[s];
-    n = n < 0 ? 0 : min(n, p.cap_tokens);
-    const int n_splits = max(1, (n + p.split_tokens - 1) / p.split_tokens);
-    if (n_splits == 1) return;  // the decode kernel wrote this row itself
-
-    const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + (size_t)unit * p.max_splits;
-    const float* os = p.ws_o + (size_t)unit * p.max_splits * D;
-
     float mx = -INFINITY;
-    for (int k = lane; k < n_splits; k += 32) {
-        const float2 v = ml[k];
+    for (int k = lane; k < n; k += 32) {
+        const float2 v = *reinterpret_cast<const float2*>(ml + (size_t)k * ml_step);
         if (v.y > 0.f) mx = fmaxf(mx, v.x);
     }
 #pragma unroll
@@ -751,20 +747,20 @@ __device__ __forceinline__ void reduce_unit(const ReduceParams& p, int unit, int
 #pragma unroll
     for (int d = 0; d < DL; ++d) acc[d] = 0.f;
     float wsum = 0.f;
-    // Splits in batches of RB: the batch's loads are all issued before its
+    // States in batches of RB: the batch's loads are all issued before its
     // accumulation, so a warp waits one memory round trip per batch rather
-    // than per split; the accumulation order (k ascending) is unchanged.
+    // than per state; the accumulation order (k ascending) is unchanged.
     constexpr int RB = 8;
-    for (int k0 = 0; k0 < n_splits; k0 += RB) {
+    for (int k0 = 0; k0 < n; k0 += RB) {
         float2 mlv[RB];
         float x[RB][DL];
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
             const int k = k0 + u;
             mlv[u] = make_float2(0.f, 0.f);
-            if (k < n_splits) {
-                mlv[u] = ml[k];
-                const float* ok = os + (size_t)k * D + lane * DL;
+            if (k < n) {
+                mlv[u] = *reinterpret_cast<const float2*>(ml + (size_t)k * ml_step);
+                const float* ok = o + (size_t)k * o_step + lane * DL;
                 if constexpr (DL == 4) {
                     const float4 t = *reinterpret_cast<const float4*>(ok);
                     x[u][0] = t.x;
@@ -780,7 +776,7 @@ __device__ __forceinline__ void reduce_unit(const ReduceParams& p, int unit, int
         }
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
-            if (k0 + u >= n_splits || !(mlv[u].y > 0.f)) continue;
+            if (k0 + u >= n || !(mlv[u].y > 0.f)) continue;
             const float w = mlv[u].y * exp2f(mlv[u].x - mx);
             wsum += w;
 #pragma unroll
@@ -791,7 +787,22 @@ __device__ __forceinline__ void reduce_unit(const ReduceParams& p, int unit, int
     float v[DL];
 #pragma unroll
     for (int d = 0; d < DL; ++d) v[d] = acc[d] * inv;
-    store_row<DL>(p.out, (size_t)unit * D + lane * DL, p.out_dtype, v);
+    store_row<DL>(out, out_off + lane * DL, out_dtype, v);
+}
+
+// One warp per (sequence, query head): merges the partial states of its
+// splits ([unit][split] in the workspace).
+template <int D>
+__device__ __forceinline__ void reduce_unit(const ReduceParams& p, int unit, int lane) {
+    if (unit >= p.num_seqs * p.n_heads) return;
+    const int s = unit / p.n_heads;
+    int n = p.context_lens[s];
+    n = n < 0 ? 0 : min(n, p.cap_tokens);
+    const int n_splits = max(1, (n + p.split_tokens - 1) / p.split_tokens);
+    if (n_splits == 1) return;  // the decode kernel wrote this row itself
+    merge_states<D>(p.ws_ml + (size_t)unit * p.max_splits * 2, 2,
+                    p.ws_o + (size_t)unit * p.max_splits * D, D, n_splits, p.out,
+                    (size_t)unit * D, p.out_dtype, lane);
 }
 
 template <int D>

@@ -17,7 +17,8 @@ struct DecodeLaunch {
     dim3 block;
     size_t smem_bytes;
     cudaStream_t stream;
-    int sm_count;   // the stream kernel sizes its grid from it
+    int sm_count;    // the stream kernel sizes its grid from it
+    int max_ctas;    // stream kernel: at most this many CTAs (the workspace's bound)
 };
 
 // Launch paged_decode_kernel<D, BS, QPW, T> for T = __nv_bfloat16 / __half.
@@ -27,10 +28,11 @@ cudaError_t launch_decode_f16(int D, int BS, int QPW, const DecodeLaunch& L);
 // Launch paged_decode_mma_kernel<D, BS, T> (tensor-core path for query-head groups).
 cudaError_t launch_decode_mma_bf16(int D, int BS, const DecodeLaunch& L);
 cudaError_t launch_decode_mma_f16(int D, int BS, const DecodeLaunch& L);
-// Launch paged_decode_mma_stream_kernel<D, BS, T> on every SM (resident CTAs
-// streaming the work units; L.grid is ignored).
-cudaError_t launch_decode_stream_bf16(int D, int BS, const DecodeLaunch& L);
-cudaError_t launch_decode_stream_f16(int D, int BS, const DecodeLaunch& L);
+// Launch paged_decode_mma_stream_kernel<D, BS, T> on every SM (as many CTAs
+// as stay resident, at most L.max_ctas; L.grid is ignored).  *ctas receives
+// the grid size, which the boundary merge launch must repeat.
+cudaError_t launch_decode_stream_bf16(int D, int BS, const DecodeLaunch& L, int* ctas);
+cudaError_t launch_decode_stream_f16(int D, int BS, const DecodeLaunch& L, int* ctas);
 
 struct MultiQueryLaunch {
     CUtensorMap tm_q;   // tcgen05 kernel only

@@ -229,51 +229,79 @@ __device__ __forceinline__ void mma_heads_chunk(MmaHeads<D>& st, uint32_t kbase,
     }
 }
 
-// The unit's result: normalised rows of the real query heads qh0 .. qh0+G-1
-// to the output (one split) or to the split partials.
+// Sum of each query head's softmax weights over the warp: lane (gid, tig)
+// holds heads 2 tig and 2 tig + 1 for its token rows; the other token rows
+// sit in the lanes of the same tig.
 template <int D>
-__device__ __forceinline__ void mma_heads_finish(const MmaHeads<D>& st, const DecodeParams& p,
-                                                 int s, int qh0, int G, int n_splits, int split,
-                                                 int lane) {
-    const int gid = lane >> 2, tig = lane & 3;
-    float l0 = st.l[0], l1 = st.l[1];
+__device__ __forceinline__ void mma_heads_sums(const MmaHeads<D>& st, float& l0, float& l1) {
+    l0 = st.l[0];
+    l1 = st.l[1];
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+}
+
+// A partial state (normalised O, M, L) per real query head hh < G: row
+// row0 + hh * row_step of ws_o ([rows, D]) and ws_ml ([rows, 2]).
+template <int D>
+__device__ __forceinline__ void mma_heads_partial(const MmaHeads<D>& st, float* ws_o,
+                                                  float* ws_ml, size_t row0, size_t row_step,
+                                                  int G, int lane) {
+    const int gid = lane >> 2, tig = lane & 3;
+    float l0, l1;
+    mma_heads_sums<D>(st, l0, l1);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int hh = 2 * tig + e;
         if (hh >= G) continue;
         const float l = e ? l1 : l0;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int qh = qh0 + hh;
-        if (n_splits == 1) {
-            const size_t row = ((size_t)s * p.n_heads + qh) * D;
+        const size_t unit = row0 + (size_t)hh * row_step;
 #pragma unroll
-            for (int j = 0; j < D / 16; ++j) {
-                const float a = st.o[j][e] * inv, b = st.o[j][2 + e] * inv;
-                const size_t d0 = row + j * 16 + gid, d1 = d0 + 8;
-                if (p.out_dtype == PKV_F32) {
-                    reinterpret_cast<float*>(p.out)[d0] = a;
-                    reinterpret_cast<float*>(p.out)[d1] = b;
-                } else {
-                    const uint32_t w = pack_out(a, b, p.out_dtype);
-                    reinterpret_cast<uint16_t*>(p.out)[d0] = (uint16_t)(w & 0xffffu);
-                    reinterpret_cast<uint16_t*>(p.out)[d1] = (uint16_t)(w >> 16);
-                }
-            }
-        } else {
-            const size_t unit = ((size_t)s * p.n_heads + qh) * p.max_splits + split;
+        for (int j = 0; j < D / 16; ++j) {
+            ws_o[unit * D + j * 16 + gid] = st.o[j][e] * inv;
+            ws_o[unit * D + j * 16 + gid + 8] = st.o[j][2 + e] * inv;
+        }
+        if (gid == 0) *reinterpret_cast<float2*>(ws_ml + unit * 2) = make_float2(st.m[e], l);
+    }
+}
+
+// The unit's result: normalised rows of the real query heads qh0 .. qh0+G-1
+// to the output (one split) or to the split partials.
+template <int D>
+__device__ __forceinline__ void mma_heads_finish(const MmaHeads<D>& st, const DecodeParams& p,
+                                                 int s, int qh0, int G, int n_splits, int split,
+                                                 int lane) {
+    if (n_splits != 1) {
+        mma_heads_partial<D>(st, p.ws_o, p.ws_ml,
+                             ((size_t)s * p.n_heads + qh0) * p.max_splits + split, p.max_splits,
+                             G, lane);
+        return;
+    }
+    const int gid = lane >> 2, tig = lane & 3;
+    float l0, l1;
+    mma_heads_sums<D>(st, l0, l1);
 #pragma unroll
-            for (int j = 0; j < D / 16; ++j) {
-                p.ws_o[unit * D + j * 16 + gid] = st.o[j][e] * inv;
-                p.ws_o[unit * D + j * 16 + gid + 8] = st.o[j][2 + e] * inv;
+    for (int e = 0; e < 2; ++e) {
+        const int hh = 2 * tig + e;
+        if (hh >= G) continue;
+        const float l = e ? l1 : l0;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const size_t row = ((size_t)s * p.n_heads + qh0 + hh) * D;
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+            const float a = st.o[j][e] * inv, b = st.o[j][2 + e] * inv;
+            const size_t d0 = row + j * 16 + gid, d1 = d0 + 8;
+            if (p.out_dtype == PKV_F32) {
+                reinterpret_cast<float*>(p.out)[d0] = a;
+                reinterpret_cast<float*>(p.out)[d1] = b;
+            } else {
+                const uint32_t w = pack_out(a, b, p.out_dtype);
+                reinterpret_cast<uint16_t*>(p.out)[d0] = (uint16_t)(w & 0xffffu);
+                reinterpret_cast<uint16_t*>(p.out)[d1] = (uint16_t)(w >> 16);
             }
-            if (gid == 0)
-                *reinterpret_cast<float2*>(p.ws_ml + unit * 2) =
-                    make_float2(st.m[e], l);
         }
     }
 }

@@ -137,7 +137,8 @@ def test_grouped_heads_both_paths(lib, tuning, mma, D, B, H, Hk, dtype, out_dtyp
     (128, 32, 8, 16, 32075, 1024),   # gqa_prefix: 32K contexts, 256 (seq, head-group) units
     (16, 32, 32, 32, 32769, 1024),   # long_context (2 kv heads per CTA: 256 units)
     (256, 32, 8, 16, 16385, 512),    # continuous: 512 units, more than 2 x SMs
-    (256, 32, 8, 16, 1235, 128),     # continuous as generated (longest 1235): streaming decode
+    (256, 32, 8, 16, 1235, 1248),    # continuous as generated (longest 1235): streaming decode,
+                                     # no split (the whole page-rounded context)
     (128, 32, 8, 16, 2048, 512),     # GQA up to 2K tokens: one CTA per unit
     (4, 8, 8, 16, 201, 208),         # tiny: one split of the whole (page-rounded) context
     (4096, 32, 8, 16, 4096, 4096),   # many units: no split at all
@@ -146,8 +147,9 @@ def test_automatic_split_length(lib, S, H, Hk, B, max_ctx, expect):
     """The automatic split length: 512 tokens; 1024 when the longest
     context is 8K tokens or more and there are at most 2 x SMs (sequence,
     head-group) units; the whole context when the units fill the GPU 16
-    times over (sizes for GB300's 152 SMs); 128 tokens for the streaming
-    tensor-core decode (groups of 4 or 8, longest context at most 1536)."""
+    times over (sizes for GB300's 152 SMs); the whole context for the
+    streaming tensor-core decode (groups of 4 or 8, longest context at most
+    1536), which cuts the work at its CTAs' shares instead of splits."""
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("unit thresholds are stated for 152 SMs")
     assert lib.decode_split_tokens(S, H, Hk, 128, B, max_ctx) == expect

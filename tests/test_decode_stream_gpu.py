@@ -1,8 +1,11 @@
-"""The tensor-core decode run as resident CTAs streaming the work units
-(paged_decode_mma_stream_kernel, selected by the decode_stream tuning knob):
-through the C ABI, against the fp64 oracle and bit for bit against the
-one-CTA-per-unit kernel (the arithmetic of a unit is the same), with empty
-contexts, ragged tails, splits, fused appends and bad block ids."""
+"""The tensor-core decode run as resident CTAs that each take an exactly equal
+share of the pages (paged_decode_mma_stream_kernel plus its boundary merge,
+selected by the decode_stream tuning knob or automatically for short
+contexts): through the C ABI, against the fp64 oracle, with empty contexts,
+ragged tails, runs cut by many share boundaries, fewer pages than CTAs,
+fused appends and bad block ids.  Its results depend only on the inputs and
+the device (the shares follow from the lengths and the grid), so repeated
+calls agree bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -31,52 +34,101 @@ def _bits(t):
         t.contiguous().view(torch.int32)
 
 
-def _abs_v(case):
+def _abs_v(case, seq_ids=None):
     """sum_t w_t |V_t| per output element, on demand (the tensor-core
     consumer's hi + lo weight rounding term of the parity bound)."""
     return lambda: parallel.decode_two_pass(case.q, case.k_pool, case.v_pool.abs(),
-                                            case.block_tables, case.context_lens, case.scale)
+                                            case.block_tables, case.context_lens, case.scale,
+                                            seq_ids=seq_ids)
 
 
-def _both(lib, tuning, case, split, **kw):
-    """(per-unit kernel output, stream kernel output) of one decode with the
-    same split length (split 0: the stream kernel's automatic one, which the
-    per-unit kernel is then given explicitly), plus the stream kernel's
-    output with the automatic split."""
-    dev = to_device(case)
+def _stream(tuning, case, dev=None, **kw):
+    """Two stream decodes of the case (automatic split): asserted bit-equal,
+    the first returned."""
+    dev = dev if dev is not None else to_device(case)
     tuning(decode_stream=1)
-    auto = None
-    if split == 0:
-        auto = run_decode(case, split_tokens=0, dev=dev, **kw)
-        split = lib.decode_split_tokens(case.S, case.H, case.Hk, case.D, case.B,
-                                        int(case.context_lens.max()))
-    b = run_decode(case, split_tokens=split, dev=dev, **kw)
-    tuning(decode_stream=0)
-    a = run_decode(case, split_tokens=split, dev=dev, **kw)
+    a = run_decode(case, split_tokens=0, dev=dev, **kw)
+    b = run_decode(case, split_tokens=0, dev=dev, **kw)
     torch.cuda.synchronize()
-    if auto is not None:
-        assert torch.equal(_bits(auto), _bits(b))
-    return a, b
+    assert torch.equal(_bits(a), _bits(b)), "stream decode not repeatable"
+    return a
+
+
+def _check(lib, case, got, what):
+    ref = parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
+                                   case.context_lens, case.scale)
+    assert_attention_close(got, ref, case.out_dtype, what, abs_weighted=_abs_v(case),
+                           kv_dtype=case.dtype)
+    assert lib.device_errors(clear=True) == 0
 
 
 @pytest.mark.parametrize("D,B", [(128, 16), (64, 16), (128, 32), (64, 32)])
 @pytest.mark.parametrize("H,Hk", [(32, 8), (16, 2), (8, 1)])
-@pytest.mark.parametrize("split", [0, 2, 8])
-def test_stream_equals_per_unit_kernel(lib, tuning, D, B, H, Hk, split):
+def test_stream_matches_oracle(lib, tuning, D, B, H, Hk):
     lens = [0, 1, 15, 16, 17, 33, 0, 70, 2 * B * 8 + 3, 5, 300, 1, 64, 0, 129, 31]
     case = wl.make_case(5, lens_override=lens, H=H, Hk=Hk, D=D, B=B, d2d_pairs=0,
-                        h2d_pairs=0, host_pool_blocks=1, poison=True, seed=D + B + H + split)
-    a, b = _both(lib, tuning, case, split * B)
-    assert torch.equal(_bits(a), _bits(b))
-    ref = orc.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
-                              case.context_lens, case.scale)
-    assert_attention_close(b, ref, case.out_dtype, f"D={D} B={B} {H}/{Hk} split {split}",
-                           abs_weighted=_abs_v(case), kv_dtype=case.dtype)
-    assert lib.device_errors(clear=True) == 0
+                        h2d_pairs=0, host_pool_blocks=1, poison=True, seed=D + B + H)
+    out = _stream(tuning, case)
+    _check(lib, case, out, f"D={D} B={B} {H}/{Hk}")
+
+
+@pytest.mark.parametrize("lens,H,Hk", [
+    ([20000], 32, 8),                 # one long context cut by every share boundary
+    ([9000, 3, 0, 4100, 17], 8, 1),   # long runs next to short ones
+    ([16, 1, 31], 32, 8),             # fewer pages than CTAs: one share per page
+    ([0, 0, 0], 32, 4),               # no pages at all: zero rows only
+    ([1] * 700, 16, 2),               # one-page runs only: no workspace, no merge
+])
+def test_stream_share_boundaries(lib, tuning, lens, H, Hk):
+    case = wl.make_case(5, lens_override=lens, H=H, Hk=Hk, D=128, B=16, d2d_pairs=0,
+                        h2d_pairs=0, host_pool_blocks=1, poison=True, seed=len(lens) + H)
+    out = _stream(tuning, case)
+    if max(lens) <= 16:
+        assert lib.decode_workspace_bytes(case.S, H, Hk, 128, 16, max(lens), 0) == 0
+    _check(lib, case, out, f"lens {lens[:5]}")
+
+
+def test_stream_ignores_workspace_contents(lib, tuning):
+    """The partial states are written before the merge reads them: a
+    workspace full of NaN gives the same bits as a zeroed one."""
+    import paged_kv_decode_26_gb300 as pkv
+    case = wl.make_case(5, S=64, lens=("pareto", 1.5, 16, 4000), d2d_pairs=0, h2d_pairs=0,
+                        host_pool_blocks=1, seed=5)
+    dev = to_device(case)
+    tuning(decode_stream=1)
+    mcl = int(case.context_lens.max())
+    outs = []
+    for fill in (0.0, float("nan")):
+        ws = pkv.alloc_decode_workspace(dev["q"], dev["k_pool"], mcl)
+        assert ws is not None and ws.numel() > 0
+        ws.view(torch.float32)[: ws.numel() // 4].fill_(fill)
+        out = torch.empty(case.S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+        pkv.paged_attn_decode(out, dev["q"], dev["k_pool"], dev["v_pool"], dev["block_tables"],
+                              dev["context_lens"], case.scale, mcl, workspace=ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(outs[0]), _bits(outs[1]))
+    _check(lib, case, outs[0], "workspace contents")
+
+
+def test_explicit_split_runs_the_per_unit_kernel(lib, tuning):
+    """An explicit split length is honoured: the per-unit kernel runs (its
+    bits with the knob on and off agree)."""
+    case = wl.make_case(5, S=40, lens=("pareto", 1.5, 16, 3000), d2d_pairs=0, h2d_pairs=0,
+                        host_pool_blocks=1, seed=9)
+    dev = to_device(case)
+    outs = []
+    for mode in (0, 1):
+        tuning(decode_stream=mode)
+        outs.append(run_decode(case, split_tokens=64, dev=dev))
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(outs[0]), _bits(outs[1]))
+    _check(lib, case, outs[1], "explicit split")
 
 
 @pytest.mark.parametrize("config,extra", [
     (5, dict(S=300, lens=("pareto", 1.5, 16, 2000))),
+    (5, dict(S=64, lens=("pareto", 1.5, 16, 16384))),
     (3, dict(S=40, lens=("loguniform", 1, 3000), share_blocks=8)),
     (5, dict(S=2048, lens=("uniform", 0, 40))),          # the most sequences the kernel takes
     (5, dict(S=2049, lens=("uniform", 0, 40))),          # one more: the per-unit kernel runs
@@ -85,14 +137,12 @@ def test_stream_workload_mixes(lib, tuning, config, extra):
     if config == 5:
         extra = dict(extra, d2d_pairs=0, h2d_pairs=0, host_pool_blocks=1)
     case = wl.make_case(config, poison=True, seed=17, **extra)
-    for split in (0, 64):
-        a, b = _both(lib, tuning, case, split)
-        assert torch.equal(_bits(a), _bits(b))
-    ref = parallel.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
-                                   case.context_lens, case.scale)
-    assert_attention_close(b, ref, case.out_dtype, f"config {config}",
-                           abs_weighted=_abs_v(case), kv_dtype=case.dtype)
-    assert lib.device_errors(clear=True) == 0
+    out = _stream(tuning, case)
+    if case.S > 2048:
+        tuning(decode_stream=0)
+        ref_bits = run_decode(case, split_tokens=0)
+        assert torch.equal(_bits(out), _bits(ref_bits))
+    _check(lib, case, out, f"config {config} S={case.S}")
 
 
 def test_stream_fused_append_equals_two_calls(lib, tuning):
@@ -150,17 +200,43 @@ def test_stream_bad_block_ids_are_flagged(lib, tuning):
     bt[1, 2] = case.num_blocks + 5
     bt[1, 3] = -7
     dev = to_device(case)
-    outs = []
-    for mode in (0, 1):
-        tuning(decode_stream=mode)
-        outs.append(run_decode(case, split_tokens=32, dev=dev, tables=bt.cuda()))
-        torch.cuda.synchronize()
-        assert lib.device_errors(clear=True) & 0x1
     keep = [0, 2, 3, 4, 5]
-    assert torch.equal(_bits(outs[0]), _bits(outs[1]))
     ref = orc.decode_two_pass(case.q, case.k_pool, case.v_pool, case.block_tables,
                               case.context_lens, case.scale, seq_ids=keep)
-    assert_attention_close(outs[1][keep], ref, case.out_dtype, kv_dtype=case.dtype,
-                           abs_weighted=lambda: orc.decode_two_pass(
-                               case.q, case.k_pool, case.v_pool.abs(), case.block_tables,
-                               case.context_lens, case.scale, seq_ids=keep))
+    for mode in (0, 1):
+        tuning(decode_stream=mode)
+        out = run_decode(case, split_tokens=0, dev=dev, tables=bt.cuda())
+        torch.cuda.synchronize()
+        assert lib.device_errors(clear=True) & 0x1
+        assert torch.isfinite(out.float()).all()
+        assert_attention_close(out[keep], ref, case.out_dtype, f"mode {mode}",
+                               kv_dtype=case.dtype, abs_weighted=_abs_v(case, keep))
+
+
+def test_stream_workspace_does_not_grow_with_sequences(lib, tuning):
+    """Two partial-state slots per CTA: the workspace of a short-context
+    decode does not grow with the number of sequences and fits the no-alloc
+    entry point's built-in scratch, whose output then equals the workspace
+    call's bit for bit."""
+    import ctypes as C
+    tuning(decode_stream=1)
+    ws = {S: lib.decode_workspace_bytes(S, 32, 8, 128, 16, 200, 0) for S in (64, 512, 2048)}
+    # (64 sequences take two kv heads per CTA and more CTAs per SM: other slots)
+    assert 0 < ws[2048] == ws[512] <= ws[64] <= 16 << 20   # PKV_NOALLOC_SCRATCH_BYTES
+    case = wl.make_case(5, S=2048, lens=("uniform", 1, 200), d2d_pairs=0, h2d_pairs=0,
+                        host_pool_blocks=1, seed=77)
+    dev = to_device(case)
+    mcl = int(case.context_lens.max())
+    ref = run_decode(case, split_tokens=0, dev=dev)
+    out = torch.empty_like(ref)
+    ptr = lambda t: C.c_void_p(t.data_ptr())
+    dt = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
+    st = lib.lib().paged_attn_decode_noalloc(
+        ptr(out), dt[out.dtype], ptr(dev["q"]), ptr(dev["k_pool"]), ptr(dev["v_pool"]),
+        dt[case.dtype], ptr(dev["block_tables"]), case.max_blocks_per_seq,
+        ptr(dev["context_lens"]), case.S, case.H, case.Hk, case.D, case.B, case.num_blocks,
+        case.scale, mcl, 0, C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(out), _bits(ref))
+    _check(lib, case, out, "2048 short contexts")
