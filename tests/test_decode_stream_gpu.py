@@ -240,3 +240,61 @@ def test_stream_workspace_does_not_grow_with_sequences(lib, tuning):
     torch.cuda.synchronize()
     assert torch.equal(_bits(out), _bits(ref))
     _check(lib, case, out, "2048 short contexts")
+
+
+def test_stream_repeated_calls_on_one_workspace(lib, tuning):
+    """The same decode 300 times on one workspace (its partial states and
+    boundary records overwritten every call) gives the first call's bits
+    every time."""
+    import paged_kv_decode_26_gb300 as pkv
+    tuning(decode_stream=1)
+    case = wl.make_case(5, S=48, lens=("pareto", 1.5, 16, 3000), d2d_pairs=0, h2d_pairs=0,
+                        host_pool_blocks=1, seed=13)
+    dev = to_device(case)
+    mcl = int(case.context_lens.max())
+    ws = pkv.alloc_decode_workspace(dev["q"], dev["k_pool"], mcl)
+    first = None
+    outs = []
+    for i in range(300):
+        out = torch.empty(case.S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+        pkv.paged_attn_decode(out, dev["q"], dev["k_pool"], dev["v_pool"], dev["block_tables"],
+                              dev["context_lens"], case.scale, mcl, workspace=ws)
+        if i == 0:
+            first = out
+        elif i % 50 == 0 or i == 299:
+            outs.append(out)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(_bits(o), _bits(first))
+    _check(lib, case, first, "300 calls")
+
+
+def test_stream_calls_on_two_streams(lib, tuning):
+    """Two stream decodes in flight at once (two CUDA streams, own
+    workspaces, each with its boundary merge as a dependent launch): each
+    equals its own single-stream result."""
+    import paged_kv_decode_26_gb300 as pkv
+    tuning(decode_stream=1)
+    cases = [wl.make_case(5, S=S, lens=("pareto", 1.5, 16, 2500), d2d_pairs=0, h2d_pairs=0,
+                          host_pool_blocks=1, seed=seed) for S, seed in ((96, 21), (64, 22))]
+    devs = [to_device(c) for c in cases]
+    alone = [run_decode(c, split_tokens=0, dev=d) for c, d in zip(cases, devs)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    wss = []
+    for c, d in zip(cases, devs):
+        mcl = int(c.context_lens.max())
+        wss.append(pkv.alloc_decode_workspace(d["q"], d["k_pool"], mcl))
+        outs.append(torch.empty(c.S, c.H, c.D, dtype=c.out_dtype, device="cuda"))
+    torch.cuda.synchronize()
+    for rep in range(20):
+        for c, d, st, o, ws in zip(cases, devs, streams, outs, wss):
+            with torch.cuda.stream(st):
+                pkv.paged_attn_decode(o, d["q"], d["k_pool"], d["v_pool"], d["block_tables"],
+                                      d["context_lens"], c.scale, int(c.context_lens.max()),
+                                      workspace=ws)
+    torch.cuda.synchronize()
+    for a, o in zip(alone, outs):
+        assert torch.equal(_bits(a), _bits(o))
+    assert lib.device_errors(clear=True) == 0
