@@ -49,8 +49,9 @@
 namespace pkv {
 
 constexpr int kStreamMaxSeqs = 2048;     // context lengths held in shared memory
-constexpr int kStreamBatchChunks = 32;   // chunks whose block ids one lookup fetches
-constexpr int kStreamBatchPages = 128;   // pages of one lookup
+constexpr int kStreamBatchChunks = 32;   // chunks whose block ids one lookup fetches (one a lane)
+constexpr int kStreamBatchPages = 128;   // pages of one lookup (a multiple of 32)
+static_assert(kStreamBatchPages % 32 == 0, "a lookup spreads its pages over a warp");
 
 // Slot record flags.
 constexpr int kSlotFirst = 1;   // first page of the CTA's piece of the run (query rows in the slot)
@@ -299,13 +300,16 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     int* s_bid = reinterpret_cast<int*>(s_chunk + kStreamBatchChunks);
     int* s_len = s_bid + kStreamBatchPages;   // clamped lengths [S]
     int* s_pref = s_len + S;                  // page prefix sums [S + 1]
-    int* s_var = s_pref + S + 1;   // (unused), abort, slots issued, queued chunks
+    int* s_var = s_pref + S + 1;   // batch pages, abort, slots issued, queued chunks
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // barriers first: their set-up overlaps the context-length loads
+    // barriers and tensor-map prefetches first: they overlap the
+    // context-length loads
     if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
         s_var[1] = 0;   // abort
         s_var[2] = 0;   // slots issued
         for (int st = 0; st < stages; ++st) {
@@ -326,10 +330,6 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     if (warp == 0) {
         // ================= producer =================
         const uint64_t policy = l2_policy_evict_first();
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
         int g = 0;   // slots issued so far (lane 0)
         // walk cursor (lane 0): position x = sequence cs, head group ch, page ci
         long long x = P0;
@@ -377,21 +377,41 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                     }
                 }
                 s_var[3] = nc;
+                s_var[0] = npg;
             }
             __syncwarp();
             const int nc = s_var[3];
             if (nc == 0) break;
-            // ---- block ids of every queued chunk (all lanes, independent loads)
-            for (int ui = 0; ui < nc; ++ui) {
-                const StreamChunk u = s_chunk[ui];
-                const int* row = p.block_tables + (size_t)u.s * p.max_blocks_per_seq + u.i0;
-                for (int i = lane; i < u.n; i += 32) {
-                    int b = row[i];
+            // ---- block ids of every queued page: lane l takes the batch's
+            // pages l, l + 32, ... (its chunk found by a forward scan of the
+            // chunks' first offsets) and issues all its loads before any
+            // store, so the batch costs one memory round trip however many
+            // chunks it holds
+            {
+                const int npg = s_var[0];
+                constexpr int PER_LANE = kStreamBatchPages / 32;
+                int bid[PER_LANE];
+                int ci = 0;
+#pragma unroll
+                for (int j = 0; j < PER_LANE; ++j) {
+                    const int f = lane + 32 * j;
+                    bid[j] = -1;
+                    if (f < npg) {
+                        while (ci + 1 < nc && s_chunk[ci + 1].first <= f) ++ci;
+                        const int s_of = s_chunk[ci].s, i_of = s_chunk[ci].i0 + (f - s_chunk[ci].first);
+                        bid[j] = p.block_tables[(size_t)s_of * p.max_blocks_per_seq + i_of];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < PER_LANE; ++j) {
+                    const int f = lane + 32 * j;
+                    if (f >= npg) continue;
+                    int b = bid[j];
                     if (b < 0 || b >= p.num_blocks) {
                         raise_error(p.errors, PKV_DEVERR_BLOCK_ID);
                         b = -1;
                     }
-                    s_bid[u.first + i] = b;
+                    s_bid[f] = b;
                 }
             }
             // ---- fused append: the chunk holding a run's last page writes
@@ -401,11 +421,17 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                 constexpr int VEC = 16 / (int)sizeof(T);
                 const int per_row = HPC * D / VEC;
                 const size_t row = (size_t)p.n_kv_heads * D;
+                // every chunk's slot at once, lane ui holding chunk ui's
+                // (at most kStreamBatchChunks = 32 chunks)
+                int64_t my_slot = -1;
+                if (lane < nc) {
+                    const StreamChunk u = s_chunk[lane];
+                    if (u.i0 + u.n == (s_len[u.s] + BS - 1) / BS) my_slot = p.slot_mapping[u.s];
+                }
                 for (int ui = 0; ui < nc; ++ui) {
-                    const StreamChunk u = s_chunk[ui];
-                    if (u.i0 + u.n != (s_len[u.s] + BS - 1) / BS) continue;
-                    const int64_t slot_row = p.slot_mapping[u.s];
+                    const int64_t slot_row = __shfl_sync(0xffffffffu, my_slot, ui);
                     if (slot_row < 0) continue;
+                    const StreamChunk u = s_chunk[ui];
                     if (slot_row >= (int64_t)p.num_blocks * BS) {
                         if (u.hg == 0 && lane == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
                         continue;
