@@ -137,7 +137,8 @@ bool supported_shape(int n_heads, int n_kv_heads, int head_dim, int block_size) 
 //     128-byte swizzle: one 64-element half of one head's page per load,
 //     landing as [B][64] with each 128-byte row's 16-byte chunks permuted.
 cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, pkv_dtype dt, int num_blocks,
-                            int block_size, int n_kv_heads, int head_dim, int hpc, bool mma) {
+                            int block_size, int n_kv_heads, int head_dim, int hpc, bool mma,
+                            int box_rows) {
     auto encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t es = 2;
@@ -146,7 +147,8 @@ cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, pkv_dtype dt, in
     cuuint64_t dims[4] = {inner, rows, (cuuint64_t)block_size, (cuuint64_t)num_blocks};
     cuuint64_t strides[3] = {inner * es, (cuuint64_t)n_kv_heads * head_dim * es,
                              (cuuint64_t)block_size * n_kv_heads * head_dim * es};
-    cuuint32_t box[4] = {(cuuint32_t)inner, mma ? 1u : (cuuint32_t)hpc, (cuuint32_t)block_size, 1};
+    const cuuint32_t rows_per_box = box_rows > 0 ? (cuuint32_t)box_rows : (cuuint32_t)block_size;
+    cuuint32_t box[4] = {(cuuint32_t)inner, mma ? 1u : (cuuint32_t)hpc, rows_per_box, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = encode(map, dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -609,6 +611,17 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
     if ((e = encode_pool_map(&L.tm_v, vmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
                              head_dim, c.hpc, c.mma)) != cudaSuccess)
         return cuda_fail(e);
+    if (c.stream) {
+        // half-block boxes for the last block of a context that fills at
+        // most half of it (the streaming decode's many short contexts)
+        if ((e = encode_pool_map(&L.tm_kh, kmap_base, kv_dtype, map_blocks, block_size,
+                                 n_kv_heads, head_dim, c.hpc, c.mma, block_size / 2)) !=
+                cudaSuccess ||
+            (e = encode_pool_map(&L.tm_vh, vmap_base, kv_dtype, map_blocks, block_size,
+                                 n_kv_heads, head_dim, c.hpc, c.mma, block_size / 2)) !=
+                cudaSuccess)
+            return cuda_fail(e);
+    }
 
     pkv::DecodeParams& p = L.p;
     p.out = out;

@@ -43,8 +43,10 @@ bool table_tokens_fit(int max_blocks_per_seq, int block_size);
 bool supported_shape(int n_heads, int n_kv_heads, int head_dim, int block_size);
 
 // The pool [num_blocks, B, Hk, D] as a 4-D tensor for TMA (see capi.cu).
+// box_rows: token rows per box (0: the whole block).
 cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, pkv_dtype dt, int num_blocks,
-                            int block_size, int n_kv_heads, int head_dim, int hpc, bool mma);
+                            int block_size, int n_kv_heads, int head_dim, int hpc, bool mma,
+                            int box_rows = 0);
 
 // The cuTensorMapEncodeTiled entry point of the driver (NULL if absent).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

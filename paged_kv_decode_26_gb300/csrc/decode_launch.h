@@ -12,6 +12,8 @@ namespace pkv {
 struct DecodeLaunch {
     CUtensorMap tm_k;
     CUtensorMap tm_v;
+    CUtensorMap tm_kh;   // stream kernel: boxes of half a block
+    CUtensorMap tm_vh;
     DecodeParams p;
     dim3 grid;
     dim3 block;

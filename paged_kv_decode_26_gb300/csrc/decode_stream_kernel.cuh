@@ -265,6 +265,8 @@ template <int D, int BS, typename T>
 __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     paged_decode_mma_stream_kernel(const __grid_constant__ CUtensorMap tm_k,
                                    const __grid_constant__ CUtensorMap tm_v,
+                                   const __grid_constant__ CUtensorMap tm_kh,
+                                   const __grid_constant__ CUtensorMap tm_vh,
                                    const __grid_constant__ DecodeParams p) {
     constexpr int HALVES = D / 64;        // 128-byte boxes per token row
     constexpr uint32_t BOX = BS * 128;    // bytes of one [BS x 64] box
@@ -310,6 +312,8 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_kh);
+        prefetch_tensormap(&tm_vh);
         s_var[1] = 0;   // abort
         s_var[2] = 0;   // slots issued
         for (int st = 0; st < stages; ++st) {
@@ -479,7 +483,12 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                         r.flags = (first ? kSlotFirst | (u.flags & kSlotHead) : 0) |
                                   (i == u.n - 1 ? (u.flags & kSlotLast) : 0) |
                                   (u.flags & kSlotWhole) | (b >= 0 ? kSlotValid : 0);
-                        const uint32_t bytes = (b >= 0 ? stage_bytes : 0u) + (first ? q_bytes : 0u);
+                        // a context's last block holding at most half a block
+                        // of its tokens: only that half is loaded (the rows
+                        // past the context are masked by the consumers)
+                        const bool half = n - (u.i0 + i) * BS <= BS / 2;
+                        const uint32_t kv_bytes = half ? stage_bytes / 2 : stage_bytes;
+                        const uint32_t bytes = (b >= 0 ? kv_bytes : 0u) + (first ? q_bytes : 0u);
                         if (bytes == 0) {
                             mbar_arrive(&full[st]);
                             continue;
@@ -490,12 +499,14 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                                         policy);
                         if (b >= 0) {
                             unsigned char* dst = ring + (size_t)st * stage_bytes;
+                            const CUtensorMap* mk = half ? &tm_kh : &tm_k;
+                            const CUtensorMap* mv = half ? &tm_vh : &tm_v;
                             for (int hh = 0; hh < HPC; ++hh) {
                                 const int hrow = (u.hg * HPC + hh) * HALVES;
                                 for (int h = 0; h < HALVES; ++h) {
-                                    tma_load_4d(dst + hh * head_bytes + h * BOX, &tm_k,
-                                                &full[st], 0, hrow + h, 0, b, policy);
-                                    tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, &tm_v,
+                                    tma_load_4d(dst + hh * head_bytes + h * BOX, mk, &full[st],
+                                                0, hrow + h, 0, b, policy);
+                                    tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, mv,
                                                 &full[st], 0, hrow + h, 0, b, policy);
                                 }
                             }
