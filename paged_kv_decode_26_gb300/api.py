@@ -40,6 +40,33 @@ def _need_cuda(name: str, t: torch.Tensor):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _need_all_cuda(names, tensors) -> None:
+    """_need_cuda over several tensors; the per-name pass runs only when one
+    fails (the decode calls sit on a serving loop's critical path)."""
+    for t in tensors:
+        if not (t.is_cuda and t.is_contiguous()):
+            for name, u in zip(names, tensors):
+                _need_cuda(name, u)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    """_stream_ptr as a plain integer (ctypes converts it for a void* argument)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _addr(t: Optional[torch.Tensor]) -> int:
+    """_ptr as a plain integer."""
+    return t.data_ptr() if t is not None and t.numel() else 0
+
+
+_DECODE_NAMES = ("out", "q", "k_pool", "v_pool", "block_tables", "context_lens")
+_APPEND_NAMES = _DECODE_NAMES + ("k_new", "v_new", "slot_mapping")
+
+
 def set_tuning(**knobs) -> None:
     """Override launch shapes for tests and tuning sweeps, e.g.
     ``set_tuning(decode_hpc=2, mq_tc=0)``; a value of None restores the
@@ -94,14 +121,12 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     """out[s,h] = softmax(scale * q[s,h] . K^T) V over the paged context of s.
     Shapes: q/out [S, H, D], pools [num_blocks, B, Hk, D], block_tables int32
     [S, max_blocks], context_lens int32 [S]."""
-    for name, t in (("out", out), ("q", q), ("k_pool", k_pool), ("v_pool", v_pool),
-                    ("block_tables", block_tables), ("context_lens", context_lens)):
-        _need_cuda(name, t)
+    _need_all_cuda(_DECODE_NAMES, (out, q, k_pool, v_pool, block_tables, context_lens))
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise ValueError("block_tables and context_lens must be int32")
     S, H, D = q.shape
     nb, B, Hk, D2 = k_pool.shape
-    if (D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != (S, H, D)
+    if (D2 != D or v_pool.shape != k_pool.shape or out.shape != q.shape
             or q.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype
             or block_tables.dim() != 2 or block_tables.shape[0] != S
             or context_lens.shape != (S,)):
@@ -109,11 +134,11 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     if workspace is None:
         workspace = alloc_decode_workspace(q, k_pool, max_context_len, split_tokens)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib().paged_attn_decode(_ptr(out), _DT[out.dtype], _ptr(q), _ptr(k_pool), _ptr(v_pool),
-                                 _DT[k_pool.dtype], _ptr(block_tables), block_tables.shape[1],
-                                 _ptr(context_lens), S, H, Hk, D, B, nb, float(scale),
-                                 int(max_context_len), int(split_tokens), _ptr(workspace),
-                                 ws_bytes, _stream_ptr(stream))
+    st = lib().paged_attn_decode(out.data_ptr(), _DT[out.dtype], q.data_ptr(), _addr(k_pool),
+                                 _addr(v_pool), _DT[k_pool.dtype], block_tables.data_ptr(),
+                                 block_tables.shape[1], context_lens.data_ptr(), S, H, Hk, D, B,
+                                 nb, float(scale), int(max_context_len), int(split_tokens),
+                                 _addr(workspace), ws_bytes, _stream_handle(stream))
     check(st, "paged_attn_decode")
     return out
 
@@ -128,20 +153,18 @@ def paged_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.T
     """kv_append(k_pool, v_pool, k_new, v_new, slot_mapping) then
     paged_attn_decode(...) in one launch; context_lens counts the appended
     token.  No other sequence of the call may read a page that holds a slot."""
-    for name, t in (("out", out), ("q", q), ("k_pool", k_pool), ("v_pool", v_pool),
-                    ("block_tables", block_tables), ("context_lens", context_lens),
-                    ("k_new", k_new), ("v_new", v_new), ("slot_mapping", slot_mapping)):
-        _need_cuda(name, t)
+    _need_all_cuda(_APPEND_NAMES, (out, q, k_pool, v_pool, block_tables, context_lens, k_new,
+                                   v_new, slot_mapping))
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise ValueError("block_tables and context_lens must be int32")
     if slot_mapping.dtype != torch.int64:
         raise ValueError("slot_mapping must be int64")
     S, H, D = q.shape
     nb, B, Hk, D2 = k_pool.shape
-    if (D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != (S, H, D)
+    if (D2 != D or v_pool.shape != k_pool.shape or out.shape != q.shape
             or q.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype
             or block_tables.dim() != 2 or block_tables.shape[0] != S
-            or context_lens.shape != (S,) or tuple(k_new.shape) != (S, Hk, D)
+            or context_lens.shape != (S,) or k_new.shape != (S, Hk, D)
             or k_new.shape != v_new.shape or k_new.dtype != k_pool.dtype
             or v_new.dtype != k_pool.dtype or slot_mapping.shape != (S,)):
         raise ValueError("inconsistent shapes or dtypes")
@@ -149,10 +172,11 @@ def paged_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.T
         workspace = alloc_decode_workspace(q, k_pool, max_context_len, split_tokens)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib().paged_attn_decode_append(
-        _ptr(out), _DT[out.dtype], _ptr(q), _ptr(k_pool), _ptr(v_pool), _DT[k_pool.dtype],
-        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S, H, Hk, D, B, nb,
-        float(scale), int(max_context_len), int(split_tokens), _ptr(workspace), ws_bytes,
-        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _stream_ptr(stream))
+        out.data_ptr(), _DT[out.dtype], q.data_ptr(), _addr(k_pool), _addr(v_pool),
+        _DT[k_pool.dtype], block_tables.data_ptr(), block_tables.shape[1],
+        context_lens.data_ptr(), S, H, Hk, D, B, nb, float(scale), int(max_context_len),
+        int(split_tokens), _addr(workspace), ws_bytes, k_new.data_ptr(), v_new.data_ptr(),
+        slot_mapping.data_ptr(), _stream_handle(stream))
     check(st, "paged_attn_decode_append")
     return out
 

@@ -211,3 +211,26 @@ def test_tuning_knob_names_match_the_header():
                 for m in re.finditer(r"PKV_TUNE_(\w+)\s*=\s*(\d+)", text))
     count = enum.pop("count")
     assert enum == _lib.TUNE_KNOBS and count == len(enum)
+
+
+def test_binding_rejects_host_tensors_by_name():
+    """The decode bindings check every tensor before any call into the
+    library; a host tensor is named in the error (no GPU needed)."""
+    import torch
+    import paged_kv_decode_26_gb300 as pkv
+    S, H, Hk, D, B, nb = 2, 8, 2, 64, 16, 4
+    t = dict(out=torch.zeros(S, H, D), q=torch.zeros(S, H, D, dtype=torch.float16),
+             k_pool=torch.zeros(nb, B, Hk, D, dtype=torch.float16),
+             v_pool=torch.zeros(nb, B, Hk, D, dtype=torch.float16),
+             block_tables=torch.zeros(S, 2, dtype=torch.int32),
+             context_lens=torch.ones(S, dtype=torch.int32))
+    with pytest.raises(ValueError, match="out must be a CUDA tensor"):
+        pkv.paged_attn_decode(t["out"], t["q"], t["k_pool"], t["v_pool"], t["block_tables"],
+                              t["context_lens"], 0.125, 1)
+    new = dict(k_new=torch.zeros(S, Hk, D, dtype=torch.float16),
+               v_new=torch.zeros(S, Hk, D, dtype=torch.float16),
+               slot_mapping=torch.zeros(S, dtype=torch.int64))
+    with pytest.raises(ValueError, match="out must be a CUDA tensor"):
+        pkv.paged_attn_decode_append(t["out"], t["q"], t["k_pool"], t["v_pool"],
+                                     t["block_tables"], t["context_lens"], 0.125, 1,
+                                     new["k_new"], new["v_new"], new["slot_mapping"])
