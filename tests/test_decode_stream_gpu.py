@@ -298,3 +298,17 @@ def test_stream_calls_on_two_streams(lib, tuning):
     for a, o in zip(alone, outs):
         assert torch.equal(_bits(a), _bits(o))
     assert lib.device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("dtype,out_dtype", [(torch.float16, torch.float32),
+                                             (torch.float16, torch.float16),
+                                             (torch.bfloat16, torch.float32)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_stream_dtypes(lib, tuning, dtype, out_dtype, D):
+    """fp16 and bf16 K/V with fp16, bf16 and fp32 outputs, including
+    contexts whose last block is at most half full (half-block loads)."""
+    lens = [1, 7, 8, 9, 16, 17, 24, 25, 40, 300, 0, 129]
+    case = wl.make_case(5, lens_override=lens, D=D, dtype=dtype, out_dtype=out_dtype,
+                        d2d_pairs=0, h2d_pairs=0, host_pool_blocks=1, poison=True, seed=D + 3)
+    out = _stream(tuning, case)
+    _check(lib, case, out, f"{dtype} -> {out_dtype}, D={D}")
