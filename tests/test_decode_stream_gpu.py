@@ -312,3 +312,14 @@ def test_stream_dtypes(lib, tuning, dtype, out_dtype, D):
                         d2d_pairs=0, h2d_pairs=0, host_pool_blocks=1, poison=True, seed=D + 3)
     out = _stream(tuning, case)
     _check(lib, case, out, f"{dtype} -> {out_dtype}, D={D}")
+
+
+def test_stream_group_of_two_forced(lib, tuning):
+    """Groups of 2 take the tensor-core consumer only when forced
+    (decode_mma=1); the streaming decode then handles them too."""
+    lens = [0, 5, 16, 17, 33, 300, 1000, 9, 64]
+    case = wl.make_case(5, lens_override=lens, H=16, Hk=8, d2d_pairs=0, h2d_pairs=0,
+                        host_pool_blocks=1, poison=True, seed=2)
+    tuning(decode_mma=1)
+    out = _stream(tuning, case)
+    _check(lib, case, out, "groups of 2, forced tensor-core consumer")
