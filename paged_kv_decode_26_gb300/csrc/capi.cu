@@ -211,13 +211,18 @@ constexpr int kDenseMaxSeqs = 1024;
 
 
 // Heads per CTA, ring depth and warp roles.  A pipeline stage holds one page
-// of K and V for the CTA's kv heads: HPC * head_dim = 512 elements, i.e.
-// 1 KB contiguous per token row and 32 KB (block size 16) or 64 KB (block
-// size 32) per stage.  Three stages keep two CTAs (block size 16) or one CTA
-// (block size 32) resident per SM with ~192 KB of loads in flight per SM,
-// which measured best on GB300 for both block sizes.  The knobs
-// PKV_TUNE_DECODE_HPC, _STAGES, _WPT and _QPW override the choice (for
-// tuning sweeps).
+// of K and V for the CTA's kv heads: at head_dim 128, HPC = 4 heads are 512
+// elements, i.e. 1 KB contiguous per token row and 32 KB (block size 16) or
+// 64 KB (block size 32) per stage.  Three stages keep two CTAs (block size
+// 16) or one CTA (block size 32) resident per SM with ~192 KB of loads in
+// flight per SM, which measured best on GB300 for both block sizes.  At
+// head_dim 64 four heads per CTA (16 KB stages, four CTAs per SM) beat
+// eight (32 KB stages) on GB300: GQA 32/8 at log-uniform lengths 0.82
+// against 0.64 of the copy peak, 32K-token MHA 1.045 against 1.029, the
+// tiny workload's 1100 problems in one batched launch 0.89-0.91 against
+// 0.87; 4K-token MHA 0.961 against 0.972.  The knobs PKV_TUNE_DECODE_HPC,
+// _STAGES, _WPT and _QPW override the choice (for tuning sweeps).
+constexpr int kHeadsPerCta = 4;
 void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size, int hpc_target,
                       DecodeConfig* c) {
     const int G = n_heads / n_kv_heads;
@@ -269,7 +274,7 @@ void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size,
 
 void shape_config(int n_heads, int n_kv_heads, int head_dim, int block_size, DecodeConfig* c) {
     shape_config_hpc(n_heads, n_kv_heads, head_dim, block_size,
-                     tuning(PKV_TUNE_DECODE_HPC, 512 / head_dim), c);
+                     tuning(PKV_TUNE_DECODE_HPC, kHeadsPerCta), c);
 }
 
 int auto_split_tokens(int num_seqs, int n_kv_heads, int hpc, int block_size, int max_context_len,
