@@ -50,6 +50,7 @@ namespace pkv {
 
 constexpr int kStreamMaxSeqs = 2048;     // context lengths held in shared memory
 constexpr int kStreamBatchChunks = 32;   // chunks whose block ids one lookup fetches (one a lane)
+static_assert(kStreamBatchChunks <= 32, "the append slots of a batch are read one chunk a lane");
 constexpr int kStreamBatchPages = 128;   // pages of one lookup (a multiple of 32)
 static_assert(kStreamBatchPages % 32 == 0, "a lookup spreads its pages over a warp");
 
