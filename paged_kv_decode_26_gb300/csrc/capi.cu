@@ -616,17 +616,12 @@ pkv_status decode_impl(void* out, pkv_dtype out_dtype, const void* q, const void
     if ((e = encode_pool_map(&L.tm_v, vmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
                              head_dim, c.hpc, c.mma)) != cudaSuccess)
         return cuda_fail(e);
-    if (c.stream) {
-        // half-block boxes for the last block of a context that fills at
-        // most half of it (the streaming decode's many short contexts)
-        if ((e = encode_pool_map(&L.tm_kh, kmap_base, kv_dtype, map_blocks, block_size,
-                                 n_kv_heads, head_dim, c.hpc, c.mma, block_size / 2)) !=
-                cudaSuccess ||
-            (e = encode_pool_map(&L.tm_vh, vmap_base, kv_dtype, map_blocks, block_size,
-                                 n_kv_heads, head_dim, c.hpc, c.mma, block_size / 2)) !=
-                cudaSuccess)
-            return cuda_fail(e);
-    }
+    // half-block boxes for a context's last block that it fills at most half
+    if ((e = encode_pool_map(&L.tm_kh, kmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
+                             head_dim, c.hpc, c.mma, block_size / 2)) != cudaSuccess ||
+        (e = encode_pool_map(&L.tm_vh, vmap_base, kv_dtype, map_blocks, block_size, n_kv_heads,
+                             head_dim, c.hpc, c.mma, block_size / 2)) != cudaSuccess)
+        return cuda_fail(e);
 
     pkv::DecodeParams& p = L.p;
     p.out = out;
@@ -904,7 +899,11 @@ PKV_API pkv_status pkv_decode_batched_plan(pkv_decode_plan* plan,
         if ((e = encode_pool_map(&b.tm_k, kb, kv_dtype, mb, block_size, n_kv_heads, head_dim,
                                  c.hpc, c.mma)) != cudaSuccess ||
             (e = encode_pool_map(&b.tm_v, vb, kv_dtype, mb, block_size, n_kv_heads, head_dim,
-                                 c.hpc, c.mma)) != cudaSuccess)
+                                 c.hpc, c.mma)) != cudaSuccess ||
+            (e = encode_pool_map(&b.tm_kh, kb, kv_dtype, mb, block_size, n_kv_heads, head_dim,
+                                 c.hpc, c.mma, block_size / 2)) != cudaSuccess ||
+            (e = encode_pool_map(&b.tm_vh, vb, kv_dtype, mb, block_size, n_kv_heads, head_dim,
+                                 c.hpc, c.mma, block_size / 2)) != cudaSuccess)
             return cuda_fail(e);
         pkv::DecodeParams& p = b.p;
         p.out = q.out;

@@ -18,6 +18,8 @@ namespace pkv {
 struct BatchedProblem {
     CUtensorMap tm_k;
     CUtensorMap tm_v;
+    CUtensorMap tm_kh;   // boxes of half a block (a short last block)
+    CUtensorMap tm_vh;
     DecodeParams p;
     ReduceParams r;
 };
@@ -43,7 +45,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int z = blockIdx.z;
     const int i = problem_of(seq_begin, num_problems, z);
     const BatchedProblem& b = probs[i];
-    decode_cta<D, BS, QPW, T>(&b.tm_k, &b.tm_v, b.p, blockIdx.x, blockIdx.y, z - seq_begin[i]);
+    decode_cta<D, BS, QPW, T>(&b.tm_k, &b.tm_v, &b.tm_kh, &b.tm_vh, b.p, blockIdx.x, blockIdx.y,
+                              z - seq_begin[i]);
 }
 
 template <int D, int BS, typename T>
@@ -54,7 +57,8 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     const int z = blockIdx.z;
     const int i = problem_of(seq_begin, num_problems, z);
     const BatchedProblem& b = probs[i];
-    decode_mma_cta<D, BS, T>(&b.tm_k, &b.tm_v, b.p, blockIdx.x, blockIdx.y, z - seq_begin[i]);
+    decode_mma_cta<D, BS, T>(&b.tm_k, &b.tm_v, &b.tm_kh, &b.tm_vh, b.p, blockIdx.x, blockIdx.y,
+                             z - seq_begin[i]);
 }
 
 // Split merge over every problem: one warp per global (sequence, query head).

@@ -202,9 +202,12 @@ __device__ __forceinline__ void consumer_sync(int n_threads) {
 // ------------------------------------------------------------ the kernel
 
 // One CTA's work: (sequence s, kv-head group hg, context split `split`) of
-// the problem described by p, its K/V pools seen through tm_k / tm_v.
+// the problem described by p, its K/V pools seen through tm_k / tm_v (and
+// tm_kh / tm_vh, boxes of half a block, for a last block whose tokens fit
+// its first half).
 template <int D, int BS, int QPW, typename T>
 __device__ __forceinline__ void decode_cta(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                           const CUtensorMap* tm_kh, const CUtensorMap* tm_vh,
                                            const DecodeParams& p, int split, int hg, int s) {
     constexpr int LPR = D / 8;                   // lanes per K/V row (8 dims each)
     constexpr int TPI = 32 / LPR;                // rows per warp iteration
@@ -285,6 +288,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* tm_k, const CUtens
         if (lane == 0) {
             prefetch_tensormap(tm_k);
             prefetch_tensormap(tm_v);
+            prefetch_tensormap(tm_kh);
+            prefetch_tensormap(tm_vh);
             const uint64_t policy = l2_policy_evict_first();
             int i = 0;
             for (; i < n_pages; ++i) {
@@ -298,10 +303,15 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* tm_k, const CUtens
                 if (*reinterpret_cast<volatile int*>(s_abort)) break;
                 const int b = s_bid[i];
                 if (b >= 0) {
+                    // a last block holding at most half a block of tokens:
+                    // only its first half is loaded (the consumers mask the
+                    // rows past the context, whatever the slot holds there)
+                    const bool half = tok_end - (tok_begin + i * BS) <= BS / 2;
                     unsigned char* dst = tiles + (size_t)st * 2 * tile_bytes;
-                    mbar_arrive_expect_tx(&full[st], 2 * tile_bytes);
-                    tma_load_4d(dst, tm_k, &full[st], 0, hg * HPC, 0, b, policy);
-                    tma_load_4d(dst + tile_bytes, tm_v, &full[st], 0, hg * HPC, 0, b, policy);
+                    mbar_arrive_expect_tx(&full[st], half ? tile_bytes : 2 * tile_bytes);
+                    tma_load_4d(dst, half ? tm_kh : tm_k, &full[st], 0, hg * HPC, 0, b, policy);
+                    tma_load_4d(dst + tile_bytes, half ? tm_vh : tm_v, &full[st], 0, hg * HPC, 0,
+                                b, policy);
                 } else {
                     mbar_arrive(&full[st]);
                 }
@@ -703,11 +713,13 @@ template <int D, int BS, int QPW, typename T>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_kh,
+                        const __grid_constant__ CUtensorMap tm_vh,
                         const __grid_constant__ DecodeParams p) {
     launch_dependents();  // the split merge may start its CTAs (they wait)
     int split, hg, s;
     if (!decode_unit<BS>(p, split, hg, s)) return;
-    decode_cta<D, BS, QPW, T>(&tm_k, &tm_v, p, split, hg, s);
+    decode_cta<D, BS, QPW, T>(&tm_k, &tm_v, &tm_kh, &tm_vh, p, split, hg, s);
 }
 
 // ------------------------------------------------------------ split merge

@@ -12,7 +12,7 @@ namespace pkv {
 struct DecodeLaunch {
     CUtensorMap tm_k;
     CUtensorMap tm_v;
-    CUtensorMap tm_kh;   // stream kernel: boxes of half a block
+    CUtensorMap tm_kh;   // boxes of half a block (a short last block)
     CUtensorMap tm_vh;
     DecodeParams p;
     dim3 grid;

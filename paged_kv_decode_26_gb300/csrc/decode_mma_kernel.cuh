@@ -306,9 +306,12 @@ __device__ __forceinline__ void mma_heads_finish(const MmaHeads<D>& st, const De
     }
 }
 
-// One CTA's work (sequence s, kv-head group hg, split) of the problem p.
+// One CTA's work (sequence s, kv-head group hg, split) of the problem p
+// (tm_kh / tm_vh: boxes of half a block, for a last block whose tokens fit
+// its first half).
 template <int D, int BS, typename T>
 __device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                               const CUtensorMap* tm_kh, const CUtensorMap* tm_vh,
                                                const DecodeParams& p, int split, int hg, int s) {
     constexpr int HALVES = D / 64;        // 128-byte boxes per token row
     constexpr uint32_t BOX = BS * 128;    // bytes of one [BS x 64] box
@@ -376,6 +379,8 @@ __device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CU
         if (lane == 0) {
             prefetch_tensormap(tm_k);
             prefetch_tensormap(tm_v);
+            prefetch_tensormap(tm_kh);
+            prefetch_tensormap(tm_vh);
             const uint64_t policy = l2_policy_evict_first();
             int i = 0;
             for (; i < n_pages; ++i) {
@@ -389,14 +394,20 @@ __device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CU
                 if (*reinterpret_cast<volatile int*>(s_abort)) break;
                 const int b = s_bid[i];
                 if (b >= 0) {
+                    // a last block holding at most half a block of tokens:
+                    // only its first half is loaded (the consumers mask the
+                    // rows past the context)
+                    const bool half = tok_end - (tok_begin + i * BS) <= BS / 2;
+                    const CUtensorMap* mk = half ? tm_kh : tm_k;
+                    const CUtensorMap* mv = half ? tm_vh : tm_v;
                     unsigned char* dst = ring + (size_t)st * stage_bytes;
-                    mbar_arrive_expect_tx(&full[st], stage_bytes);
+                    mbar_arrive_expect_tx(&full[st], half ? stage_bytes / 2 : stage_bytes);
                     for (int hh = 0; hh < HPC; ++hh) {
                         const int row = (hg * HPC + hh) * HALVES;
                         for (int h = 0; h < HALVES; ++h) {
-                            tma_load_4d(dst + hh * head_bytes + h * BOX, tm_k, &full[st], 0,
+                            tma_load_4d(dst + hh * head_bytes + h * BOX, mk, &full[st], 0,
                                         row + h, 0, b, policy);
-                            tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, tm_v,
+                            tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, mv,
                                         &full[st], 0, row + h, 0, b, policy);
                         }
                     }
@@ -454,11 +465,13 @@ template <int D, int BS, typename T>
 __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_kh,
+                            const __grid_constant__ CUtensorMap tm_vh,
                             const __grid_constant__ DecodeParams p) {
     launch_dependents();  // the split merge may start its CTAs (they wait)
     int split, hg, s;
     if (!decode_unit<BS>(p, split, hg, s)) return;
-    decode_mma_cta<D, BS, T>(&tm_k, &tm_v, p, split, hg, s);
+    decode_mma_cta<D, BS, T>(&tm_k, &tm_v, &tm_kh, &tm_vh, p, split, hg, s);
 }
 
 }  // namespace pkv
