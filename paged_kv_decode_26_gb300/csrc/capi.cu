@@ -395,6 +395,33 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
                          split_tokens;
     c->max_splits = ms < 1 ? 1 : (int)ms;
     c->max_pages = split_tokens / block_size;
+    // A grid that fits in one wave of resident CTAs: no CTA waits for a slot,
+    // each waits only on its own chain of page loads and page work, so more
+    // consumer warps and a deeper ring cost nothing.  Two warps take turns
+    // on a kv head's pages, and the ring holds as many pages (8, 6 or 4) as
+    // keep the grid in one wave.  GB300, CUDA graphs of L2 flush + decode:
+    // the tiny workload 9.1 -> 7.0 us, 2 MHA sequences of 100-300 tokens
+    // 11.9 -> 8.3 us, 4 of 1-2K tokens 31.0 -> 22.8 us, one of 8K tokens
+    // 33.4 -> 27.9 us (256 CTAs, two per SM).
+    if (!c->stream && !c->mma && !tuned(PKV_TUNE_DECODE_WPT) &&
+        !tuned(PKV_TUNE_DECODE_STAGES) && c->wpt == 1 &&
+        c->hpc * c->wpk * 2 <= pkv::kMaxConsumerWarps) {
+        const long long ctas = (long long)num_seqs * (n_kv_heads / c->hpc) * c->max_splits;
+        const size_t limit = smem_optin > 0 ? smem_optin : (size_t)227 * 1024;
+        const size_t per_sm_bytes = smem_per_sm > 0 ? (size_t)smem_per_sm : (size_t)228 * 1024;
+        for (int stages = 8; stages >= 4; stages -= 2) {
+            const size_t smem = pkv::decode_smem_bytes(head_dim, block_size, c->qpw, 2, c->hpc,
+                                                       c->wpk, 2, stages, c->max_pages);
+            if (smem > limit) continue;
+            const long long per_sm = (long long)(per_sm_bytes / (smem + 1024));
+            if (ctas <= (long long)(sm_count > 0 ? sm_count : 1) * per_sm) {
+                c->wpt = 2;
+                c->stages = stages;
+                c->threads = 32 * (1 + c->hpc * c->wpk * c->wpt);
+                break;
+            }
+        }
+    }
     if (c->stream)
         c->smem = pkv::decode_stream_smem_bytes(head_dim, block_size, n_heads / n_kv_heads, 2,
                                                 c->hpc, c->stages, num_seqs);
