@@ -148,8 +148,8 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
  * and there are at most 2 x SMs (sequence, kv-head group) units; the whole
  * context (no split, no merge) when the units fill the SMs 16 times over;
  * the whole context when the decode streams through resident CTAs (groups
- * of 4 or 8 query heads, at most 2048 sequences, max_context_len at most
- * 1536: many short contexts), which cut the work at equal page shares
+ * of 4 or 8 query heads, 2 to 2048 sequences, max_context_len at most
+ * 4096), which cut the work at equal page shares
  * instead of at splits; rounded to whole blocks and capped at the context.
  * Returns 0 for an unsupported shape.
  */

@@ -187,14 +187,22 @@ struct DecodeConfig {
 
 constexpr int kDefaultSplitTokens = 512;
 // The streaming decode is chosen (knob PKV_TUNE_DECODE_STREAM unset) for
-// tensor-core decodes with the automatic split whose longest context is at
-// most this long, with a two-page ring.  GB300, decode call by CUDA events:
-// continuous-batching step (256 sequences, Pareto lengths, longest 1235
-// tokens, 32 / 8 heads) 25.6 us against 37.5 us one CTA per unit; with
-// longer contexts the per-unit kernel's three-page ring streams faster
-// (128 sequences of U[256, 2048] tokens: 96.9 against 86.7 us; 32K-token
-// log-uniform GQA: 431 against 398 us).
-constexpr int kStreamMaxContext = 1536;
+// tensor-core decodes with the automatic split of two or more sequences
+// whose longest context is at most this long, with a two-page ring.  Its
+// equal page shares do not depend on how the lengths are spread, while one
+// CTA per unit waits on the longest unit.  GB300, 32 / 8 heads, CUDA graphs
+// of L2 flush + decode, streaming against one CTA per unit:
+//   continuous-batching step (256 Pareto lengths, longest 1235): 21.9 / 37.5 us
+//   768 / 1024 / 2048 Pareto lengths: 44.5 / 83.1, 53.8 / 107.0, 90.9 / 233.0 us
+//   8 of U[1500, 3000]: 24.2 / 28.2 us; 2 of U[2000, 4096]: 21.7 / 24.6 us
+//   shared-prefix GQA, log-uniform to 2048 / 4096: 57.9 / 64.3, 91.1 / 92.1 us
+//   uniform batches: 128 of U[256, 2048] 106.5 / 112.5, 256 of U[2048, 4096]
+//   486.7 / 473.6, 2048 of U[1, 4096] 2516 / 2452 us
+// Past 4096 tokens the per-unit kernel's three-page ring wins where prefix
+// blocks are shared (log-uniform to 8192: 146.7 / 133.6 us; to 32768: 427.9
+// / 397.9 us), and so it does for a single sequence (U[3000, 4096]: 25.2 /
+// 24.5 us).
+constexpr int kStreamMaxContext = 4096;
 constexpr int kStreamStages = 2;
 // Few (sequence, head-group) units with contexts of 8K tokens or more: every
 // unit is cut into many pieces anyway, and at 1024 tokens a piece the GPU stays
@@ -359,7 +367,8 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
     c->stream = allow_stream && split_tokens == 0 && c->mma && c->wpt == 1 &&
                 num_seqs <= pkv::kStreamMaxSeqs && all_pages <= 0x7fffffffLL &&
                 full <= 0x7fffffffLL &&
-                (stream_knob >= 0 ? stream_knob != 0 : max_context_len <= kStreamMaxContext);
+                (stream_knob >= 0 ? stream_knob != 0
+                                  : num_seqs >= 2 && max_context_len <= kStreamMaxContext);
     c->stream_ctas = 0;
     if (c->stream) {
         // its shared memory must fit (the per-unit kernel runs otherwise)

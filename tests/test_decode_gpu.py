@@ -139,7 +139,10 @@ def test_grouped_heads_both_paths(lib, tuning, mma, D, B, H, Hk, dtype, out_dtyp
     (256, 32, 8, 16, 16385, 512),    # continuous: 512 units, more than 2 x SMs
     (256, 32, 8, 16, 1235, 1248),    # continuous as generated (longest 1235): streaming decode,
                                      # no split (the whole page-rounded context)
-    (128, 32, 8, 16, 2048, 512),     # GQA up to 2K tokens: one CTA per unit
+    (128, 32, 8, 16, 4096, 4096),    # GQA up to 4K tokens: streaming decode
+    (128, 32, 8, 16, 4104, 512),     # GQA past 4K tokens: one CTA per unit
+    (1, 32, 8, 16, 4096, 512),       # one sequence: one CTA per unit
+    (128, 32, 8, 16, 8192, 1024),    # 8K tokens, few units: longer splits
     (4, 8, 8, 16, 201, 208),         # tiny: one split of the whole (page-rounded) context
     (4096, 32, 8, 16, 4096, 4096),   # many units: no split at all
 ])
@@ -148,8 +151,9 @@ def test_automatic_split_length(lib, S, H, Hk, B, max_ctx, expect):
     context is 8K tokens or more and there are at most 2 x SMs (sequence,
     head-group) units; the whole context when the units fill the GPU 16
     times over (sizes for GB300's 152 SMs); the whole context for the
-    streaming tensor-core decode (groups of 4 or 8, longest context at most
-    1536), which cuts the work at its CTAs' shares instead of splits."""
+    streaming tensor-core decode (groups of 4 or 8, 2 to 2048 sequences,
+    longest context at most 4096), which cuts the work at its CTAs' shares
+    instead of splits."""
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("unit thresholds are stated for 152 SMs")
     assert lib.decode_split_tokens(S, H, Hk, 128, B, max_ctx) == expect
