@@ -94,7 +94,7 @@ PKV_API int pkv_version(void);
  */
 #define PKV_TUNE_AUTO (-2147483647 - 1)
 typedef enum pkv_tune_knob {
-    PKV_TUNE_DECODE_MMA = 0,      /* 0/1: tensor-core decode consumer off/on (groups >= 2) */
+    PKV_TUNE_DECODE_MMA = 0,      /* 0/1: tensor-core decode consumer off/on (any group) */
     PKV_TUNE_DECODE_HPC = 1,      /* kv heads per decode CTA */
     PKV_TUNE_DECODE_STAGES = 2,   /* decode ring depth, 2..8 */
     PKV_TUNE_DECODE_WPT = 3,      /* decode warps taking turns on a head's pages */

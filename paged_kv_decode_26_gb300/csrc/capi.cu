@@ -236,7 +236,7 @@ void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size,
     const int G = n_heads / n_kv_heads;
     // Groups of four or more query heads per kv head make each page a small
     // dense contraction: the tensor-core consumer takes them.
-    c->mma = tuning(PKV_TUNE_DECODE_MMA, G >= 4 ? 1 : 0) != 0 && G >= 2;
+    c->mma = tuning(PKV_TUNE_DECODE_MMA, G >= 4 ? 1 : 0) != 0;
     if (c->mma) {
         c->qpw = G;
         c->wpk = 1;

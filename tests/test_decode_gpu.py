@@ -116,12 +116,12 @@ def test_launch_configurations(lib, tuning, config, knobs):
 
 @pytest.mark.parametrize("mma", ["0", "1"])
 @pytest.mark.parametrize("D,B", [(64, 16), (128, 16), (64, 32), (128, 32)])
-@pytest.mark.parametrize("H,Hk", [(8, 4), (16, 4), (32, 4)])
+@pytest.mark.parametrize("H,Hk", [(4, 4), (8, 4), (16, 4), (32, 4)])
 @pytest.mark.parametrize("dtype,out_dtype", [(torch.bfloat16, torch.bfloat16),
                                              (torch.float16, torch.float32)])
 def test_grouped_heads_both_paths(lib, tuning, mma, D, B, H, Hk, dtype, out_dtype):
-    """Query-head groups of 2, 4 and 8 on the CUDA-core and the tensor-core
-    consumer, ragged tails and NaN padding included."""
+    """One query head per kv head and groups of 2, 4 and 8 on the CUDA-core
+    and the tensor-core consumer, ragged tails and NaN padding included."""
     tuning(decode_mma=mma)
     case = wl.make_case(3, S=4, lens=("uniform", 1, 400), H=H, Hk=Hk, D=D, B=B, dtype=dtype,
                         out_dtype=out_dtype, share_blocks=2, poison=True, seed=H + D + B)

@@ -323,3 +323,19 @@ def test_stream_group_of_two_forced(lib, tuning):
     tuning(decode_mma=1)
     out = _stream(tuning, case)
     _check(lib, case, out, "groups of 2, forced tensor-core consumer")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_stream_one_head_per_kv_head_forced(lib, tuning, D):
+    """One query head per kv head (MHA) on the tensor-core consumer (forced):
+    the streaming decode and the per-unit kernel, against the oracle."""
+    lens = [0, 5, 16, 17, 33, 300, 1000, 9, 64, 1, 2049, 128]
+    case = wl.make_case(5, lens_override=lens, H=8, Hk=8, D=D, d2d_pairs=0, h2d_pairs=0,
+                        host_pool_blocks=1, poison=True, seed=11 + D)
+    tuning(decode_mma=1)
+    out = _stream(tuning, case)
+    _check(lib, case, out, f"MHA D={D}, streaming tensor-core decode")
+    tuning(decode_stream=0)
+    for split in (0, 64):
+        got = run_decode(case, split_tokens=split)
+        _check(lib, case, got, f"MHA D={D}, per-unit tensor-core decode, split {split}")
