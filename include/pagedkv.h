@@ -149,7 +149,8 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_he
  * context (no split, no merge) when the units fill the SMs 16 times over;
  * the whole context when the decode streams through resident CTAs (groups
  * of 4 or 8 query heads, 2 to 2048 sequences, max_context_len at most
- * 4096), which cut the work at equal page shares
+ * 4096; or any group size and context length from 256 to 2048 sequences),
+ * which cut the work at equal page shares
  * instead of at splits; rounded to whole blocks and capped at the context.
  * Returns 0 for an unsupported shape.
  */

@@ -203,6 +203,18 @@ constexpr int kDefaultSplitTokens = 512;
 // / 397.9 us), and so it does for a single sequence (U[3000, 4096]: 25.2 /
 // 24.5 us).
 constexpr int kStreamMaxContext = 4096;
+// From this many sequences the streaming decode is taken for any group size
+// (MHA and groups of 2 then run on the tensor-core consumer) and any context
+// length.  Large batches are where lengths spread (continuous batching) and
+// where one CTA per unit waits longest on its longest unit.  GB300, CUDA
+// graphs of flush + decode, streaming against one CTA per unit:
+//   GQA 32 / 8, Pareto lengths past 4K tokens: 512 seqs 32.0 / 60.3 us,
+//   2048 seqs 93.1 / 226.3 us; uniform 512 of U[4096, 8192] 1888 / 1901 us,
+//   1024 of U[1, 16384] 5047 / 5273 us; shared prefixes (512 seqs,
+//   log-uniform to 8192) 591 / 529 us
+//   MHA 32 / 32, Pareto lengths: 256 seqs 53.5 / 71.2 us, 640 seqs 104.8 /
+//   197.9 us; uniform 256 of U[512, 4096] 1422 / 1318 us
+constexpr int kStreamManySeqs = 256;
 constexpr int kStreamStages = 2;
 // Few (sequence, head-group) units with contexts of 8K tokens or more: every
 // unit is cut into many pieces anyway, and at 1024 tokens a piece the GPU stays
@@ -232,11 +244,12 @@ constexpr int kDenseMaxSeqs = 1024;
 // _STAGES, _WPT and _QPW override the choice (for tuning sweeps).
 constexpr int kHeadsPerCta = 4;
 void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size, int hpc_target,
-                      DecodeConfig* c) {
+                      DecodeConfig* c, bool prefer_mma = false) {
     const int G = n_heads / n_kv_heads;
     // Groups of four or more query heads per kv head make each page a small
-    // dense contraction: the tensor-core consumer takes them.
-    c->mma = tuning(PKV_TUNE_DECODE_MMA, G >= 4 ? 1 : 0) != 0;
+    // dense contraction: the tensor-core consumer takes them (and any group
+    // when the streaming decode, which runs on it, is preferred).
+    c->mma = tuning(PKV_TUNE_DECODE_MMA, G >= 4 || prefer_mma ? 1 : 0) != 0;
     if (c->mma) {
         c->qpw = G;
         c->wpk = 1;
@@ -280,9 +293,10 @@ void shape_config_hpc(int n_heads, int n_kv_heads, int head_dim, int block_size,
     c->threads = 32 * (1 + c->hpc * c->wpk * c->wpt);
 }
 
-void shape_config(int n_heads, int n_kv_heads, int head_dim, int block_size, DecodeConfig* c) {
+void shape_config(int n_heads, int n_kv_heads, int head_dim, int block_size, DecodeConfig* c,
+                  bool prefer_mma = false) {
     shape_config_hpc(n_heads, n_kv_heads, head_dim, block_size,
-                     tuning(PKV_TUNE_DECODE_HPC, kHeadsPerCta), c);
+                     tuning(PKV_TUNE_DECODE_HPC, kHeadsPerCta), c, prefer_mma);
 }
 
 int auto_split_tokens(int num_seqs, int n_kv_heads, int hpc, int block_size, int max_context_len,
@@ -345,14 +359,19 @@ int cta_order(int max_splits, int num_seqs) {
 pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, int block_size,
                        int max_context_len, int split_tokens, int sm_count, DecodeConfig* c,
                        bool allow_stream = true, size_t smem_optin = 0, int smem_per_sm = 0) {
-    shape_config(n_heads, n_kv_heads, head_dim, block_size, c);
+    const int stream_knob = tuning(PKV_TUNE_DECODE_STREAM, -1);
+    // Many sequences: the streaming decode for any group size and context
+    // length (on the tensor-core consumer), unless the knob says otherwise.
+    const bool many = allow_stream && split_tokens == 0 && stream_knob != 0 &&
+                      num_seqs >= kStreamManySeqs && num_seqs <= pkv::kStreamMaxSeqs;
+    shape_config(n_heads, n_kv_heads, head_dim, block_size, c, many);
     // Too few (sequence, head-group) units to occupy the SMs: two kv heads per
     // CTA give more, shorter CTAs (measured on the tiny workload, 4 sequences
     // x 8 kv heads: 12.6 us per call instead of 14.8 us with 8 heads per CTA).
     if (!tuned(PKV_TUNE_DECODE_HPC) && c->hpc > 2 &&
         (long long)num_seqs * (n_kv_heads / c->hpc) < (sm_count > 0 ? sm_count : 1)) {
         DecodeConfig narrow;
-        shape_config_hpc(n_heads, n_kv_heads, head_dim, block_size, 2, &narrow);
+        shape_config_hpc(n_heads, n_kv_heads, head_dim, block_size, 2, &narrow, many);
         *c = narrow;
     }
     // The whole longest context, in whole blocks.
@@ -363,12 +382,11 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
     // 32-bit positions.  It cuts no context into splits (the work is cut at
     // the CTAs' shares instead), so the split length is the whole context.
     const long long all_pages = (long long)num_seqs * n_kv_heads * (full / block_size);
-    const int stream_knob = tuning(PKV_TUNE_DECODE_STREAM, -1);
     c->stream = allow_stream && split_tokens == 0 && c->mma && c->wpt == 1 &&
                 num_seqs <= pkv::kStreamMaxSeqs && all_pages <= 0x7fffffffLL &&
                 full <= 0x7fffffffLL &&
                 (stream_knob >= 0 ? stream_knob != 0
-                                  : num_seqs >= 2 && max_context_len <= kStreamMaxContext);
+                                  : many || (num_seqs >= 2 && max_context_len <= kStreamMaxContext));
     c->stream_ctas = 0;
     if (c->stream) {
         // its shared memory must fit (the per-unit kernel runs otherwise)
@@ -389,6 +407,9 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
             c->stream_ctas = (sm_count > 0 ? sm_count : 1) * per_sm;
         }
     }
+    // The tensor-core consumer was taken for small groups only to stream.
+    if (many && !c->stream && !tuned(PKV_TUNE_DECODE_MMA) && n_heads / n_kv_heads < 4)
+        shape_config(n_heads, n_kv_heads, head_dim, block_size, c);
     if (split_tokens == 0) {
         split_tokens = c->stream ? (int)full
                                  : auto_split_tokens(num_seqs, n_kv_heads, c->hpc, block_size,

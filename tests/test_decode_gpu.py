@@ -136,13 +136,16 @@ def test_grouped_heads_both_paths(lib, tuning, mma, D, B, H, Hk, dtype, out_dtyp
     (64, 32, 32, 16, 4097, 512),     # llama7b_mha: 4K contexts keep 512-token splits
     (128, 32, 8, 16, 32075, 1024),   # gqa_prefix: 32K contexts, 256 (seq, head-group) units
     (16, 32, 32, 32, 32769, 1024),   # long_context (2 kv heads per CTA: 256 units)
-    (256, 32, 8, 16, 16385, 512),    # continuous: 512 units, more than 2 x SMs
+    (255, 32, 8, 16, 16385, 512),    # 510 units, more than 2 x SMs: 512 tokens
     (256, 32, 8, 16, 1235, 1248),    # continuous as generated (longest 1235): streaming decode,
                                      # no split (the whole page-rounded context)
     (128, 32, 8, 16, 4096, 4096),    # GQA up to 4K tokens: streaming decode
     (128, 32, 8, 16, 4104, 512),     # GQA past 4K tokens: one CTA per unit
     (1, 32, 8, 16, 4096, 512),       # one sequence: one CTA per unit
     (128, 32, 8, 16, 8192, 1024),    # 8K tokens, few units: longer splits
+    (256, 32, 8, 16, 20000, 20000),  # 256 sequences or more: streaming at any length
+    (256, 32, 32, 16, 4096, 4096),   # ... and for MHA
+    (255, 32, 32, 16, 4096, 512),    # one fewer MHA sequence: one CTA per unit
     (4, 8, 8, 16, 201, 208),         # tiny: one split of the whole (page-rounded) context
     (4096, 32, 8, 16, 4096, 4096),   # many units: no split at all
 ])
@@ -152,8 +155,8 @@ def test_automatic_split_length(lib, S, H, Hk, B, max_ctx, expect):
     head-group) units; the whole context when the units fill the GPU 16
     times over (sizes for GB300's 152 SMs); the whole context for the
     streaming tensor-core decode (groups of 4 or 8, 2 to 2048 sequences,
-    longest context at most 4096), which cuts the work at its CTAs' shares
-    instead of splits."""
+    longest context at most 4096; any group and length from 256 to 2048
+    sequences), which cuts the work at its CTAs' shares instead of splits."""
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("unit thresholds are stated for 152 SMs")
     assert lib.decode_split_tokens(S, H, Hk, 128, B, max_ctx) == expect
