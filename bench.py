@@ -10,7 +10,11 @@ decode over the context including that token, in one call
 (paged_attn_decode_append: the decode CTA of each sequence's last split
 writes the token's rows before it loads the pages).  The metric is KV
 bytes read per second (logical K+V bytes of every sequence's context) and
-sequence-steps per second.
+sequence-steps per second.  The end-to-end figure (`e2e`) times the same
+step from pinned host buffers, one library call per step (a HostStep
+prepared once; paged_attn_decode_append_host: the step's packed inputs
+copied in, append + decode, the output copied back, the stream
+synchronised).
 
 Under torchrun each rank runs its own replica (own sequences, own pools):
 decode is data-parallel by sequence with no exchange, so scaling is weak and
@@ -778,11 +782,24 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
         h2d_bytes = host["inputs"].numel()        # the staging buffer, copied whole
         d2h_bytes = host["out"].numel() * host["out"].element_size()
 
-        def e2e_step():
-            devb["inputs"].copy_(host["inputs"], non_blocking=True)
-            run_step()
-            host["out"].copy_(devb["out"], non_blocking=True)
-            stream.synchronize()
+        if R == 1 and not with_swaps and not use_graph and not args.batched:
+            # the library's one-call step from host memory: the staging
+            # buffer in, append + decode, the output back, the stream synced
+            r0, e2e_call = reps[0], "HostStep.run (paged_attn_decode_append_host)"
+            host_step = pkv.HostStep(
+                [(host["inputs"], devb["inputs"])], host["out"], r0["out"], r0["q"],
+                r0["k_pool"], r0["v_pool"], r0["bt"], r0["lens"], case.scale, r0["max_ctx"],
+                r0["k_new"], r0["v_new"], r0["slots"], split_tokens=args.split,
+                workspace=r0["ws"], stream=stream)
+            e2e_step = host_step.run
+        else:
+            e2e_call = "copy in, the step, copy out, stream synchronize"
+
+            def e2e_step():
+                devb["inputs"].copy_(host["inputs"], non_blocking=True)
+                run_step()
+                host["out"].copy_(devb["out"], non_blocking=True)
+                stream.synchronize()
 
         for _ in range(3):
             e2e_step()
@@ -803,7 +820,7 @@ def measure(args, rank, world, dev, pkv, wl, *, full):
         e2e_ms, = reduce_over_ranks([e2e_ms], "max", dist, world, dev)
         e2e = {"value": job_gbs(total_kv, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-               "ms_per_step": e2e_ms, "steps": n_e2e}
+               "ms_per_step": e2e_ms, "steps": n_e2e, "call": e2e_call}
 
     return dict(case=case, reps=reps, R=R, S=S, ms=ms, dec_ms=dec_ms, kv_read=kv_read,
                 kv_unique=kv_unique, io_bytes=io_bytes, total_kv=total_kv,

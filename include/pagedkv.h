@@ -230,6 +230,47 @@ PKV_API pkv_status paged_attn_decode_append(
     const void* k_new, const void* v_new, const int64_t* slot_mapping, void* stream);
 
 /*
+ * One host-to-device copy of paged_attn_decode_append_host: `bytes` bytes
+ * from host address `host` (pinned memory gives asynchronous copies) to
+ * device address `device`.
+ */
+typedef struct {
+    const void* host;
+    void* device;
+    size_t bytes;
+} pkv_copy;
+
+/*
+ * paged_attn_decode_append_host -- one serving step from host memory in one
+ * call ([SWAP] serving loop: the step's inputs arrive from the host, the
+ * attention output goes back to it): on `stream`, in order,
+ *   1. the n_h2d copies h2d[i] (host to device; a copy of 0 bytes is
+ *      skipped), which typically move the step's q, k_new, v_new,
+ *      block_tables, context_lens and slot_mapping -- packed in one staging
+ *      buffer they are one copy;
+ *   2. paged_attn_decode_append with the remaining arguments (all device
+ *      pointers, as there);
+ *   3. a device-to-host copy of the first out_bytes bytes of `out` to
+ *      out_host (none when out_bytes is 0);
+ *   4. with synchronize nonzero, a wait for the stream, so that out_host
+ *      holds the result on return.
+ * The caller owns every buffer; the host buffers must stay valid until the
+ * copies complete (pinned host memory makes them asynchronous).  Invalid
+ * copy arguments (a negative n_h2d, a missing list, a copy without an
+ * address, out_bytes larger than `out`, a missing out_host) are refused
+ * with PKV_ERR_INVALID before anything is issued; a refusal by
+ * paged_attn_decode_append comes after the copies of step 1 were issued and
+ * issues nothing more.
+ */
+PKV_API pkv_status paged_attn_decode_append_host(
+    const pkv_copy* h2d, int n_h2d, void* out_host, size_t out_bytes, int synchronize,
+    void* out, pkv_dtype out_dtype, const void* q, void* k_pool, void* v_pool, pkv_dtype kv_dtype,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int n_heads, int n_kv_heads, int head_dim, int block_size, int num_blocks,
+    float scale, int max_context_len, int split_tokens, void* workspace, size_t workspace_bytes,
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, void* stream);
+
+/*
  * Batched decode -- many independent decode problems (each with its own
  * K/V pools, block tables, lengths, queries and outputs, and optionally a
  * fused append) in one launch.  The problems share the head counts,

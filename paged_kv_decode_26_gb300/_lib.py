@@ -44,6 +44,9 @@ SIGNATURES = {
                                _i, _i, _p, _sz, _p]),
     "paged_attn_decode_append": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i,
                                       _i, _f, _i, _i, _p, _sz, _p, _p, _p, _p]),
+    "paged_attn_decode_append_host": (_i, [_p, _i, _p, _sz, _i, _p, _i, _p, _p, _p, _i, _p, _i,
+                                           _p, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p, _sz, _p,
+                                           _p, _p, _p]),
     "pkv_decode_batched_workspace_bytes": (_sz, [_p, _i, _i, _i, _i, _i, _i, _i]),
     "pkv_decode_batched_plan": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p, _sz,
                                      _p]),

@@ -143,16 +143,9 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     return out
 
 
-def paged_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
-                             v_pool: torch.Tensor, block_tables: torch.Tensor,
-                             context_lens: torch.Tensor, scale: float, max_context_len: int,
-                             k_new: torch.Tensor, v_new: torch.Tensor,
-                             slot_mapping: torch.Tensor, split_tokens: int = 0,
-                             workspace: Optional[torch.Tensor] = None,
-                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """kv_append(k_pool, v_pool, k_new, v_new, slot_mapping) then
-    paged_attn_decode(...) in one launch; context_lens counts the appended
-    token.  No other sequence of the call may read a page that holds a slot."""
+def _append_args(out, q, k_pool, v_pool, block_tables, context_lens, scale, max_context_len,
+                 k_new, v_new, slot_mapping, split_tokens, workspace, stream) -> tuple:
+    """Checked C arguments of paged_attn_decode_append (its order)."""
     _need_all_cuda(_APPEND_NAMES, (out, q, k_pool, v_pool, block_tables, context_lens, k_new,
                                    v_new, slot_mapping))
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
@@ -171,14 +164,100 @@ def paged_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.T
     if workspace is None:
         workspace = alloc_decode_workspace(q, k_pool, max_context_len, split_tokens)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return (out.data_ptr(), _DT[out.dtype], q.data_ptr(), _addr(k_pool), _addr(v_pool),
+            _DT[k_pool.dtype], block_tables.data_ptr(), block_tables.shape[1],
+            context_lens.data_ptr(), S, H, Hk, D, B, nb, float(scale), int(max_context_len),
+            int(split_tokens), _addr(workspace), ws_bytes, k_new.data_ptr(), v_new.data_ptr(),
+            slot_mapping.data_ptr(), _stream_handle(stream))
+
+
+def paged_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                             v_pool: torch.Tensor, block_tables: torch.Tensor,
+                             context_lens: torch.Tensor, scale: float, max_context_len: int,
+                             k_new: torch.Tensor, v_new: torch.Tensor,
+                             slot_mapping: torch.Tensor, split_tokens: int = 0,
+                             workspace: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """kv_append(k_pool, v_pool, k_new, v_new, slot_mapping) then
+    paged_attn_decode(...) in one launch; context_lens counts the appended
+    token.  No other sequence of the call may read a page that holds a slot."""
     st = lib().paged_attn_decode_append(
-        out.data_ptr(), _DT[out.dtype], q.data_ptr(), _addr(k_pool), _addr(v_pool),
-        _DT[k_pool.dtype], block_tables.data_ptr(), block_tables.shape[1],
-        context_lens.data_ptr(), S, H, Hk, D, B, nb, float(scale), int(max_context_len),
-        int(split_tokens), _addr(workspace), ws_bytes, k_new.data_ptr(), v_new.data_ptr(),
-        slot_mapping.data_ptr(), _stream_handle(stream))
+        *_append_args(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                      max_context_len, k_new, v_new, slot_mapping, split_tokens, workspace,
+                      stream))
     check(st, "paged_attn_decode_append")
     return out
+
+
+class _Copy(C.Structure):
+    """pkv_copy of include/pagedkv.h."""
+    _fields_ = [("host", C.c_void_p), ("device", C.c_void_p), ("bytes", C.c_size_t)]
+
+
+class HostStep:
+    """A serving step from host memory, prepared once: every
+    (host tensor, device tensor) pair of `copies` is copied host to device
+    (the host tensor's bytes; pinned memory copies asynchronously), then
+    paged_attn_decode_append runs on the device tensors, then `out` is
+    copied back into `out_host` (a CPU tensor of the same shape and dtype),
+    and with `synchronize` the step returns once the stream is idle -- one
+    library call (paged_attn_decode_append_host) per run().  The arguments
+    are checked and marshalled here, so run() issues the copies at once.
+    Between runs the tensors' contents may change (the step's inputs, the
+    pools, the lengths), not their addresses; max_context_len must bound
+    every context of every run.  `stream` is fixed here (None: the current
+    stream now)."""
+
+    def __init__(self, copies, out_host: torch.Tensor, out: torch.Tensor, q: torch.Tensor,
+                 k_pool: torch.Tensor, v_pool: torch.Tensor, block_tables: torch.Tensor,
+                 context_lens: torch.Tensor, scale: float, max_context_len: int,
+                 k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                 split_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None, synchronize: bool = True):
+        if workspace is None:
+            workspace = alloc_decode_workspace(q, k_pool, max_context_len, split_tokens)
+        args = _append_args(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                            max_context_len, k_new, v_new, slot_mapping, split_tokens, workspace,
+                            stream)
+        pairs = list(copies)
+        arr = (_Copy * max(1, len(pairs)))()
+        for i, (h, d) in enumerate(pairs):
+            if h.is_cuda or not d.is_cuda:
+                raise ValueError("each copy is a (host tensor, device tensor) pair")
+            nbytes = h.numel() * h.element_size()
+            if not (h.is_contiguous() and d.is_contiguous()) or \
+                    d.numel() * d.element_size() < nbytes:
+                raise ValueError("copies need contiguous tensors and room on the device")
+            arr[i].host, arr[i].device, arr[i].bytes = h.data_ptr(), d.data_ptr(), nbytes
+        if out_host.is_cuda or out_host.shape != out.shape or out_host.dtype != out.dtype or \
+                not out_host.is_contiguous():
+            raise ValueError("out_host must be a contiguous CPU tensor shaped like out")
+        # the tensors stay referenced while the step may run
+        self._keep = (pairs, out_host, out, q, k_pool, v_pool, block_tables, context_lens,
+                      k_new, v_new, slot_mapping, workspace)
+        self._fn = lib().paged_attn_decode_append_host
+        self._args = (arr, len(pairs), out_host.data_ptr(), out.numel() * out.element_size(),
+                      1 if synchronize else 0) + args
+        self.out_host = out_host
+
+    def run(self) -> torch.Tensor:
+        check(self._fn(*self._args), "paged_attn_decode_append_host")
+        return self.out_host
+
+
+def paged_attn_decode_append_host(copies, out_host: torch.Tensor, out: torch.Tensor,
+                                  q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  scale: float, max_context_len: int, k_new: torch.Tensor,
+                                  v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                                  split_tokens: int = 0,
+                                  workspace: Optional[torch.Tensor] = None,
+                                  stream: Optional[torch.cuda.Stream] = None,
+                                  synchronize: bool = True) -> torch.Tensor:
+    """One HostStep, prepared and run once (see HostStep)."""
+    return HostStep(copies, out_host, out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                    max_context_len, k_new, v_new, slot_mapping, split_tokens, workspace, stream,
+                    synchronize).run()
 
 
 class _Problem(C.Structure):

@@ -801,6 +801,45 @@ PKV_API pkv_status paged_attn_decode_append(
                        workspace_bytes, k_new, v_new, slot_mapping, stream);
 }
 
+PKV_API pkv_status paged_attn_decode_append_host(
+    const pkv_copy* h2d, int n_h2d, void* out_host, size_t out_bytes, int synchronize,
+    void* out, pkv_dtype out_dtype, const void* q, void* k_pool, void* v_pool, pkv_dtype kv_dtype,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int n_heads, int n_kv_heads, int head_dim, int block_size, int num_blocks,
+    float scale, int max_context_len, int split_tokens, void* workspace, size_t workspace_bytes,
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, void* stream) {
+    if (n_h2d < 0 || (n_h2d > 0 && !h2d)) return invalid("h2d must list n_h2d copies");
+    for (int i = 0; i < n_h2d; ++i)
+        if (h2d[i].bytes > 0 && (!h2d[i].host || !h2d[i].device))
+            return invalid("a host-to-device copy without a host or device address");
+    if (out_bytes > 0) {
+        if (!out_host || !out) return invalid("out_host and out are required when out_bytes > 0");
+        const size_t es = out_dtype == PKV_F32 ? 4 : 2;
+        if (num_seqs < 0 || n_heads < 0 || head_dim < 0 ||
+            out_bytes > (size_t)num_seqs * n_heads * head_dim * es)
+            return invalid("out_bytes exceeds the output");
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    for (int i = 0; i < n_h2d; ++i) {
+        if (h2d[i].bytes == 0) continue;
+        if ((e = cudaMemcpyAsync(h2d[i].device, h2d[i].host, h2d[i].bytes, cudaMemcpyHostToDevice,
+                                 st)))
+            return cuda_fail(e);
+    }
+    const pkv_status s = paged_attn_decode_append(
+        out, out_dtype, q, k_pool, v_pool, kv_dtype, block_tables, max_blocks_per_seq,
+        context_lens, num_seqs, n_heads, n_kv_heads, head_dim, block_size, num_blocks, scale,
+        max_context_len, split_tokens, workspace, workspace_bytes, k_new, v_new, slot_mapping,
+        stream);
+    if (s != PKV_OK) return s;
+    if (out_bytes > 0 &&
+        (e = cudaMemcpyAsync(out_host, out, out_bytes, cudaMemcpyDeviceToHost, st)))
+        return cuda_fail(e);
+    if (synchronize && (e = cudaStreamSynchronize(st))) return cuda_fail(e);
+    return PKV_OK;
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------ batched decode

@@ -115,6 +115,25 @@ def test_append_rejects_invalid_arguments(L):
     assert L.kv_append(FAKE, FAKE, FAKE, FAKE, 1, FAKE, 0, 8, 128, 16, 4, NULL) == 0
 
 
+def test_host_step_refuses_bad_copies_before_issuing_any(L):
+    """paged_attn_decode_append_host checks its copy arguments before it
+    issues anything (no device is touched: the addresses are never used)."""
+    from paged_kv_decode_26_gb300.api import _Copy
+    dec = (FAKE, 1, FAKE, FAKE, FAKE, 1, FAKE, 4, FAKE, 2, 8, 8, 128, 16, 10, 0.1, 64, 0, NULL, 0,
+           FAKE, FAKE, FAKE, NULL)
+    one = (_Copy * 1)()
+    one[0].host, one[0].device, one[0].bytes = 4096, 0, 64           # no device address
+    assert L.paged_attn_decode_append_host(one, 1, FAKE, 0, 0, *dec) == 1
+    assert L.paged_attn_decode_append_host(None, 1, FAKE, 0, 0, *dec) == 1    # no list
+    assert L.paged_attn_decode_append_host(one, -1, FAKE, 0, 0, *dec) == 1
+    ok = (_Copy * 1)()
+    ok[0].host, ok[0].device, ok[0].bytes = 4096, 8192, 0            # empty copy: skipped
+    assert L.paged_attn_decode_append_host(ok, 1, NULL, 16, 0, *dec) == 1     # no out_host
+    # more bytes back than the output holds (2 x 8 x 128 bf16 = 4096 bytes)
+    assert L.paged_attn_decode_append_host(ok, 1, FAKE, 4098, 0, *dec) == 1
+    assert L.pkv_last_error_detail()
+
+
 def test_swap_rejects_invalid_arguments(L):
     assert L.swap_blocks(FAKE, FAKE, 24, FAKE, 1, 4, 4, NULL) == 1      # not a multiple of 16
     assert L.swap_blocks(FAKE, FAKE, 0, FAKE, 1, 4, 4, NULL) == 1

@@ -375,3 +375,89 @@ def test_decode_append_equals_two_calls(lib, config, split):
     ref = _oracle(case, lens=lens, tables=bt, k=k1, v=v1)
     assert_attention_close(o2, ref, case.out_dtype, f"config {config}", kv_dtype=case.dtype,
                            abs_weighted=_abs_v(case, lens=lens, tables=bt, k=k1, v=v1))
+
+
+@pytest.mark.parametrize("config", [1, 2, 5])
+def test_host_step_equals_device_call(lib, config):
+    """paged_attn_decode_append_host (the step's inputs packed in one pinned
+    host buffer, copied in, appended and decoded, the output copied back,
+    the stream synchronised) leaves the same pools and output, bit for bit,
+    as copying the inputs and calling paged_attn_decode_append; out_host
+    holds the device output."""
+    import paged_kv_decode_26_gb300 as pkv
+    extra = {"d2d_pairs": 0, "h2d_pairs": 0, "host_pool_blocks": 1} if config == 5 else {}
+    case = wl.make_case(config, S=8 if config != 1 else None, poison=True, seed=config + 60,
+                        **extra)
+    S = case.S
+    bm = pkv.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)
+    bt = case.block_tables.clone()
+    need = int(((case.context_lens + 1 + case.B - 1) // case.B).max())
+    if need > bt.shape[1]:
+        bt = torch.cat([bt, torch.full((S, need - bt.shape[1]), -1, dtype=torch.int32)], 1)
+    lens = case.context_lens.clone()
+    slots = torch.empty(S, dtype=torch.int64)
+    bm.append_slots(bt, lens, slots)
+    gen = torch.Generator().manual_seed(config + 60)
+    k_new = torch.randn(S, case.Hk, case.D, generator=gen).to(case.dtype)
+    v_new = torch.randn(S, case.Hk, case.D, generator=gen).to(case.dtype)
+    max_ctx = int(lens.max())
+    # one pinned staging buffer and its device twin, each input at a 256-byte offset
+    parts = [case.q, k_new, v_new, bt, lens, slots]
+    offs, o = [], 0
+    for t in parts:
+        offs.append(o)
+        o += (t.numel() * t.element_size() + 255) // 256 * 256
+    hbuf = torch.zeros(o, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(o, dtype=torch.uint8, device="cuda")
+
+    def views(buf):
+        return [buf[a:a + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                for a, t in zip(offs, parts)]
+    for hv, t in zip(views(hbuf), parts):
+        hv.copy_(t)
+    q_d, kn_d, vn_d, bt_d, lens_d, slots_d = views(dbuf)
+    results = []
+    for host_call in (False, True):
+        kp, vp = case.k_pool.cuda(), case.v_pool.cuda()
+        out = torch.zeros(S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+        out_h = torch.full((S, case.H, case.D), float("nan"), dtype=case.out_dtype).pin_memory()
+        dbuf.zero_()
+        torch.cuda.synchronize()
+        if host_call:
+            pkv.paged_attn_decode_append_host([(hbuf, dbuf)], out_h, out, q_d, kp, vp, bt_d,
+                                              lens_d, case.scale, max_ctx, kn_d, vn_d, slots_d)
+        else:
+            dbuf.copy_(hbuf)
+            pkv.paged_attn_decode_append(out, q_d, kp, vp, bt_d, lens_d, case.scale, max_ctx,
+                                         kn_d, vn_d, slots_d)
+            out_h.copy_(out)
+        torch.cuda.synchronize()
+        assert pkv.device_errors(clear=True) == 0
+        results.append((out_h.clone(), kp.cpu(), vp.cpu(), out.cpu()))
+    (o1, k1, v1, _), (o2, k2, v2, dev2) = results
+    iv = torch.int16 if o1.element_size() == 2 else torch.int32
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+    assert torch.equal(o1.view(iv), o2.view(iv))
+    assert torch.equal(o2.view(iv), dev2.view(iv))
+    ref = _oracle(case, lens=lens, tables=bt, k=k2, v=v2)
+    assert_attention_close(o2, ref, case.out_dtype, f"host step, config {config}",
+                           kv_dtype=case.dtype,
+                           abs_weighted=_abs_v(case, lens=lens, tables=bt, k=k2, v=v2))
+    # prepared once, run twice with new host inputs in between: each run
+    # equals the device call on the inputs of that run (the append writes
+    # the same rows again, so the pools stay as they are)
+    kp, vp = k2.cuda(), v2.cuda()
+    out = torch.zeros(S, case.H, case.D, dtype=case.out_dtype, device="cuda")
+    out_h = torch.empty(S, case.H, case.D, dtype=case.out_dtype).pin_memory()
+    step = pkv.HostStep([(hbuf, dbuf)], out_h, out, q_d, kp, vp, bt_d, lens_d, case.scale,
+                        max_ctx, kn_d, vn_d, slots_d)
+    q_h = views(hbuf)[0]
+    for sign in (1.0, -1.0):
+        q_h.copy_(case.q * sign)
+        got = step.run().clone()
+        ref_out = torch.zeros_like(out)
+        pkv.paged_attn_decode(ref_out, q_d, kp, vp, bt_d, lens_d, case.scale, max_ctx)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(iv), ref_out.cpu().view(iv)), f"HostStep run, sign {sign}"
+    assert pkv.device_errors(clear=True) == 0
