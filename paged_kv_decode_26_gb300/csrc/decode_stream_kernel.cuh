@@ -52,6 +52,7 @@ constexpr int kStreamMaxSeqs = 2048;     // context lengths held in shared memor
 constexpr int kStreamBatchChunks = 32;   // chunks whose block ids one lookup fetches (one a lane)
 static_assert(kStreamBatchChunks <= 32, "the append slots of a batch are read one chunk a lane");
 constexpr int kStreamBatchPages = 128;   // pages of one lookup (a multiple of 32)
+constexpr int kAppendRound = 8;          // appended 16-byte vectors a lane loads per round
 static_assert(kStreamBatchPages % 32 == 0, "a lookup spreads its pages over a warp");
 
 // Slot record flags.
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    __shared__ int s_app[kStreamBatchChunks];   // chunks of a batch that append, in order
 
     // barriers and tensor-map prefetches first: they overlap the
     // context-length loads
@@ -387,11 +389,12 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
             __syncwarp();
             const int nc = s_var[3];
             if (nc == 0) break;
-            // ---- block ids of every queued page: lane l takes the batch's
+            // ---- block ids of every queued page, the append slots and the
+            // first round of the appended rows: lane l takes the batch's
             // pages l, l + 32, ... (its chunk found by a forward scan of the
             // chunks' first offsets) and issues all its loads before any
             // store, so the batch costs one memory round trip however many
-            // chunks it holds
+            // chunks it holds, plus one per further round of appended rows
             {
                 const int npg = s_var[0];
                 constexpr int PER_LANE = kStreamBatchPages / 32;
@@ -407,6 +410,68 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                         bid[j] = p.block_tables[(size_t)s_of * p.max_blocks_per_seq + i_of];
                     }
                 }
+                // ---- fused append: a chunk holding a run's last page writes
+                // the new token's rows of its heads before that page loads
+                // (the token's row lies in the last page, which no other CTA
+                // reads).  Its slot sits in lane ui (chunk ui), and the
+                // appended rows are spread over the lanes as one list of
+                // 16-byte vectors: chunk s_app[a], vector i of its K then V
+                // rows, for item a * 2 * per_row + i.
+                constexpr int VEC = 16 / (int)sizeof(T);
+                const int per_row = HPC * D / VEC;
+                const size_t row = (size_t)p.n_kv_heads * D;
+                int64_t my_slot = -1;
+                unsigned need = 0;
+                if (p.slot_mapping != nullptr) {
+                    bool mine = false;
+                    if (lane < nc) {
+                        const StreamChunk u = s_chunk[lane];
+                        mine = u.i0 + u.n == (s_len[u.s] + BS - 1) / BS;
+                        if (mine) my_slot = p.slot_mapping[u.s];
+                    }
+                    need = __ballot_sync(0xffffffffu, mine);
+                    if (mine) s_app[__popc(need & ((1u << lane) - 1u))] = lane;
+                    __syncwarp();
+                }
+                const int items = __popc(need) * 2 * per_row;
+                uint4 val[kAppendRound];
+                auto append_load = [&](int r) {
+#pragma unroll
+                    for (int k = 0; k < kAppendRound; ++k) {
+                        const int f = (r * kAppendRound + k) * 32 + lane;
+                        if (f < items) {
+                            const int a = f / (2 * per_row), i = f - a * 2 * per_row;
+                            const StreamChunk u = s_chunk[s_app[a]];
+                            const bool is_v = i >= per_row;
+                            const int j = (is_v ? i - per_row : i) * VEC;
+                            const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) +
+                                           (size_t)u.s * row + (size_t)u.hg * HPC * D + j;
+                            val[k] = *reinterpret_cast<const uint4*>(src);
+                        }
+                    }
+                };
+                auto append_store = [&](int r) {
+#pragma unroll
+                    for (int k = 0; k < kAppendRound; ++k) {
+                        const int f = (r * kAppendRound + k) * 32 + lane;
+                        const int a = f < items ? f / (2 * per_row) : 0;
+                        const int ui = items > 0 ? s_app[a] : 0;
+                        const int64_t slot_row = __shfl_sync(0xffffffffu, my_slot, ui);
+                        if (f >= items || slot_row < 0) continue;
+                        const StreamChunk u = s_chunk[ui];
+                        const int i = f - a * 2 * per_row;
+                        if (slot_row >= (int64_t)p.num_blocks * BS) {
+                            if (u.hg == 0 && i == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
+                            continue;
+                        }
+                        const bool is_v = i >= per_row;
+                        const int j = (is_v ? i - per_row : i) * VEC;
+                        T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) +
+                                 (size_t)slot_row * row + (size_t)u.hg * HPC * D + j;
+                        *reinterpret_cast<uint4*>(dst) = val[k];
+                    }
+                };
+                if (items > 0) append_load(0);
 #pragma unroll
                 for (int j = 0; j < PER_LANE; ++j) {
                     const int f = lane + 32 * j;
@@ -418,40 +483,12 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                     }
                     s_bid[f] = b;
                 }
-            }
-            // ---- fused append: the chunk holding a run's last page writes
-            // the new token's rows of its heads before that page loads (the
-            // token's row lies in the last page, which no other CTA reads)
-            if (p.slot_mapping != nullptr) {
-                constexpr int VEC = 16 / (int)sizeof(T);
-                const int per_row = HPC * D / VEC;
-                const size_t row = (size_t)p.n_kv_heads * D;
-                // every chunk's slot at once, lane ui holding chunk ui's
-                // (at most kStreamBatchChunks = 32 chunks)
-                int64_t my_slot = -1;
-                if (lane < nc) {
-                    const StreamChunk u = s_chunk[lane];
-                    if (u.i0 + u.n == (s_len[u.s] + BS - 1) / BS) my_slot = p.slot_mapping[u.s];
+                const int rounds = (items + 32 * kAppendRound - 1) / (32 * kAppendRound);
+                for (int r = 0; r < rounds; ++r) {
+                    if (r > 0) append_load(r);
+                    append_store(r);
                 }
-                for (int ui = 0; ui < nc; ++ui) {
-                    const int64_t slot_row = __shfl_sync(0xffffffffu, my_slot, ui);
-                    if (slot_row < 0) continue;
-                    const StreamChunk u = s_chunk[ui];
-                    if (slot_row >= (int64_t)p.num_blocks * BS) {
-                        if (u.hg == 0 && lane == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
-                        continue;
-                    }
-                    const size_t off_new = (size_t)u.s * row + (size_t)u.hg * HPC * D;
-                    const size_t off_pool = (size_t)slot_row * row + (size_t)u.hg * HPC * D;
-                    for (int i = lane; i < 2 * per_row; i += 32) {
-                        const bool is_v = i >= per_row;
-                        const int j = (is_v ? i - per_row : i) * VEC;
-                        const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) + off_new + j;
-                        T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) + off_pool + j;
-                        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-                    }
-                }
-                asm volatile("fence.proxy.async.global;" ::: "memory");
+                if (items > 0) asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             __syncwarp();
             // ---- issue every page of the batch (lane 0)

@@ -341,18 +341,19 @@ def test_stream_one_head_per_kv_head_forced(lib, tuning, D):
         _check(lib, case, got, f"MHA D={D}, per-unit tensor-core decode, split {split}")
 
 
-@pytest.mark.parametrize("H,Hk,lens", [
-    (8, 8, ("pareto", 1.5, 16, 16384)),      # MHA, a long tail
-    (16, 8, ("uniform", 1, 600)),            # groups of 2
-    (16, 4, ("pareto", 1.2, 16, 20000)),     # groups of 4 past 4096 tokens
+@pytest.mark.parametrize("H,Hk,lens,D,B", [
+    (8, 8, ("pareto", 1.5, 16, 16384), 128, 16),    # MHA, a long tail
+    (8, 8, ("pareto", 1.5, 16, 16384), 64, 32),     # ... head_dim 64, 32-token blocks
+    (16, 8, ("uniform", 1, 600), 128, 16),          # groups of 2
+    (16, 4, ("pareto", 1.2, 16, 20000), 128, 16),   # groups of 4 past 4096 tokens
 ])
-def test_many_sequences_stream_automatically(lib, tuning, H, Hk, lens):
+def test_many_sequences_stream_automatically(lib, tuning, H, Hk, lens, D, B):
     """From 256 sequences the automatic choice is the streaming decode for
     any group size and context length: its output equals the forced
     streaming tensor-core decode bit for bit and the oracle's within the
     tolerance."""
-    case = wl.make_case(5, S=300, lens=lens, H=H, Hk=Hk, d2d_pairs=0, h2d_pairs=0,
-                        host_pool_blocks=1, poison=True, seed=H + Hk)
+    case = wl.make_case(5, S=300, lens=lens, H=H, Hk=Hk, D=D, B=B, d2d_pairs=0, h2d_pairs=0,
+                        host_pool_blocks=1, poison=True, seed=H + Hk + D)
     dev = to_device(case)
     auto = run_decode(case, split_tokens=0, dev=dev)
     tuning(decode_mma=1, decode_stream=1)
