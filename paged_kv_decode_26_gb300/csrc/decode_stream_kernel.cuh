@@ -52,7 +52,9 @@ constexpr int kStreamMaxSeqs = 2048;     // context lengths held in shared memor
 constexpr int kStreamBatchChunks = 32;   // chunks whose block ids one lookup fetches (one a lane)
 static_assert(kStreamBatchChunks <= 32, "the append slots of a batch are read one chunk a lane");
 constexpr int kStreamBatchPages = 128;   // pages of one lookup (a multiple of 32)
-constexpr int kAppendRound = 8;          // appended 16-byte vectors a lane loads per round
+constexpr int kAppendPerLane = 8;        // 16-byte vectors of one chunk's appended rows a lane holds
+static_assert(2 * kMmaMaxWarps * 128 * 2 / 16 <= 32 * kAppendPerLane,
+              "the appended K and V rows of a chunk fit the warp's registers");
 static_assert(kStreamBatchPages % 32 == 0, "a lookup spreads its pages over a warp");
 
 // Slot record flags.
@@ -390,15 +392,15 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
             const int nc = s_var[3];
             if (nc == 0) break;
             // ---- block ids of every queued page, the append slots and the
-            // first round of the appended rows: lane l takes the batch's
-            // pages l, l + 32, ... (its chunk found by a forward scan of the
+            // first appending run's new rows: lane l takes the batch's pages
+            // l, l + 32, ... (its chunk found by a forward scan of the
             // chunks' first offsets) and issues all its loads before any
-            // store, so the batch costs one memory round trip however many
-            // chunks it holds, plus one per further round of appended rows
+            // store, so the batch starts after one memory round trip however
+            // many chunks it holds
+            const int npg = s_var[0];
+            constexpr int PER_LANE = kStreamBatchPages / 32;
+            int bid[PER_LANE];
             {
-                const int npg = s_var[0];
-                constexpr int PER_LANE = kStreamBatchPages / 32;
-                int bid[PER_LANE];
                 int ci = 0;
 #pragma unroll
                 for (int j = 0; j < PER_LANE; ++j) {
@@ -410,149 +412,156 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                         bid[j] = p.block_tables[(size_t)s_of * p.max_blocks_per_seq + i_of];
                     }
                 }
-                // ---- fused append: a chunk holding a run's last page writes
-                // the new token's rows of its heads before that page loads
-                // (the token's row lies in the last page, which no other CTA
-                // reads).  Its slot sits in lane ui (chunk ui), and the
-                // appended rows are spread over the lanes as one list of
-                // 16-byte vectors: chunk s_app[a], vector i of its K then V
-                // rows, for item a * 2 * per_row + i.
-                constexpr int VEC = 16 / (int)sizeof(T);
-                const int per_row = HPC * D / VEC;
-                const size_t row = (size_t)p.n_kv_heads * D;
-                int64_t my_slot = -1;
-                unsigned need = 0;
-                if (p.slot_mapping != nullptr) {
-                    bool mine = false;
-                    if (lane < nc) {
-                        const StreamChunk u = s_chunk[lane];
-                        mine = u.i0 + u.n == (s_len[u.s] + BS - 1) / BS;
-                        if (mine) my_slot = p.slot_mapping[u.s];
-                    }
-                    need = __ballot_sync(0xffffffffu, mine);
-                    if (mine) s_app[__popc(need & ((1u << lane) - 1u))] = lane;
-                    __syncwarp();
+            }
+            // ---- fused append: a chunk holding a run's last page writes the
+            // new token's rows of its heads before that page loads (the
+            // token's row lies in the last page, which no other CTA reads).
+            // Its slot sits in lane ui (chunk ui); s_app lists the appending
+            // chunks in order.  The rows of the next appending chunk are
+            // loaded ahead (16-byte vectors spread over the lanes) while the
+            // pages before its last one are issued, and stored just before
+            // that page.
+            constexpr int VEC = 16 / (int)sizeof(T);
+            const int per_row = HPC * D / VEC;      // vectors of one K (or V) row of the heads
+            const size_t row = (size_t)p.n_kv_heads * D;
+            int64_t my_slot = -1;
+            unsigned need = 0;
+            if (p.slot_mapping != nullptr) {
+                bool mine = false;
+                if (lane < nc) {
+                    const StreamChunk u = s_chunk[lane];
+                    mine = u.i0 + u.n == (s_len[u.s] + BS - 1) / BS;
+                    if (mine) my_slot = p.slot_mapping[u.s];
                 }
-                const int items = __popc(need) * 2 * per_row;
-                uint4 val[kAppendRound];
-                auto append_load = [&](int r) {
+                need = __ballot_sync(0xffffffffu, mine);
+                if (mine) s_app[__popc(need & ((1u << lane) - 1u))] = lane;
+                __syncwarp();
+            }
+            const int n_app = __popc(need);
+            uint4 val[kAppendPerLane];
+            auto append_load = [&](int a) {   // the rows of appending chunk a
+                const StreamChunk u = s_chunk[s_app[a]];
 #pragma unroll
-                    for (int k = 0; k < kAppendRound; ++k) {
-                        const int f = (r * kAppendRound + k) * 32 + lane;
-                        if (f < items) {
-                            const int a = f / (2 * per_row), i = f - a * 2 * per_row;
-                            const StreamChunk u = s_chunk[s_app[a]];
-                            const bool is_v = i >= per_row;
-                            const int j = (is_v ? i - per_row : i) * VEC;
-                            const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) +
-                                           (size_t)u.s * row + (size_t)u.hg * HPC * D + j;
-                            val[k] = *reinterpret_cast<const uint4*>(src);
-                        }
+                for (int k = 0; k < kAppendPerLane; ++k) {
+                    const int i = k * 32 + lane;
+                    if (i < 2 * per_row) {
+                        const bool is_v = i >= per_row;
+                        const int j = (is_v ? i - per_row : i) * VEC;
+                        const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) +
+                                       (size_t)u.s * row + (size_t)u.hg * HPC * D + j;
+                        val[k] = *reinterpret_cast<const uint4*>(src);
                     }
-                };
-                auto append_store = [&](int r) {
+                }
+            };
+            auto append_store = [&](int a) {  // ... into the pool row of its slot
+                const int ui = s_app[a];
+                const int64_t slot_row = __shfl_sync(0xffffffffu, my_slot, ui);
+                const StreamChunk u = s_chunk[ui];
+                if (slot_row < 0) return;
+                if (slot_row >= (int64_t)p.num_blocks * BS) {
+                    if (u.hg == 0 && lane == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
+                    return;
+                }
 #pragma unroll
-                    for (int k = 0; k < kAppendRound; ++k) {
-                        const int f = (r * kAppendRound + k) * 32 + lane;
-                        const int a = f < items ? f / (2 * per_row) : 0;
-                        const int ui = items > 0 ? s_app[a] : 0;
-                        const int64_t slot_row = __shfl_sync(0xffffffffu, my_slot, ui);
-                        if (f >= items || slot_row < 0) continue;
-                        const StreamChunk u = s_chunk[ui];
-                        const int i = f - a * 2 * per_row;
-                        if (slot_row >= (int64_t)p.num_blocks * BS) {
-                            if (u.hg == 0 && i == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
-                            continue;
-                        }
+                for (int k = 0; k < kAppendPerLane; ++k) {
+                    const int i = k * 32 + lane;
+                    if (i < 2 * per_row) {
                         const bool is_v = i >= per_row;
                         const int j = (is_v ? i - per_row : i) * VEC;
                         T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) +
                                  (size_t)slot_row * row + (size_t)u.hg * HPC * D + j;
                         *reinterpret_cast<uint4*>(dst) = val[k];
                     }
-                };
-                if (items > 0) append_load(0);
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            };
+            if (n_app > 0) append_load(0);
 #pragma unroll
-                for (int j = 0; j < PER_LANE; ++j) {
-                    const int f = lane + 32 * j;
-                    if (f >= npg) continue;
-                    int b = bid[j];
-                    if (b < 0 || b >= p.num_blocks) {
-                        raise_error(p.errors, PKV_DEVERR_BLOCK_ID);
-                        b = -1;
-                    }
-                    s_bid[f] = b;
+            for (int j = 0; j < PER_LANE; ++j) {
+                const int f = lane + 32 * j;
+                if (f >= npg) continue;
+                int b = bid[j];
+                if (b < 0 || b >= p.num_blocks) {
+                    raise_error(p.errors, PKV_DEVERR_BLOCK_ID);
+                    b = -1;
                 }
-                const int rounds = (items + 32 * kAppendRound - 1) / (32 * kAppendRound);
-                for (int r = 0; r < rounds; ++r) {
-                    if (r > 0) append_load(r);
-                    append_store(r);
-                }
-                if (items > 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+                s_bid[f] = b;
             }
             __syncwarp();
-            // ---- issue every page of the batch (lane 0)
-            if (lane == 0) {
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                for (int ui = 0; ui < nc && !stop; ++ui) {
-                    const StreamChunk u = s_chunk[ui];
-                    const int n = s_len[u.s];
-                    const T* qsrc = reinterpret_cast<const T*>(p.q) +
-                                    ((size_t)u.s * p.n_heads + (size_t)u.hg * HPC * G) * D;
-                    for (int i = 0; i < u.n; ++i, ++g) {
-                        const int st = g % stages;
-                        if (g >= stages &&
-                            !mbar_wait(&empty[st], ((g / stages) - 1) & 1, p.errors)) {
-                            *s_abort = 1;
-                            stop = true;
-                            break;
-                        }
-                        if (*s_abort) {
-                            stop = true;
-                            break;
-                        }
-                        const int b = s_bid[u.first + i];
-                        const bool first = i == 0 && (u.flags & kSlotFirst);
-                        StreamSlot& r = slot[st];
-                        r.s = u.s;
-                        r.hg = u.hg;
-                        r.page = u.i0 + i;
-                        r.n_tok = n;
-                        r.flags = (first ? kSlotFirst | (u.flags & kSlotHead) : 0) |
-                                  (i == u.n - 1 ? (u.flags & kSlotLast) : 0) |
-                                  (u.flags & kSlotWhole) | (b >= 0 ? kSlotValid : 0);
-                        // a context's last block holding at most half a block
-                        // of its tokens: only that half is loaded (the rows
-                        // past the context are masked by the consumers)
-                        const bool half = n - (u.i0 + i) * BS <= BS / 2;
-                        const uint32_t kv_bytes = half ? stage_bytes / 2 : stage_bytes;
-                        const uint32_t bytes = (b >= 0 ? kv_bytes : 0u) + (first ? q_bytes : 0u);
-                        if (bytes == 0) {
-                            mbar_arrive(&full[st]);
-                            continue;
-                        }
-                        mbar_arrive_expect_tx(&full[st], bytes);
-                        if (first)
-                            bulk_load_q(qbuf + (size_t)st * q_bytes, qsrc, q_bytes, &full[st],
-                                        policy);
-                        if (b >= 0) {
-                            unsigned char* dst = ring + (size_t)st * stage_bytes;
-                            const CUtensorMap* mk = half ? &tm_kh : &tm_k;
-                            const CUtensorMap* mv = half ? &tm_vh : &tm_v;
-                            for (int hh = 0; hh < HPC; ++hh) {
-                                const int hrow = (u.hg * HPC + hh) * HALVES;
-                                for (int h = 0; h < HALVES; ++h) {
-                                    tma_load_4d(dst + hh * head_bytes + h * BOX, mk, &full[st],
-                                                0, hrow + h, 0, b, policy);
-                                    tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, mv,
-                                                &full[st], 0, hrow + h, 0, b, policy);
-                                }
+            // ---- issue the pages of chunk ui in [i_begin, i_end) (lane 0)
+            auto issue_pages = [&](int ui, int i_begin, int i_end) {
+                const StreamChunk u = s_chunk[ui];
+                const int n = s_len[u.s];
+                const T* qsrc = reinterpret_cast<const T*>(p.q) +
+                                ((size_t)u.s * p.n_heads + (size_t)u.hg * HPC * G) * D;
+                for (int i = i_begin; i < i_end; ++i, ++g) {
+                    const int st = g % stages;
+                    if (g >= stages &&
+                        !mbar_wait(&empty[st], ((g / stages) - 1) & 1, p.errors)) {
+                        *s_abort = 1;
+                        stop = true;
+                        return;
+                    }
+                    if (*s_abort) {
+                        stop = true;
+                        return;
+                    }
+                    const int b = s_bid[u.first + i];
+                    const bool first = i == 0 && (u.flags & kSlotFirst);
+                    StreamSlot& r = slot[st];
+                    r.s = u.s;
+                    r.hg = u.hg;
+                    r.page = u.i0 + i;
+                    r.n_tok = n;
+                    r.flags = (first ? kSlotFirst | (u.flags & kSlotHead) : 0) |
+                              (i == u.n - 1 ? (u.flags & kSlotLast) : 0) |
+                              (u.flags & kSlotWhole) | (b >= 0 ? kSlotValid : 0);
+                    // a context's last block holding at most half a block of
+                    // its tokens: only that half is loaded (the rows past the
+                    // context are masked by the consumers)
+                    const bool half = n - (u.i0 + i) * BS <= BS / 2;
+                    const uint32_t kv_bytes = half ? stage_bytes / 2 : stage_bytes;
+                    const uint32_t bytes = (b >= 0 ? kv_bytes : 0u) + (first ? q_bytes : 0u);
+                    if (bytes == 0) {
+                        mbar_arrive(&full[st]);
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(&full[st], bytes);
+                    if (first)
+                        bulk_load_q(qbuf + (size_t)st * q_bytes, qsrc, q_bytes, &full[st],
+                                    policy);
+                    if (b >= 0) {
+                        unsigned char* dst = ring + (size_t)st * stage_bytes;
+                        const CUtensorMap* mk = half ? &tm_kh : &tm_k;
+                        const CUtensorMap* mv = half ? &tm_vh : &tm_v;
+                        for (int hh = 0; hh < HPC; ++hh) {
+                            const int hrow = (u.hg * HPC + hh) * HALVES;
+                            for (int h = 0; h < HALVES; ++h) {
+                                tma_load_4d(dst + hh * head_bytes + h * BOX, mk, &full[st], 0,
+                                            hrow + h, 0, b, policy);
+                                tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, mv,
+                                            &full[st], 0, hrow + h, 0, b, policy);
                             }
                         }
                     }
                 }
+            };
+            int a_next = 0;   // the next appending chunk (its rows are in val)
+            for (int ui = 0; ui < nc && !stop; ++ui) {
+                const bool app = (need >> ui) & 1u;
+                const int n_pages = s_chunk[ui].n;
+                if (lane == 0) issue_pages(ui, 0, app ? n_pages - 1 : n_pages);
+                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+                if (stop || !app) continue;
+                append_store(a_next);
+                __syncwarp();
+                if (++a_next < n_app) append_load(a_next);
+                if (lane == 0) {
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    issue_pages(ui, n_pages - 1, n_pages);
+                }
+                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
             }
-            stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
             __syncwarp();
         }
         // ---- end of the stream: a record without pages
