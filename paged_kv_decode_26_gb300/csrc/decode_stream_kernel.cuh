@@ -52,9 +52,6 @@ constexpr int kStreamMaxSeqs = 2048;     // context lengths held in shared memor
 constexpr int kStreamBatchChunks = 32;   // chunks whose block ids one lookup fetches (one a lane)
 static_assert(kStreamBatchChunks <= 32, "the append slots of a batch are read one chunk a lane");
 constexpr int kStreamBatchPages = 128;   // pages of one lookup (a multiple of 32)
-constexpr int kAppendPerLane = 8;        // 16-byte vectors of one chunk's appended rows a lane holds
-static_assert(2 * kMmaMaxWarps * 128 * 2 / 16 <= 32 * kAppendPerLane,
-              "the appended K and V rows of a chunk fit the warp's registers");
 static_assert(kStreamBatchPages % 32 == 0, "a lookup spreads its pages over a warp");
 
 // Slot record flags.
@@ -63,6 +60,7 @@ constexpr int kSlotLast = 2;    // last page of the piece: write the result
 constexpr int kSlotWhole = 4;   // the run lies inside this CTA's share: result to the output
 constexpr int kSlotValid = 8;   // the page's block id was in range (else the page is skipped)
 constexpr int kSlotHead = 16;   // the piece starts the CTA's share inside a run begun before it
+constexpr int kSlotAppend = 32;  // the page's last token is this step's new row (in the slot's row buffer)
 
 // Consecutive pages of one run queued by the producer, with where their
 // block ids start in the batch buffer.
@@ -77,6 +75,7 @@ struct StreamChunk {
 
 // What the producer tells the consumers about the page in one ring slot.
 struct StreamSlot {
+    long long pool_off;   // kSlotAppend: element offset of the new row of the group's heads
     int s;      // sequence (-1: end of the stream)
     int hg;     // kv-head group
     int page;   // page of the sequence
@@ -85,14 +84,16 @@ struct StreamSlot {
 };
 
 // Shared memory of one CTA (must match the carve-up in the kernel): 1 KB
-// alignment slack, the ring of K/V pages, the query rows of each slot,
-// barriers, slot records, the chunk queue and block ids of one batch, the
-// clamped lengths and their page prefix sums, a few words.
+// alignment slack, the ring of K/V pages, the query rows of each slot, the
+// new token's K and V rows of each slot (fused append), barriers, slot
+// records, the chunk queue and block ids of one batch, the clamped lengths
+// and their page prefix sums, a few words.
 inline size_t decode_stream_smem_bytes(int D, int BS, int G, int elem_bytes, int hpc,
                                        int stages, int num_seqs) {
     const size_t ring = (size_t)stages * 2 * hpc * D * BS * elem_bytes;
     const size_t qs = (size_t)stages * hpc * G * D * elem_bytes;
-    return 1024 + ring + qs + (size_t)stages * 2 * sizeof(uint64_t) +
+    const size_t rows = (size_t)stages * 2 * hpc * D * elem_bytes;
+    return 1024 + ring + qs + rows + (size_t)stages * 2 * sizeof(uint64_t) +
            (size_t)stages * sizeof(StreamSlot) + kStreamBatchChunks * sizeof(StreamChunk) +
            (size_t)kStreamBatchPages * sizeof(int) + (size_t)(2 * num_seqs + 1) * sizeof(int) +
            8 * sizeof(int);
@@ -297,9 +298,12 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
     const uint32_t head_bytes = HALVES * BOX;              // one kv head's K (or V) page
     const uint32_t stage_bytes = 2 * HPC * head_bytes;     // K then V for HPC heads
     const uint32_t q_bytes = (uint32_t)(HPC * G * D * sizeof(T));   // query rows of a run
+    const uint32_t row_bytes = (uint32_t)(HPC * D * sizeof(T));      // one token's K (or V) row
     unsigned char* ring = smem;
     unsigned char* qbuf = ring + (size_t)stages * stage_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(qbuf + (size_t)stages * q_bytes);
+    unsigned char* nbuf = qbuf + (size_t)stages * q_bytes;   // new K then V row per slot
+    const uint32_t ring_addr = smem_addr(ring), nbuf_addr = smem_addr(nbuf);
+    uint64_t* full = reinterpret_cast<uint64_t*>(nbuf + (size_t)stages * 2 * row_bytes);
     uint64_t* empty = full + stages;
     StreamSlot* slot = reinterpret_cast<StreamSlot*>(empty + stages);
     StreamChunk* s_chunk = reinterpret_cast<StreamChunk*>(slot + stages);
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    __shared__ int s_app[kStreamBatchChunks];   // chunks of a batch that append, in order
+    __shared__ long long s_aslot[kStreamBatchChunks];   // append slot of each chunk (-1: none)
 
     // barriers and tensor-map prefetches first: they overlap the
     // context-length loads
@@ -391,12 +395,11 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
             __syncwarp();
             const int nc = s_var[3];
             if (nc == 0) break;
-            // ---- block ids of every queued page, the append slots and the
-            // first appending run's new rows: lane l takes the batch's pages
-            // l, l + 32, ... (its chunk found by a forward scan of the
-            // chunks' first offsets) and issues all its loads before any
-            // store, so the batch starts after one memory round trip however
-            // many chunks it holds
+            // ---- block ids of every queued page and the append slots:
+            // lane l takes the batch's pages l, l + 32, ... (its chunk found
+            // by a forward scan of the chunks' first offsets) and issues all
+            // its loads before any store, so the batch starts after one
+            // memory round trip however many chunks it holds
             const int npg = s_var[0];
             constexpr int PER_LANE = kStreamBatchPages / 32;
             int bid[PER_LANE];
@@ -413,69 +416,20 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                     }
                 }
             }
-            // ---- fused append: a chunk holding a run's last page writes the
-            // new token's rows of its heads before that page loads (the
-            // token's row lies in the last page, which no other CTA reads).
-            // Its slot sits in lane ui (chunk ui); s_app lists the appending
-            // chunks in order.  The rows of the next appending chunk are
-            // loaded ahead (16-byte vectors spread over the lanes) while the
-            // pages before its last one are issued, and stored just before
-            // that page.
-            constexpr int VEC = 16 / (int)sizeof(T);
-            const int per_row = HPC * D / VEC;      // vectors of one K (or V) row of the heads
-            const size_t row = (size_t)p.n_kv_heads * D;
-            int64_t my_slot = -1;
-            unsigned need = 0;
-            if (p.slot_mapping != nullptr) {
-                bool mine = false;
-                if (lane < nc) {
+            // ---- fused append: the page holding a run's last token also
+            // brings the token's new K and V rows of its heads (bulk copies
+            // into the slot's row buffer); its consumers put them into the
+            // page and write them to the pool (no other CTA reads that page),
+            // so nothing waits for the pool write.  The slot of chunk ui
+            // (when it ends its run) loads with the block ids.
+            if (lane < nc) {
+                long long sl = -1;
+                if (p.slot_mapping != nullptr) {
                     const StreamChunk u = s_chunk[lane];
-                    mine = u.i0 + u.n == (s_len[u.s] + BS - 1) / BS;
-                    if (mine) my_slot = p.slot_mapping[u.s];
+                    if (u.i0 + u.n == (s_len[u.s] + BS - 1) / BS) sl = p.slot_mapping[u.s];
                 }
-                need = __ballot_sync(0xffffffffu, mine);
-                if (mine) s_app[__popc(need & ((1u << lane) - 1u))] = lane;
-                __syncwarp();
+                s_aslot[lane] = sl;
             }
-            const int n_app = __popc(need);
-            uint4 val[kAppendPerLane];
-            auto append_load = [&](int a) {   // the rows of appending chunk a
-                const StreamChunk u = s_chunk[s_app[a]];
-#pragma unroll
-                for (int k = 0; k < kAppendPerLane; ++k) {
-                    const int i = k * 32 + lane;
-                    if (i < 2 * per_row) {
-                        const bool is_v = i >= per_row;
-                        const int j = (is_v ? i - per_row : i) * VEC;
-                        const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) +
-                                       (size_t)u.s * row + (size_t)u.hg * HPC * D + j;
-                        val[k] = *reinterpret_cast<const uint4*>(src);
-                    }
-                }
-            };
-            auto append_store = [&](int a) {  // ... into the pool row of its slot
-                const int ui = s_app[a];
-                const int64_t slot_row = __shfl_sync(0xffffffffu, my_slot, ui);
-                const StreamChunk u = s_chunk[ui];
-                if (slot_row < 0) return;
-                if (slot_row >= (int64_t)p.num_blocks * BS) {
-                    if (u.hg == 0 && lane == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
-                    return;
-                }
-#pragma unroll
-                for (int k = 0; k < kAppendPerLane; ++k) {
-                    const int i = k * 32 + lane;
-                    if (i < 2 * per_row) {
-                        const bool is_v = i >= per_row;
-                        const int j = (is_v ? i - per_row : i) * VEC;
-                        T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) +
-                                 (size_t)slot_row * row + (size_t)u.hg * HPC * D + j;
-                        *reinterpret_cast<uint4*>(dst) = val[k];
-                    }
-                }
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-            };
-            if (n_app > 0) append_load(0);
 #pragma unroll
             for (int j = 0; j < PER_LANE; ++j) {
                 const int f = lane + 32 * j;
@@ -488,80 +442,86 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                 s_bid[f] = b;
             }
             __syncwarp();
-            // ---- issue the pages of chunk ui in [i_begin, i_end) (lane 0)
-            auto issue_pages = [&](int ui, int i_begin, int i_end) {
-                const StreamChunk u = s_chunk[ui];
-                const int n = s_len[u.s];
-                const T* qsrc = reinterpret_cast<const T*>(p.q) +
-                                ((size_t)u.s * p.n_heads + (size_t)u.hg * HPC * G) * D;
-                for (int i = i_begin; i < i_end; ++i, ++g) {
-                    const int st = g % stages;
-                    if (g >= stages &&
-                        !mbar_wait(&empty[st], ((g / stages) - 1) & 1, p.errors)) {
-                        *s_abort = 1;
-                        stop = true;
-                        return;
+            // ---- issue every page of the batch (lane 0)
+            if (lane == 0) {
+                const size_t row = (size_t)p.n_kv_heads * D;
+                for (int ui = 0; ui < nc && !stop; ++ui) {
+                    const StreamChunk u = s_chunk[ui];
+                    const int n = s_len[u.s];
+                    const T* qsrc = reinterpret_cast<const T*>(p.q) +
+                                    ((size_t)u.s * p.n_heads + (size_t)u.hg * HPC * G) * D;
+                    long long slot_row = s_aslot[ui];
+                    if (slot_row >= (long long)p.num_blocks * BS) {
+                        // outside the pool: skipped and flagged (once a sequence)
+                        if (u.hg == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
+                        slot_row = -1;
                     }
-                    if (*s_abort) {
-                        stop = true;
-                        return;
-                    }
-                    const int b = s_bid[u.first + i];
-                    const bool first = i == 0 && (u.flags & kSlotFirst);
-                    StreamSlot& r = slot[st];
-                    r.s = u.s;
-                    r.hg = u.hg;
-                    r.page = u.i0 + i;
-                    r.n_tok = n;
-                    r.flags = (first ? kSlotFirst | (u.flags & kSlotHead) : 0) |
-                              (i == u.n - 1 ? (u.flags & kSlotLast) : 0) |
-                              (u.flags & kSlotWhole) | (b >= 0 ? kSlotValid : 0);
-                    // a context's last block holding at most half a block of
-                    // its tokens: only that half is loaded (the rows past the
-                    // context are masked by the consumers)
-                    const bool half = n - (u.i0 + i) * BS <= BS / 2;
-                    const uint32_t kv_bytes = half ? stage_bytes / 2 : stage_bytes;
-                    const uint32_t bytes = (b >= 0 ? kv_bytes : 0u) + (first ? q_bytes : 0u);
-                    if (bytes == 0) {
-                        mbar_arrive(&full[st]);
-                        continue;
-                    }
-                    mbar_arrive_expect_tx(&full[st], bytes);
-                    if (first)
-                        bulk_load_q(qbuf + (size_t)st * q_bytes, qsrc, q_bytes, &full[st],
-                                    policy);
-                    if (b >= 0) {
-                        unsigned char* dst = ring + (size_t)st * stage_bytes;
-                        const CUtensorMap* mk = half ? &tm_kh : &tm_k;
-                        const CUtensorMap* mv = half ? &tm_vh : &tm_v;
-                        for (int hh = 0; hh < HPC; ++hh) {
-                            const int hrow = (u.hg * HPC + hh) * HALVES;
-                            for (int h = 0; h < HALVES; ++h) {
-                                tma_load_4d(dst + hh * head_bytes + h * BOX, mk, &full[st], 0,
-                                            hrow + h, 0, b, policy);
-                                tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, mv,
-                                            &full[st], 0, hrow + h, 0, b, policy);
+                    for (int i = 0; i < u.n; ++i, ++g) {
+                        const int st = g % stages;
+                        if (g >= stages &&
+                            !mbar_wait(&empty[st], ((g / stages) - 1) & 1, p.errors)) {
+                            *s_abort = 1;
+                            stop = true;
+                            break;
+                        }
+                        if (*s_abort) {
+                            stop = true;
+                            break;
+                        }
+                        const int b = s_bid[u.first + i];
+                        const bool first = i == 0 && (u.flags & kSlotFirst);
+                        const bool app = i == u.n - 1 && slot_row >= 0;
+                        StreamSlot& r = slot[st];
+                        r.pool_off = app ? slot_row * (long long)row + (long long)u.hg * HPC * D : -1;
+                        r.s = u.s;
+                        r.hg = u.hg;
+                        r.page = u.i0 + i;
+                        r.n_tok = n;
+                        r.flags = (first ? kSlotFirst | (u.flags & kSlotHead) : 0) |
+                                  (i == u.n - 1 ? (u.flags & kSlotLast) : 0) |
+                                  (u.flags & kSlotWhole) | (b >= 0 ? kSlotValid : 0) |
+                                  (app ? kSlotAppend : 0);
+                        // a context's last block holding at most half a block
+                        // of its tokens: only that half is loaded (the rows
+                        // past the context are masked by the consumers)
+                        const bool half = n - (u.i0 + i) * BS <= BS / 2;
+                        const uint32_t kv_bytes = half ? stage_bytes / 2 : stage_bytes;
+                        const uint32_t bytes = (b >= 0 ? kv_bytes : 0u) + (first ? q_bytes : 0u) +
+                                               (app ? 2 * row_bytes : 0u);
+                        if (bytes == 0) {
+                            mbar_arrive(&full[st]);
+                            continue;
+                        }
+                        mbar_arrive_expect_tx(&full[st], bytes);
+                        if (first)
+                            bulk_load_q(qbuf + (size_t)st * q_bytes, qsrc, q_bytes, &full[st],
+                                        policy);
+                        if (app) {
+                            const size_t off = (size_t)u.s * row + (size_t)u.hg * HPC * D;
+                            unsigned char* nb = nbuf + (size_t)st * 2 * row_bytes;
+                            bulk_load_q(nb, static_cast<const T*>(p.k_new) + off, row_bytes,
+                                        &full[st], policy);
+                            bulk_load_q(nb + row_bytes, static_cast<const T*>(p.v_new) + off,
+                                        row_bytes, &full[st], policy);
+                        }
+                        if (b >= 0) {
+                            unsigned char* dst = ring + (size_t)st * stage_bytes;
+                            const CUtensorMap* mk = half ? &tm_kh : &tm_k;
+                            const CUtensorMap* mv = half ? &tm_vh : &tm_v;
+                            for (int hh = 0; hh < HPC; ++hh) {
+                                const int hrow = (u.hg * HPC + hh) * HALVES;
+                                for (int h = 0; h < HALVES; ++h) {
+                                    tma_load_4d(dst + hh * head_bytes + h * BOX, mk, &full[st],
+                                                0, hrow + h, 0, b, policy);
+                                    tma_load_4d(dst + (HPC + hh) * head_bytes + h * BOX, mv,
+                                                &full[st], 0, hrow + h, 0, b, policy);
+                                }
                             }
                         }
                     }
                 }
-            };
-            int a_next = 0;   // the next appending chunk (its rows are in val)
-            for (int ui = 0; ui < nc && !stop; ++ui) {
-                const bool app = (need >> ui) & 1u;
-                const int n_pages = s_chunk[ui].n;
-                if (lane == 0) issue_pages(ui, 0, app ? n_pages - 1 : n_pages);
-                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-                if (stop || !app) continue;
-                append_store(a_next);
-                __syncwarp();
-                if (++a_next < n_app) append_load(a_next);
-                if (lane == 0) {
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    issue_pages(ui, n_pages - 1, n_pages);
-                }
-                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
             }
+            stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
             __syncwarp();
         }
         // ---- end of the stream: a record without pages
@@ -595,8 +555,38 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                 *s_abort = 1;
                 break;
             }
-            const StreamSlot r = slot[slot_i];
+            // the producer rewrites the record only after this slot is released
+            const StreamSlot& r = slot[slot_i];
             if (r.s < 0) break;
+            if (r.flags & kSlotAppend) {
+                // the page's last token is this step's new row: this kv
+                // head's K and V rows come from the slot's row buffer into
+                // the page (row t of each swizzled box) and into the pool
+                constexpr int CH = D / 8;   // 16-byte pieces of one row of one head
+                if (lane < 2 * CH) {
+                    const bool is_v = lane >= CH;
+                    const int idx = is_v ? lane - CH : lane;
+                    const uint32_t src = nbuf_addr + slot_i * 2 * row_bytes +
+                                         (is_v ? row_bytes : 0u) +
+                                         (uint32_t)(kv_local * D + idx * 8) * (uint32_t)sizeof(T);
+                    uint32_t w0, w1, w2, w3;
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(src));
+                    if (r.flags & kSlotValid) {
+                        const int t = r.n_tok - 1 - r.page * BS;
+                        const uint32_t box = ring_addr + slot_i * stage_bytes +
+                                             ((is_v ? HPC : 0) + kv_local) * head_bytes +
+                                             (idx >> 3) * BOX + swz(t, idx & 7);
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                                     :: "r"(box), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) + r.pool_off +
+                             kv_local * D + idx * 8;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(w0, w1, w2, w3);
+                }
+                __syncwarp();
+            }
             if (r.flags & kSlotFirst) {
                 head = (r.flags & kSlotHead) != 0;
                 // query rows of this run's kv head (loaded into the slot)
@@ -610,7 +600,9 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1)
                 const uint32_t vbase = smem_addr(ring + (size_t)slot_i * stage_bytes +
                                                  (HPC + kv_local) * head_bytes);
                 const int page_tok = r.page * BS;
-#pragma unroll
+                // one 16-token chunk at a time (32-token blocks: two chunks
+                // interleaved need more than the 168 registers a thread has)
+#pragma unroll 1
                 for (int c = 0; c < BS / 16; ++c) {
                     const int valid = min(16, r.n_tok - (page_tok + c * 16));
                     if (valid <= 0) break;
