@@ -211,10 +211,11 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
 /*
  * paged_attn_decode_append -- kv_append followed by paged_attn_decode, in
  * one launch: the decode CTA that reads each sequence's last block (of its
- * last split, or of its streaming share) first writes k_new[s] and v_new[s] ([num_seqs, n_kv_heads, head_dim] of kv_dtype,
- * 16-byte aligned) into pool row slot_mapping[s] (int64 [num_seqs], 8-byte
- * aligned; -1 skips, a slot outside the pool is skipped and flagged
- * PKV_DEVERR_SLOT) for its kv heads, then decodes.  context_lens already
+ * last split, or of its streaming share) writes k_new[s] and v_new[s]
+ * ([num_seqs, n_kv_heads, head_dim] of kv_dtype, 16-byte aligned) into pool
+ * row slot_mapping[s] (int64 [num_seqs], 8-byte aligned; -1 skips, a slot
+ * outside the pool is skipped and flagged PKV_DEVERR_SLOT) for its kv
+ * heads, and attends to them as the context's last token.  context_lens already
  * counts the appended token ([SWAP] serving loop: append, then attend; the
  * host allocator's append_slots gives both).  Same outputs and pool bytes
  * as the two calls, provided no other sequence of the call reads the page
