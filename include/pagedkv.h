@@ -21,8 +21,10 @@
  *
  * Conventions for every entry point:
  *   - Buffers belong to the caller.  The library allocates no device memory
- *     and never synchronises a stream; all work is enqueued on `stream`
- *     (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *     and synchronises nothing unless asked to (paged_attn_decode_append_host
+ *     with synchronize set; the pkv_device_errors diagnostic); all work is
+ *     enqueued on `stream` (a cudaStream_t passed as void*, NULL = the legacy
+ *     default stream).
  *   - "device" pointers must be device memory of the current CUDA device
  *     (or host memory the device can address, where stated).
  *   - Arguments are validated on the host before anything is launched; an
