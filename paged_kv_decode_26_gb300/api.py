@@ -214,6 +214,8 @@ class HostStep:
                  k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                  split_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None, synchronize: bool = True):
+        _need_all_cuda(_APPEND_NAMES, (out, q, k_pool, v_pool, block_tables, context_lens, k_new,
+                                       v_new, slot_mapping))
         if workspace is None:
             workspace = alloc_decode_workspace(q, k_pool, max_context_len, split_tokens)
         args = _append_args(out, q, k_pool, v_pool, block_tables, context_lens, scale,

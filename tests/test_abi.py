@@ -253,3 +253,8 @@ def test_binding_rejects_host_tensors_by_name():
         pkv.paged_attn_decode_append(t["out"], t["q"], t["k_pool"], t["v_pool"],
                                      t["block_tables"], t["context_lens"], 0.125, 1,
                                      new["k_new"], new["v_new"], new["slot_mapping"])
+    for step in (pkv.paged_attn_decode_append_host, pkv.HostStep):
+        with pytest.raises(ValueError, match="out must be a CUDA tensor"):
+            step([], torch.zeros(S, H, D), t["out"], t["q"], t["k_pool"], t["v_pool"],
+                 t["block_tables"], t["context_lens"], 0.125, 1, new["k_new"], new["v_new"],
+                 new["slot_mapping"])
