@@ -390,18 +390,34 @@ pkv_status make_config(int num_seqs, int n_heads, int n_kv_heads, int head_dim, 
     c->stream_ctas = 0;
     if (c->stream) {
         // its shared memory must fit (the per-unit kernel runs otherwise)
-        const int stages = tuned(PKV_TUNE_DECODE_STAGES) ? c->stages : kStreamStages;
+        int stages = tuned(PKV_TUNE_DECODE_STAGES) ? c->stages : kStreamStages;
         const size_t limit = smem_optin > 0 ? smem_optin : (size_t)227 * 1024;
-        const size_t smem = pkv::decode_stream_smem_bytes(head_dim, block_size,
-                                                          n_heads / n_kv_heads, 2, c->hpc,
-                                                          stages, num_seqs);
+        const size_t per_sm_bytes = smem_per_sm > 0 ? (size_t)smem_per_sm : (size_t)228 * 1024;
+        auto stream_smem = [&](int st) {
+            return pkv::decode_stream_smem_bytes(head_dim, block_size, n_heads / n_kv_heads, 2,
+                                                 c->hpc, st, num_seqs);
+        };
+        size_t smem = stream_smem(stages);
+        // A third page in the ring where it costs no resident CTA (each CTA
+        // also holds 1 KB of static shared memory and 1 KB the system
+        // reserves): MHA and groups of 2 at
+        // head_dim 128 with up to a few hundred sequences.  GB300, CUDA graphs
+        // of flush + decode, MHA 32 heads, two pages / three: 256 Pareto
+        // lengths 54.4 / 52.1 us, 384 Pareto 69.8 / 66.9 us, 320 of
+        // U[512, 4096] 1828 / 1745 us, 256 of U[1, 1024] 336.4 / 318.9 us.
+        if (!tuned(PKV_TUNE_DECODE_STAGES)) {
+            const size_t smem3 = stream_smem(stages + 1);
+            if (smem3 <= limit &&
+                per_sm_bytes / (smem3 + 2048) == per_sm_bytes / (smem + 2048)) {
+                stages += 1;
+                smem = smem3;
+            }
+        }
         if (smem > limit) {
             c->stream = false;
         } else {
             c->stages = stages;
             // an upper bound of the resident CTAs (shared memory alone)
-            const size_t per_sm_bytes =
-                smem_per_sm > 0 ? (size_t)smem_per_sm : (size_t)228 * 1024;
             int per_sm = (int)(per_sm_bytes / smem);
             per_sm = per_sm < 1 ? 1 : (per_sm > 32 ? 32 : per_sm);
             c->stream_ctas = (sm_count > 0 ? sm_count : 1) * per_sm;
