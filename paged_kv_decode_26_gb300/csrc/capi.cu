@@ -212,8 +212,8 @@ constexpr int kStreamMaxContext = 4096;
 //   2048 seqs 93.1 / 226.3 us; uniform 512 of U[4096, 8192] 1888 / 1901 us,
 //   1024 of U[1, 16384] 5047 / 5273 us; shared prefixes (512 seqs,
 //   log-uniform to 8192) 591 / 529 us
-//   MHA 32 / 32, Pareto lengths: 256 seqs 53.5 / 71.2 us, 640 seqs 104.8 /
-//   197.9 us; uniform 256 of U[512, 4096] 1422 / 1318 us
+//   MHA 32 / 32, Pareto lengths: 256 seqs 52.1 / 71.6 us, 640 seqs 104.8 /
+//   197.9 us; uniform 256 of U[512, 4096] 1348 / 1298 us
 constexpr int kStreamManySeqs = 256;
 constexpr int kStreamStages = 2;
 // Few (sequence, head-group) units with contexts of 8K tokens or more: every
