@@ -188,7 +188,8 @@ struct DecodeConfig {
 constexpr int kDefaultSplitTokens = 512;
 // The streaming decode is chosen (knob PKV_TUNE_DECODE_STREAM unset) for
 // tensor-core decodes with the automatic split of two or more sequences
-// whose longest context is at most this long, with a two-page ring.  Its
+// whose longest context is at most this long, with a two-page ring (three
+// where that costs no resident CTA, below).  Its
 // equal page shares do not depend on how the lengths are spread, while one
 // CTA per unit waits on the longest unit.  GB300, 32 / 8 heads, CUDA graphs
 // of L2 flush + decode, streaming against one CTA per unit:

@@ -35,11 +35,13 @@
 //
 // Each CTA: a producer warp and one consumer warp per kv head of the group.
 // The producer walks the CTA's positions in batches of chunks (pieces of
-// runs), looks up all their block ids at once, writes any fused appends, then
-// keeps the page ring full across run boundaries.  Each ring slot carries a
-// record of the page's run and whether it starts the CTA's piece of the run
-// (the query rows come along in the slot), ends it, and whether the run is
-// whole.  A record without pages ends the stream.  Sequences with an empty
+// runs), looks up all their block ids (and append slots) at once, then keeps
+// the page ring full across run boundaries.  Each ring slot carries a record
+// of the page's run and whether it starts the CTA's piece of the run (the
+// query rows come along in the slot), ends it, and whether the run is whole;
+// the slot of a run's last page also brings the step's new K and V rows when
+// the call appends, which the consumers put into the page and the pool.  A
+// record without pages ends the stream.  Sequences with an empty
 // context get their zero rows from the CTA whose share holds their (empty)
 // place in the layout.
 #pragma once
