@@ -85,27 +85,61 @@ struct DecodeParams {
 // visible to the TMA loads that follow the CTA barrier.  The last split is
 // the only one whose pages hold the new token's position (splits are
 // page-aligned), so no other CTA of the sequence reads that row.
+//
+// The slot and the rows depend on the sequence only, so every CTA loads them
+// together with the context length (append_load: the slot and this thread's
+// 16-byte vector of the rows -- 2 * HPC * D / 8 vectors, never more than the
+// CTA's threads at D <= 128), and the last split's CTA stores them once it
+// knows it is the last (append_store): no memory round trip of its own.
+struct AppendRow {
+    int64_t slot;   // -1: nothing to append
+    uint4 v;        // this thread's vector of the new K then V rows
+};
+
 template <int D, int BS, typename T>
-__device__ __forceinline__ void fused_append(const DecodeParams& p, int s, int hg, int HPC,
-                                             bool last_split) {
-    if (p.slot_mapping == nullptr || !last_split) return;
-    const int64_t slot = p.slot_mapping[s];
-    if (slot < 0) return;
-    if (slot >= (int64_t)p.num_blocks * BS) {
+__device__ __forceinline__ AppendRow append_load(const DecodeParams& p, int s, int hg, int HPC) {
+    AppendRow a;
+    a.slot = -1;
+    a.v = make_uint4(0u, 0u, 0u, 0u);
+    if (p.slot_mapping == nullptr) return a;
+    a.slot = p.slot_mapping[s];
+    constexpr int VEC = 16 / (int)sizeof(T);           // elements per 16-byte vector
+    const int per_row = HPC * D / VEC;                  // vectors of this CTA's heads
+    const int i = (int)threadIdx.x;
+    if (i < 2 * per_row) {
+        const bool is_v = i >= per_row;
+        const int j = (is_v ? i - per_row : i) * VEC;
+        const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) +
+                       (size_t)s * p.n_kv_heads * D + (size_t)hg * HPC * D + j;
+        a.v = *reinterpret_cast<const uint4*>(src);
+    }
+    return a;
+}
+
+template <int D, int BS, typename T>
+__device__ __forceinline__ void append_store(const DecodeParams& p, const AppendRow& a, int s,
+                                             int hg, int HPC, bool last_split) {
+    if (p.slot_mapping == nullptr || !last_split || a.slot < 0) return;
+    if (a.slot >= (int64_t)p.num_blocks * BS) {
         if (threadIdx.x == 0 && hg == 0) raise_error(p.errors, PKV_DEVERR_SLOT);
         return;
     }
-    constexpr int VEC = 16 / (int)sizeof(T);           // elements per 16-byte vector
-    const int per_row = HPC * D / VEC;                  // vectors of this CTA's heads
+    constexpr int VEC = 16 / (int)sizeof(T);
+    const int per_row = HPC * D / VEC;
     const size_t row = (size_t)p.n_kv_heads * D;        // elements of one token row
     const size_t off_new = (size_t)s * row + (size_t)hg * HPC * D;
-    const size_t off_pool = (size_t)slot * row + (size_t)hg * HPC * D;
+    const size_t off_pool = (size_t)a.slot * row + (size_t)hg * HPC * D;
     for (int i = threadIdx.x; i < 2 * per_row; i += blockDim.x) {
         const bool is_v = i >= per_row;
         const int j = (is_v ? i - per_row : i) * VEC;
-        const T* src = static_cast<const T*>(is_v ? p.v_new : p.k_new) + off_new + j;
         T* dst = static_cast<T*>(is_v ? p.v_pool : p.k_pool) + off_pool + j;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        // the vector loaded with the length; any beyond one a thread (not
+        // the case for the launch shapes used) copied here
+        const uint4 v = i == (int)threadIdx.x
+                            ? a.v
+                            : *reinterpret_cast<const uint4*>(
+                                  static_cast<const T*>(is_v ? p.v_new : p.k_new) + off_new + j);
+        *reinterpret_cast<uint4*>(dst) = v;
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -233,6 +267,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* tm_k, const CUtens
 
     // ---- this CTA's token range (clamped to what the grid and table cover)
     int n = p.context_lens[s];
+    const AppendRow app = append_load<D, BS, T>(p, s, hg, HPC);   // same round trip
     const int cap = min(p.max_blocks_per_seq * BS, p.max_splits * p.split_tokens);
     if (n < 0 || n > cap) {
         if (split == 0 && hg == 0 && threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONTEXT);
@@ -268,7 +303,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* tm_k, const CUtens
         }
         s_bid[i] = b;
     }
-    fused_append<D, BS, T>(p, s, hg, HPC, split == n_splits - 1);
+    append_store<D, BS, T>(p, app, s, hg, HPC, split == n_splits - 1);
     if (threadIdx.x == 0) {
         for (int st = 0; st < p.stages; ++st) {
             mbar_init(&full[st], 1);

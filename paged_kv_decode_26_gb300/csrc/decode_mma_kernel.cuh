@@ -327,6 +327,7 @@ __device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CU
     }
 
     int n = p.context_lens[s];
+    const AppendRow app = append_load<D, BS, T>(p, s, hg, HPC);   // same round trip
     const int cap = min(p.max_blocks_per_seq * BS, p.max_splits * p.split_tokens);
     if (n < 0 || n > cap) {
         if (split == 0 && hg == 0 && threadIdx.x == 0) raise_error(p.errors, PKV_DEVERR_CONTEXT);
@@ -359,7 +360,7 @@ __device__ __forceinline__ void decode_mma_cta(const CUtensorMap* tm_k, const CU
         }
         s_bid[i] = b;
     }
-    fused_append<D, BS, T>(p, s, hg, HPC, split == n_splits - 1);
+    append_store<D, BS, T>(p, app, s, hg, HPC, split == n_splits - 1);
     if (threadIdx.x == 0) {
         for (int st = 0; st < p.stages; ++st) {
             mbar_init(&full[st], 1);
