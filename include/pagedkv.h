@@ -217,7 +217,9 @@ PKV_API pkv_status paged_attn_decode(void* out, pkv_dtype out_dtype, const void*
  * ([num_seqs, n_kv_heads, head_dim] of kv_dtype, 16-byte aligned) into pool
  * row slot_mapping[s] (int64 [num_seqs], 8-byte aligned; -1 skips, a slot
  * outside the pool is skipped and flagged PKV_DEVERR_SLOT) for its kv
- * heads, and attends to them as the context's last token.  context_lens already
+ * heads, and attends to them as the context's last token: slot_mapping[s]
+ * must be the pool row of token context_lens[s] - 1 through the block table
+ * (what the block manager's append_slots gives).  context_lens already
  * counts the appended token ([SWAP] serving loop: append, then attend; the
  * host allocator's append_slots gives both).  Same outputs and pool bytes
  * as the two calls, provided no other sequence of the call reads the page
