@@ -145,15 +145,17 @@ def test_stream_workload_mixes(lib, tuning, config, extra):
     _check(lib, case, out, f"config {config} S={case.S}")
 
 
-def test_stream_fused_append_equals_two_calls(lib, tuning):
+@pytest.mark.parametrize("H,Hk,D", [(32, 8, 128), (8, 8, 128), (8, 8, 64)])
+def test_stream_fused_append_equals_two_calls(lib, tuning, H, Hk, D):
     """paged_attn_decode_append on the stream kernel gives the pools and the
     output of kv_append followed by paged_attn_decode, bit for bit; a slot
     of -1 appends nothing, a slot past the pool is skipped and flagged, an
-    empty context still receives its row."""
+    empty context still receives its row.  Groups of 4 and MHA (the
+    tensor-core consumer forced; a three-page ring at head_dim 128)."""
     import paged_kv_decode_26_gb300 as pkv
-    tuning(decode_stream=1)
-    case = wl.make_case(5, S=24, lens=("pareto", 1.5, 16, 600), d2d_pairs=0, h2d_pairs=0,
-                        host_pool_blocks=1, poison=True, seed=31)
+    tuning(decode_mma=1, decode_stream=1)
+    case = wl.make_case(5, S=24, lens=("pareto", 1.5, 16, 600), H=H, Hk=Hk, D=D, d2d_pairs=0,
+                        h2d_pairs=0, host_pool_blocks=1, poison=True, seed=31 + H + D)
     S = case.S
     bm = pkv.BlockManager(case.num_blocks, case.B, free_ids=case.free_ids)
     bt = case.block_tables.clone()
