@@ -160,6 +160,33 @@ PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, i
                                     int block_size, int max_context_len);
 
 /*
+ * The launch shape the automatic choice (tuning knobs as currently set)
+ * takes for a decode problem on a device with sm_count SMs, smem_optin
+ * bytes of shared memory a block may use and smem_per_sm bytes an SM holds
+ * (GB300: 152, 232448, 233472) -- host arithmetic only, no device is
+ * touched, so it serves to inspect and test the choice anywhere.
+ * split_tokens 0 asks for the automatic split, as in paged_attn_decode.
+ * PKV_ERR_INVALID / PKV_ERR_UNSUPPORTED as paged_attn_decode would return
+ * for the shape; *shape is written on PKV_OK.  No page has a counterpart.
+ */
+typedef struct {
+    int kernel;              /* 0 CUDA-core per unit, 1 tensor-core per unit, 2 streaming */
+    int split_tokens;        /* tokens per work unit (the whole context when streaming) */
+    int max_splits;          /* grid extent over splits (per-unit kernels) */
+    int heads_per_cta;       /* kv heads per CTA */
+    int stages;              /* pages in each CTA's ring */
+    int warps_per_token;     /* consumer warps taking turns on a head's pages */
+    int threads;             /* threads per CTA */
+    int stream_ctas;         /* streaming: the most CTAs the grid takes (else 0) */
+    size_t smem_bytes;       /* dynamic shared memory per CTA */
+} pkv_decode_shape;
+
+PKV_API pkv_status pkv_decode_launch_shape(int num_seqs, int n_heads, int n_kv_heads,
+                                           int head_dim, int block_size, int max_context_len,
+                                           int split_tokens, int sm_count, int smem_optin,
+                                           int smem_per_sm, pkv_decode_shape* shape);
+
+/*
  * paged_attn_decode -- for every sequence s and query head h:
  *
  *     out[s,h,:] = sum_t softmax_t(scale * q[s,h,:] . K_t) * V_t,

@@ -40,6 +40,7 @@ SIGNATURES = {
     "pkv_device_errors": (_i, [C.POINTER(C.c_uint32), _i]),
     "pkv_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "pkv_decode_split_tokens": (_i, [_i, _i, _i, _i, _i, _i]),
+    "pkv_decode_launch_shape": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _p]),
     "paged_attn_decode": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i, _i, _f,
                                _i, _i, _p, _sz, _p]),
     "paged_attn_decode_append": (_i, [_p, _i, _p, _p, _p, _i, _p, _i, _p, _i, _i, _i, _i, _i,

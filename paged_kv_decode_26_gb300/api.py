@@ -102,6 +102,34 @@ def decode_split_tokens(num_seqs: int, n_heads: int, n_kv_heads: int, head_dim: 
                                              max_context_len))
 
 
+class _Shape(C.Structure):
+    """pkv_decode_shape of include/pagedkv.h."""
+    _fields_ = [("kernel", C.c_int), ("split_tokens", C.c_int), ("max_splits", C.c_int),
+                ("heads_per_cta", C.c_int), ("stages", C.c_int), ("warps_per_token", C.c_int),
+                ("threads", C.c_int), ("stream_ctas", C.c_int), ("smem_bytes", C.c_size_t)]
+
+
+_KERNELS = ("cuda_core", "tensor_core", "streaming")
+
+
+def decode_launch_shape(num_seqs: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                        block_size: int, max_context_len: int, split_tokens: int = 0,
+                        sm_count: int = 152, smem_optin: int = 232448,
+                        smem_per_sm: int = 233472) -> dict:
+    """The launch shape the automatic choice takes for a decode problem on a
+    device with these facts (default: GB300's), by host arithmetic only --
+    kernel ("cuda_core", "tensor_core" or "streaming"), split_tokens,
+    max_splits, heads_per_cta, stages, warps_per_token, threads,
+    stream_ctas, smem_bytes."""
+    sh = _Shape()
+    check(lib().pkv_decode_launch_shape(num_seqs, n_heads, n_kv_heads, head_dim, block_size,
+                                        max_context_len, split_tokens, sm_count, smem_optin,
+                                        smem_per_sm, C.byref(sh)), "pkv_decode_launch_shape")
+    out = {name: getattr(sh, name) for name, _ in _Shape._fields_}
+    out["kernel"] = _KERNELS[sh.kernel]
+    return out
+
+
 def alloc_decode_workspace(q: torch.Tensor, k_pool: torch.Tensor, max_context_len: int,
                            split_tokens: int = 0) -> Optional[torch.Tensor]:
     S, H, D = q.shape

@@ -602,6 +602,36 @@ PKV_API int pkv_decode_split_tokens(int num_seqs, int n_heads, int n_kv_heads, i
     return c.split_tokens;
 }
 
+PKV_API pkv_status pkv_decode_launch_shape(int num_seqs, int n_heads, int n_kv_heads,
+                                           int head_dim, int block_size, int max_context_len,
+                                           int split_tokens, int sm_count, int smem_optin,
+                                           int smem_per_sm, pkv_decode_shape* shape) {
+    if (!shape) return invalid("shape is required");
+    if (num_seqs < 0 || max_context_len < 0 || sm_count < 1 || smem_optin < 1 ||
+        smem_per_sm < 1)
+        return invalid("negative sizes, or no SMs / shared memory");
+    if (n_kv_heads <= 0 || n_heads <= 0 || n_heads % n_kv_heads)
+        return invalid("n_heads must be a positive multiple of n_kv_heads");
+    if (!supported_shape(n_heads, n_kv_heads, head_dim, block_size))
+        return unsupported("head_dim, block_size or query-head group");
+    DecodeConfig c;
+    const pkv_status st = make_config(num_seqs, n_heads, n_kv_heads, head_dim, block_size,
+                                      max_context_len, split_tokens, sm_count, &c, true,
+                                      (size_t)smem_optin, smem_per_sm);
+    if (st != PKV_OK) return st;
+    if (c.smem > (size_t)smem_optin) return unsupported("shared memory of this configuration");
+    shape->kernel = c.stream ? 2 : (c.mma ? 1 : 0);
+    shape->split_tokens = c.split_tokens;
+    shape->max_splits = c.max_splits;
+    shape->heads_per_cta = c.hpc;
+    shape->stages = c.stages;
+    shape->warps_per_token = c.wpt;
+    shape->threads = c.threads;
+    shape->stream_ctas = c.stream ? c.stream_ctas : 0;
+    shape->smem_bytes = c.smem;
+    return PKV_OK;
+}
+
 PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int n_heads, int n_kv_heads,
                                           int head_dim, int block_size, int max_context_len,
                                           int split_tokens) {
